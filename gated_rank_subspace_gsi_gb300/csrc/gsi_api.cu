@@ -1,0 +1,222 @@
+// gsi_api.cu -- the C ABI declared in include/gsi.h: argument checks, handle
+// and workspace lifetime, and dispatch to the decode (T = 1) and batched
+// (T > 1) paths.  Page: "Technical summary: Gated Subspace Inference for
+// transformer acceleration", sections 2.1-2.2.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <new>
+
+#include "gsi_device.cuh"
+#include "gsi_internal.h"
+#include "gsi_tc_gemm.h"
+
+namespace {
+
+constexpr int64_t kDefaultMaxT = 512;
+
+bool valid_k(int64_t k) {
+  return k == 16 || k == 32 || k == 64 || k == 128 || k == 256 || k == 512;
+}
+
+gsi_status_t check_shape(int64_t d_out, int64_t d, int64_t k) {
+  if (d_out <= 0 || d <= 0 || k <= 0) return GSI_ERR_UNSUPPORTED_SHAPE;
+  if (d % 8 != 0 || d_out % 8 != 0 || !valid_k(k) || k > d) return GSI_ERR_UNSUPPORTED_SHAPE;
+  if (d_out > (int64_t(1) << 30) || d > (int64_t(1) << 24)) return GSI_ERR_UNSUPPORTED_SHAPE;
+  return GSI_OK;
+}
+
+gsi_status_t grow_batched(gsi_handle* h, int64_t max_T) {
+  if (max_T <= h->max_T) return GSI_OK;
+  const size_t bytes = gsi::batched_workspace_bytes(max_T, h->d, h->k);
+  void* p = nullptr;
+  if (cudaMalloc(&p, bytes) != cudaSuccess) return GSI_ERR_NOMEM;
+  if (cudaMemset(p, 0, bytes) != cudaSuccess) {
+    cudaFree(p);
+    return GSI_ERR_CUDA;
+  }
+  if (h->bws) {
+    cudaDeviceSynchronize();
+    cudaFree(h->bws);
+  }
+  h->bws = p;
+  h->bws_bytes = bytes;
+  gsi::batched_bind_workspace(h, p, max_T);
+  return gsi::tc_gemm_prepare(h);
+}
+
+gsi_status_t grow_staging(gsi_handle* h, int64_t T) {
+  if (T <= h->st_T) return GSI_OK;
+  const size_t bytes = size_t(T) * (h->d * 2 + h->d_out * 4 + 4 + 1) + 1024;
+  void* p = nullptr;
+  if (cudaMalloc(&p, bytes) != cudaSuccess) return GSI_ERR_NOMEM;
+  if (h->st_dev) {
+    cudaDeviceSynchronize();
+    cudaFree(h->st_dev);
+  }
+  h->st_dev = p;
+  h->st_bytes = bytes;
+  h->st_T = T;
+  return GSI_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* gsi_status_string(gsi_status_t s) {
+  switch (s) {
+    case GSI_OK: return "GSI_OK";
+    case GSI_ERR_INVALID_ARG: return "GSI_ERR_INVALID_ARG: null or misaligned pointer, NaN eps, or T < 0";
+    case GSI_ERR_UNSUPPORTED_SHAPE:
+      return "GSI_ERR_UNSUPPORTED_SHAPE: need d % 8 == 0, d_out % 8 == 0, k in {16,32,64,128,256,512}, k <= d";
+    case GSI_ERR_NOMEM: return "GSI_ERR_NOMEM: allocation failed";
+    case GSI_ERR_CUDA: return "GSI_ERR_CUDA: a CUDA call or kernel launch failed";
+    case GSI_ERR_WORKSPACE: return "GSI_ERR_WORKSPACE: T exceeds the reserved workspace (call gsi_reserve)";
+    case GSI_ERR_TIMEOUT: return "GSI_ERR_TIMEOUT: a bounded device-side wait ran out";
+  }
+  return "unknown gsi_status_t";
+}
+
+gsi_status_t gsi_create(const void* W, const void* V_k, const void* M, int64_t d_out, int64_t d,
+                        int64_t k, float eps, gsi_handle_t* out) {
+  if (!out) return GSI_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!W || !V_k || !M || std::isnan(eps)) return GSI_ERR_INVALID_ARG;
+  if (!gsi::aligned16(W) || !gsi::aligned16(V_k) || !gsi::aligned16(M)) return GSI_ERR_INVALID_ARG;
+  gsi_status_t st = check_shape(d_out, d, k);
+  if (st != GSI_OK) return st;
+
+  gsi_handle* h = new (std::nothrow) gsi_handle();
+  if (!h) return GSI_ERR_NOMEM;
+  h->W = static_cast<const __nv_bfloat16*>(W);
+  h->V = static_cast<const __nv_bfloat16*>(V_k);
+  h->M = static_cast<const __nv_bfloat16*>(M);
+  h->d_out = d_out;
+  h->d = d;
+  h->k = k;
+  h->eps = eps;
+  if (cudaGetDevice(&h->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
+    delete h;
+    return GSI_ERR_CUDA;
+  }
+  // fixed workspace: Gram matrix, decode accumulators, barrier words, status
+  h->dec_acc_stride = int(k + 4);
+  const size_t gram_b = size_t(k) * k * 4;
+  const size_t acc_b = size_t(2) * h->dec_acc_stride * 4;
+  const size_t ws = ((gram_b + 255) / 256 + (acc_b + 255) / 256 + 1) * 256;
+  if (cudaMalloc(&h->ws, ws) != cudaSuccess) {
+    delete h;
+    return GSI_ERR_NOMEM;
+  }
+  h->ws_bytes = ws;
+  char* p = static_cast<char*>(h->ws);
+  h->gram = reinterpret_cast<float*>(p);
+  p += (gram_b + 255) / 256 * 256;
+  h->dec_acc = reinterpret_cast<float*>(p);
+  p += (acc_b + 255) / 256 * 256;
+  h->dec_bar = reinterpret_cast<uint32_t*>(p);
+  h->status = reinterpret_cast<uint32_t*>(p + 64);
+  st = GSI_OK;
+  if (cudaMemset(h->ws, 0, ws) != cudaSuccess) st = GSI_ERR_CUDA;
+  if (st == GSI_OK) st = gsi::decode_configure(h);
+  if (st == GSI_OK) st = gsi::gram_launch(h->V, d, k, h->gram, nullptr);
+  if (st == GSI_OK) st = grow_batched(h, kDefaultMaxT);
+  if (st == GSI_OK) st = grow_staging(h, kDefaultMaxT);
+  if (st == GSI_OK && cudaDeviceSynchronize() != cudaSuccess) st = GSI_ERR_CUDA;
+  if (st != GSI_OK) {
+    gsi_destroy(h);
+    return st;
+  }
+  *out = h;
+  return GSI_OK;
+}
+
+gsi_status_t gsi_forward(gsi_handle_t h, const void* x, int64_t T, float* y, uint8_t* gate,
+                         float* rho, cudaStream_t stream) {
+  if (!h || T < 0) return GSI_ERR_INVALID_ARG;
+  if (T == 0) return GSI_OK;
+  if (!x || !y || !gsi::aligned16(x) || !gsi::aligned16(y)) return GSI_ERR_INVALID_ARG;
+  if (T == 1) return gsi::decode_launch(h, x, y, gate, rho, stream);
+  if (T > h->max_T) return GSI_ERR_WORKSPACE;
+  return gsi::batched_launch(h, x, T, y, gate, rho, stream);
+}
+
+gsi_status_t gsi_forward_host(gsi_handle_t h, const void* x_host, int64_t T, float* y_host,
+                              uint8_t* gate_host, float* rho_host, cudaStream_t stream) {
+  if (!h || T < 0) return GSI_ERR_INVALID_ARG;
+  if (T == 0) return GSI_OK;
+  if (!x_host || !y_host) return GSI_ERR_INVALID_ARG;
+  if (T > h->st_T || (T > 1 && T > h->max_T)) return GSI_ERR_WORKSPACE;
+  char* p = static_cast<char*>(h->st_dev);
+  void* xd = p;
+  p += (size_t(h->st_T) * h->d * 2 + 255) / 256 * 256;
+  float* yd = reinterpret_cast<float*>(p);
+  p += (size_t(h->st_T) * h->d_out * 4 + 255) / 256 * 256;
+  float* rd = reinterpret_cast<float*>(p);
+  p += (size_t(h->st_T) * 4 + 255) / 256 * 256;
+  uint8_t* gd = reinterpret_cast<uint8_t*>(p);
+  if (cudaMemcpyAsync(xd, x_host, size_t(T) * h->d * 2, cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    return GSI_ERR_CUDA;
+  gsi_status_t st = gsi_forward(h, xd, T, yd, gd, rd, stream);
+  if (st != GSI_OK) return st;
+  if (cudaMemcpyAsync(y_host, yd, size_t(T) * h->d_out * 4, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return GSI_ERR_CUDA;
+  if (gate_host && cudaMemcpyAsync(gate_host, gd, size_t(T), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return GSI_ERR_CUDA;
+  if (rho_host && cudaMemcpyAsync(rho_host, rd, size_t(T) * 4, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return GSI_ERR_CUDA;
+  return GSI_OK;
+}
+
+gsi_status_t gsi_precompute_M(const void* W, const void* V_k, void* M, int64_t d_out, int64_t d,
+                              int64_t k, cudaStream_t stream) {
+  if (!W || !V_k || !M) return GSI_ERR_INVALID_ARG;
+  if (!gsi::aligned16(W) || !gsi::aligned16(V_k) || !gsi::aligned16(M)) return GSI_ERR_INVALID_ARG;
+  gsi_status_t st = check_shape(d_out, d, k);
+  if (st != GSI_OK) return st;
+  return gsi::precompute_M_launch(static_cast<const __nv_bfloat16*>(W),
+                                  static_cast<const __nv_bfloat16*>(V_k),
+                                  static_cast<__nv_bfloat16*>(M), d_out, d, k, stream);
+}
+
+gsi_status_t gsi_reserve(gsi_handle_t h, int64_t max_T) {
+  if (!h || max_T < 0 || max_T > (int64_t(1) << 24)) return GSI_ERR_INVALID_ARG;
+  gsi_status_t st = grow_batched(h, max_T);
+  if (st != GSI_OK) return st;
+  st = grow_staging(h, std::max<int64_t>(max_T, 1));
+  if (st != GSI_OK) return st;
+  return cudaDeviceSynchronize() == cudaSuccess ? GSI_OK : GSI_ERR_CUDA;
+}
+
+gsi_status_t gsi_device_status(gsi_handle_t h, cudaStream_t stream) {
+  if (!h) return GSI_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return GSI_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, h->status, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return GSI_ERR_CUDA;
+  if (word) {
+    const uint32_t zero = 0;
+    if (cudaMemcpy(h->status, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+      return GSI_ERR_CUDA;
+  }
+  return (word & gsi::kStatusTimeout) ? GSI_ERR_TIMEOUT : GSI_OK;
+}
+
+void gsi_destroy(gsi_handle_t h) {
+  if (!h) return;
+  cudaDeviceSynchronize();
+  if (h->ws) cudaFree(h->ws);
+  if (h->bws) cudaFree(h->bws);
+  if (h->st_dev) cudaFree(h->st_dev);
+  delete h;
+}
+
+int gsi_forward_launch_count(gsi_handle_t h, int64_t T) {
+  if (!h || T <= 0) return 0;
+  if (T == 1) return 1;
+  return gsi::batched_launch_count(h, T);
+}
+
+}  // extern "C"

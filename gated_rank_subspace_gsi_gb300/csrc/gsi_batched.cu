@@ -1,0 +1,295 @@
+// gsi_batched.cu -- the T > 1 path of the GSI gated linear map.
+//
+// Page: "Technical summary: Gated Subspace Inference for transformer
+// acceleration" [GSI], sections 2.1-2.2.  For T tokens at once:
+//   1. projection   G = X V_k (T x k) and ||x_t||^2            (section 2.1)
+//   2. gate         ||r_t||^2 = ||x_t||^2 - 2 g_t.g_t + g_t^T Gm g_t with
+//                   Gm = V_k^T V_k (exact identity for r = x - V_k g),
+//                   rho_t = ||r_t|| / ||x_t||, gate_t = !(rho_t < eps)
+//   3. compaction   stable partition of 0..T-1 by gate into index lists
+//   4. gather       fast tokens' g_t (as bf16 hi + lo pairs) and slow tokens'
+//                   x_t into dense operand blocks
+//   5. GEMMs        Y_fast = G_fast M^T and Y_slow = X_slow W^T on the
+//                   tcgen05 tensor cores (gsi_tc_gemm.cu), each output row
+//                   scattered back to its token's row of y.
+// Counts of fast and slow tokens stay on the device; GEMM CTAs whose token
+// tile lies past the count exit before reading weights.
+#include <algorithm>
+#include <cfloat>
+
+#include "gsi_device.cuh"
+#include "gsi_internal.h"
+#include "gsi_tc_gemm.h"
+
+namespace gsi {
+namespace {
+
+constexpr int kProjRows = 64;    // V_k rows per CTA
+constexpr int kProjTok = 16;     // tokens per CTA
+constexpr int kGateTok = 8;      // tokens per CTA in the gate kernel
+
+// G[t][a] += sum_{i in chunk} x[t][i] V[i][a]; sx[t] += sum_{i in chunk} x[t][i]^2.
+template <int K>
+__global__ void __launch_bounds__(256) proj_kernel(const __nv_bfloat16* __restrict__ x,
+                                                   const __nv_bfloat16* __restrict__ V,
+                                                   int T, int d, float* __restrict__ G,
+                                                   float* __restrict__ sx) {
+  __shared__ float sxv[kProjTok][kProjRows + 1];
+  const int i0 = blockIdx.x * kProjRows, t0 = blockIdx.y * kProjTok;
+  const int nrow = min(kProjRows, d - i0), ntok = min(kProjTok, T - t0);
+  for (int q = threadIdx.x; q < kProjTok * kProjRows; q += blockDim.x) {
+    const int t = q / kProjRows, i = q % kProjRows;
+    sxv[t][i] = (t < ntok && i < nrow) ? __bfloat162float(x[size_t(t0 + t) * d + i0 + i]) : 0.f;
+  }
+  __syncthreads();
+  for (int a = threadIdx.x; a < K; a += blockDim.x) {
+    float acc[kProjTok];
+#pragma unroll
+    for (int t = 0; t < kProjTok; ++t) acc[t] = 0.f;
+    for (int i = 0; i < nrow; ++i) {
+      const float v = __bfloat162float(V[size_t(i0 + i) * K + a]);
+#pragma unroll
+      for (int t = 0; t < kProjTok; ++t) acc[t] = fmaf(v, sxv[t][i], acc[t]);
+    }
+    for (int t = 0; t < ntok; ++t) red_add_f32(G + size_t(t0 + t) * K + a, acc[t]);
+  }
+  if (threadIdx.x < ntok) {
+    float s = 0.f;
+    for (int i = 0; i < nrow; ++i) s = fmaf(sxv[threadIdx.x][i], sxv[threadIdx.x][i], s);
+    red_add_f32(sx + t0 + threadIdx.x, s);
+  }
+}
+
+// rho and gate of kGateTok tokens per CTA.
+template <int K>
+__global__ void __launch_bounds__(256) gate_kernel(const float* __restrict__ G,
+                                                   const float* __restrict__ sx,
+                                                   const float* __restrict__ gram, int T,
+                                                   float eps, uint8_t* __restrict__ gate_int,
+                                                   uint8_t* __restrict__ gate_out,
+                                                   float* __restrict__ rho_out) {
+  __shared__ float sg[kGateTok][K];
+  __shared__ float sred[kGateTok][2][8];
+  const int t0 = blockIdx.x * kGateTok;
+  const int ntok = min(kGateTok, T - t0);
+  for (int q = threadIdx.x; q < kGateTok * K; q += blockDim.x) {
+    const int t = q / K, a = q % K;
+    sg[t][a] = t < ntok ? G[size_t(t0 + t) * K + a] : 0.f;
+  }
+  __syncthreads();
+  float quad[kGateTok], gg[kGateTok];
+#pragma unroll
+  for (int t = 0; t < kGateTok; ++t) quad[t] = gg[t] = 0.f;
+  for (int a = threadIdx.x; a < K; a += blockDim.x) {
+    float hg[kGateTok];
+#pragma unroll
+    for (int t = 0; t < kGateTok; ++t) hg[t] = 0.f;
+    for (int b = 0; b < K; ++b) {
+      const float gm = gram[size_t(b) * K + a];  // Gm is symmetric: row b, column a
+#pragma unroll
+      for (int t = 0; t < kGateTok; ++t) hg[t] = fmaf(gm, sg[t][b], hg[t]);
+    }
+#pragma unroll
+    for (int t = 0; t < kGateTok; ++t) {
+      quad[t] = fmaf(sg[t][a], hg[t], quad[t]);
+      gg[t] = fmaf(sg[t][a], sg[t][a], gg[t]);
+    }
+  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int t = 0; t < kGateTok; ++t) {
+    const float q = warp_sum_xor<32>(quad[t]);
+    const float g2 = warp_sum_xor<32>(gg[t]);
+    if (lane == 0) {
+      sred[t][0][warp] = q;
+      sred[t][1][warp] = g2;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < ntok) {
+    const int t = threadIdx.x;
+    float q = 0.f, g2 = 0.f;
+    for (int w = 0; w < int(blockDim.x / 32); ++w) {
+      q += sred[t][0][w];
+      g2 += sred[t][1][w];
+    }
+    const float sxv = sx[t0 + t];
+    float rho;
+    if (!(fabsf(sxv) <= FLT_MAX)) {
+      rho = __int_as_float(0x7FC00000);
+    } else if (sxv == 0.f) {
+      rho = 0.f;
+    } else {
+      float sr = sxv - 2.f * g2 + q;
+      if (!(sr >= 0.f)) sr = (sr == sr) ? 0.f : sr;
+      rho = sqrtf(sr / sxv);
+    }
+    const uint8_t slow = (rho < eps) ? 0 : 1;
+    gate_int[t0 + t] = slow;
+    if (gate_out) gate_out[t0 + t] = slow;
+    if (rho_out) rho_out[t0 + t] = rho;
+  }
+}
+
+// Stable partition of token indices by gate; one CTA of 1024 threads.
+__global__ void __launch_bounds__(1024) compact_kernel(const uint8_t* __restrict__ gate, int T,
+                                                       int32_t* __restrict__ idx_fast,
+                                                       int32_t* __restrict__ idx_slow,
+                                                       int32_t* __restrict__ count) {
+  __shared__ int s_warp[32];
+  __shared__ int s_base;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) s_base = 0;
+  __syncthreads();
+  for (int c0 = 0; c0 < T; c0 += 1024) {
+    const int t = c0 + tid;
+    const int flag = (t < T) ? int(gate[t] != 0) : 0;
+    // inclusive warp scan of slow flags
+    int v = flag;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xFFFFFFFFu, v, o);
+      if (lane >= o) v += n;
+    }
+    if (lane == 31) s_warp[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+      int w = s_warp[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xFFFFFFFFu, w, o);
+        if (lane >= o) w += n;
+      }
+      s_warp[lane] = w;  // inclusive prefix over warps
+    }
+    __syncthreads();
+    const int before_warp = warp ? s_warp[warp - 1] : 0;
+    const int slow_before = s_base + before_warp + v - flag;  // exclusive, global
+    if (t < T) {
+      if (flag) idx_slow[slow_before] = t;
+      else idx_fast[t - slow_before] = t;
+    }
+    __syncthreads();
+    if (tid == 0) s_base += s_warp[31];
+    __syncthreads();
+  }
+  if (tid == 0) {
+    count[0] = T - s_base;  // n_fast
+    count[1] = s_base;      // n_slow
+  }
+}
+
+// Gather: fast tokens -> row j of the G_fast planes, hi = bf16(g) in plane 0
+// and lo = bf16(g - hi) in plane 1 (hi + lo carries g to ~2^-16 relative);
+// slow tokens -> X_slow rows (bf16 copies of x).  One CTA per token.
+template <int K>
+__global__ void __launch_bounds__(256) gather_kernel(const __nv_bfloat16* __restrict__ x,
+                                                     const float* __restrict__ G,
+                                                     const uint8_t* __restrict__ gate,
+                                                     const int32_t* __restrict__ idx_fast,
+                                                     const int32_t* __restrict__ idx_slow,
+                                                     const int32_t* __restrict__ count, int d,
+                                                     int max_T, __nv_bfloat16* __restrict__ Gf,
+                                                     __nv_bfloat16* __restrict__ Xs) {
+  const int j = blockIdx.x;  // position in the concatenated [fast | slow] list
+  const int n_fast = count[0], n_slow = count[1];
+  if (j < n_fast) {
+    const int t = idx_fast[j];
+    for (int a = threadIdx.x; a < K; a += blockDim.x) {
+      const float g = G[size_t(t) * K + a];
+      const __nv_bfloat16 hi = __float2bfloat16_rn(g);
+      const __nv_bfloat16 lo = __float2bfloat16_rn(g - __bfloat162float(hi));
+      Gf[size_t(j) * K + a] = hi;
+      Gf[(size_t(max_T) + j) * K + a] = lo;
+    }
+  } else if (j < n_fast + n_slow) {
+    const int js = j - n_fast;
+    const int t = idx_slow[js];
+    const uint4* src = reinterpret_cast<const uint4*>(x + size_t(t) * d);
+    uint4* dst = reinterpret_cast<uint4*>(Xs + size_t(js) * d);
+    for (int i = threadIdx.x; i < d / 8; i += blockDim.x) dst[i] = src[i];
+  }
+}
+
+template <int K>
+gsi_status_t launch_front(gsi_handle* h, const void* x, int T, uint8_t* gate, float* rho,
+                          cudaStream_t s) {
+  const auto* xb = static_cast<const __nv_bfloat16*>(x);
+  if (cudaMemsetAsync(h->bG, 0, size_t(T) * K * sizeof(float), s) != cudaSuccess) return GSI_ERR_CUDA;
+  if (cudaMemsetAsync(h->bsx, 0, size_t(T) * sizeof(float), s) != cudaSuccess) return GSI_ERR_CUDA;
+  dim3 pg(unsigned((h->d + kProjRows - 1) / kProjRows), unsigned((T + kProjTok - 1) / kProjTok));
+  proj_kernel<K><<<pg, 256, 0, s>>>(xb, h->V, T, int(h->d), h->bG, h->bsx);
+  gate_kernel<K><<<(T + kGateTok - 1) / kGateTok, 256, 0, s>>>(h->bG, h->bsx, h->gram, T, h->eps,
+                                                               h->bgate, gate, rho);
+  compact_kernel<<<1, 1024, 0, s>>>(h->bgate, T, h->bidx_fast, h->bidx_slow, h->bcount);
+  gather_kernel<K><<<T, 256, 0, s>>>(xb, h->bG, h->bgate, h->bidx_fast, h->bidx_slow, h->bcount,
+                                     int(h->d), int(h->max_T), h->bGf, h->bXs);
+  return cudaGetLastError() == cudaSuccess ? GSI_OK : GSI_ERR_CUDA;
+}
+
+size_t align256(size_t v) { return (v + 255) / 256 * 256; }
+
+}  // namespace
+
+size_t batched_workspace_bytes(int64_t max_T, int64_t d, int64_t k) {
+  size_t b = 0;
+  b += align256(size_t(max_T) * k * 4);      // bG
+  b += align256(size_t(max_T) * 4);          // bsx
+  b += align256(size_t(max_T));              // bgate
+  b += align256(size_t(max_T) * 4) * 2;      // idx lists
+  b += align256(16);                         // counts
+  b += align256(size_t(max_T) * 2 * k * 2);  // bGf
+  b += align256(size_t(max_T) * d * 2);      // bXs
+  return b;
+}
+
+void batched_bind_workspace(gsi_handle* h, void* base, int64_t max_T) {
+  char* p = static_cast<char*>(base);
+  auto take = [&](size_t bytes) { char* r = p; p += align256(bytes); return r; };
+  h->bG = reinterpret_cast<float*>(take(size_t(max_T) * h->k * 4));
+  h->bsx = reinterpret_cast<float*>(take(size_t(max_T) * 4));
+  h->bgate = reinterpret_cast<uint8_t*>(take(size_t(max_T)));
+  h->bidx_fast = reinterpret_cast<int32_t*>(take(size_t(max_T) * 4));
+  h->bidx_slow = reinterpret_cast<int32_t*>(take(size_t(max_T) * 4));
+  h->bcount = reinterpret_cast<int32_t*>(take(16));
+  h->bGf = reinterpret_cast<__nv_bfloat16*>(take(size_t(max_T) * 2 * h->k * 2));
+  h->bXs = reinterpret_cast<__nv_bfloat16*>(take(size_t(max_T) * h->d * 2));
+  h->max_T = max_T;
+}
+
+int batched_launch_count(const gsi_handle* h, int64_t T) {
+  (void)h;
+  return T > 1 ? 4 + tc_gemm_launch_count() : 0;
+}
+
+gsi_status_t batched_launch(gsi_handle* h, const void* x, int64_t T, float* y, uint8_t* gate,
+                            float* rho, cudaStream_t s) {
+  gsi_status_t st;
+  switch (h->k) {
+    case 16: st = launch_front<16>(h, x, int(T), gate, rho, s); break;
+    case 32: st = launch_front<32>(h, x, int(T), gate, rho, s); break;
+    case 64: st = launch_front<64>(h, x, int(T), gate, rho, s); break;
+    case 128: st = launch_front<128>(h, x, int(T), gate, rho, s); break;
+    case 256: st = launch_front<256>(h, x, int(T), gate, rho, s); break;
+    case 512: st = launch_front<512>(h, x, int(T), gate, rho, s); break;
+    default: return GSI_ERR_UNSUPPORTED_SHAPE;
+  }
+  if (st != GSI_OK) return st;
+  TcGemmArgs g;
+  g.W = h->W;
+  g.M = h->M;
+  g.Gf = h->bGf;
+  g.Xs = h->bXs;
+  g.idx_fast = h->bidx_fast;
+  g.idx_slow = h->bidx_slow;
+  g.count = h->bcount;
+  g.y = y;
+  g.T = int(T);
+  g.d_out = int(h->d_out);
+  g.d = int(h->d);
+  g.k = int(h->k);
+  g.status = h->status;
+  return tc_gemm_launch(h, g, s);
+}
+
+}  // namespace gsi

@@ -1,0 +1,89 @@
+// gsi_internal.h -- host-side handle layout and the launchers that the C ABI
+// (gsi_api.cu) calls.  Not part of the public interface (include/gsi.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "gsi.h"
+
+struct gsi_handle {
+  // Borrowed operands (section 2.1 of the GSI summary): W (d_out x d),
+  // V_k (d x k), M = W V_k (d_out x k), all bf16 row-major, device memory.
+  const __nv_bfloat16* W = nullptr;
+  const __nv_bfloat16* V = nullptr;
+  const __nv_bfloat16* M = nullptr;
+  int64_t d_out = 0, d = 0, k = 0;
+  float eps = 0.f;
+  int device = 0;
+  int num_sms = 0;
+
+  // ---- decode path (T = 1): one fused persistent kernel ------------------
+  int dec_grid = 0;          // CTAs (all co-resident; one per SM at most)
+  int dec_rows_M = 0;        // rows of M / W per CTA
+  int dec_rows_V = 0;        // rows of V_k per CTA
+  bool dec_stage_M = false;  // M slice staged in shared memory by bulk copy
+  bool dec_stage_V = false;  // V slice staged in shared memory by bulk copy
+  size_t dec_smem = 0;       // dynamic shared memory bytes
+  bool use_pdl = true;       // programmatic dependent launch between kernels
+
+  // ---- device workspace (one allocation) --------------------------------
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  float* gram = nullptr;       // k x k fp32, V_k^T V_k (batched path)
+  float* dec_acc = nullptr;    // 2 x acc_stride fp32: g (k), ||x||^2, ||r||^2
+  int dec_acc_stride = 0;
+  uint32_t* dec_bar = nullptr; // [0] arrival counter, [1] launch epoch
+  uint32_t* status = nullptr;  // device status word (kStatus* bits)
+
+  // batched path, sized for max_T tokens
+  int64_t max_T = 0;
+  void* bws = nullptr;         // separate allocation, regrown by gsi_reserve
+  size_t bws_bytes = 0;
+  float* bG = nullptr;         // max_T x k   projections g_t
+  float* bsx = nullptr;        // max_T       ||x_t||^2
+  uint8_t* bgate = nullptr;    // max_T       internal copy of the gates
+  int32_t* bidx_fast = nullptr;// max_T       token indices of fast tokens
+  int32_t* bidx_slow = nullptr;// max_T       token indices of slow tokens
+  int32_t* bcount = nullptr;   // [0] n_fast, [1] n_slow
+  __nv_bfloat16* bGf = nullptr;// [2][max_T][k] gathered g of fast tokens (hi, lo planes)
+  __nv_bfloat16* bXs = nullptr;// max_T x d   gathered x of slow tokens
+
+  // TMA tensor maps of the tcgen05 GEMMs (CUtensorMap, 128 bytes each):
+  // W, M, G_fast hi plane, G_fast lo plane, X_slow
+  alignas(64) unsigned char tmaps[5][128] = {};
+
+  // host staging for gsi_forward_host
+  void* st_dev = nullptr;
+  size_t st_bytes = 0;
+  int64_t st_T = 0;
+};
+
+namespace gsi {
+
+// Decode path (gsi_decode.cu)
+gsi_status_t decode_configure(gsi_handle* h);
+gsi_status_t decode_launch(gsi_handle* h, const void* x, float* y, uint8_t* gate,
+                           float* rho, cudaStream_t s);
+
+// Batched path (gsi_batched.cu)
+gsi_status_t batched_launch(gsi_handle* h, const void* x, int64_t T, float* y,
+                            uint8_t* gate, float* rho, cudaStream_t s);
+int batched_launch_count(const gsi_handle* h, int64_t T);
+size_t batched_workspace_bytes(int64_t max_T, int64_t d, int64_t k);
+void batched_bind_workspace(gsi_handle* h, void* base, int64_t max_T);
+
+// One-off operand preparation (gsi_prep.cu)
+gsi_status_t gram_launch(const __nv_bfloat16* V, int64_t d, int64_t k, float* gram,
+                         cudaStream_t s);
+gsi_status_t precompute_M_launch(const __nv_bfloat16* W, const __nv_bfloat16* V,
+                                 __nv_bfloat16* M, int64_t d_out, int64_t d, int64_t k,
+                                 cudaStream_t s);
+
+inline bool aligned16(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+}  // namespace gsi

@@ -1,0 +1,328 @@
+// gsi_tc_gemm.cu -- the two dense contractions of the batched GSI path on
+// the sm_103a tcgen05 tensor cores, written with inline PTX (TMA, mbarrier,
+// tcgen05.mma / commit / ld, TMEM alloc).
+//
+// Page: "Technical summary: Gated Subspace Inference for transformer
+// acceleration" [GSI], section 2.2: fast tokens take y = M g, slow tokens
+// take y = W x.  After compaction (gsi_batched.cu) both are GEMMs:
+//   Y_slow^T (d_out x n_slow) = W (d_out x d)  . X_slow^T
+//   Y_fast^T (d_out x n_fast) = M (d_out x k)  . (G_hi + G_lo)^T
+// Weights sit in the MMA's M dimension ("swap AB"), so each weight tile is
+// read from HBM by exactly one CTA and the token count sets N (16..256, a
+// runtime value in the instruction descriptor).  G_fast is carried as two
+// bf16 planes hi = bf16(g), lo = bf16(g - hi); both accumulate into the same
+// TMEM tile, which keeps g to ~2^-16 relative although the operands are bf16.
+//
+// CTA layout (192 threads): warp 0 issues TMA loads (one elected lane),
+// warp 1 allocates TMEM and issues tcgen05.mma (one elected lane), warps 2-5
+// drain the fp32 accumulator from TMEM (tcgen05.ld 32x32b) and scatter each
+// token column to its row of y.  A 4-stage mbarrier ring of 128x64 (A) and
+// 256x64 (B) bf16 tiles, 128-byte swizzled, feeds the MMAs.
+#include <cuda.h>
+
+#include <algorithm>
+#include <cstring>
+
+#include "gsi_device.cuh"
+#include "gsi_internal.h"
+#include "gsi_tc_gemm.h"
+
+namespace gsi {
+namespace {
+
+constexpr int kBM = 128;           // weight rows per tile (MMA M)
+constexpr int kBN = 256;           // token rows per tile (max MMA N)
+constexpr int kBK = 64;            // K elements per stage (128 bytes of bf16)
+constexpr int kStages = 4;
+constexpr int kABytes = kBM * kBK * 2;   // 16 KiB
+constexpr int kBBytes = kBN * kBK * 2;   // 32 KiB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kTcThreads = 192;
+constexpr int kTmemCols = 256;
+constexpr size_t kTcSmem = size_t(kStages) * kStageBytes + 1024;  // + alignment slack
+
+// ---- tcgen05 / TMA wrappers ------------------------------------------------
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];"
+      :: "r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1),
+         "r"(smem_addr(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+               :: "r"(smem_addr(dst_smem)), "r"(ncols) : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+      :: "r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32"
+      " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15,"
+      " %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31},"
+      " [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major tile whose rows are 128 bytes
+// (64 bf16) and swizzled in 8-row / 1024-byte atoms by TMA's 128-byte mode:
+// start address >> 4 in bits 0-13, leading-byte offset 16 B (unused by this
+// layout), stride-byte offset 1024 B between 8-row groups, descriptor
+// version 1 (bits 46-47), layout type 2 = 128-byte swizzle (bits 61-63).
+__device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
+  uint64_t desc = 0;
+  desc |= uint64_t((saddr >> 4) & 0x3FFFu);
+  desc |= uint64_t(1u) << 16;
+  desc |= uint64_t(1024u >> 4) << 32;
+  desc |= uint64_t(1u) << 46;
+  desc |= uint64_t(2u) << 61;
+  return desc;
+}
+// Instruction descriptor, kind::f16: fp32 accumulator (bits 4-5 = 1), A and
+// B bf16 (bits 7-9 = 1, bits 10-12 = 1), both K-major, N >> 3 in bits 17-22,
+// M >> 4 in bits 24-28.
+__device__ __forceinline__ uint32_t idesc_bf16_f32(int m, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(n >> 3) << 17) | (uint32_t(m >> 4) << 24);
+}
+
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                             int* s_abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*reinterpret_cast<volatile int*>(s_abort)) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      atomicOr(status, kStatusTimeout);
+      *reinterpret_cast<volatile int*>(s_abort) = 1;
+      return false;
+    }
+  }
+  return true;
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmM,
+                   const __grid_constant__ CUtensorMap tmGhi,
+                   const __grid_constant__ CUtensorMap tmGlo,
+                   const __grid_constant__ CUtensorMap tmXs, TcGemmArgs a) {
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ uint64_t full_bar[kStages];
+  __shared__ uint64_t empty_bar[kStages];
+  __shared__ uint64_t accum_bar;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ int s_issued;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int o0 = blockIdx.x * kBM;
+  const int n_tiles = (a.T + kBN - 1) / kBN;
+  const bool is_slow = int(blockIdx.y) < n_tiles;
+  const int jt = is_slow ? int(blockIdx.y) : int(blockIdx.y) - n_tiles;
+  const int n = is_slow ? a.count[1] : a.count[0];
+  const int j0 = jt * kBN;
+  if (j0 >= n) return;  // uniform: this token tile is empty
+  const int nvalid = min(kBN, n - j0);
+  const int N = (nvalid + 15) & ~15;
+  const int kb_half = (a.k + kBK - 1) / kBK;
+  const int num_kb = is_slow ? (a.d + kBK - 1) / kBK : 2 * kb_half;
+  const int32_t* idx = is_slow ? a.idx_slow : a.idx_fast;
+
+  const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
+  unsigned char* tiles = smem_raw + (base - smem_addr(smem_raw));
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(&accum_bar, 1);
+    s_abort = 0;
+    s_issued = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(&s_tmem, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int kb = 0;
+      for (; kb < num_kb; ++kb) {
+        const int s = kb % kStages;
+        if (kb >= kStages &&
+            !wait_bounded(&empty_bar[s], ((kb / kStages) & 1) ^ 1, a.status, &s_abort))
+          break;
+        unsigned char* sa = tiles + size_t(s) * kStageBytes;
+        unsigned char* sb = sa + kABytes;
+        mbar_arrive_expect_tx(&full_bar[s], kStageBytes);
+        if (is_slow) {
+          tma_load_2d(sa, &tmW, kb * kBK, o0, &full_bar[s]);
+          tma_load_2d(sb, &tmXs, kb * kBK, j0, &full_bar[s]);
+        } else {
+          const int plane = kb / kb_half, kk = kb % kb_half;
+          tma_load_2d(sa, &tmM, kk * kBK, o0, &full_bar[s]);
+          tma_load_2d(sb, plane ? &tmGlo : &tmGhi, kk * kBK, j0, &full_bar[s]);
+        }
+      }
+      s_issued = kb;
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(kBM, N);
+      for (int kb = 0; kb < num_kb; ++kb) {
+        const int s = kb % kStages;
+        if (!wait_bounded(&full_bar[s], (kb / kStages) & 1, a.status, &s_abort)) break;
+        tc_fence_after();
+        const uint32_t sa = base + uint32_t(s) * kStageBytes;
+        const uint32_t sb = sa + kABytes;
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk)
+          tc_mma_bf16(tmem, sw128_kmajor_desc(sa + kk * 32), sw128_kmajor_desc(sb + kk * 32), idesc,
+                      (kb | kk) != 0 ? 1u : 0u);
+        tc_commit(&empty_bar[s]);
+      }
+      tc_commit(&accum_bar);
+    }
+  } else {
+    // epilogue: warps 2..5 own TMEM lane quarters (warp % 4)
+    const int q = warp & 3;
+    const bool ok = wait_bounded(&accum_bar, 0, a.status, &s_abort);
+    tc_fence_after();
+    const int o = o0 + q * 32 + lane;
+    for (int c0 = 0; c0 < N; c0 += 32) {
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(tmem + (uint32_t(q * 32) << 16) + uint32_t(c0), r);
+      if (ok && o < a.d_out) {
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+          const int j = c0 + jj;
+          if (j < nvalid) {
+            const int tok = __ldg(idx + j0 + j);
+            a.y[size_t(tok) * a.d_out + o] = __uint_as_float(r[jj]);
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && s_abort) {
+    // make sure no bulk copy is still writing into this CTA's shared memory
+    const int issued = s_issued;
+    for (int kb = max(0, issued - kStages); kb < issued; ++kb) {
+      const int s = kb % kStages;
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(&full_bar[s], (kb / kStages) & 1) &&
+             globaltimer_ns() - t0 < kWaitLimitNs) {
+      }
+    }
+  }
+  if (warp == 1) {
+    if (lane == 0) {  // all MMAs done before the accumulator is released
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(&accum_bar, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+      }
+    }
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---- host side: tensor maps ---------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 row-major tensor (rows x cols), box of box_rows x 64 columns,
+// 128-byte swizzle, zero fill outside the tensor.
+bool encode_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {uint32_t(kBK), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int tc_gemm_launch_count() { return 1; }
+
+gsi_status_t tc_gemm_prepare(gsi_handle* h) {
+  static_assert(sizeof(CUtensorMap) == 128, "tensor map size");
+  CUtensorMap* maps = reinterpret_cast<CUtensorMap*>(h->tmaps);
+  const uint64_t mt = uint64_t(h->max_T);
+  bool ok = encode_2d(&maps[0], h->W, uint64_t(h->d_out), uint64_t(h->d), kBM) &&
+            encode_2d(&maps[1], h->M, uint64_t(h->d_out), uint64_t(h->k), kBM) &&
+            encode_2d(&maps[2], h->bGf, mt, uint64_t(h->k), kBN) &&
+            encode_2d(&maps[3], h->bGf + size_t(mt) * h->k, mt, uint64_t(h->k), kBN) &&
+            encode_2d(&maps[4], h->bXs, mt, uint64_t(h->d), kBN);
+  if (!ok) return GSI_ERR_CUDA;
+  if (cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(kTcSmem)) != cudaSuccess)
+    return GSI_ERR_CUDA;
+  return GSI_OK;
+}
+
+gsi_status_t tc_gemm_launch(gsi_handle* h, const TcGemmArgs& a, cudaStream_t s) {
+  const CUtensorMap* maps = reinterpret_cast<const CUtensorMap*>(h->tmaps);
+  const int n_tiles = (a.T + kBN - 1) / kBN;
+  dim3 grid(unsigned((a.d_out + kBM - 1) / kBM), unsigned(2 * n_tiles));
+  tc_gemm_kernel<<<grid, kTcThreads, kTcSmem, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], a);
+  return cudaGetLastError() == cudaSuccess ? GSI_OK : GSI_ERR_CUDA;
+}
+
+}  // namespace gsi

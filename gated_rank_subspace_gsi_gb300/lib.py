@@ -1,0 +1,201 @@
+"""ctypes binding of libgsi.so, the C ABI in include/gsi.h.
+
+Argument marshalling only: every step of the gated map runs in the library's
+CUDA kernels.  Functions keep the C names.  Tensors are torch tensors (device
+memory for everything except the *_host variant); PyTorch supplies memory and
+streams and nothing else.  If libgsi.so is missing it is built with nvcc; if
+that is impossible the import fails loudly: there is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+GSI_OK = 0
+GSI_ERR_INVALID_ARG = 1
+GSI_ERR_UNSUPPORTED_SHAPE = 2
+GSI_ERR_NOMEM = 3
+GSI_ERR_CUDA = 4
+GSI_ERR_WORKSPACE = 5
+GSI_ERR_TIMEOUT = 6
+
+# every function declared in include/gsi.h
+EXPORTS = ("gsi_create", "gsi_forward", "gsi_forward_host", "gsi_precompute_M",
+           "gsi_reserve", "gsi_device_status", "gsi_destroy", "gsi_status_string",
+           "gsi_forward_launch_count")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class GsiError(RuntimeError):
+    """A call into libgsi returned a status other than GSI_OK."""
+
+    def __init__(self, status: int, what: str):
+        self.status = int(status)
+        msg = _load().gsi_status_string(self.status).decode()
+        super().__init__(f"{what}: {msg}")
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if not os.path.exists(path):
+            _build.build()
+        lib = ctypes.CDLL(path)
+        P, I64 = ctypes.c_void_p, ctypes.c_int64
+        lib.gsi_create.argtypes = [P, P, P, I64, I64, I64, ctypes.c_float, ctypes.POINTER(P)]
+        lib.gsi_create.restype = ctypes.c_int
+        lib.gsi_forward.argtypes = [P, P, I64, P, P, P, P]
+        lib.gsi_forward.restype = ctypes.c_int
+        lib.gsi_forward_host.argtypes = [P, P, I64, P, P, P, P]
+        lib.gsi_forward_host.restype = ctypes.c_int
+        lib.gsi_precompute_M.argtypes = [P, P, P, I64, I64, I64, P]
+        lib.gsi_precompute_M.restype = ctypes.c_int
+        lib.gsi_reserve.argtypes = [P, I64]
+        lib.gsi_reserve.restype = ctypes.c_int
+        lib.gsi_device_status.argtypes = [P, P]
+        lib.gsi_device_status.restype = ctypes.c_int
+        lib.gsi_destroy.argtypes = [P]
+        lib.gsi_destroy.restype = None
+        lib.gsi_status_string.argtypes = [ctypes.c_int]
+        lib.gsi_status_string.restype = ctypes.c_char_p
+        lib.gsi_forward_launch_count.argtypes = [P, I64]
+        lib.gsi_forward_launch_count.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def library():
+    """The loaded ctypes library (built on first use if missing)."""
+    return _load()
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(st: int, what: str):
+    if st != GSI_OK:
+        raise GsiError(st, what)
+
+
+def gsi_status_string(status: int) -> str:
+    return _load().gsi_status_string(int(status)).decode()
+
+
+def gsi_create(W, V_k, M, eps: float) -> ctypes.c_void_p:
+    """Handle for one gated linear.  W (d_out x d), V_k (d x k), M (d_out x k):
+    bf16 CUDA tensors, borrowed (keep them alive and unchanged)."""
+    d_out, d = W.shape
+    d2, k = V_k.shape
+    if d2 != d or tuple(M.shape) != (d_out, k):
+        raise ValueError("W, V_k and M shapes disagree")
+    h = ctypes.c_void_p()
+    _check(_load().gsi_create(_ptr(W), _ptr(V_k), _ptr(M), d_out, d, k, float(eps),
+                              ctypes.byref(h)), "gsi_create")
+    return h
+
+
+def gsi_forward(h, x, y, gate=None, rho=None, stream=None, T=None):
+    """y (T x d_out fp32), gate (T uint8) and rho (T fp32) of the gated map on
+    x (T x d bf16), all CUDA tensors; asynchronous on `stream`."""
+    T = x.shape[0] if T is None else T
+    _check(_load().gsi_forward(h, _ptr(x), T, _ptr(y), _ptr(gate), _ptr(rho), _stream(stream)),
+           "gsi_forward")
+
+
+def gsi_forward_host(h, x_host, y_host, gate_host=None, rho_host=None, stream=None, T=None):
+    """gsi_forward on host (CPU, ideally pinned) tensors; copies are queued on
+    `stream`, which the caller synchronises before reading the outputs."""
+    T = x_host.shape[0] if T is None else T
+    _check(_load().gsi_forward_host(h, _ptr(x_host), T, _ptr(y_host), _ptr(gate_host),
+                                    _ptr(rho_host), _stream(stream)), "gsi_forward_host")
+
+
+def gsi_precompute_M(W, V_k, M, stream=None):
+    """M = bf16(W V_k) on the GPU (fp32 accumulation)."""
+    d_out, d = W.shape
+    _, k = V_k.shape
+    _check(_load().gsi_precompute_M(_ptr(W), _ptr(V_k), _ptr(M), d_out, d, k, _stream(stream)),
+           "gsi_precompute_M")
+
+
+def gsi_reserve(h, max_T: int):
+    _check(_load().gsi_reserve(h, int(max_T)), "gsi_reserve")
+
+
+def gsi_device_status(h, stream=None) -> int:
+    """Synchronise the stream, return (and clear) the handle's device status."""
+    return int(_load().gsi_device_status(h, _stream(stream)))
+
+
+def gsi_destroy(h):
+    if h is not None:
+        _load().gsi_destroy(h)
+
+
+def gsi_forward_launch_count(h, T: int) -> int:
+    return int(_load().gsi_forward_launch_count(h, int(T)))
+
+
+class GatedLinear:
+    """One gated linear (W, V_k, M, eps) bound to a libgsi handle.
+
+    Holds references to the borrowed tensors so they outlive the handle.
+    """
+
+    def __init__(self, W, V_k, M, eps: float, max_T: int = 0):
+        import torch
+        for name, t in (("W", W), ("V_k", V_k), ("M", M)):
+            if not (t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous()):
+                raise TypeError(f"{name} must be a contiguous bf16 CUDA tensor")
+        self.W, self.V_k, self.M, self.eps = W, V_k, M, float(eps)
+        self.d_out, self.d = W.shape
+        self.k = V_k.shape[1]
+        self.h = gsi_create(W, V_k, M, eps)
+        if max_T > 0:
+            gsi_reserve(self.h, max_T)
+
+    def forward(self, x, y=None, gate=None, rho=None, stream=None):
+        import torch
+        T = x.shape[0]
+        if y is None:
+            y = torch.empty((T, self.d_out), dtype=torch.float32, device=x.device)
+        gsi_forward(self.h, x, y, gate, rho, stream)
+        return y
+
+    __call__ = forward
+
+    def status(self, stream=None) -> int:
+        return gsi_device_status(self.h, stream)
+
+    def close(self):
+        if self.h is not None:
+            gsi_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

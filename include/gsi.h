@@ -1,0 +1,133 @@
+/*
+ * gsi.h -- C ABI of the GB300 (sm_103a) Gated Subspace Inference linear map.
+ *
+ * The operation is the one defined on the page "Technical summary: Gated
+ * Subspace Inference for transformer acceleration":
+ *   section 2.1, eq. 1:  x = V_k V_k^T x + r      (r is the residual)
+ *   section 2.1, eq. 2:  y = W x = (W V_k)(V_k^T x) + W r = M g + W r,
+ *                        with g = V_k^T x and the cached image M = W V_k
+ *   section 2.2:         rho = ||r|| / ||x|| per token;
+ *                        rho <  eps -> fast path, y = M g
+ *                        rho >= eps -> slow path, y = W x
+ *
+ * Conventions shared by every entry point
+ *   - All tensors are dense, row-major, contiguous.
+ *       W    d_out x d    bf16          (the linear's weight)
+ *       V_k  d x k        bf16          (orthonormal rank-k basis)
+ *       M    d_out x k    bf16          (cached image W V_k)
+ *       x    T x d        bf16          (T tokens)
+ *       y    T x d_out    fp32          (outputs)
+ *       gate T            uint8         (1 = slow path taken, 0 = fast path)
+ *       rho  T            fp32          (residual ratio per token)
+ *   - Pointers are DEVICE pointers unless the name says _host, and must be
+ *     16-byte aligned.  Shapes must satisfy d % 8 == 0, k % 16 == 0,
+ *     d_out % 8 == 0, 16 <= k <= 256 (else GSI_ERR_UNSUPPORTED_SHAPE).
+ *   - eps is an fp32 threshold compared as "rho < eps"; a tie goes to the
+ *     slow path; eps <= 0 makes every token slow, eps = +inf makes every
+ *     token with finite rho fast; NaN eps is GSI_ERR_INVALID_ARG.
+ *   - A token with ||x|| = 0 has rho = 0.  A token containing NaN or Inf
+ *     has rho = NaN and takes the slow path.  rho is computed in fp32, so a
+ *     token whose squared norm is outside the fp32 normal range
+ *     (roughly ||x|| > 1e19 or ||x|| < 1e-18) is outside the supported range.
+ *   - Errors in arguments are reported synchronously by the return value.
+ *     Kernel-side problems (a bounded wait that ran out) set a device status
+ *     word that gsi_device_status() reads.  Nothing here traps or asserts on
+ *     the device.
+ */
+#ifndef GSI_H
+#define GSI_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct gsi_handle *gsi_handle_t;
+
+typedef enum {
+    GSI_OK = 0,
+    GSI_ERR_INVALID_ARG = 1,       /* null pointer, misalignment, NaN eps, T < 0 */
+    GSI_ERR_UNSUPPORTED_SHAPE = 2, /* d, k, d_out outside the rules above */
+    GSI_ERR_NOMEM = 3,             /* a device or host allocation failed */
+    GSI_ERR_CUDA = 4,              /* a CUDA runtime call or launch failed */
+    GSI_ERR_WORKSPACE = 5,         /* T larger than the reserved workspace */
+    GSI_ERR_TIMEOUT = 6            /* a device-side bounded wait ran out */
+} gsi_status_t;
+
+/* Create a handle for one gated linear (section 2.1: W, V_k and M).
+ *   W, V_k, M : device pointers, BORROWED: they must stay valid and unchanged
+ *               for the handle's lifetime (nothing is copied).
+ *   eps       : the gate threshold of section 2.2.
+ *   out       : receives the handle.
+ * The handle owns a small workspace (gate reductions, token index lists,
+ * gathered operands) sized for T <= 512 tokens per call; gsi_reserve()
+ * grows it.  Computes the Gram matrix V_k^T V_k (k x k) once.  Synchronises
+ * the device once.  Thread-safe with respect to other handles. */
+gsi_status_t gsi_create(const void *W, const void *V_k, const void *M,
+                        int64_t d_out, int64_t d, int64_t k, float eps,
+                        gsi_handle_t *out);
+
+/* The gated map of sections 2.1-2.2 on T tokens.
+ *   x     : T x d bf16 (device).
+ *   y     : T x d_out fp32 (device), written in token order.
+ *   gate  : T uint8 (device) or NULL.
+ *   rho   : T fp32 (device) or NULL.
+ *   stream: CUDA stream; the call is asynchronous, allocates nothing, never
+ *           synchronises, and may be captured in a CUDA graph.
+ * T == 0 is a no-op.  T > reserved workspace -> GSI_ERR_WORKSPACE.
+ * Calls on one handle must be ordered on the GPU (one stream, or streams
+ * joined by events): the handle's workspace is shared by its calls.
+ * T == 1 runs the decode path (one fused kernel: projection, gate, and the
+ * GEMV that reads M on the fast path or W on the slow path); T > 1 runs the
+ * batched path (projection, gate, compaction of the token indices, and
+ * tensor-core GEMMs M G_fast^T and W X_slow^T scattered back). */
+gsi_status_t gsi_forward(gsi_handle_t h, const void *x, int64_t T, float *y,
+                         uint8_t *gate, float *rho, cudaStream_t stream);
+
+/* gsi_forward on HOST buffers: copies x (T x d bf16) to device staging
+ * buffers owned by the handle, runs the map, and copies y (T x d_out fp32),
+ * gate and rho (either may be NULL) back to the host buffers.  All work is
+ * queued on `stream`; with page-locked (pinned) host buffers the call
+ * returns before the copies finish and the caller synchronises the stream
+ * before reading y; with pageable buffers the CUDA runtime may block.
+ * Staging buffers grow with gsi_reserve(). */
+gsi_status_t gsi_forward_host(gsi_handle_t h, const void *x_host, int64_t T,
+                              float *y_host, uint8_t *gate_host,
+                              float *rho_host, cudaStream_t stream);
+
+/* The cached image of section 2.1 (eq. 2): M = bf16(W V_k), computed with
+ * fp32 accumulation and one round-to-nearest-even per entry.  W (d_out x d),
+ * V_k (d x k) inputs and M (d_out x k) output are device pointers owned by
+ * the caller.  Asynchronous on `stream`; allocates nothing. */
+gsi_status_t gsi_precompute_M(const void *W, const void *V_k, void *M,
+                              int64_t d_out, int64_t d, int64_t k,
+                              cudaStream_t stream);
+
+/* Grow the handle's workspace (device and host-staging) to max_T tokens per
+ * call.  Synchronises the device.  Never shrinks. */
+gsi_status_t gsi_reserve(gsi_handle_t h, int64_t max_T);
+
+/* Synchronise `stream`, then read and clear the handle's device status
+ * word: GSI_OK, or GSI_ERR_TIMEOUT if a bounded device-side wait ran out in
+ * a kernel of this handle since the last check (its outputs are then not
+ * valid). */
+gsi_status_t gsi_device_status(gsi_handle_t h, cudaStream_t stream);
+
+/* Release the handle and its workspace (not W, V_k or M).  Synchronises the
+ * device.  NULL is ignored. */
+void gsi_destroy(gsi_handle_t h);
+
+/* Static description of a status code. */
+const char *gsi_status_string(gsi_status_t s);
+
+/* Kernel launches that gsi_forward(h, ..., T, ...) issues for this T (for
+ * launch accounting); 0 for T <= 0. */
+int gsi_forward_launch_count(gsi_handle_t h, int64_t T);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GSI_H */

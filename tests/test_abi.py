@@ -1,0 +1,79 @@
+"""The C-ABI library loads and exports every symbol include/gsi.h declares,
+and its host-side argument checks answer without touching a GPU (CPU only)."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_functions():
+    with open(os.path.join(ROOT, "include", "gsi.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gsi_[a-zA-Z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def cl():
+    from gated_rank_subspace_gsi_gb300 import build, lib
+    build.build()
+    return lib.library()
+
+
+def test_header_declares_the_boundary():
+    fns = header_functions()
+    for name in ("gsi_create", "gsi_forward", "gsi_precompute_M", "gsi_destroy",
+                 "gsi_reserve", "gsi_device_status", "gsi_status_string",
+                 "gsi_forward_host"):
+        assert name in fns
+
+
+def test_library_exports_every_declared_symbol(cl):
+    from gated_rank_subspace_gsi_gb300 import lib
+    fns = header_functions()
+    for name in fns:
+        assert hasattr(cl, name), f"{name} declared in gsi.h but not exported"
+    assert set(lib.EXPORTS) == set(fns)
+
+
+def test_status_strings(cl):
+    for s in range(7):
+        assert cl.gsi_status_string(s)
+    assert b"UNSUPPORTED" in cl.gsi_status_string(2)
+
+
+def _create(cl, W, V, M, d_out, d, k, eps):
+    h = ctypes.c_void_p()
+    return cl.gsi_create(W, V, M, d_out, d, k, ctypes.c_float(eps), ctypes.byref(h))
+
+
+def test_host_argument_checks(cl):
+    """Checks that reject before any CUDA call (fake, never dereferenced
+    pointer values)."""
+    A = ctypes.c_void_p(0x10000)       # 16-byte aligned fake addresses
+    B = ctypes.c_void_p(0x20000)
+    C = ctypes.c_void_p(0x30000)
+    MIS = ctypes.c_void_p(0x10008)     # misaligned
+    assert _create(cl, None, B, C, 64, 64, 16, 0.1) == 1
+    assert _create(cl, MIS, B, C, 64, 64, 16, 0.1) == 1
+    assert _create(cl, A, B, C, 64, 64, 16, math.nan) == 1
+    assert _create(cl, A, B, C, 64, 60, 16, 0.1) == 2     # d % 8
+    assert _create(cl, A, B, C, 60, 64, 16, 0.1) == 2     # d_out % 8
+    assert _create(cl, A, B, C, 64, 64, 24, 0.1) == 2     # k not a supported size
+    assert _create(cl, A, B, C, 64, 64, 128, 0.1) == 2    # k > d
+    assert _create(cl, A, B, C, 0, 64, 16, 0.1) == 2
+    h = ctypes.c_void_p()
+    assert cl.gsi_create(A, B, C, 64, 64, 16, ctypes.c_float(0.1), None) == 1
+    assert cl.gsi_forward(None, A, 1, B, None, None, None) == 1
+    assert cl.gsi_forward_host(None, A, 1, B, None, None, None) == 1
+    assert cl.gsi_precompute_M(MIS, B, C, 64, 64, 16, None) == 1
+    assert cl.gsi_precompute_M(A, B, C, 64, 64, 17, None) == 2
+    assert cl.gsi_reserve(None, 8) == 1
+    assert cl.gsi_device_status(None, None) == 1
+    assert cl.gsi_forward_launch_count(None, 1) == 0
+    cl.gsi_destroy(None)
+    del h

@@ -1,0 +1,216 @@
+"""GPU parity of the gated map against the fp64 oracle, through the C ABI.
+
+Small and ragged shapes spanning several tiles, both paths (T = 1 decode and
+T > 1 batched), the degenerate cases of the method (eps = 0, eps = inf,
+x = 0, NaN, tokens at the threshold), workspace limits, host buffers and
+CUDA-graph replay.  Tolerances: gates exact outside |rho - eps| <= 1e-4, y
+within 2e-3 of max|y_ref| per token, rho within 1e-4.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import gsi_inputs as gi
+from gsi_testlib import GpuLinear, check_against_oracle, to_bits, to_dev
+
+pytestmark = pytest.mark.gpu
+
+# (d_out, d, k): ragged d_out / d against 128-row MMA tiles, 64-wide K blocks,
+# and the decode kernel's per-CTA slices; every supported k.
+SHAPES = [(24, 64, 16), (40, 136, 32), (96, 264, 64), (200, 512, 128), (2304, 768, 256),
+          (136, 1024, 512), (1000, 4104, 256)]
+
+
+def spread_rho(eps: float, T: int, seed: int) -> np.ndarray:
+    """Residual targets on both sides of eps, none within bf16 reach of it."""
+    rng = np.random.default_rng(seed)
+    choices = np.array([0.0, 0.2, 0.5, 0.8, 1.25, 2.0, 4.0]) * eps
+    r = rng.choice(choices, size=T)
+    r = np.where(r == 0.0, 0.001, r)
+    return np.minimum(r, 0.95)
+
+
+def make_case(d_out, d, k, eps, T, seed):
+    W = gi.gaussian_weights(d_out, d, seed)
+    basis = gi.random_basis(d, k, seed, n_sub=min(200, k))
+    X = gi.tokens(basis, spread_rho(eps, T, seed), seed)
+    return W, basis, X
+
+
+@pytest.mark.parametrize("d_out,d,k", SHAPES)
+def test_precompute_M(gsi, orc, d_out, d, k):
+    W, basis, _ = make_case(d_out, d, k, 0.1, 1, 1)
+    lin = GpuLinear(gsi, orc, W, basis.V_bits, 0.1)
+    ref = orc.precompute_M_bf16(W, basis.V_bits).astype(np.int32)
+    got = to_bits(lin.M_dev).astype(np.int32)
+    # same sign and within one bf16 ulp (adjacent bit patterns of one sign)
+    diff = np.abs(got - ref)
+    assert diff.max() <= 1, diff.max()
+    assert (diff == 0).mean() >= 0.99
+    lin.close()
+
+
+@pytest.mark.parametrize("d_out,d,k", SHAPES)
+def test_decode_T1(gsi, orc, d_out, d, k):
+    eps = 0.10
+    W, basis, X = make_case(d_out, d, k, eps, 14, 2)
+    lin = GpuLinear(gsi, orc, W, basis.V_bits, eps)
+    y, g, r = lin.forward(X, one_by_one=True)
+    rep = check_against_oracle(orc, lin, X, y, g, r, what=f"decode {d_out}x{d}x{k}")
+    assert 0 < rep["n_slow"] < 14
+    lin.close()
+
+
+@pytest.mark.parametrize("d_out,d,k", SHAPES)
+@pytest.mark.parametrize("T", [2, 3, 17, 64, 300])
+def test_batched(gsi, orc, d_out, d, k, T):
+    eps = 0.10
+    W, basis, X = make_case(d_out, d, k, eps, T, 3 + T)
+    lin = GpuLinear(gsi, orc, W, basis.V_bits, eps)
+    y, g, r = lin.forward(X)
+    check_against_oracle(orc, lin, X, y, g, r, what=f"batched T={T} {d_out}x{d}x{k}")
+    lin.close()
+
+
+@pytest.mark.parametrize("T", [1, 40])
+def test_eps_zero_and_inf(gsi, orc, T):
+    """eps = 0: every token slow, y = W x.  eps = inf: every token fast."""
+    d_out, d, k = 384, 1024, 128
+    W, basis, X = make_case(d_out, d, k, 0.1, T, 9)
+    for eps, want in ((0.0, 1), (math.inf, 0)):
+        lin = GpuLinear(gsi, orc, W, basis.V_bits, eps)
+        y, g, r = lin.forward(X, one_by_one=(T == 1))
+        assert (g == want).all()
+        check_against_oracle(orc, lin, X, y, g, r, what=f"eps={eps}")
+        lin.close()
+
+
+@pytest.mark.parametrize("path", ["decode", "batched"])
+def test_special_tokens(gsi, orc, path):
+    """x = 0 (rho = 0, fast, y = 0), NaN (slow, NaN out), Inf (slow), a pure
+    residual token (rho ~ 1), an in-span token (rho ~ 0), and large / small
+    token scales inside the supported range."""
+    d_out, d, k = 256, 512, 64
+    eps = 0.1
+    W, basis, X = make_case(d_out, d, k, eps, 8, 11)
+    Xf = gi.bf16_bits_to_f64(X)
+    Xf[0] = 0.0
+    Xf[1, 5] = np.nan
+    Xf[2, 7] = np.inf
+    Xf[3] = gi.bf16_bits_to_f64(gi.tokens(basis, np.array([1.0]), 12))[0]
+    Xf[4] = gi.bf16_bits_to_f64(gi.tokens(basis, np.array([0.0]), 13))[0]
+    Xf[5] *= 2.0 ** 40
+    Xf[6] *= 2.0 ** -40
+    Xb = gi.to_bf16_bits(np.where(np.isnan(Xf), 0, Xf))
+    Xb[1, 5] = 0x7FC0
+    Xb[2, 7] = 0x7F80
+    lin = GpuLinear(gsi, orc, W, basis.V_bits, eps)
+    y, g, r = lin.forward(Xb, one_by_one=(path == "decode"))
+    assert g[0] == 0 and r[0] == 0 and (y[0] == 0).all()
+    assert g[1] == 1 and np.isnan(r[1]) and np.isnan(y[1]).all()
+    assert g[2] == 1 and np.isnan(r[2])
+    assert g[3] == 1 and abs(r[3] - 1.0) < 1e-2
+    assert g[4] == 0 and r[4] < 1e-2
+    check_against_oracle(orc, lin, Xb[[0, 1, 3, 4, 5, 6, 7]], y[[0, 1, 3, 4, 5, 6, 7]],
+                         g[[0, 1, 3, 4, 5, 6, 7]], r[[0, 1, 3, 4, 5, 6, 7]], what=path)
+    lin.close()
+
+
+@pytest.mark.parametrize("path", ["decode", "batched"])
+def test_threshold_band(gsi, orc, path):
+    """Tokens placed just either side of eps: outside the 1e-4 band the gate
+    must match the oracle exactly; inside it, it must follow the GPU's rho."""
+    d_out, d, k = 192, 1024, 128
+    W, basis, X0 = make_case(d_out, d, k, 0.1, 1, 21)
+    V = gi.bf16_bits_to_f64(basis.V_bits)
+    rng = np.random.default_rng(5)
+    toks = []
+    for t in range(32):
+        # tune eps instead of the token: pick a token, compute its oracle rho,
+        # and set offsets relative to that rho
+        toks.append(gi.tokens(basis, np.array([0.1 * (0.5 + rng.random())]), 100 + t)[0])
+    Xb = np.stack(toks)
+    rho_ref = orc.forward(None, V, None, 0.1, gi.bf16_bits_to_f64(Xb))["rho"]
+    # one eps for all: the median rho, so tokens sit at many small offsets
+    eps = float(np.float32(np.median(rho_ref) + 3e-5))
+    lin = GpuLinear(gsi, orc, W, basis.V_bits, eps)
+    y, g, r = lin.forward(Xb, one_by_one=(path == "decode"))
+    rep = check_against_oracle(orc, lin, Xb, y, g, r, what=f"band {path}")
+    assert 0 < rep["n_slow"] < 32
+    lin.close()
+
+
+def test_T0_workspace_and_reserve(gsi, orc):
+    import torch
+    d_out, d, k = 128, 256, 32
+    W, basis, X = make_case(d_out, d, k, 0.1, 600, 31)
+    lin = GpuLinear(gsi, orc, W, basis.V_bits, 0.1)
+    x = to_dev(X)
+    y = torch.zeros((600, d_out), dtype=torch.float32, device="cuda")
+    gsi.gsi_forward(lin.h, x[:0], y, T=0)                    # no-op
+    with pytest.raises(gsi.GsiError) as ei:
+        gsi.gsi_forward(lin.h, x, y)                          # 600 > default 512
+    assert ei.value.status == gsi.GSI_ERR_WORKSPACE
+    gsi.gsi_reserve(lin.h, 600)
+    y2, g2, r2 = lin.forward(X)
+    check_against_oracle(orc, lin, X, y2, g2, r2, what="after reserve")
+    assert gsi.gsi_forward_launch_count(lin.h, 1) == 1
+    assert gsi.gsi_forward_launch_count(lin.h, 600) >= 2
+    lin.close()
+
+
+@pytest.mark.parametrize("T", [1, 33])
+def test_forward_host(gsi, orc, T):
+    """The host-buffer entry point gives the device path's results."""
+    import torch
+    d_out, d, k = 512, 1024, 128
+    W, basis, X = make_case(d_out, d, k, 0.1, T, 41)
+    lin = GpuLinear(gsi, orc, W, basis.V_bits, 0.1)
+    xh = torch.from_numpy(X.view(np.int16)).view(torch.bfloat16).pin_memory()
+    yh = torch.empty((T, d_out), dtype=torch.float32).pin_memory()
+    gh = torch.empty((T,), dtype=torch.uint8).pin_memory()
+    rh = torch.empty((T,), dtype=torch.float32).pin_memory()
+    s = torch.cuda.current_stream()
+    gsi.gsi_forward_host(lin.h, xh, yh, gh, rh, s)
+    s.synchronize()
+    check_against_oracle(orc, lin, X, yh.numpy(), gh.numpy(), rh.numpy(), what="host")
+    lin.close()
+
+
+def test_graph_replay_decode(gsi, orc):
+    """A CUDA graph of many T = 1 calls over two handles replays correctly
+    (exercises the device-side launch epoch and grid barrier counters)."""
+    import torch
+    d_out, d, k = 1024, 2048, 256
+    eps = 0.1
+    W, basis, X = make_case(d_out, d, k, eps, 24, 51)
+    lin = GpuLinear(gsi, orc, W, basis.V_bits, eps)
+    W2, basis2, X2 = make_case(512, 1024, 128, eps, 24, 52)
+    lin2 = GpuLinear(gsi, orc, W2, basis2.V_bits, eps)
+    x = to_dev(X)
+    x2 = to_dev(X2)
+    y = torch.zeros((24, d_out), dtype=torch.float32, device="cuda")
+    y2 = torch.zeros((24, 512), dtype=torch.float32, device="cuda")
+    g = torch.zeros((24,), dtype=torch.uint8, device="cuda")
+    r = torch.zeros((24,), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        gsi.gsi_forward(lin.h, x[:1], y[:1], g[:1], r[:1], s)   # warm-up outside capture
+        s.synchronize()
+        with torch.cuda.graph(graph, stream=s):
+            for t in range(24):
+                gsi.gsi_forward(lin.h, x[t:t + 1], y[t:t + 1], g[t:t + 1], r[t:t + 1], s)
+                gsi.gsi_forward(lin2.h, x2[t:t + 1], y2[t:t + 1], None, None, s)
+    for rep in range(3):
+        y.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert gsi.gsi_device_status(lin.h) == 0 and gsi.gsi_device_status(lin2.h) == 0
+        check_against_oracle(orc, lin, X, y.cpu().numpy(), g.cpu().numpy(), r.cpu().numpy(),
+                             what=f"graph replay {rep}")
+    yy, gg, rr = lin2.forward(X2, one_by_one=True)
+    assert np.abs(yy - y2.cpu().numpy()).max() <= 2e-3 * np.abs(yy).max()
+    lin.close()
+    lin2.close()
