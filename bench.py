@@ -1,0 +1,510 @@
+"""Benchmark of the GSI gated linear map on GB300.
+
+Workload (one "step"): the GPT-J-6B-shaped decoder layer at decode, T = 1:
+512 sequential tokens, each through three gated linears -- the stacked
+q/k/v/fc_in linear (4096 -> 28672), out_proj (4096 -> 4096) and fc_out
+(16384 -> 4096) -- with k = 256, eps = 0.10 and exactly one slow token (in
+all three linears), i.e. 1536 gsi_forward calls per step, captured in one
+CUDA graph.  Inputs are seeded synthetic draws (no trained weights exist
+here).  The per-token working set (32 MB) would fit in L2, so the layer is
+replicated R times (V_k, M and the handle per replica; W shared, as it is
+read only by the slow token) and token t uses replica t mod R: each step
+streams ~17 GB and no replica is reused within R x 32 MB >= 4 x L2.
+
+Reported (one JSON line on rank 0): us per gated linear (the metric), the
+effective HBM GB/s and its fraction of the measured copy peak (and of
+8 TB/s), a roofline object for the decode kernel, an end-to-end number
+through the host-buffer entry point, the oracle timed on the host cores,
+and the SM clocks sampled during the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gsi|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "µs per gated linear & effective HBM GB/s (GPT-J 4096 shapes, B=1) vs roofline"
+UNIT = "us per gated linear"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+DECODE_SRC = os.path.join(ROOT, "gated_rank_subspace_gsi_gb300", "csrc", "gsi_decode.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gsi_decode_kernel__gptj_layer_traffic.txt")
+
+
+# --------------------------------------------------------------------------
+# distributed plumbing (replicas only: no data-path collective)
+# --------------------------------------------------------------------------
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """The slowest rank's time (weak scaling: every rank does the same work)."""
+    if world == 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(value)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------
+# peaks, clocks, traffic
+# --------------------------------------------------------------------------
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["nvidia-smi unavailable"])
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return dict(sm_mhz=statistics.median(sm) if sm else None,
+                    sm_max_mhz=max(smax) if smax else None,
+                    samples=len(sm), reasons=sorted(reasons))
+
+
+def kernel_traffic():
+    """DRAM bytes per decode-kernel launch from the committed ncu summary,
+    if it was taken on the decode kernel source as it is now."""
+    try:
+        with open(DECODE_SRC, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+        vals = {}
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    vals[k.strip()] = v.strip()
+        if vals.get("decode_source_sha256_16") != sha:
+            return None
+        return float(vals["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# --------------------------------------------------------------------------
+# the workload
+# --------------------------------------------------------------------------
+
+def build_layer(n_tokens: int, replicas: int):
+    """Device tensors and handles of the GPT-J decode layer workload."""
+    import torch
+
+    import gsi_inputs as gi
+    from gated_rank_subspace_gsi_gb300 import lib
+
+    wl = gi.gptj_layer(n_tokens)
+    slow = gi.slow_positions(n_tokens, wl.extra["n_slow"], wl.seed)
+    layer = []
+    for li, spec in enumerate(wl.linears):
+        W = gi.gaussian_weights(spec.d_out, spec.d, wl.seed, li, device="cuda")
+        basis = gi.random_basis(spec.d, spec.k, wl.seed, li)
+        rs = gi.rho_targets(n_tokens, spec.rho_fast, spec.rho_slow, slow, wl.seed, li)
+        X = gi.tokens(basis, rs, wl.seed, li)
+        V = torch.from_numpy(basis.V_bits.view(np.int16)).view(torch.bfloat16).cuda()
+        M = torch.empty((spec.d_out, spec.k), dtype=torch.bfloat16, device="cuda")
+        lib.gsi_precompute_M(W, V, M)
+        reps = []
+        for r in range(replicas):
+            Vr = V if r == 0 else V.clone()
+            Mr = M if r == 0 else M.clone()
+            torch.cuda.synchronize()
+            h = lib.gsi_create(W, Vr, Mr, spec.eps)
+            reps.append((Vr, Mr, h))
+        x = torch.from_numpy(X.view(np.int16)).view(torch.bfloat16).cuda()
+        layer.append(dict(spec=spec, W=W, reps=reps, x=x, X_bits=X, basis=basis,
+                          y=torch.zeros((n_tokens, spec.d_out), dtype=torch.float32, device="cuda"),
+                          gate=torch.zeros((n_tokens,), dtype=torch.uint8, device="cuda"),
+                          rho=torch.zeros((n_tokens,), dtype=torch.float32, device="cuda")))
+    torch.cuda.synchronize()
+    return wl, slow, layer
+
+
+def step_bytes(layer, slow) -> float:
+    """Algorithmic bytes of one step: per gated linear V_k + (M or W) + x + y
+    (fp32) + gate + rho; the fast path needs no Gram matrix."""
+    total = 0.0
+    for L in layer:
+        s = L["spec"]
+        per_fast = s.d * s.k * 2 + s.d_out * s.k * 2 + s.d * 2 + s.d_out * 4 + 5
+        per_slow = s.d * s.k * 2 + s.d_out * s.d * 2 + s.d * 2 + s.d_out * 4 + 5
+        n_slow = int(slow.sum())
+        total += per_fast * (len(slow) - n_slow) + per_slow * n_slow
+    return total
+
+
+def capture_step(layer, n_tokens, replicas, stream, handles_subset=None, host=None):
+    import torch
+
+    from gated_rank_subspace_gsi_gb300 import lib
+    g = torch.cuda.CUDAGraph()
+    idx = range(len(layer)) if handles_subset is None else handles_subset
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for t in range(n_tokens):
+                r = t % replicas
+                for li in idx:
+                    L = layer[li]
+                    h = L["reps"][r][2]
+                    if host is None:
+                        lib.gsi_forward(h, L["x"][t:t + 1], L["y"][t:t + 1], L["gate"][t:t + 1],
+                                        L["rho"][t:t + 1], stream)
+                    else:
+                        H = host[li]
+                        lib.gsi_forward_host(h, H["x"][t:t + 1], H["y"][t:t + 1],
+                                             H["gate"][t:t + 1], H["rho"][t:t + 1], stream)
+    return g
+
+
+def replay(graph, stream, n: int):
+    """Replay on `stream` (a graph launches on torch's current stream)."""
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(n):
+            graph.replay()
+
+
+def time_graph(graph, stream, reps: int, warmup: int):
+    import torch
+    replay(graph, stream, warmup)
+    stream.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    replay(graph, stream, reps)
+    e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / reps  # ms per replay
+
+
+def cpu_baseline(layer, slow, budget_s: float = 12.0):
+    """The fp64 oracle as it stands, on this host's cores, on a bounded
+    sample of the step: the slow token plus fast tokens until the budget."""
+    import oracle
+    orc = oracle.default()
+    prep = []
+    for L in layer:
+        s = L["spec"]
+        W_bits = L["W"].view(__import__("torch").int16).cpu().numpy().view(np.uint16)
+        M_ref = orc.precompute_M_bf16(W_bits, L["basis"].V_bits)
+        prep.append((orc.bf16_decode(W_bits), orc.bf16_decode(L["basis"].V_bits),
+                     orc.bf16_decode(M_ref), float(np.float32(s.eps)), L["X_bits"]))
+    order = list(np.nonzero(slow)[0]) + [t for t in range(len(slow)) if not slow[t]]
+    n_lin = 0
+    t0 = time.perf_counter()
+    for t in order:
+        for (W, V, M, eps, X) in prep:
+            orc.forward(W, V, M, eps, orc.bf16_decode(X[t:t + 1]))
+            n_lin += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    n_tok = n_lin // len(prep)
+    return dict(value=dt / n_lin * 1e6, unit=UNIT, cores=orc.num_threads(), kind="oracle",
+                sample=f"{n_tok} decode tokens x 3 gated linears of the step (the slow "
+                       f"token first, then fast tokens), fp64 C oracle, {dt:.1f} s")
+
+
+# --------------------------------------------------------------------------
+# arms
+# --------------------------------------------------------------------------
+
+def run_gsi(args, world, rank, local):
+    import torch
+
+    from gated_rank_subspace_gsi_gb300 import lib
+    torch.cuda.set_device(local)
+    lib.library()
+    n_tokens = 512
+    props = torch.cuda.get_device_properties(local)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
+    per_token = 32.44e6
+    replicas = max(16, int(math.ceil(4 * l2 / per_token)))
+    wl, slow, layer = build_layer(n_tokens, replicas)
+    nbytes = step_bytes(layer, slow)
+    n_lin = n_tokens * len(layer)
+    stream = torch.cuda.Stream()
+
+    graph = capture_step(layer, n_tokens, replicas, stream)
+    for L in layer:
+        L["gate"].fill_(7)
+    torch.cuda.synchronize()
+    replay(graph, stream, max(args.warmup, 3))
+    stream.synchronize()
+    for L in layer:
+        st = lib.gsi_device_status(L["reps"][0][2], stream)
+        if st != 0:
+            raise RuntimeError(f"device status: {lib.gsi_status_string(st)}")
+        if not np.array_equal(L["gate"].cpu().numpy().astype(bool), slow):
+            raise RuntimeError("gates differ from the generated slow/fast mix")
+
+    # ---- timed region: K steps, barrier + synchronize on both sides -------
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    replay(graph, stream, args.steps)
+    e1.record(stream)
+    e1.synchronize()
+    torch.cuda.synchronize()
+    barrier(world)
+    ms_local = e0.elapsed_time(e1) / args.steps
+    clk = clocks.stop()
+    ms = max_over_ranks(ms_local, world)
+
+    us_per_lin = ms * 1e3 / n_lin
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peak, peak_kind = hbm_peak()
+
+    # ---- per-linear breakdown (each linear alone, 512 calls per graph) ----
+    per = {}
+    for li, L in enumerate(layer):
+        g1 = capture_step(layer, n_tokens, replicas, stream, handles_subset=[li])
+        ms1 = time_graph(g1, stream, reps=5, warmup=2)
+        s = L["spec"]
+        b1 = (s.d * s.k * 2 + s.d * 2 + s.d_out * 4 + 5) * n_tokens + \
+            (s.d_out * s.k * 2) * (n_tokens - int(slow.sum())) + s.d_out * s.d * 2 * int(slow.sum())
+        per[s.name] = dict(us_per_call=round(ms1 * 1e3 / n_tokens, 3),
+                           gbs=round(b1 / (ms1 * 1e-3) / 1e9, 1))
+        del g1
+
+    # ---- end to end: host buffers through gsi_forward_host ---------------
+    host = []
+    h2d = d2h = 0
+    for L in layer:
+        s = L["spec"]
+        H = dict(x=L["x"].cpu().pin_memory(),
+                 y=torch.empty((n_tokens, s.d_out), dtype=torch.float32).pin_memory(),
+                 gate=torch.empty((n_tokens,), dtype=torch.uint8).pin_memory(),
+                 rho=torch.empty((n_tokens,), dtype=torch.float32).pin_memory())
+        host.append(H)
+        h2d += n_tokens * s.d * 2
+        d2h += n_tokens * (s.d_out * 4 + 1 + 4)
+    ge = capture_step(layer, n_tokens, replicas, stream, host=host)
+    ms_e2e = max_over_ranks(time_graph(ge, stream, reps=max(3, args.steps // 2), warmup=2), world)
+    if not np.array_equal(host[0]["gate"].numpy().astype(bool), slow):
+        raise RuntimeError("end-to-end gates differ from the generated mix")
+
+    launches = args.steps * n_lin
+    out = {
+        "metric": METRIC,
+        "value": round(us_per_lin, 4),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded Gaussian weights, QR bases, activations with set residual ratios)",
+        "impl": "gsi",
+        "config": {
+            "workload": "gptj_layer_decode: 512 sequential T=1 tokens x 3 gated linears "
+                        "(4096->28672 stacked qkv+fc_in, 4096->4096 out_proj, 16384->4096 fc_out), "
+                        "k=256, eps=0.10, 1 slow token (0.2%)",
+            "gated_linears_per_step": n_lin,
+            "replicas": replicas,
+            "l2": f"inputs larger than L2: {replicas} replicas x 32.4 MB per token, "
+                  f"{nbytes / 1e9:.2f} GB streamed per step, L2 {l2 / 2**20:.0f} MiB",
+            "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+        },
+        "effective_hbm_gbs": round(gbs * world, 1),
+        "frac_of_measured_hbm": round(gbs / peak, 4),
+        "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
+        "us_per_layer": round(ms * 1e3 / n_tokens, 3),
+        "per_linear": per,
+        "algorithmic_bytes_per_step": int(nbytes),
+        "roofline": {
+            "bound": "hbm",
+            "achieved": round(gbs, 1),
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": round(gbs / peak, 4),
+            "traffic": kernel_traffic(),
+            "kernel": "gsi_decode_kernel<256>",
+            "peak_kind": f"{peak_kind} HBM copy",
+            "bytes_per_launch": round(nbytes / n_lin, 1),
+            "us_per_launch": round(us_per_lin, 4),
+        },
+        "e2e": {
+            "value": round(ms_e2e * 1e3 / n_lin, 4),
+            "unit": UNIT,
+            "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "how": "gsi_forward_host per call (pinned host x in, y/gate/rho out), graph-captured step",
+        },
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(layer, slow, budget_s=args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def run_reference(args, world, rank):
+    """The oracle (fp64 C) on the host cores, each step a bounded sample of the
+    decode layer workload: 8 tokens x 3 gated linears, slow token included in
+    the first step."""
+    if rank != 0:
+        return
+    import oracle
+
+    import gsi_inputs as gi
+    orc = oracle.default()
+    wl = gi.gptj_layer()
+    n = wl.extra["n_tokens"]
+    slow = gi.slow_positions(n, wl.extra["n_slow"], wl.seed)
+    prep = []
+    for li, spec in enumerate(wl.linears):
+        inp = gi.make_linear_inputs(spec, n, 0, wl.seed, tag=li, slow_mask=slow)
+        Wd = orc.bf16_decode(inp.W)
+        Vd = orc.bf16_decode(inp.V_bits)
+        Md = orc.bf16_decode(orc.bf16_encode(orc.precompute_M(Wd, Vd)))
+        prep.append((Wd, Vd, Md, float(np.float32(spec.eps)), inp.X_bits))
+    order = list(np.nonzero(slow)[0]) + [t for t in range(n) if not slow[t]]
+    per_step = 8
+
+    def one_step(s):
+        toks = [order[(s * per_step + i) % n] for i in range(per_step)]
+        for t in toks:
+            for (W, V, M, eps, X) in prep:
+                orc.forward(W, V, M, eps, orc.bf16_decode(X[t:t + 1]))
+
+    for s in range(args.warmup):
+        one_step(s)
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        one_step(args.warmup + s)
+    dt = time.perf_counter() - t0
+    n_lin = args.steps * per_step * len(prep)
+    v = dt / n_lin * 1e6
+    out = {
+        "metric": METRIC, "value": round(v, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference",
+        "config": {"workload": "gptj_layer_decode (oracle sample: 8 tokens x 3 gated linears per step)"},
+        "cpu_baseline": {"value": round(v, 3), "unit": UNIT, "cores": orc.num_threads(),
+                         "kind": "oracle",
+                         "sample": f"{per_step} decode tokens x 3 gated linears per step, "
+                                   f"{args.steps} steps"},
+        "e2e": {"value": round(v, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gsi", "reference"], default="gsi")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_setup(args.gpus)
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_gsi(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -382,7 +382,14 @@ gsi_status_t decode_configure(gsi_handle* h) {
     lay = decode_smem(int(h->d), int(h->k), rows_M, rows_V, stage_M, stage_V);
   }
   if (lay.total + static_smem > size_t(max_optin)) return GSI_ERR_UNSUPPORTED_SHAPE;
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(lay.total)) != cudaSuccess)
+  // The limit is a property of the kernel function, shared by every handle
+  // with this k: raise it to the device maximum once, never per handle.
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return GSI_ERR_CUDA;
+  const int fn_limit = max_optin - int(fa.sharedSizeBytes);
+  if (int(lay.total) > fn_limit) return GSI_ERR_UNSUPPORTED_SHAPE;
+  if (fa.maxDynamicSharedSizeBytes < fn_limit &&
+      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, fn_limit) != cudaSuccess)
     return GSI_ERR_CUDA;
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kDecThreads, lay.total) != cudaSuccess)
