@@ -455,3 +455,83 @@ gsi_status_t decode_launch(gsi_handle* h, const void* x, float* y, uint8_t* gate
 }
 
 }  // namespace gsi
+
+// ---------------------------------------------------------------------------
+// gsi_forward_noalloc: the decode kernel above, run without a handle and with
+// its scratch (reduction buffers, arrival counter, launch epoch, status word)
+// in a fixed file-scope device array instead of handle-owned memory.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace gsi {
+namespace {
+
+constexpr int kNoAllocMaxK = 512;                      // largest k the scratch holds
+constexpr int kNoAllocAccStride = kNoAllocMaxK + 4;    // floats per accumulator buffer
+constexpr size_t kNoAllocAccBytes = size_t(2) * kNoAllocAccStride * sizeof(float);
+constexpr size_t kNoAllocBarOffset = (kNoAllocAccBytes + 127) / 128 * 128;
+constexpr size_t kNoAllocBytes = kNoAllocBarOffset + 128;  // + counter, epoch, status
+
+// 4.4 KB per GPU that loads the library, held until the process exits.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+unsigned char* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once
+// per device (the host-side symbol is only a stand-in, never a device address).
+gsi_status_t noalloc_scratch(int dev, unsigned char** out) {
+  if (dev < 0 || dev >= kMaxDevices) return GSI_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return GSI_ERR_CUDA;
+    g_noalloc_ptr[dev] = static_cast<unsigned char*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return GSI_OK;
+}
+
+}  // namespace
+}  // namespace gsi
+
+extern "C" gsi_status_t gsi_forward_noalloc(const void* W, const void* V_k, const void* M,
+                                            int64_t d_out, int64_t d, int64_t k, float eps,
+                                            const void* x, float* y, uint8_t* gate, float* rho,
+                                            cudaStream_t stream) {
+  using namespace gsi;
+  if (!W || !V_k || !M || !x || !y || eps != eps) return GSI_ERR_INVALID_ARG;
+  if (!aligned16(W) || !aligned16(V_k) || !aligned16(M) || !aligned16(x) || !aligned16(y))
+    return GSI_ERR_INVALID_ARG;
+  if (d_out <= 0 || d <= 0 || d % 8 != 0 || d_out % 8 != 0 || k > d ||
+      (k != 16 && k != 32 && k != 64 && k != 128 && k != 256 && k != 512) ||
+      d_out > (int64_t(1) << 30) || d > (int64_t(1) << 24))
+    return GSI_ERR_UNSUPPORTED_SHAPE;
+  if (k > kNoAllocMaxK) return GSI_ERR_WORKSPACE;  // beyond the fixed scratch
+  gsi_handle h;  // configuration only: no memory is allocated for it
+  h.W = static_cast<const __nv_bfloat16*>(W);
+  h.V = static_cast<const __nv_bfloat16*>(V_k);
+  h.M = static_cast<const __nv_bfloat16*>(M);
+  h.d_out = d_out;
+  h.d = d;
+  h.k = k;
+  h.eps = eps;
+  if (cudaGetDevice(&h.device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&h.num_sms, cudaDevAttrMultiProcessorCount, h.device) != cudaSuccess)
+    return GSI_ERR_CUDA;
+  unsigned char* scratch = nullptr;
+  gsi_status_t st = noalloc_scratch(h.device, &scratch);
+  if (st != GSI_OK) return st;
+  st = decode_configure(&h);
+  if (st != GSI_OK) return st;
+  h.dec_acc = reinterpret_cast<float*>(scratch);
+  h.dec_acc_stride = kNoAllocAccStride;
+  h.dec_bar = reinterpret_cast<uint32_t*>(scratch + kNoAllocBarOffset);
+  h.status = reinterpret_cast<uint32_t*>(scratch + kNoAllocBarOffset + 64);
+  h.use_pdl = false;
+  // Every call starts from zeroed accumulators, counter and epoch, whatever
+  // shape the previous call on this device had.
+  if (cudaMemsetAsync(scratch, 0, kNoAllocBytes, stream) != cudaSuccess) return GSI_ERR_CUDA;
+  return decode_launch(&h, x, y, gate, rho, stream);
+}

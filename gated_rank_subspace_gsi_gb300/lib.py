@@ -25,7 +25,7 @@ GSI_ERR_TIMEOUT = 6
 # every function declared in include/gsi.h
 EXPORTS = ("gsi_create", "gsi_forward", "gsi_forward_host", "gsi_precompute_M",
            "gsi_reserve", "gsi_device_status", "gsi_destroy", "gsi_status_string",
-           "gsi_forward_launch_count")
+           "gsi_forward_launch_count", "gsi_forward_noalloc")
 
 _lock = threading.Lock()
 _lib = None
@@ -68,6 +68,8 @@ def _load():
         lib.gsi_status_string.restype = ctypes.c_char_p
         lib.gsi_forward_launch_count.argtypes = [P, I64]
         lib.gsi_forward_launch_count.restype = ctypes.c_int
+        lib.gsi_forward_noalloc.argtypes = [P, P, P, I64, I64, I64, ctypes.c_float, P, P, P, P, P]
+        lib.gsi_forward_noalloc.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -156,6 +158,17 @@ def gsi_destroy(h):
 
 def gsi_forward_launch_count(h, T: int) -> int:
     return int(_load().gsi_forward_launch_count(h, int(T)))
+
+
+def gsi_forward_noalloc(W, V_k, M, eps: float, x, y, gate=None, rho=None, stream=None):
+    """One token of the gated map with no handle and no allocation (for
+    callers whose device memory is owned by another allocator); its scratch is
+    a fixed array inside the library, shared by all calls on a device."""
+    d_out, d = W.shape
+    _, k = V_k.shape
+    _check(_load().gsi_forward_noalloc(_ptr(W), _ptr(V_k), _ptr(M), d_out, d, k, float(eps),
+                                       _ptr(x), _ptr(y), _ptr(gate), _ptr(rho), _stream(stream)),
+           "gsi_forward_noalloc")
 
 
 class GatedLinear:

@@ -126,6 +126,31 @@ const char *gsi_status_string(gsi_status_t s);
  * launch accounting); 0 for T <= 0. */
 int gsi_forward_launch_count(gsi_handle_t h, int64_t T);
 
+/* One token (T = 1) of the gated map without a handle and without allocating:
+ * for callers that cannot call cudaMalloc -- code running inside a framework
+ * or server whose allocator owns all device memory (a pooling or caching
+ * allocator that must see every allocation), or a fixed-memory deployment
+ * where the first call must not fail for lack of memory.  The paper has no
+ * counterpart to this entry point; it is an interface convenience.
+ *   W, V_k, M, x, y, gate, rho, d_out, d, k, eps: as in gsi_create and
+ *   gsi_forward (device pointers, 16-byte aligned; gate, rho may be NULL).
+ * The kernel's scratch (about 4.4 KB: two reduction buffers of up to
+ * k + 4 = 516 floats, an arrival counter, a launch epoch and a status word)
+ * lives in a fixed array that every GPU loading this library holds until
+ * the process exits; k above 512 is rejected with GSI_ERR_WORKSPACE.  No
+ * cudaMalloc, cudaFree or allocating library routine is called.  The first
+ * call on a device looks up that array's device address (once per device,
+ * with the device current); make that first call before any stream capture.
+ * Each call clears the scratch on `stream` before its kernel; all calls share
+ * the one array, so calls that overlap on the GPU (different streams, no
+ * ordering) race and give wrong results.  Device-side timeouts of this
+ * entry point are not reported (there is no handle to read them from).
+ * Asynchronous on `stream`. */
+gsi_status_t gsi_forward_noalloc(const void *W, const void *V_k, const void *M,
+                                 int64_t d_out, int64_t d, int64_t k, float eps,
+                                 const void *x, float *y, uint8_t *gate,
+                                 float *rho, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
