@@ -74,6 +74,8 @@ const char* gsi_status_string(gsi_status_t s) {
     case GSI_ERR_CUDA: return "GSI_ERR_CUDA: a CUDA call or kernel launch failed";
     case GSI_ERR_WORKSPACE: return "GSI_ERR_WORKSPACE: T exceeds the reserved workspace (call gsi_reserve)";
     case GSI_ERR_TIMEOUT: return "GSI_ERR_TIMEOUT: a bounded device-side wait ran out";
+    case GSI_ERR_LAUNCH:
+      return "GSI_ERR_LAUNCH: a kernel found its launch configuration inconsistent and did nothing";
   }
   return "unknown gsi_status_t";
 }
@@ -105,7 +107,8 @@ gsi_status_t gsi_create(const void* W, const void* V_k, const void* M, int64_t d
   h->dec_acc_stride = int(k + 4);
   const size_t gram_b = size_t(k) * k * 4;
   const size_t acc_b = size_t(2) * h->dec_acc_stride * 4;
-  const size_t ws = ((gram_b + 255) / 256 + (acc_b + 255) / 256 + 1) * 256;
+  auto r256 = [](size_t v) { return (v + 255) / 256 * 256; };
+  const size_t ws = r256(gram_b) + r256(acc_b) + 256;
   if (cudaMalloc(&h->ws, ws) != cudaSuccess) {
     delete h;
     return GSI_ERR_NOMEM;
@@ -113,15 +116,15 @@ gsi_status_t gsi_create(const void* W, const void* V_k, const void* M, int64_t d
   h->ws_bytes = ws;
   char* p = static_cast<char*>(h->ws);
   h->gram = reinterpret_cast<float*>(p);
-  p += (gram_b + 255) / 256 * 256;
+  p += r256(gram_b);
   h->dec_acc = reinterpret_cast<float*>(p);
-  p += (acc_b + 255) / 256 * 256;
+  p += r256(acc_b);
   h->dec_bar = reinterpret_cast<uint32_t*>(p);
   h->status = reinterpret_cast<uint32_t*>(p + 64);
   st = GSI_OK;
   if (cudaMemset(h->ws, 0, ws) != cudaSuccess) st = GSI_ERR_CUDA;
   if (st == GSI_OK) st = gsi::decode_configure(h);
-  if (st == GSI_OK) st = gsi::gram_launch(h->V, d, k, h->gram, nullptr);
+  if (st == GSI_OK) st = gsi::gram_launch(h->V, d, k, h->gram, nullptr, nullptr);
   if (st == GSI_OK) st = grow_batched(h, kDefaultMaxT);
   if (st == GSI_OK) st = grow_staging(h, kDefaultMaxT);
   if (st == GSI_OK && cudaDeviceSynchronize() != cudaSuccess) st = GSI_ERR_CUDA;
@@ -201,6 +204,7 @@ gsi_status_t gsi_device_status(gsi_handle_t h, cudaStream_t stream) {
     if (cudaMemcpy(h->status, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
       return GSI_ERR_CUDA;
   }
+  if (word & gsi::kStatusBadLaunch) return GSI_ERR_LAUNCH;
   return (word & gsi::kStatusTimeout) ? GSI_ERR_TIMEOUT : GSI_OK;
 }
 

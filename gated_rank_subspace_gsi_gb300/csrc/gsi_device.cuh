@@ -15,6 +15,7 @@ namespace gsi {
 
 // Bits of the per-handle device status word.
 constexpr uint32_t kStatusTimeout = 1u;
+constexpr uint32_t kStatusBadLaunch = 2u;  // a kernel saw an inconsistent launch and did nothing
 
 // Limit of every device-side spin wait (nanoseconds of %globaltimer).
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s

@@ -77,7 +77,7 @@ void batched_bind_workspace(gsi_handle* h, void* base, int64_t max_T);
 
 // One-off operand preparation (gsi_prep.cu)
 gsi_status_t gram_launch(const __nv_bfloat16* V, int64_t d, int64_t k, float* gram,
-                         cudaStream_t s);
+                         __nv_bfloat16* E, cudaStream_t s);
 gsi_status_t precompute_M_launch(const __nv_bfloat16* W, const __nv_bfloat16* V,
                                  __nv_bfloat16* M, int64_t d_out, int64_t d, int64_t k,
                                  cudaStream_t s);

@@ -1,6 +1,7 @@
 // gsi_prep.cu -- one-off operand preparation for the GSI gated linear map.
 //
-//   gram:         Gm = V_k^T V_k (k x k), accumulated in fp64 and stored fp32.
+//   gram:         Gm = V_k^T V_k (k x k), accumulated in fp64 and stored fp32,
+//                 and E = Gm - I stored bf16 (the decode kernel's correction).
 //                 Used by the batched path to form ||r||^2 without a second
 //                 pass over V_k: ||x - V_k g||^2 = ||x||^2 - 2 g.g + g^T Gm g,
 //                 an identity for any V_k (eq. 1 of section 2.1 of the page
@@ -20,7 +21,8 @@ constexpr int kGramRows = 64;
 
 // One CTA per 16 x 16 tile of Gm; V_k rows staged 64 at a time.
 __global__ void __launch_bounds__(256) gram_kernel(const __nv_bfloat16* __restrict__ V, int d, int k,
-                                                   float* __restrict__ gram) {
+                                                   float* __restrict__ gram,
+                                                   __nv_bfloat16* __restrict__ E) {
   __shared__ float sa[kGramRows][kGramTile];
   __shared__ float sb[kGramRows][kGramTile];
   const int a0 = blockIdx.y * kGramTile, b0 = blockIdx.x * kGramTile;
@@ -39,6 +41,8 @@ __global__ void __launch_bounds__(256) gram_kernel(const __nv_bfloat16* __restri
     __syncthreads();
   }
   gram[size_t(a0 + ta) * k + b0 + tb] = float(acc);
+  // E = Gm - I from the fp64 sum, so its small entries keep their precision
+  if (E) E[size_t(a0 + ta) * k + b0 + tb] = __double2bfloat16(acc - (a0 + ta == b0 + tb ? 1.0 : 0.0));
 }
 
 constexpr int kMTileO = 64;  // rows of W / M per CTA
@@ -95,9 +99,10 @@ __global__ void __launch_bounds__(256) precompute_M_kernel(const __nv_bfloat16* 
 
 }  // namespace
 
-gsi_status_t gram_launch(const __nv_bfloat16* V, int64_t d, int64_t k, float* gram, cudaStream_t s) {
+gsi_status_t gram_launch(const __nv_bfloat16* V, int64_t d, int64_t k, float* gram,
+                         __nv_bfloat16* E, cudaStream_t s) {
   dim3 grid(unsigned(k / kGramTile), unsigned(k / kGramTile));
-  gram_kernel<<<grid, 256, 0, s>>>(V, int(d), int(k), gram);
+  gram_kernel<<<grid, 256, 0, s>>>(V, int(d), int(k), gram, E);
   return cudaGetLastError() == cudaSuccess ? GSI_OK : GSI_ERR_CUDA;
 }
 

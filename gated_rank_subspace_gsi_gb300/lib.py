@@ -21,6 +21,7 @@ GSI_ERR_NOMEM = 3
 GSI_ERR_CUDA = 4
 GSI_ERR_WORKSPACE = 5
 GSI_ERR_TIMEOUT = 6
+GSI_ERR_LAUNCH = 7
 
 # every function declared in include/gsi.h
 EXPORTS = ("gsi_create", "gsi_forward", "gsi_forward_host", "gsi_precompute_M",

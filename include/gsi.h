@@ -53,7 +53,8 @@ typedef enum {
     GSI_ERR_NOMEM = 3,             /* a device or host allocation failed */
     GSI_ERR_CUDA = 4,              /* a CUDA runtime call or launch failed */
     GSI_ERR_WORKSPACE = 5,         /* T larger than the reserved workspace */
-    GSI_ERR_TIMEOUT = 6            /* a device-side bounded wait ran out */
+    GSI_ERR_TIMEOUT = 6,           /* a device-side bounded wait ran out */
+    GSI_ERR_LAUNCH = 7             /* a kernel saw an inconsistent launch and did nothing */
 } gsi_status_t;
 
 /* Create a handle for one gated linear (section 2.1: W, V_k and M).
@@ -110,9 +111,10 @@ gsi_status_t gsi_precompute_M(const void *W, const void *V_k, void *M,
 gsi_status_t gsi_reserve(gsi_handle_t h, int64_t max_T);
 
 /* Synchronise `stream`, then read and clear the handle's device status
- * word: GSI_OK, or GSI_ERR_TIMEOUT if a bounded device-side wait ran out in
- * a kernel of this handle since the last check (its outputs are then not
- * valid). */
+ * word: GSI_OK; GSI_ERR_TIMEOUT if a bounded device-side wait ran out in a
+ * kernel of this handle since the last check; GSI_ERR_LAUNCH if a kernel
+ * found its launch configuration inconsistent and returned without work.
+ * In both error cases the outputs are not valid. */
 gsi_status_t gsi_device_status(gsi_handle_t h, cudaStream_t stream);
 
 /* Release the handle and its workspace (not W, V_k or M).  Synchronises the

@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(cl):
 
 
 def test_status_strings(cl):
-    for s in range(7):
+    for s in range(8):
         assert cl.gsi_status_string(s)
     assert b"UNSUPPORTED" in cl.gsi_status_string(2)
 
