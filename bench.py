@@ -41,8 +41,9 @@ METRIC = "µs per gated linear & effective HBM GB/s (GPT-J 4096 shapes, B=1) vs 
 UNIT = "us per gated linear"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-DECODE_SRC = os.path.join(ROOT, "gated_rank_subspace_gsi_gb300", "csrc", "gsi_decode.cu")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gsi_decode_kernel__gptj_layer_traffic.txt")
+DECODE_KERNEL = "gsi_decode3_kernel<256>"
+DECODE_SRC = os.path.join(ROOT, "gated_rank_subspace_gsi_gb300", "csrc", "gsi_decode3.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gsi_decode3_kernel__gptj_layer_traffic.txt")
 
 
 # --------------------------------------------------------------------------
@@ -201,17 +202,26 @@ def build_layer(n_tokens: int, replicas: int):
     return wl, slow, layer
 
 
+def correction_bytes(k: int) -> int:
+    """The packed bf16 triangle of E = V_k^T V_k - I that every one-token call
+    reads to form ||r|| (rows padded to 8-column chunks): (k^2 + 8k) / 2
+    entries of 2 bytes."""
+    return (k * k + 8 * k) // 2 * 2
+
+
+def linear_bytes(s, n_tokens: int, n_slow: int) -> float:
+    """Algorithmic bytes of n_tokens one-token calls of one gated linear:
+    V_k + correction triangle + x + y (fp32) + gate + rho per call, plus M
+    per fast call or W per slow call."""
+    per_call = s.d * s.k * 2 + correction_bytes(s.k) + s.d * 2 + s.d_out * 4 + 5
+    return (per_call * n_tokens + s.d_out * s.k * 2 * (n_tokens - n_slow)
+            + s.d_out * s.d * 2 * n_slow)
+
+
 def step_bytes(layer, slow) -> float:
-    """Algorithmic bytes of one step: per gated linear V_k + (M or W) + x + y
-    (fp32) + gate + rho; the fast path needs no Gram matrix."""
-    total = 0.0
-    for L in layer:
-        s = L["spec"]
-        per_fast = s.d * s.k * 2 + s.d_out * s.k * 2 + s.d * 2 + s.d_out * 4 + 5
-        per_slow = s.d * s.k * 2 + s.d_out * s.d * 2 + s.d * 2 + s.d_out * 4 + 5
-        n_slow = int(slow.sum())
-        total += per_fast * (len(slow) - n_slow) + per_slow * n_slow
-    return total
+    """Algorithmic bytes of one step (all gated linears, all tokens)."""
+    n_slow = int(slow.sum())
+    return float(sum(linear_bytes(L["spec"], len(slow), n_slow) for L in layer))
 
 
 def capture_step(layer, n_tokens, replicas, stream, handles_subset=None, host=None):
@@ -347,8 +357,7 @@ def run_gsi(args, world, rank, local):
         g1 = capture_step(layer, n_tokens, replicas, stream, handles_subset=[li])
         ms1 = time_graph(g1, stream, reps=5, warmup=2)
         s = L["spec"]
-        b1 = (s.d * s.k * 2 + s.d * 2 + s.d_out * 4 + 5) * n_tokens + \
-            (s.d_out * s.k * 2) * (n_tokens - int(slow.sum())) + s.d_out * s.d * 2 * int(slow.sum())
+        b1 = linear_bytes(s, n_tokens, int(slow.sum()))
         per[s.name] = dict(us_per_call=round(ms1 * 1e3 / n_tokens, 3),
                            gbs=round(b1 / (ms1 * 1e-3) / 1e9, 1))
         del g1
@@ -411,7 +420,7 @@ def run_gsi(args, world, rank, local):
             "unit": "GB/s",
             "frac": round(gbs / peak, 4),
             "traffic": kernel_traffic(),
-            "kernel": "gsi_decode_kernel<256>",
+            "kernel": DECODE_KERNEL,
             "peak_kind": f"{peak_kind} HBM copy",
             "bytes_per_launch": round(nbytes / n_lin, 1),
             "us_per_launch": round(us_per_lin, 4),

@@ -103,12 +103,16 @@ gsi_status_t gsi_create(const void* W, const void* V_k, const void* M, int64_t d
     delete h;
     return GSI_ERR_CUDA;
   }
-  // fixed workspace: Gram matrix, decode accumulators, barrier words, status
+  // fixed workspace: Gram matrix, decode accumulators, the packed correction
+  // triangle and accumulators of the one-barrier kernel, barrier words, status
   h->dec_acc_stride = int(k + 4);
+  const bool want3 = k <= 256;
   const size_t gram_b = size_t(k) * k * 4;
   const size_t acc_b = size_t(2) * h->dec_acc_stride * 4;
+  const size_t F_b = want3 ? gsi::gram_packed_size(int(k)) * 2 : 0;
+  const size_t acc3_b = want3 ? gsi::decode3_acc_floats(k) * 4 : 0;
   auto r256 = [](size_t v) { return (v + 255) / 256 * 256; };
-  const size_t ws = r256(gram_b) + r256(acc_b) + 256;
+  const size_t ws = r256(gram_b) + r256(acc_b) + r256(F_b) + r256(acc3_b) + 256;
   if (cudaMalloc(&h->ws, ws) != cudaSuccess) {
     delete h;
     return GSI_ERR_NOMEM;
@@ -119,12 +123,21 @@ gsi_status_t gsi_create(const void* W, const void* V_k, const void* M, int64_t d
   p += r256(gram_b);
   h->dec_acc = reinterpret_cast<float*>(p);
   p += r256(acc_b);
+  if (want3) {
+    h->dec3_F = reinterpret_cast<__nv_bfloat16*>(p);
+    p += r256(F_b);
+    h->dec3_acc = reinterpret_cast<float*>(p);
+    p += r256(acc3_b);
+  }
   h->dec_bar = reinterpret_cast<uint32_t*>(p);
   h->status = reinterpret_cast<uint32_t*>(p + 64);
+  h->dec3_bar = reinterpret_cast<uint32_t*>(p + 128);
   st = GSI_OK;
   if (cudaMemset(h->ws, 0, ws) != cudaSuccess) st = GSI_ERR_CUDA;
   if (st == GSI_OK) st = gsi::decode_configure(h);
-  if (st == GSI_OK) st = gsi::gram_launch(h->V, d, k, h->gram, nullptr, nullptr);
+  // the one-barrier kernel serves T = 1 whenever its shape fits
+  if (st == GSI_OK && want3) h->dec3_ok = gsi::decode3_configure(h) == GSI_OK;
+  if (st == GSI_OK) st = gsi::gram_launch(h->V, d, k, h->gram, h->dec3_F, nullptr);
   if (st == GSI_OK) st = grow_batched(h, kDefaultMaxT);
   if (st == GSI_OK) st = grow_staging(h, kDefaultMaxT);
   if (st == GSI_OK && cudaDeviceSynchronize() != cudaSuccess) st = GSI_ERR_CUDA;
@@ -141,7 +154,9 @@ gsi_status_t gsi_forward(gsi_handle_t h, const void* x, int64_t T, float* y, uin
   if (!h || T < 0) return GSI_ERR_INVALID_ARG;
   if (T == 0) return GSI_OK;
   if (!x || !y || !gsi::aligned16(x) || !gsi::aligned16(y)) return GSI_ERR_INVALID_ARG;
-  if (T == 1) return gsi::decode_launch(h, x, y, gate, rho, stream);
+  if (T == 1)
+    return h->dec3_ok ? gsi::decode3_launch(h, x, y, gate, rho, stream)
+                      : gsi::decode_launch(h, x, y, gate, rho, stream);
   if (T > h->max_T) return GSI_ERR_WORKSPACE;
   return gsi::batched_launch(h, x, T, y, gate, rho, stream);
 }

@@ -1,0 +1,561 @@
+// gsi_decode3.cu -- the T = 1 (decode) path of the GSI gated linear map as one
+// persistent kernel per call with ONE grid-wide exchange (k <= 256).
+//
+// Page: "Technical summary: Gated Subspace Inference for transformer
+// acceleration" [GSI].  Per token x (section 2.1 eq. 1-2, section 2.2):
+//   g = V_k^T x,  rho = ||x - V_k g|| / ||x||,
+//   y = M g if rho < eps (fast path), y = W x otherwise (slow path).
+//
+// The residual norm comes from the identity
+//   ||x - V_k g||^2 = ||x||^2 - g.g + g^T E g,   E = V_k^T V_k - I,
+// which holds for any V_k (expand the square and use V_k^T x = g).  The
+// correction g^T E g is a k x k quadratic form on data every CTA already has
+// once g is known, so unlike the explicit residual it needs no second pass
+// over V_k and no second exchange between CTAs.  E is stored as a packed
+// bf16 triangle F (gsi_internal.h), made once per handle in fp64.
+//
+// Work split.  G co-resident CTAs (at most one per SM); CTA c owns d / G rows
+// of V_k and d_out / G output rows (of M and of W).  Before it waits on the
+// previous kernel (programmatic dependent launch) each CTA starts 1-D bulk
+// copies of its V_k slice, its M slice and F into shared memory: none depends
+// on x, so these reads overlap the previous kernel's tail.
+//   phase 1   partial g_c = V_c^T x_c and ||x_c||^2, added with vector
+//             red.add into one of kCopies accumulator copies (copy c % 8),
+//             which spreads the atomic traffic over 8 addresses per word;
+//             then the grid barrier (release add / acquire poll)
+//   phase 2   every CTA sums the copies in a fixed order (the same g, bit for
+//             bit, in every CTA, hence the same gate), then forms g^T E g and
+//             g.g from F and the speculative fast-path rows M_c g, 8 rows per
+//             warp step (group_dot)
+//   phase 3   thread 0 forms rho and the gate; the CTA stores M_c g, or, on
+//             the rare slow token, streams its rows of W from HBM for W_c x.
+// The accumulators are double-buffered by a launch epoch kept on the device:
+// CTA 0 zeroes the buffer the next launch uses, so no memset is needed and
+// the kernel replays in a CUDA graph.
+#include <algorithm>
+#include <cfloat>
+
+#include "gsi_device.cuh"
+#include "gsi_internal.h"
+
+namespace gsi {
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
+constexpr int kCopies = 8;  // accumulator copies of (g, ||x||^2)
+
+struct Decode3Args {
+  const __nv_bfloat16* W;
+  const __nv_bfloat16* V;
+  const __nv_bfloat16* M;
+  const __nv_bfloat16* F;
+  const __nv_bfloat16* x;
+  float* y;
+  uint8_t* gate;
+  float* rho;
+  int d_out, d;
+  float eps;
+  int rows_M, rows_V;
+  int stage_M, stage_V, stage_F;
+  float* acc;      // [2][kCopies][acc_stride]
+  int acc_stride;  // >= k + 1, multiple of 4
+  uint32_t* bar;   // [0] arrival counter, [1] launch epoch
+  uint32_t* status;
+};
+
+// Lane geometry: a row of K bf16 values is K / 8 16-byte chunks, one per lane
+// of a row group of LPR = K / 8 lanes (K <= 256, so LPR <= 32).
+template <int K>
+struct Lanes3 {
+  static_assert(K >= 16 && K <= 256 && (K & (K - 1)) == 0, "k in {16, ..., 256}");
+  static constexpr int LPR = K / 8;             // lanes per row
+  static constexpr int RPI = 32 / LPR;          // row groups per warp
+  static constexpr int NB = LPR < 8 ? LPR : 8;  // rows per row group per step
+  static constexpr int RS = RPI * NB;           // rows per warp step
+};
+
+__device__ __forceinline__ void red_release_u32(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t dynamic_smem_bytes() {
+  uint32_t v;
+  asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(v));
+  return v;
+}
+
+// Dot products of NB rows at once.  Lane li of a row group of LPR lanes holds
+// v[i], its 8-column partial of row i (i < NB).  A butterfly over sub-groups
+// of NB lanes (offsets NB/2 .. 1; each step a lane keeps one half of its rows
+// and sends the other half) leaves lane li the sub-group sum of row li % NB;
+// xor steps over offsets NB .. LPR/2 then add the sub-groups.  Cost:
+// NB - 1 + log2(LPR / NB) shuffles for NB rows.
+template <int LPR, int NB>
+__device__ __forceinline__ float group_dot(float (&v)[NB], int li) {
+#pragma unroll
+  for (int o = NB / 2; o >= 1; o >>= 1) {
+    const bool up = (li & o) != 0;
+#pragma unroll
+    for (int i = 0; i < o; ++i) {
+      const float send = up ? v[i] : v[i + o];
+      const float keep = up ? v[i + o] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, o);
+    }
+  }
+  float r = v[0];
+#pragma unroll
+  for (int o = NB; o < LPR; o <<= 1) r += __shfl_xor_sync(0xFFFFFFFFu, r, o);
+  return r;
+}
+
+__device__ __forceinline__ float warp_sum_all(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+// Dynamic shared-memory layout (byte offsets), identical on host and device.
+struct Smem3 {
+  size_t sM, sV, sF, wpart, xs, g, ys, total;
+};
+__host__ __device__ inline size_t al3(size_t v, size_t a) { return (v + a - 1) / a * a; }
+__host__ __device__ inline Smem3 smem3_layout(int K, int rows_M, int rows_V, bool stage_M,
+                                              bool stage_V, bool stage_F) {
+  Smem3 s;
+  size_t o = 0;
+  s.sM = o;    o = al3(o + (stage_M ? size_t(rows_M) * K * 2 : 0), 128);
+  s.sV = o;    o = al3(o + (stage_V ? size_t(rows_V) * K * 2 : 0), 128);
+  s.sF = o;    o = al3(o + (stage_F ? gram_packed_size(K) * 2 : 0), 128);
+  s.wpart = o; o = al3(o + size_t(kWarps) * K * 4, 16);
+  s.xs = o;    o = al3(o + size_t(rows_V) * 4, 16);
+  s.g = o;     o = al3(o + size_t(K) * 4, 16);
+  s.ys = o;    o = al3(o + size_t(rows_M) * 4, 128);
+  s.total = o;
+  return s;
+}
+
+template <int K>
+__global__ void __launch_bounds__(kThreads, 1) gsi_decode3_kernel(Decode3Args a) {
+  using L = Lanes3<K>;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ uint64_t s_bar;
+  __shared__ uint32_t s_epoch;
+  __shared__ int s_ok;
+  __shared__ float s_sx;
+  __shared__ float s_qw[kWarps], s_ggw[kWarps];
+  __shared__ float s_rho;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int cta = blockIdx.x, G = gridDim.x;
+  const Smem3 lay = smem3_layout(K, a.rows_M, a.rows_V, a.stage_M, a.stage_V, a.stage_F);
+  // Launch self-check (uniform over the grid, before any wait): a launch that
+  // does not cover d and d_out, or got less shared memory than its layout,
+  // does nothing and reports it.
+  if (blockDim.x != kThreads || int64_t(G) * a.rows_M < a.d_out || int64_t(G) * a.rows_V < a.d ||
+      dynamic_smem_bytes() < lay.total) {
+    if (cta == 0 && tid == 0) atomicOr(a.status, kStatusBadLaunch);
+    return;
+  }
+  const int m0 = cta * a.rows_M;
+  const int nM = max(0, min(a.d_out, m0 + a.rows_M) - m0);
+  const int v0 = cta * a.rows_V;
+  const int nV = max(0, min(a.d, v0 + a.rows_V) - v0);
+  const int slot = lane / L::LPR, li = lane % L::LPR;
+
+  __nv_bfloat16* sM = reinterpret_cast<__nv_bfloat16*>(smem + lay.sM);
+  __nv_bfloat16* sV = reinterpret_cast<__nv_bfloat16*>(smem + lay.sV);
+  __nv_bfloat16* sF = reinterpret_cast<__nv_bfloat16*>(smem + lay.sF);
+  float* s_wpart = reinterpret_cast<float*>(smem + lay.wpart);  // [warps][K]
+  float* s_xs = reinterpret_cast<float*>(smem + lay.xs);        // [rows_V]
+  float* s_g = reinterpret_cast<float*>(smem + lay.g);          // [K]
+  float* s_ys = reinterpret_cast<float*>(smem + lay.ys);        // [rows_M]
+
+  // ---- prologue: stage this CTA's weights (independent of x) ------------
+  const uint32_t bytes_M = a.stage_M ? uint32_t(nM) * K * 2 : 0u;
+  const uint32_t bytes_V = a.stage_V ? uint32_t(nV) * K * 2 : 0u;
+  const uint32_t bytes_F = a.stage_F ? uint32_t(gram_packed_size(K)) * 2 : 0u;
+  if (tid == 0) {
+    mbar_init(&s_bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    mbar_arrive_expect_tx(&s_bar, bytes_M + bytes_V + bytes_F);
+    constexpr uint32_t kChunk = 32768;
+    const char* gV = reinterpret_cast<const char*>(a.V + size_t(v0) * K);
+    for (uint32_t off = 0; off < bytes_V; off += kChunk)
+      bulk_g2s(reinterpret_cast<char*>(sV) + off, gV + off, min(kChunk, bytes_V - off), &s_bar);
+    const char* gF = reinterpret_cast<const char*>(a.F);
+    for (uint32_t off = 0; off < bytes_F; off += kChunk)
+      bulk_g2s(reinterpret_cast<char*>(sF) + off, gF + off, min(kChunk, bytes_F - off), &s_bar);
+    const char* gM = reinterpret_cast<const char*>(a.M + size_t(m0) * K);
+    for (uint32_t off = 0; off < bytes_M; off += kChunk)
+      bulk_g2s(reinterpret_cast<char*>(sM) + off, gM + off, min(kChunk, bytes_M - off), &s_bar);
+  }
+  pdl_launch_dependents();
+  pdl_wait();  // x and this handle's workspace are now safe to touch
+
+  // ---- phase 1: x slice, partial g and ||x_c||^2 ---------------------------
+  if (tid == 0) s_epoch = ld_cg_u32(a.bar + 1);
+  for (int i = tid; i < nV; i += kThreads) s_xs[i] = bf16_to_f32(a.x[v0 + i]);
+  bool ok = mbar_wait_bounded(&s_bar, 0, a.status);
+  ok = __syncthreads_and(ok) != 0;
+  const uint32_t e = s_epoch;
+  float* acc = a.acc + size_t(e & 1u) * kCopies * a.acc_stride;
+  if (cta == 0) {  // clear the buffers the next launch accumulates into
+    float* nxt = a.acc + size_t((e + 1u) & 1u) * kCopies * a.acc_stride;
+    for (int i = tid; i < kCopies * a.acc_stride; i += kThreads) nxt[i] = 0.f;
+  }
+  const int nVw = ok ? nV : 0;
+  const int nMw = ok ? nM : 0;
+  const __nv_bfloat16* Vs = a.stage_V ? sV : a.V + size_t(v0) * K;
+  const __nv_bfloat16* Ms = a.stage_M ? sM : a.M + size_t(m0) * K;
+  const __nv_bfloat16* Fs = a.stage_F ? sF : a.F;
+  if (warp == kWarps - 1) {  // ||x_c||^2 (x_i^2 is exact in fp32 for bf16 x_i)
+    float sx = 0.f;
+    for (int i = lane; i < nVw; i += 32) sx = fmaf(s_xs[i], s_xs[i], sx);
+    sx = warp_sum_all(sx);
+    if (lane == 0) s_sx = sx;
+  }
+  {
+    float accg[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) accg[j] = 0.f;
+    for (int r = warp * L::RPI + slot; r < nVw; r += kWarps * L::RPI) {
+      const float xi = s_xs[r];
+      const uint4 v = *reinterpret_cast<const uint4*>(Vs + size_t(r) * K + li * 8);
+      float f[8];
+      bf16x8_to_f32(v, f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) accg[j] = fmaf(f[j], xi, accg[j]);
+    }
+#pragma unroll
+    for (int o = L::LPR; o < 32; o <<= 1)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) accg[j] += __shfl_xor_sync(0xFFFFFFFFu, accg[j], o);
+    if (slot == 0) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) s_wpart[warp * K + li * 8 + j] = accg[j];
+    }
+  }
+  __syncthreads();
+  float* my_copy = acc + size_t(cta % kCopies) * a.acc_stride;
+  if (nVw > 0) {
+    for (int t = tid; t < K / 4; t += kThreads) {
+      float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) s4[q] += s_wpart[w * K + t * 4 + q];
+      red_add_v4_f32(my_copy + t * 4, s4[0], s4[1], s4[2], s4[3]);
+    }
+    if (tid == 0) red_add_f32(my_copy + K, s_sx);
+  }
+
+  // ---- the grid barrier ---------------------------------------------------
+  __syncthreads();
+  if (tid == 0) {
+    const uint32_t target = (e + 1u) * uint32_t(G);
+    red_release_u32(a.bar, 1u);
+    int good = 1;
+    if (static_cast<int32_t>(ld_acquire_gpu(a.bar) - target) < 0) {
+      const uint64_t t0 = globaltimer_ns();
+      while (static_cast<int32_t>(ld_acquire_gpu(a.bar) - target) < 0) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+          atomicOr(a.status, kStatusTimeout);
+          good = 0;
+          break;
+        }
+      }
+    }
+    s_ok = good;
+  }
+  __syncthreads();
+  ok = ok && s_ok;
+
+  // ---- phase 2: g (same order in every CTA), g^T E g, g.g, speculative M g --
+  for (int t = tid; t < K; t += kThreads) {
+    float gsum = 0.f;
+#pragma unroll
+    for (int c = 0; c < kCopies; ++c) gsum += ld_cg_f32(acc + size_t(c) * a.acc_stride + t);
+    s_g[t] = gsum;
+  }
+  if (tid == 0) {
+    float sx = 0.f;
+#pragma unroll
+    for (int c = 0; c < kCopies; ++c) sx += ld_cg_f32(acc + size_t(c) * a.acc_stride + K);
+    s_sx = sx;
+  }
+  __syncthreads();
+  float gl[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) gl[j] = s_g[li * 8 + j];
+  // g^T E g = sum_a g_a (F_a . g): row a of F starts at column 8 floor(a / 8),
+  // so lane li covers chunk li - floor(a / 8) of it when that is >= 0.
+  float qsum = 0.f, ggsum = 0.f;
+  for (int rb = warp * L::RS; rb < K; rb += kWarps * L::RS) {
+    float v[L::NB];
+#pragma unroll
+    for (int i = 0; i < L::NB; ++i) {
+      const int row = rb + slot * L::NB + i;
+      const int q8 = row >> 3;
+      float dot = 0.f;
+      if (row < K && li >= q8) {
+        const uint4 fv = *reinterpret_cast<const uint4*>(
+            Fs + gram_packed_offset(row, K) + size_t(li - q8) * 8);
+        float f[8];
+        bf16x8_to_f32(fv, f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) dot = fmaf(f[j], gl[j], dot);
+      }
+      v[i] = dot;
+    }
+    const float rowdot = group_dot<L::LPR, L::NB>(v, li);
+    const int row = rb + slot * L::NB + li % L::NB;
+    if (li < L::NB && row < K) {
+      const float ga = s_g[row];
+      qsum = fmaf(ga, rowdot, qsum);
+      ggsum = fmaf(ga, ga, ggsum);
+    }
+  }
+  qsum = warp_sum_all(qsum);
+  ggsum = warp_sum_all(ggsum);
+  if (lane == 0) {
+    s_qw[warp] = qsum;
+    s_ggw[warp] = ggsum;
+  }
+  // speculative fast path: this CTA's rows of M g
+  for (int rb = warp * L::RS; rb < nMw; rb += kWarps * L::RS) {
+    float v[L::NB];
+#pragma unroll
+    for (int i = 0; i < L::NB; ++i) {
+      const int r = rb + slot * L::NB + i;
+      float dot = 0.f;
+      if (r < nMw) {
+        const uint4 mv = *reinterpret_cast<const uint4*>(Ms + size_t(r) * K + li * 8);
+        float f[8];
+        bf16x8_to_f32(mv, f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) dot = fmaf(f[j], gl[j], dot);
+      }
+      v[i] = dot;
+    }
+    const float yr = group_dot<L::LPR, L::NB>(v, li);
+    const int r = rb + slot * L::NB + li % L::NB;
+    if (li < L::NB && r < nMw) s_ys[r] = yr;
+  }
+  __syncthreads();
+
+  // ---- gate ------------------------------------------------------------------
+  if (tid == 0) {
+    // fp32 throughout: the sums' relative error (~1e-7 of ||x||^2) moves rho by
+    // ~1e-6 near any practical eps, and fp64 is slow on this part
+    float quad = 0.f, gg = 0.f;
+    for (int w = 0; w < kWarps; ++w) {
+      quad += s_qw[w];
+      gg += s_ggw[w];
+    }
+    const float sx = s_sx;
+    float rho;
+    if (!(fabsf(sx) <= FLT_MAX)) {
+      rho = __int_as_float(0x7FC00000);  // non-finite x: NaN, slow path
+    } else if (sx == 0.f) {
+      rho = 0.f;
+    } else {
+      float sr = (sx - gg) + quad;
+      if (!(sr >= 0.f)) sr = (sr == sr) ? 0.f : sr;
+      rho = sqrtf(sr / sx);
+    }
+    s_rho = rho;
+    if (cta == 0) {
+      if (a.gate) a.gate[0] = (rho < a.eps) ? 0 : 1;
+      if (a.rho) a.rho[0] = rho;
+    }
+  }
+  __syncthreads();
+  const bool slow = !(s_rho < a.eps);
+
+  // ---- phase 3: the branch the gate picked ---------------------------------
+  if (ok) {
+    if (!slow) {
+      for (int r = tid; r < nMw; r += kThreads) a.y[m0 + r] = s_ys[r];
+    } else {
+      // W_c x, W streamed from HBM, 4 rows per warp
+      const int nch = a.d / 8;
+      const uint4* x4 = reinterpret_cast<const uint4*>(a.x);
+      for (int rb = warp * 4; rb < nM; rb += kWarps * 4) {
+        float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint4* wr[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int r = min(rb + q, nM - 1);
+          wr[q] = reinterpret_cast<const uint4*>(a.W + size_t(m0 + r) * a.d);
+        }
+        int j = lane;
+        for (; j + 32 < nch; j += 64) {
+          uint4 w0[4], w1[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            w0[q] = ld_stream_v4(wr[q] + j);
+            w1[q] = ld_stream_v4(wr[q] + j + 32);
+          }
+          float xa[8], xb[8];
+          bf16x8_to_f32(x4[j], xa);
+          bf16x8_to_f32(x4[j + 32], xb);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float f[8];
+            bf16x8_to_f32(w0[q], f);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) acc4[q] = fmaf(f[t], xa[t], acc4[q]);
+            bf16x8_to_f32(w1[q], f);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) acc4[q] = fmaf(f[t], xb[t], acc4[q]);
+          }
+        }
+        for (; j < nch; j += 32) {
+          float xa[8];
+          bf16x8_to_f32(x4[j], xa);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float f[8];
+            bf16x8_to_f32(ld_stream_v4(wr[q] + j), f);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) acc4[q] = fmaf(f[t], xa[t], acc4[q]);
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc4[q] = warp_sum_xor<32>(acc4[q]);
+        if (lane == 0) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (rb + q < nM) a.y[m0 + rb + q] = acc4[q];
+        }
+      }
+    }
+  }
+  if (cta == 0 && tid == 0) {
+    __threadfence();
+    a.bar[1] = e + 1u;  // every CTA read the epoch before the barrier
+  }
+}
+
+template <int K>
+const void* kernel3_ptr() {
+  return reinterpret_cast<const void*>(&gsi_decode3_kernel<K>);
+}
+
+const void* decode3_kernel_for(int64_t k) {
+  switch (k) {
+    case 16: return kernel3_ptr<16>();
+    case 32: return kernel3_ptr<32>();
+    case 64: return kernel3_ptr<64>();
+    case 128: return kernel3_ptr<128>();
+    case 256: return kernel3_ptr<256>();
+    default: return nullptr;
+  }
+}
+
+int acc3_stride(int64_t k) { return int((k + 1 + 3) / 4 * 4); }
+
+}  // namespace
+
+size_t decode3_acc_floats(int64_t k) { return size_t(2) * kCopies * acc3_stride(k); }
+
+gsi_status_t decode3_configure(gsi_handle* h) {
+  const void* fn = decode3_kernel_for(h->k);
+  if (!fn) return GSI_ERR_UNSUPPORTED_SHAPE;
+  int max_optin = 0;
+  if (cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device) != cudaSuccess)
+    return GSI_ERR_CUDA;
+  const int64_t rows_hint = (std::max(h->d_out, h->d) + 7) / 8;
+  const int G = int(std::max<int64_t>(1, std::min<int64_t>(h->num_sms, rows_hint)));
+  const int rows_M = int((h->d_out + G - 1) / G);
+  const int rows_V = int((h->d + G - 1) / G);
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return GSI_ERR_CUDA;
+  const int fn_limit = max_optin - int(fa.sharedSizeBytes);
+  // Stage as much as fits, dropping M first (read once per call either way),
+  // then F (read from L2 instead), then V_k.
+  bool stage_M = true, stage_V = true, stage_F = true;
+  const int K = int(h->k);
+  auto total = [&]() {
+    return smem3_layout(K, rows_M, rows_V, stage_M, stage_V, stage_F).total;
+  };
+  if (total() > size_t(fn_limit)) stage_M = false;
+  if (total() > size_t(fn_limit)) stage_F = false;
+  if (total() > size_t(fn_limit)) stage_V = false;
+  if (total() > size_t(fn_limit)) return GSI_ERR_UNSUPPORTED_SHAPE;
+  const size_t smem = total();
+  // The limit belongs to the kernel function, shared by every handle with
+  // this k: raise it to the device maximum once, never per handle.
+  if (fa.maxDynamicSharedSizeBytes < fn_limit &&
+      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, fn_limit) != cudaSuccess)
+    return GSI_ERR_CUDA;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem) != cudaSuccess)
+    return GSI_ERR_CUDA;
+  // The CTAs wait on one another: all of them must fit at once.
+  if (per_sm < 1 || int64_t(per_sm) * h->num_sms < G) return GSI_ERR_UNSUPPORTED_SHAPE;
+  h->dec3_grid = G;
+  h->dec3_rows_M = rows_M;
+  h->dec3_rows_V = rows_V;
+  h->dec3_stage_M = stage_M;
+  h->dec3_stage_V = stage_V;
+  h->dec3_stage_F = stage_F;
+  h->dec3_smem = smem;
+  return GSI_OK;
+}
+
+gsi_status_t decode3_launch(gsi_handle* h, const void* x, float* y, uint8_t* gate, float* rho,
+                            cudaStream_t s) {
+  Decode3Args a;
+  a.W = h->W;
+  a.V = h->V;
+  a.M = h->M;
+  a.F = h->dec3_F;
+  a.x = static_cast<const __nv_bfloat16*>(x);
+  a.y = y;
+  a.gate = gate;
+  a.rho = rho;
+  a.d_out = int(h->d_out);
+  a.d = int(h->d);
+  a.eps = h->eps;
+  a.rows_M = h->dec3_rows_M;
+  a.rows_V = h->dec3_rows_V;
+  a.stage_M = h->dec3_stage_M ? 1 : 0;
+  a.stage_V = h->dec3_stage_V ? 1 : 0;
+  a.stage_F = h->dec3_stage_F ? 1 : 0;
+  a.acc = h->dec3_acc;
+  a.acc_stride = acc3_stride(h->k);
+  a.bar = h->dec3_bar;
+  a.status = h->status;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(h->dec3_grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = h->dec3_smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  int na = 0;
+  if (h->use_pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  cudaError_t err;
+  switch (h->k) {
+    case 16: err = cudaLaunchKernelEx(&cfg, gsi_decode3_kernel<16>, a); break;
+    case 32: err = cudaLaunchKernelEx(&cfg, gsi_decode3_kernel<32>, a); break;
+    case 64: err = cudaLaunchKernelEx(&cfg, gsi_decode3_kernel<64>, a); break;
+    case 128: err = cudaLaunchKernelEx(&cfg, gsi_decode3_kernel<128>, a); break;
+    case 256: err = cudaLaunchKernelEx(&cfg, gsi_decode3_kernel<256>, a); break;
+    default: return GSI_ERR_UNSUPPORTED_SHAPE;
+  }
+  return err == cudaSuccess ? GSI_OK : GSI_ERR_CUDA;
+}
+
+}  // namespace gsi

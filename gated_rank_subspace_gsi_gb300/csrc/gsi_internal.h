@@ -29,6 +29,15 @@ struct gsi_handle {
   size_t dec_smem = 0;       // dynamic shared memory bytes
   bool use_pdl = true;       // programmatic dependent launch between kernels
 
+  // ---- one-barrier decode kernel (k <= 256), used when it configures -----
+  bool dec3_ok = false;
+  int dec3_grid = 0, dec3_rows_M = 0, dec3_rows_V = 0;
+  bool dec3_stage_M = false, dec3_stage_V = false, dec3_stage_F = false;
+  size_t dec3_smem = 0;
+  __nv_bfloat16* dec3_F = nullptr;  // packed correction triangle (gram_packed_size(k))
+  float* dec3_acc = nullptr;        // decode3_acc_floats(k) fp32 accumulators
+  uint32_t* dec3_bar = nullptr;     // [0] arrival counter, [1] launch epoch
+
   // ---- device workspace (one allocation) --------------------------------
   void* ws = nullptr;
   size_t ws_bytes = 0;
@@ -63,10 +72,28 @@ struct gsi_handle {
 
 namespace gsi {
 
+// Packed correction triangle F of E = V_k^T V_k - I, for the identity
+// g^T E g = sum_a g_a (F_a . g): row a holds columns b >= 8 floor(a / 8) with
+// F_ab = 2 E_ab (b > a), E_aa (b = a) and 0 (b < a), so every row starts on a
+// 16-byte boundary.  Row a = 8q + r starts at a k - 8 (4 q (q - 1) + r q).
+__host__ __device__ inline size_t gram_packed_offset(int a, int k) {
+  const size_t q = size_t(a) >> 3, r = size_t(a) & 7u;
+  return size_t(a) * size_t(k) - 8 * (4 * q * (q - (q > 0 ? 1 : 0)) + r * q);
+}
+__host__ __device__ inline size_t gram_packed_size(int k) {
+  return (size_t(k) * k + 8 * size_t(k)) / 2;
+}
+
 // Decode path (gsi_decode.cu)
 gsi_status_t decode_configure(gsi_handle* h);
 gsi_status_t decode_launch(gsi_handle* h, const void* x, float* y, uint8_t* gate,
                            float* rho, cudaStream_t s);
+
+// One-barrier decode path (gsi_decode3.cu), k <= 256
+size_t decode3_acc_floats(int64_t k);
+gsi_status_t decode3_configure(gsi_handle* h);
+gsi_status_t decode3_launch(gsi_handle* h, const void* x, float* y, uint8_t* gate,
+                            float* rho, cudaStream_t s);
 
 // Batched path (gsi_batched.cu)
 gsi_status_t batched_launch(gsi_handle* h, const void* x, int64_t T, float* y,
@@ -77,7 +104,7 @@ void batched_bind_workspace(gsi_handle* h, void* base, int64_t max_T);
 
 // One-off operand preparation (gsi_prep.cu)
 gsi_status_t gram_launch(const __nv_bfloat16* V, int64_t d, int64_t k, float* gram,
-                         __nv_bfloat16* E, cudaStream_t s);
+                         __nv_bfloat16* F, cudaStream_t s);
 gsi_status_t precompute_M_launch(const __nv_bfloat16* W, const __nv_bfloat16* V,
                                  __nv_bfloat16* M, int64_t d_out, int64_t d, int64_t k,
                                  cudaStream_t s);

@@ -1,7 +1,8 @@
 // gsi_prep.cu -- one-off operand preparation for the GSI gated linear map.
 //
 //   gram:         Gm = V_k^T V_k (k x k), accumulated in fp64 and stored fp32,
-//                 and E = Gm - I stored bf16 (the decode kernel's correction).
+//                 and the packed triangle F of E = Gm - I stored bf16 (the
+//                 one-barrier decode kernel's correction term g^T E g).
 //                 Used by the batched path to form ||r||^2 without a second
 //                 pass over V_k: ||x - V_k g||^2 = ||x||^2 - 2 g.g + g^T Gm g,
 //                 an identity for any V_k (eq. 1 of section 2.1 of the page
@@ -22,7 +23,7 @@ constexpr int kGramRows = 64;
 // One CTA per 16 x 16 tile of Gm; V_k rows staged 64 at a time.
 __global__ void __launch_bounds__(256) gram_kernel(const __nv_bfloat16* __restrict__ V, int d, int k,
                                                    float* __restrict__ gram,
-                                                   __nv_bfloat16* __restrict__ E) {
+                                                   __nv_bfloat16* __restrict__ F) {
   __shared__ float sa[kGramRows][kGramTile];
   __shared__ float sb[kGramRows][kGramTile];
   const int a0 = blockIdx.y * kGramTile, b0 = blockIdx.x * kGramTile;
@@ -40,9 +41,14 @@ __global__ void __launch_bounds__(256) gram_kernel(const __nv_bfloat16* __restri
     for (int r = 0; r < kGramRows; ++r) acc += double(sa[r][ta]) * double(sb[r][tb]);
     __syncthreads();
   }
-  gram[size_t(a0 + ta) * k + b0 + tb] = float(acc);
-  // E = Gm - I from the fp64 sum, so its small entries keep their precision
-  if (E) E[size_t(a0 + ta) * k + b0 + tb] = __double2bfloat16(acc - (a0 + ta == b0 + tb ? 1.0 : 0.0));
+  const int a = a0 + ta, b = b0 + tb;
+  gram[size_t(a) * k + b] = float(acc);
+  // F from the fp64 sum, so the small entries of E = Gm - I keep their precision
+  if (F && b >= 8 * (a / 8)) {
+    const double e = acc - (a == b ? 1.0 : 0.0);
+    const double f = b > a ? 2.0 * e : (b == a ? e : 0.0);
+    F[gram_packed_offset(a, k) + (b - 8 * (a / 8))] = __double2bfloat16(f);
+  }
 }
 
 constexpr int kMTileO = 64;  // rows of W / M per CTA
@@ -100,9 +106,9 @@ __global__ void __launch_bounds__(256) precompute_M_kernel(const __nv_bfloat16* 
 }  // namespace
 
 gsi_status_t gram_launch(const __nv_bfloat16* V, int64_t d, int64_t k, float* gram,
-                         __nv_bfloat16* E, cudaStream_t s) {
+                         __nv_bfloat16* F, cudaStream_t s) {
   dim3 grid(unsigned(k / kGramTile), unsigned(k / kGramTile));
-  gram_kernel<<<grid, 256, 0, s>>>(V, int(d), int(k), gram, E);
+  gram_kernel<<<grid, 256, 0, s>>>(V, int(d), int(k), gram, F);
   return cudaGetLastError() == cudaSuccess ? GSI_OK : GSI_ERR_CUDA;
 }
 

@@ -20,8 +20,9 @@
  *       gate T            uint8         (1 = slow path taken, 0 = fast path)
  *       rho  T            fp32          (residual ratio per token)
  *   - Pointers are DEVICE pointers unless the name says _host, and must be
- *     16-byte aligned.  Shapes must satisfy d % 8 == 0, k % 16 == 0,
- *     d_out % 8 == 0, 16 <= k <= 256 (else GSI_ERR_UNSUPPORTED_SHAPE).
+ *     16-byte aligned.  Shapes must satisfy d % 8 == 0, d_out % 8 == 0,
+ *     k in {16, 32, 64, 128, 256, 512} and k <= d (else
+ *     GSI_ERR_UNSUPPORTED_SHAPE).
  *   - eps is an fp32 threshold compared as "rho < eps"; a tie goes to the
  *     slow path; eps <= 0 makes every token slow, eps = +inf makes every
  *     token with finite rho fast; NaN eps is GSI_ERR_INVALID_ARG.
@@ -64,7 +65,9 @@ typedef enum {
  *   out       : receives the handle.
  * The handle owns a small workspace (gate reductions, token index lists,
  * gathered operands) sized for T <= 512 tokens per call; gsi_reserve()
- * grows it.  Computes the Gram matrix V_k^T V_k (k x k) once.  Synchronises
+ * grows it.  Computes the Gram matrix V_k^T V_k (k x k) once, in fp64, and
+ * from it the correction E = V_k^T V_k - I that the one-token path uses to
+ * form ||r|| without a second pass over V_k.  Synchronises
  * the device once.  Thread-safe with respect to other handles. */
 gsi_status_t gsi_create(const void *W, const void *V_k, const void *M,
                         int64_t d_out, int64_t d, int64_t k, float eps,
