@@ -203,10 +203,10 @@ def build_layer(n_tokens: int, replicas: int):
 
 
 def correction_bytes(k: int) -> int:
-    """The packed bf16 triangle of E = V_k^T V_k - I that every one-token call
-    reads to form ||r|| (rows padded to 8-column chunks): (k^2 + 8k) / 2
-    entries of 2 bytes."""
-    return (k * k + 8 * k) // 2 * 2
+    """The bf16 upper 16 x 16 tiles of E = V_k^T V_k - I that every one-token
+    call reads to form ||r||: (k/16)(k/16 + 1)/2 tiles of 512 bytes."""
+    t = k // 16
+    return t * (t + 1) // 2 * 512
 
 
 def linear_bytes(s, n_tokens: int, n_slow: int) -> float:

@@ -104,12 +104,12 @@ gsi_status_t gsi_create(const void* W, const void* V_k, const void* M, int64_t d
     return GSI_ERR_CUDA;
   }
   // fixed workspace: Gram matrix, decode accumulators, the packed correction
-  // triangle and accumulators of the one-barrier kernel, barrier words, status
+  // tiles and accumulators of the one-barrier kernel, barrier words, status
   h->dec_acc_stride = int(k + 4);
   const bool want3 = k <= 256;
   const size_t gram_b = size_t(k) * k * 4;
   const size_t acc_b = size_t(2) * h->dec_acc_stride * 4;
-  const size_t F_b = want3 ? gsi::gram_packed_size(int(k)) * 2 : 0;
+  const size_t F_b = want3 ? gsi::corr_tiles_elems(int(k)) * 2 : 0;
   const size_t acc3_b = want3 ? gsi::decode3_acc_floats(k) * 4 : 0;
   auto r256 = [](size_t v) { return (v + 255) / 256 * 256; };
   const size_t ws = r256(gram_b) + r256(acc_b) + r256(F_b) + r256(acc3_b) + 256;

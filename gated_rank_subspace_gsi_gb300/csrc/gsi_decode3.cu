@@ -11,8 +11,11 @@
 // which holds for any V_k (expand the square and use V_k^T x = g).  The
 // correction g^T E g is a k x k quadratic form on data every CTA already has
 // once g is known, so unlike the explicit residual it needs no second pass
-// over V_k and no second exchange between CTAs.  E is stored as a packed
-// bf16 triangle F (gsi_internal.h), made once per handle in fp64.
+// over V_k and no second exchange between CTAs.  E is stored once per handle
+// (made in fp64) as its upper 16 x 16 bf16 tiles in MMA operand order
+// (gsi_internal.h); the form is evaluated with warp-level bf16 MMAs against
+// g split into bf16 high and low parts (g = hi + lo to ~2^-17), accumulated
+// in fp32.
 //
 // Work split.  G co-resident CTAs (at most one per SM); CTA c owns d / G rows
 // of V_k and d_out / G output rows (of M and of W).  Before it waits on the
@@ -24,9 +27,10 @@
 //             which spreads the atomic traffic over 8 addresses per word;
 //             then the grid barrier (release add / acquire poll)
 //   phase 2   every CTA sums the copies in a fixed order (the same g, bit for
-//             bit, in every CTA, hence the same gate), then forms g^T E g and
-//             g.g from F and the speculative fast-path rows M_c g, 8 rows per
-//             warp step (group_dot)
+//             bit, in every CTA, hence the same gate); half of the warps form
+//             g^T E g and g.g (MMA over the correction tiles) while the others
+//             form the speculative fast-path rows M_c g, 8 rows per warp step
+//             (group_dot)
 //   phase 3   thread 0 forms rho and the gate; the CTA stores M_c g, or, on
 //             the rare slow token, streams its rows of W from HBM for W_c x.
 // The accumulators are double-buffered by a launch epoch kept on the device:
@@ -109,6 +113,21 @@ __device__ __forceinline__ float group_dot(float (&v)[NB], int li) {
   return r;
 }
 
+// D += A B for one 16 x 16 (A, row-major) by 16 x 8 (B, column-major) bf16
+// product with fp32 accumulation (registers in the PTX fragment layout).
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint4& a, const uint2& b) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const uint32_t l = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
+  const uint32_t h = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
+  return l | (h << 16);
+}
+
 __device__ __forceinline__ float warp_sum_all(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
@@ -117,7 +136,7 @@ __device__ __forceinline__ float warp_sum_all(float v) {
 
 // Dynamic shared-memory layout (byte offsets), identical on host and device.
 struct Smem3 {
-  size_t sM, sV, sF, wpart, xs, g, ys, total;
+  size_t sM, sV, sF, wpart, xs, g, ys, bfrag, total;
 };
 __host__ __device__ inline size_t al3(size_t v, size_t a) { return (v + a - 1) / a * a; }
 __host__ __device__ inline Smem3 smem3_layout(int K, int rows_M, int rows_V, bool stage_M,
@@ -126,11 +145,12 @@ __host__ __device__ inline Smem3 smem3_layout(int K, int rows_M, int rows_V, boo
   size_t o = 0;
   s.sM = o;    o = al3(o + (stage_M ? size_t(rows_M) * K * 2 : 0), 128);
   s.sV = o;    o = al3(o + (stage_V ? size_t(rows_V) * K * 2 : 0), 128);
-  s.sF = o;    o = al3(o + (stage_F ? gram_packed_size(K) * 2 : 0), 128);
+  s.sF = o;    o = al3(o + (stage_F ? corr_tiles_elems(K) * 2 : 0), 128);
   s.wpart = o; o = al3(o + size_t(kWarps) * K * 4, 16);
   s.xs = o;    o = al3(o + size_t(rows_V) * 4, 16);
   s.g = o;     o = al3(o + size_t(K) * 4, 16);
-  s.ys = o;    o = al3(o + size_t(rows_M) * 4, 128);
+  s.ys = o;    o = al3(o + size_t(rows_M) * 4, 16);
+  s.bfrag = o; o = al3(o + size_t(K / 16) * 32 * 8, 128);
   s.total = o;
   return s;
 }
@@ -170,11 +190,12 @@ __global__ void __launch_bounds__(kThreads, 1) gsi_decode3_kernel(Decode3Args a)
   float* s_xs = reinterpret_cast<float*>(smem + lay.xs);        // [rows_V]
   float* s_g = reinterpret_cast<float*>(smem + lay.g);          // [K]
   float* s_ys = reinterpret_cast<float*>(smem + lay.ys);        // [rows_M]
+  uint2* s_bfrag = reinterpret_cast<uint2*>(smem + lay.bfrag);  // [K / 16][32]
 
   // ---- prologue: stage this CTA's weights (independent of x) ------------
   const uint32_t bytes_M = a.stage_M ? uint32_t(nM) * K * 2 : 0u;
   const uint32_t bytes_V = a.stage_V ? uint32_t(nV) * K * 2 : 0u;
-  const uint32_t bytes_F = a.stage_F ? uint32_t(gram_packed_size(K)) * 2 : 0u;
+  const uint32_t bytes_F = a.stage_F ? uint32_t(corr_tiles_elems(K)) * 2 : 0u;
   if (tid == 0) {
     mbar_init(&s_bar, 1);
     fence_mbar_init();
@@ -288,62 +309,78 @@ __global__ void __launch_bounds__(kThreads, 1) gsi_decode3_kernel(Decode3Args a)
     s_sx = sx;
   }
   __syncthreads();
-  float gl[8];
+  // B operands of the correction MMAs: for column block J, lane l holds
+  // rows 2 (l % 4) + {0, 1, 8, 9} of the 16 x 8 block whose column 0 is the
+  // bf16 high part of g_J, column 1 the low part, the rest zero
+  constexpr int T16 = K / 16;
+  for (int t = tid; t < T16 * 32; t += kThreads) {
+    const int J = t >> 5, grp = (t & 31) >> 2, k0 = J * 16 + 2 * (t & 3);
+    float v[4] = {s_g[k0], s_g[k0 + 1], s_g[k0 + 8], s_g[k0 + 9]};
 #pragma unroll
-  for (int j = 0; j < 8; ++j) gl[j] = s_g[li * 8 + j];
-  // g^T E g = sum_a g_a (F_a . g): row a of F starts at column 8 floor(a / 8),
-  // so lane li covers chunk li - floor(a / 8) of it when that is >= 0.
-  float qsum = 0.f, ggsum = 0.f;
-  for (int rb = warp * L::RS; rb < K; rb += kWarps * L::RS) {
-    float v[L::NB];
-#pragma unroll
-    for (int i = 0; i < L::NB; ++i) {
-      const int row = rb + slot * L::NB + i;
-      const int q8 = row >> 3;
-      float dot = 0.f;
-      if (row < K && li >= q8) {
-        const uint4 fv = *reinterpret_cast<const uint4*>(
-            Fs + gram_packed_offset(row, K) + size_t(li - q8) * 8);
-        float f[8];
-        bf16x8_to_f32(fv, f);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) dot = fmaf(f[j], gl[j], dot);
-      }
-      v[i] = dot;
+    for (int q = 0; q < 4; ++q) {
+      const float hi = __bfloat162float(__float2bfloat16_rn(v[q]));
+      v[q] = grp == 0 ? hi : (grp == 1 ? v[q] - hi : 0.f);
     }
-    const float rowdot = group_dot<L::LPR, L::NB>(v, li);
-    const int row = rb + slot * L::NB + li % L::NB;
-    if (li < L::NB && row < K) {
-      const float ga = s_g[row];
-      qsum = fmaf(ga, rowdot, qsum);
-      ggsum = fmaf(ga, ga, ggsum);
-    }
+    s_bfrag[t] = make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
   }
-  qsum = warp_sum_all(qsum);
-  ggsum = warp_sum_all(ggsum);
-  if (lane == 0) {
-    s_qw[warp] = qsum;
-    s_ggw[warp] = ggsum;
-  }
-  // speculative fast path: this CTA's rows of M g
-  for (int rb = warp * L::RS; rb < nMw; rb += kWarps * L::RS) {
-    float v[L::NB];
-#pragma unroll
-    for (int i = 0; i < L::NB; ++i) {
-      const int r = rb + slot * L::NB + i;
-      float dot = 0.f;
-      if (r < nMw) {
-        const uint4 mv = *reinterpret_cast<const uint4*>(Ms + size_t(r) * K + li * 8);
-        float f[8];
-        bf16x8_to_f32(mv, f);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) dot = fmaf(f[j], gl[j], dot);
+  __syncthreads();
+  constexpr int kQuadWarps = T16 > 1 ? T16 / 2 : 1;
+  if (warp < kQuadWarps) {
+    // g^T E g = sum_I g_I . (sum_{J >= I} F_IJ g_J); this warp takes row
+    // blocks I = warp and T16 - 1 - warp (T16 + 1 tiles in all)
+    const uint4* tiles = reinterpret_cast<const uint4*>(Fs);
+    const int grp = lane >> 2;
+    float qsum = 0.f, ggsum = 0.f;
+#pragma unroll 1
+    for (int pass = 0; pass < 2; ++pass) {
+      const int I = pass == 0 ? warp : T16 - 1 - warp;
+      if (pass == 1 && I == warp) break;
+      float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+      const int base = corr_tile_index(I, I, T16) - I;  // tile (I, J) = base + J
+      int J = I;
+      for (; J + 1 < T16; J += 2) {
+        mma_16816(d0, tiles[size_t(base + J) * 32 + lane], s_bfrag[J * 32 + lane]);
+        mma_16816(d1, tiles[size_t(base + J + 1) * 32 + lane], s_bfrag[(J + 1) * 32 + lane]);
       }
-      v[i] = dot;
+      if (J < T16) mma_16816(d0, tiles[size_t(base + J) * 32 + lane], s_bfrag[J * 32 + lane]);
+      if ((lane & 3) == 0) {  // columns 0 (high) and 1 (low) of rows grp, grp + 8
+        const float g0 = s_g[I * 16 + grp], g1 = s_g[I * 16 + grp + 8];
+        qsum = fmaf(g0, (d0[0] + d0[1]) + (d1[0] + d1[1]), qsum);
+        qsum = fmaf(g1, (d0[2] + d0[3]) + (d1[2] + d1[3]), qsum);
+        ggsum = fmaf(g0, g0, fmaf(g1, g1, ggsum));
+      }
     }
-    const float yr = group_dot<L::LPR, L::NB>(v, li);
-    const int r = rb + slot * L::NB + li % L::NB;
-    if (li < L::NB && r < nMw) s_ys[r] = yr;
+    qsum = warp_sum_all(qsum);
+    ggsum = warp_sum_all(ggsum);
+    if (lane == 0) {
+      s_qw[warp] = qsum;
+      s_ggw[warp] = ggsum;
+    }
+  } else {
+    // speculative fast path: this CTA's rows of M g
+    float gl[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) gl[j] = s_g[li * 8 + j];
+    constexpr int kYWarps = kWarps - kQuadWarps;
+    for (int rb = (warp - kQuadWarps) * L::RS; rb < nMw; rb += kYWarps * L::RS) {
+      float v[L::NB];
+#pragma unroll
+      for (int i = 0; i < L::NB; ++i) {
+        const int r = rb + slot * L::NB + i;
+        float dot = 0.f;
+        if (r < nMw) {
+          const uint4 mv = *reinterpret_cast<const uint4*>(Ms + size_t(r) * K + li * 8);
+          float f[8];
+          bf16x8_to_f32(mv, f);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) dot = fmaf(f[j], gl[j], dot);
+        }
+        v[i] = dot;
+      }
+      const float yr = group_dot<L::LPR, L::NB>(v, li);
+      const int r = rb + slot * L::NB + li % L::NB;
+      if (li < L::NB && r < nMw) s_ys[r] = yr;
+    }
   }
   __syncthreads();
 
@@ -352,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1) gsi_decode3_kernel(Decode3Args a)
     // fp32 throughout: the sums' relative error (~1e-7 of ||x||^2) moves rho by
     // ~1e-6 near any practical eps, and fp64 is slow on this part
     float quad = 0.f, gg = 0.f;
-    for (int w = 0; w < kWarps; ++w) {
+    for (int w = 0; w < kQuadWarps; ++w) {
       quad += s_qw[w];
       gg += s_ggw[w];
     }

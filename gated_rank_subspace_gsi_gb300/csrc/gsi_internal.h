@@ -34,7 +34,7 @@ struct gsi_handle {
   int dec3_grid = 0, dec3_rows_M = 0, dec3_rows_V = 0;
   bool dec3_stage_M = false, dec3_stage_V = false, dec3_stage_F = false;
   size_t dec3_smem = 0;
-  __nv_bfloat16* dec3_F = nullptr;  // packed correction triangle (gram_packed_size(k))
+  __nv_bfloat16* dec3_F = nullptr;  // correction tiles (corr_tiles_elems(k))
   float* dec3_acc = nullptr;        // decode3_acc_floats(k) fp32 accumulators
   uint32_t* dec3_bar = nullptr;     // [0] arrival counter, [1] launch epoch
 
@@ -72,16 +72,26 @@ struct gsi_handle {
 
 namespace gsi {
 
-// Packed correction triangle F of E = V_k^T V_k - I, for the identity
-// g^T E g = sum_a g_a (F_a . g): row a holds columns b >= 8 floor(a / 8) with
-// F_ab = 2 E_ab (b > a), E_aa (b = a) and 0 (b < a), so every row starts on a
-// 16-byte boundary.  Row a = 8q + r starts at a k - 8 (4 q (q - 1) + r q).
-__host__ __device__ inline size_t gram_packed_offset(int a, int k) {
-  const size_t q = size_t(a) >> 3, r = size_t(a) & 7u;
-  return size_t(a) * size_t(k) - 8 * (4 * q * (q - (q > 0 ? 1 : 0)) + r * q);
+// Correction tiles of E = V_k^T V_k - I, for the identity
+// g^T E g = sum_{I <= J} g_I^T F_IJ g_J over 16 x 16 blocks: F_II = E_II and
+// F_IJ = 2 E_IJ for I < J (E is symmetric).  The k/16 (k/16 + 1) / 2 upper
+// tiles are stored row by row (I, then J >= I), 256 bf16 each, in the order
+// of the A operand of a 16 x 16 x 8 bf16 MMA: lane l (group l / 4, pair
+// l % 4) owns 8 consecutive values, its registers a0..a3 = (rows group and
+// group + 8) x (columns 2 pair, 2 pair + 1 and the same + 8), lower column in
+// the lower half of each register.
+__host__ __device__ inline int corr_tile_index(int I, int J, int t16) {
+  return I * t16 - I * (I - 1) / 2 + (J - I);
 }
-__host__ __device__ inline size_t gram_packed_size(int k) {
-  return (size_t(k) * k + 8 * size_t(k)) / 2;
+__host__ __device__ inline size_t corr_tiles_elems(int k) {
+  const size_t t = size_t(k) / 16;
+  return t * (t + 1) / 2 * 256;
+}
+// Position of E block element (r, c) (0 <= r, c < 16) inside its tile.
+__host__ __device__ inline int corr_tile_pos(int r, int c) {
+  const int lane = (r & 7) * 4 + ((c & 7) >> 1);
+  const int reg = (r >> 3) + 2 * (c >> 3);
+  return lane * 8 + reg * 2 + (c & 1);
 }
 
 // Decode path (gsi_decode.cu)

@@ -1,8 +1,9 @@
 // gsi_prep.cu -- one-off operand preparation for the GSI gated linear map.
 //
 //   gram:         Gm = V_k^T V_k (k x k), accumulated in fp64 and stored fp32,
-//                 and the packed triangle F of E = Gm - I stored bf16 (the
-//                 one-barrier decode kernel's correction term g^T E g).
+//                 and the upper 16 x 16 tiles of E = Gm - I (off-diagonal
+//                 tiles doubled) stored bf16 in MMA operand order: the
+//                 one-barrier decode kernel's correction term g^T E g.
 //                 Used by the batched path to form ||r||^2 without a second
 //                 pass over V_k: ||x - V_k g||^2 = ||x||^2 - 2 g.g + g^T Gm g,
 //                 an identity for any V_k (eq. 1 of section 2.1 of the page
@@ -44,10 +45,11 @@ __global__ void __launch_bounds__(256) gram_kernel(const __nv_bfloat16* __restri
   const int a = a0 + ta, b = b0 + tb;
   gram[size_t(a) * k + b] = float(acc);
   // F from the fp64 sum, so the small entries of E = Gm - I keep their precision
-  if (F && b >= 8 * (a / 8)) {
+  if (F && blockIdx.y <= blockIdx.x) {
     const double e = acc - (a == b ? 1.0 : 0.0);
-    const double f = b > a ? 2.0 * e : (b == a ? e : 0.0);
-    F[gram_packed_offset(a, k) + (b - 8 * (a / 8))] = __double2bfloat16(f);
+    const double f = blockIdx.y < blockIdx.x ? 2.0 * e : e;
+    const int tile = corr_tile_index(blockIdx.y, blockIdx.x, k / kGramTile);
+    F[size_t(tile) * 256 + corr_tile_pos(ta, tb)] = __double2bfloat16(f);
   }
 }
 
