@@ -61,7 +61,7 @@ struct Decode3Args {
   int d_out, d;
   float eps;
   int rows_M, rows_V;
-  int stage_M, stage_V, stage_F;
+  int stage_M;     // M slice staged in shared memory (V_k slice and F always are)
   float* acc;      // [2][kCopies][acc_stride]
   int acc_stride;  // >= k + 1, multiple of 4
   uint32_t* bar;   // [0] arrival counter, [1] launch epoch
@@ -139,13 +139,12 @@ struct Smem3 {
   size_t sM, sV, sF, wpart, xs, g, ys, bfrag, total;
 };
 __host__ __device__ inline size_t al3(size_t v, size_t a) { return (v + a - 1) / a * a; }
-__host__ __device__ inline Smem3 smem3_layout(int K, int rows_M, int rows_V, bool stage_M,
-                                              bool stage_V, bool stage_F) {
+__host__ __device__ inline Smem3 smem3_layout(int K, int rows_M, int rows_V, bool stage_M) {
   Smem3 s;
   size_t o = 0;
   s.sM = o;    o = al3(o + (stage_M ? size_t(rows_M) * K * 2 : 0), 128);
-  s.sV = o;    o = al3(o + (stage_V ? size_t(rows_V) * K * 2 : 0), 128);
-  s.sF = o;    o = al3(o + (stage_F ? corr_tiles_elems(K) * 2 : 0), 128);
+  s.sV = o;    o = al3(o + size_t(rows_V) * K * 2, 128);
+  s.sF = o;    o = al3(o + corr_tiles_elems(K) * 2, 128);
   s.wpart = o; o = al3(o + size_t(kWarps) * K * 4, 16);
   s.xs = o;    o = al3(o + size_t(rows_V) * 4, 16);
   s.g = o;     o = al3(o + size_t(K) * 4, 16);
@@ -155,7 +154,7 @@ __host__ __device__ inline Smem3 smem3_layout(int K, int rows_M, int rows_V, boo
   return s;
 }
 
-template <int K>
+template <int K, bool kStageM>
 __global__ void __launch_bounds__(kThreads, 1) gsi_decode3_kernel(Decode3Args a) {
   using L = Lanes3<K>;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -168,12 +167,12 @@ __global__ void __launch_bounds__(kThreads, 1) gsi_decode3_kernel(Decode3Args a)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int cta = blockIdx.x, G = gridDim.x;
-  const Smem3 lay = smem3_layout(K, a.rows_M, a.rows_V, a.stage_M, a.stage_V, a.stage_F);
+  const Smem3 lay = smem3_layout(K, a.rows_M, a.rows_V, kStageM);
   // Launch self-check (uniform over the grid, before any wait): a launch that
   // does not cover d and d_out, or got less shared memory than its layout,
   // does nothing and reports it.
   if (blockDim.x != kThreads || int64_t(G) * a.rows_M < a.d_out || int64_t(G) * a.rows_V < a.d ||
-      dynamic_smem_bytes() < lay.total) {
+      dynamic_smem_bytes() < lay.total || (a.stage_M != 0) != kStageM) {
     if (cta == 0 && tid == 0) atomicOr(a.status, kStatusBadLaunch);
     return;
   }
@@ -193,9 +192,9 @@ __global__ void __launch_bounds__(kThreads, 1) gsi_decode3_kernel(Decode3Args a)
   uint2* s_bfrag = reinterpret_cast<uint2*>(smem + lay.bfrag);  // [K / 16][32]
 
   // ---- prologue: stage this CTA's weights (independent of x) ------------
-  const uint32_t bytes_M = a.stage_M ? uint32_t(nM) * K * 2 : 0u;
-  const uint32_t bytes_V = a.stage_V ? uint32_t(nV) * K * 2 : 0u;
-  const uint32_t bytes_F = a.stage_F ? uint32_t(corr_tiles_elems(K)) * 2 : 0u;
+  const uint32_t bytes_M = kStageM ? uint32_t(nM) * K * 2 : 0u;
+  const uint32_t bytes_V = uint32_t(nV) * K * 2;
+  const uint32_t bytes_F = uint32_t(corr_tiles_elems(K)) * 2;
   if (tid == 0) {
     mbar_init(&s_bar, 1);
     fence_mbar_init();
@@ -230,9 +229,15 @@ __global__ void __launch_bounds__(kThreads, 1) gsi_decode3_kernel(Decode3Args a)
   }
   const int nVw = ok ? nV : 0;
   const int nMw = ok ? nM : 0;
-  const __nv_bfloat16* Vs = a.stage_V ? sV : a.V + size_t(v0) * K;
-  const __nv_bfloat16* Ms = a.stage_M ? sM : a.M + size_t(m0) * K;
-  const __nv_bfloat16* Fs = a.stage_F ? sF : a.F;
+  const __nv_bfloat16* Vs = sV;
+  const __nv_bfloat16* Ms = kStageM ? sM : a.M + size_t(m0) * K;
+  const __nv_bfloat16* Fs = sF;
+  // B operands of the correction MMAs (filled after the barrier): for column
+  // block J, lane l holds rows 2 (l % 4) + {0, 1, 8, 9} of the 16 x 8 block
+  // whose column 0 is the bf16 high part of g_J, column 1 its remainder and
+  // the other columns zero; the zero part is written here
+  constexpr int T16 = K / 16;
+  for (int t = tid; t < T16 * 24; t += kThreads) s_bfrag[(t / 24) * 32 + 8 + t % 24] = make_uint2(0u, 0u);
   if (warp == kWarps - 1) {  // ||x_c||^2 (x_i^2 is exact in fp32 for bf16 x_i)
     float sx = 0.f;
     for (int i = lane; i < nVw; i += 32) sx = fmaf(s_xs[i], s_xs[i], sx);
@@ -301,6 +306,14 @@ __global__ void __launch_bounds__(kThreads, 1) gsi_decode3_kernel(Decode3Args a)
 #pragma unroll
     for (int c = 0; c < kCopies; ++c) gsum += ld_cg_f32(acc + size_t(c) * a.acc_stride + t);
     s_g[t] = gsum;
+    // g_t is row kk = t % 16 of column block J = t / 16: register kk / 8,
+    // lane pair (kk % 8) / 2, half kk % 2 of lanes pair (high) and 4 + pair (low)
+    const __nv_bfloat16 hi = __float2bfloat16_rn(gsum);
+    const __nv_bfloat16 lo = __float2bfloat16_rn(gsum - __bfloat162float(hi));
+    const int kk = t & 15, pos = (kk >> 3) * 2 + (kk & 1), pr = (kk & 7) >> 1;
+    __nv_bfloat16* bf = reinterpret_cast<__nv_bfloat16*>(s_bfrag + (t >> 4) * 32);
+    bf[pr * 4 + pos] = hi;
+    bf[(4 + pr) * 4 + pos] = lo;
   }
   if (tid == 0) {
     float sx = 0.f;
@@ -309,47 +322,33 @@ __global__ void __launch_bounds__(kThreads, 1) gsi_decode3_kernel(Decode3Args a)
     s_sx = sx;
   }
   __syncthreads();
-  // B operands of the correction MMAs: for column block J, lane l holds
-  // rows 2 (l % 4) + {0, 1, 8, 9} of the 16 x 8 block whose column 0 is the
-  // bf16 high part of g_J, column 1 the low part, the rest zero
-  constexpr int T16 = K / 16;
-  for (int t = tid; t < T16 * 32; t += kThreads) {
-    const int J = t >> 5, grp = (t & 31) >> 2, k0 = J * 16 + 2 * (t & 3);
-    float v[4] = {s_g[k0], s_g[k0 + 1], s_g[k0 + 8], s_g[k0 + 9]};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float hi = __bfloat162float(__float2bfloat16_rn(v[q]));
-      v[q] = grp == 0 ? hi : (grp == 1 ? v[q] - hi : 0.f);
-    }
-    s_bfrag[t] = make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
-  }
-  __syncthreads();
   constexpr int kQuadWarps = T16 > 1 ? T16 / 2 : 1;
   if (warp < kQuadWarps) {
-    // g^T E g = sum_I g_I . (sum_{J >= I} F_IJ g_J); this warp takes row
-    // blocks I = warp and T16 - 1 - warp (T16 + 1 tiles in all)
+    // g^T E g = sum over tiles I <= J of g_I . (F_IJ g_J); this warp takes
+    // row blocks I1 = warp (T16 - warp tiles) and I2 = T16 - 1 - warp
+    // (warp + 1 tiles), T16 + 1 independent MMAs in all
+    constexpr int kSteps = T16 > 1 ? T16 + 1 : 1;
     const uint4* tiles = reinterpret_cast<const uint4*>(Fs);
     const int grp = lane >> 2;
-    float qsum = 0.f, ggsum = 0.f;
-#pragma unroll 1
-    for (int pass = 0; pass < 2; ++pass) {
-      const int I = pass == 0 ? warp : T16 - 1 - warp;
-      if (pass == 1 && I == warp) break;
-      float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
-      const int base = corr_tile_index(I, I, T16) - I;  // tile (I, J) = base + J
-      int J = I;
-      for (; J + 1 < T16; J += 2) {
-        mma_16816(d0, tiles[size_t(base + J) * 32 + lane], s_bfrag[J * 32 + lane]);
-        mma_16816(d1, tiles[size_t(base + J + 1) * 32 + lane], s_bfrag[(J + 1) * 32 + lane]);
-      }
-      if (J < T16) mma_16816(d0, tiles[size_t(base + J) * 32 + lane], s_bfrag[J * 32 + lane]);
-      if ((lane & 3) == 0) {  // columns 0 (high) and 1 (low) of rows grp, grp + 8
-        const float g0 = s_g[I * 16 + grp], g1 = s_g[I * 16 + grp + 8];
-        qsum = fmaf(g0, (d0[0] + d0[1]) + (d1[0] + d1[1]), qsum);
-        qsum = fmaf(g1, (d0[2] + d0[3]) + (d1[2] + d1[3]), qsum);
-        ggsum = fmaf(g0, g0, fmaf(g1, g1, ggsum));
-      }
+    const int I1 = warp, I2 = T16 - 1 - warp, n1 = T16 - warp;
+    const float g10 = s_g[I1 * 16 + grp], g11 = s_g[I1 * 16 + grp + 8];
+    const float g20 = s_g[I2 * 16 + grp], g21 = s_g[I2 * 16 + grp + 8];
+    float qsum = 0.f;
+#pragma unroll
+    for (int st = 0; st < kSteps; ++st) {
+      const bool first = st < n1;
+      const int I = first ? I1 : I2;
+      const int J = first ? I1 + st : I2 + (st - n1);
+      float d[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_16816(d, tiles[corr_tile_index(I, J, T16) * 32 + lane], s_bfrag[J * 32 + lane]);
+      // columns 0 (high) and 1 (low) of rows grp and grp + 8 (lanes with
+      // lane % 4 == 0; the other lanes hold the zero columns)
+      qsum = fmaf(first ? g10 : g20, d[0] + d[1], qsum);
+      qsum = fmaf(first ? g11 : g21, d[2] + d[3], qsum);
     }
+    float ggsum = fmaf(g10, g10, g11 * g11);
+    if (I2 != I1) ggsum = fmaf(g20, g20, fmaf(g21, g21, ggsum));
+    if ((lane & 3) != 0) qsum = ggsum = 0.f;
     qsum = warp_sum_all(qsum);
     ggsum = warp_sum_all(ggsum);
     if (lane == 0) {
@@ -479,17 +478,18 @@ __global__ void __launch_bounds__(kThreads, 1) gsi_decode3_kernel(Decode3Args a)
 }
 
 template <int K>
-const void* kernel3_ptr() {
-  return reinterpret_cast<const void*>(&gsi_decode3_kernel<K>);
+const void* kernel3_ptr(bool stage_M) {
+  return stage_M ? reinterpret_cast<const void*>(&gsi_decode3_kernel<K, true>)
+                 : reinterpret_cast<const void*>(&gsi_decode3_kernel<K, false>);
 }
 
-const void* decode3_kernel_for(int64_t k) {
+const void* decode3_kernel_for(int64_t k, bool stage_M) {
   switch (k) {
-    case 16: return kernel3_ptr<16>();
-    case 32: return kernel3_ptr<32>();
-    case 64: return kernel3_ptr<64>();
-    case 128: return kernel3_ptr<128>();
-    case 256: return kernel3_ptr<256>();
+    case 16: return kernel3_ptr<16>(stage_M);
+    case 32: return kernel3_ptr<32>(stage_M);
+    case 64: return kernel3_ptr<64>(stage_M);
+    case 128: return kernel3_ptr<128>(stage_M);
+    case 256: return kernel3_ptr<256>(stage_M);
     default: return nullptr;
   }
 }
@@ -501,8 +501,7 @@ int acc3_stride(int64_t k) { return int((k + 1 + 3) / 4 * 4); }
 size_t decode3_acc_floats(int64_t k) { return size_t(2) * kCopies * acc3_stride(k); }
 
 gsi_status_t decode3_configure(gsi_handle* h) {
-  const void* fn = decode3_kernel_for(h->k);
-  if (!fn) return GSI_ERR_UNSUPPORTED_SHAPE;
+  if (!decode3_kernel_for(h->k, true)) return GSI_ERR_UNSUPPORTED_SHAPE;
   int max_optin = 0;
   if (cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device) != cudaSuccess)
     return GSI_ERR_CUDA;
@@ -510,23 +509,20 @@ gsi_status_t decode3_configure(gsi_handle* h) {
   const int G = int(std::max<int64_t>(1, std::min<int64_t>(h->num_sms, rows_hint)));
   const int rows_M = int((h->d_out + G - 1) / G);
   const int rows_V = int((h->d + G - 1) / G);
-  cudaFuncAttributes fa;
-  if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return GSI_ERR_CUDA;
-  const int fn_limit = max_optin - int(fa.sharedSizeBytes);
-  // Stage as much as fits, dropping M first (read once per call either way),
-  // then F (read from L2 instead), then V_k.
-  bool stage_M = true, stage_V = true, stage_F = true;
   const int K = int(h->k);
-  auto total = [&]() {
-    return smem3_layout(K, rows_M, rows_V, stage_M, stage_V, stage_F).total;
-  };
-  if (total() > size_t(fn_limit)) stage_M = false;
-  if (total() > size_t(fn_limit)) stage_F = false;
-  if (total() > size_t(fn_limit)) stage_V = false;
-  if (total() > size_t(fn_limit)) return GSI_ERR_UNSUPPORTED_SHAPE;
-  const size_t smem = total();
+  // Both variants of a k have the same static shared memory.
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, decode3_kernel_for(h->k, true)) != cudaSuccess) return GSI_ERR_CUDA;
+  const int fn_limit = max_optin - int(fa.sharedSizeBytes);
+  // V_k slice and F are always staged; the M slice too when it fits (else it
+  // is read from global memory after the barrier).
+  const bool stage_M = smem3_layout(K, rows_M, rows_V, true).total <= size_t(fn_limit);
+  const size_t smem = smem3_layout(K, rows_M, rows_V, stage_M).total;
+  if (smem > size_t(fn_limit)) return GSI_ERR_UNSUPPORTED_SHAPE;
+  const void* fn = decode3_kernel_for(h->k, stage_M);
   // The limit belongs to the kernel function, shared by every handle with
   // this k: raise it to the device maximum once, never per handle.
+  if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return GSI_ERR_CUDA;
   if (fa.maxDynamicSharedSizeBytes < fn_limit &&
       cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, fn_limit) != cudaSuccess)
     return GSI_ERR_CUDA;
@@ -539,8 +535,6 @@ gsi_status_t decode3_configure(gsi_handle* h) {
   h->dec3_rows_M = rows_M;
   h->dec3_rows_V = rows_V;
   h->dec3_stage_M = stage_M;
-  h->dec3_stage_V = stage_V;
-  h->dec3_stage_F = stage_F;
   h->dec3_smem = smem;
   return GSI_OK;
 }
@@ -562,8 +556,6 @@ gsi_status_t decode3_launch(gsi_handle* h, const void* x, float* y, uint8_t* gat
   a.rows_M = h->dec3_rows_M;
   a.rows_V = h->dec3_rows_V;
   a.stage_M = h->dec3_stage_M ? 1 : 0;
-  a.stage_V = h->dec3_stage_V ? 1 : 0;
-  a.stage_F = h->dec3_stage_F ? 1 : 0;
   a.acc = h->dec3_acc;
   a.acc_stride = acc3_stride(h->k);
   a.bar = h->dec3_bar;
@@ -583,16 +575,10 @@ gsi_status_t decode3_launch(gsi_handle* h, const void* x, float* y, uint8_t* gat
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  cudaError_t err;
-  switch (h->k) {
-    case 16: err = cudaLaunchKernelEx(&cfg, gsi_decode3_kernel<16>, a); break;
-    case 32: err = cudaLaunchKernelEx(&cfg, gsi_decode3_kernel<32>, a); break;
-    case 64: err = cudaLaunchKernelEx(&cfg, gsi_decode3_kernel<64>, a); break;
-    case 128: err = cudaLaunchKernelEx(&cfg, gsi_decode3_kernel<128>, a); break;
-    case 256: err = cudaLaunchKernelEx(&cfg, gsi_decode3_kernel<256>, a); break;
-    default: return GSI_ERR_UNSUPPORTED_SHAPE;
-  }
-  return err == cudaSuccess ? GSI_OK : GSI_ERR_CUDA;
+  const void* fn = decode3_kernel_for(h->k, h->dec3_stage_M);
+  if (!fn) return GSI_ERR_UNSUPPORTED_SHAPE;
+  void* args[] = {&a};
+  return cudaLaunchKernelExC(&cfg, fn, args) == cudaSuccess ? GSI_OK : GSI_ERR_CUDA;
 }
 
 }  // namespace gsi

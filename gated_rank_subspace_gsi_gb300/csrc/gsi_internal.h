@@ -32,7 +32,7 @@ struct gsi_handle {
   // ---- one-barrier decode kernel (k <= 256), used when it configures -----
   bool dec3_ok = false;
   int dec3_grid = 0, dec3_rows_M = 0, dec3_rows_V = 0;
-  bool dec3_stage_M = false, dec3_stage_V = false, dec3_stage_F = false;
+  bool dec3_stage_M = false;        // M slice staged (V_k slice and F always are)
   size_t dec3_smem = 0;
   __nv_bfloat16* dec3_F = nullptr;  // correction tiles (corr_tiles_elems(k))
   float* dec3_acc = nullptr;        // decode3_acc_floats(k) fp32 accumulators
