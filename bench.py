@@ -168,8 +168,12 @@ def kernel_traffic():
 # the workload
 # --------------------------------------------------------------------------
 
-def build_layer(n_tokens: int, replicas: int):
-    """Device tensors and handles of the GPT-J decode layer workload."""
+def build_layer(n_tokens: int, replicas: int, prefetch: int = 1):
+    """Device tensors and handles of the GPT-J decode layer workload.  With
+    prefetch = p > 0, each handle names the handle of the call p places after
+    it in the step's order (linear i of replica r, then linear i + 1, the
+    last linear then the first of replica r + 1), so each call streams that
+    call's operands into L2."""
     import torch
 
     import gsi_inputs as gi
@@ -198,6 +202,10 @@ def build_layer(n_tokens: int, replicas: int):
                           y=torch.zeros((n_tokens, spec.d_out), dtype=torch.float32, device="cuda"),
                           gate=torch.zeros((n_tokens,), dtype=torch.uint8, device="cuda"),
                           rho=torch.zeros((n_tokens,), dtype=torch.float32, device="cuda")))
+    if prefetch > 0:
+        order = [layer[li]["reps"][r][2] for r in range(replicas) for li in range(len(layer))]
+        for i, h in enumerate(order):
+            lib.gsi_set_prefetch(h, order[(i + prefetch) % len(order)])
     torch.cuda.synchronize()
     return wl, slow, layer
 
@@ -311,7 +319,7 @@ def run_gsi(args, world, rank, local):
     l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
     per_token = 32.44e6
     replicas = max(16, int(math.ceil(4 * l2 / per_token)))
-    wl, slow, layer = build_layer(n_tokens, replicas)
+    wl, slow, layer = build_layer(n_tokens, replicas, prefetch=args.prefetch)
     nbytes = step_bytes(layer, slow)
     n_lin = n_tokens * len(layer)
     stream = torch.cuda.Stream()
@@ -406,6 +414,7 @@ def run_gsi(args, world, rank, local):
             "l2": f"inputs larger than L2: {replicas} replicas x 32.4 MB per token, "
                   f"{nbytes / 1e9:.2f} GB streamed per step, L2 {l2 / 2**20:.0f} MiB",
             "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+            "l2_prefetch_distance": args.prefetch,
         },
         "effective_hbm_gbs": round(gbs * world, 1),
         "frac_of_measured_hbm": round(gbs / peak, 4),
@@ -503,6 +512,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["gsi", "reference"], default="gsi")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefetch", type=int, default=1,
+                    help="each call prefetches into L2 the operands of the call this many "
+                         "places later (0: none)")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the per-linear breakdown and the end-to-end leg (profiling runs)")
     args = ap.parse_args(argv)

@@ -223,9 +223,28 @@ gsi_status_t gsi_device_status(gsi_handle_t h, cudaStream_t stream) {
   return (word & gsi::kStatusTimeout) ? GSI_ERR_TIMEOUT : GSI_OK;
 }
 
+gsi_status_t gsi_set_prefetch(gsi_handle_t h, gsi_handle_t next) {
+  if (!h) return GSI_ERR_INVALID_ARG;
+  if (next && next->device != h->device) return GSI_ERR_INVALID_ARG;
+  if (h->pf_next) {
+    auto& from = h->pf_next->pf_from;
+    from.erase(std::remove(from.begin(), from.end(), h), from.end());
+  }
+  h->pf_next = next;
+  if (next) next->pf_from.push_back(h);
+  return GSI_OK;
+}
+
 void gsi_destroy(gsi_handle_t h) {
   if (!h) return;
   cudaDeviceSynchronize();
+  // unlink prefetch links in both directions before the memory goes away
+  for (gsi_handle* p : h->pf_from)
+    if (p->pf_next == h) p->pf_next = nullptr;
+  if (h->pf_next && h->pf_next != h) {
+    auto& from = h->pf_next->pf_from;
+    from.erase(std::remove(from.begin(), from.end(), h), from.end());
+  }
   if (h->ws) cudaFree(h->ws);
   if (h->bws) cudaFree(h->bws);
   if (h->st_dev) cudaFree(h->st_dev);

@@ -33,6 +33,9 @@
 //             (group_dot)
 //   phase 3   thread 0 forms rho and the gate; the CTA stores M_c g, or, on
 //             the rare slow token, streams its rows of W from HBM for W_c x.
+// With a prefetch link (gsi_set_prefetch) the last warp also issues, right
+// after the barrier, L2 prefetches of its 1 / G share of the next call's
+// V_k, M and correction tiles, so the next call stages them from L2.
 // The accumulators are double-buffered by a launch epoch kept on the device:
 // CTA 0 zeroes the buffer the next launch uses, so no memset is needed and
 // the kernel replays in a CUDA graph.
@@ -66,6 +69,10 @@ struct Decode3Args {
   int acc_stride;  // >= k + 1, multiple of 4
   uint32_t* bar;   // [0] arrival counter, [1] launch epoch
   uint32_t* status;
+  // operands of the next call to prefetch into L2 (bytes 0: none), each CTA
+  // its 1 / G share
+  const char* pf[3];
+  uint32_t pf_bytes[3];
 };
 
 // Lane geometry: a row of K bf16 values is K / 8 16-byte chunks, one per lane
@@ -81,6 +88,11 @@ struct Lanes3 {
 
 __device__ __forceinline__ void red_release_u32(uint32_t* p, uint32_t v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+
+// Prefetch [p, p + bytes) into L2 (16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ uint32_t dynamic_smem_bytes() {
@@ -299,6 +311,20 @@ __global__ void __launch_bounds__(kThreads, 1) gsi_decode3_kernel(Decode3Args a)
   }
   __syncthreads();
   ok = ok && s_ok;
+  if (warp == kWarps - 1) {
+    // this CTA's share of the next call's operands, into L2.  Issued after
+    // the barrier, when the rest of this call works from shared memory: the
+    // stream then does not delay this call's x read, atomics or barrier.
+#pragma unroll
+    for (int o = 0; o < 3; ++o) {
+      const uint32_t bytes = a.pf_bytes[o];
+      const uint32_t share = (bytes / 16 + G - 1) / G * 16;
+      const uint32_t lo = min(bytes, uint32_t(cta) * share), hi = min(bytes, lo + share);
+      constexpr uint32_t kPiece = 16384;
+      for (uint32_t off = lo + uint32_t(lane) * kPiece; off < hi; off += 32u * kPiece)
+        prefetch_l2(a.pf[o] + off, min(kPiece, hi - off));
+    }
+  }
 
   // ---- phase 2: g (same order in every CTA), g^T E g, g.g, speculative M g --
   for (int t = tid; t < K; t += kThreads) {
@@ -560,6 +586,17 @@ gsi_status_t decode3_launch(gsi_handle* h, const void* x, float* y, uint8_t* gat
   a.acc_stride = acc3_stride(h->k);
   a.bar = h->dec3_bar;
   a.status = h->status;
+  // operands above 64 MiB are not prefetched (a large share of L2)
+  const gsi_handle* n = h->pf_next;
+  const int64_t kMaxPrefetch = int64_t(64) << 20;
+  const int64_t pf_b[3] = {n ? n->d * n->k * 2 : 0, n ? n->d_out * n->k * 2 : 0,
+                           (n && n->dec3_F) ? int64_t(corr_tiles_elems(int(n->k))) * 2 : 0};
+  const void* pf_p[3] = {n ? n->V : nullptr, n ? n->M : nullptr, n ? n->dec3_F : nullptr};
+  for (int o = 0; o < 3; ++o) {
+    const bool on = pf_b[o] > 0 && pf_b[o] <= kMaxPrefetch;
+    a.pf[o] = on ? static_cast<const char*>(pf_p[o]) : nullptr;
+    a.pf_bytes[o] = on ? uint32_t(pf_b[o]) : 0u;
+  }
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(h->dec3_grid);

@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <vector>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -37,6 +38,12 @@ struct gsi_handle {
   __nv_bfloat16* dec3_F = nullptr;  // correction tiles (corr_tiles_elems(k))
   float* dec3_acc = nullptr;        // decode3_acc_floats(k) fp32 accumulators
   uint32_t* dec3_bar = nullptr;     // [0] arrival counter, [1] launch epoch
+
+  // L2 prefetch link (gsi_set_prefetch): each one-token call on this handle
+  // prefetches pf_next's V_k, M and correction tiles into L2.  pf_from lists
+  // the handles whose link points here, so destroying this handle unlinks them.
+  gsi_handle* pf_next = nullptr;
+  std::vector<gsi_handle*> pf_from;
 
   // ---- device workspace (one allocation) --------------------------------
   void* ws = nullptr;

@@ -26,7 +26,7 @@ GSI_ERR_LAUNCH = 7
 # every function declared in include/gsi.h
 EXPORTS = ("gsi_create", "gsi_forward", "gsi_forward_host", "gsi_precompute_M",
            "gsi_reserve", "gsi_device_status", "gsi_destroy", "gsi_status_string",
-           "gsi_forward_launch_count", "gsi_forward_noalloc")
+           "gsi_forward_launch_count", "gsi_forward_noalloc", "gsi_set_prefetch")
 
 _lock = threading.Lock()
 _lib = None
@@ -71,6 +71,8 @@ def _load():
         lib.gsi_forward_launch_count.restype = ctypes.c_int
         lib.gsi_forward_noalloc.argtypes = [P, P, P, I64, I64, I64, ctypes.c_float, P, P, P, P, P]
         lib.gsi_forward_noalloc.restype = ctypes.c_int
+        lib.gsi_set_prefetch.argtypes = [P, P]
+        lib.gsi_set_prefetch.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -155,6 +157,12 @@ def gsi_device_status(h, stream=None) -> int:
 def gsi_destroy(h):
     if h is not None:
         _load().gsi_destroy(h)
+
+
+def gsi_set_prefetch(h, next_h):
+    """Make each one-token call on h prefetch next_h's operands into L2
+    (next_h None removes the link)."""
+    _check(_load().gsi_set_prefetch(h, next_h), "gsi_set_prefetch")
 
 
 def gsi_forward_launch_count(h, T: int) -> int:

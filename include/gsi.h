@@ -120,6 +120,22 @@ gsi_status_t gsi_reserve(gsi_handle_t h, int64_t max_T);
  * In both error cases the outputs are not valid. */
 gsi_status_t gsi_device_status(gsi_handle_t h, cudaStream_t stream);
 
+/* Name the handle of the call that follows each one-token call on h, so that
+ * h's decode kernel prefetches next's V_k, M and correction tiles into L2
+ * while h's call runs.  A one-token call is bound by the latency of its
+ * exchange between CTAs rather than by HBM bandwidth, so a fixed call order
+ * (the linears of a decoder layer, layer after layer) can stream the next
+ * call's operands from HBM in that time, and the next call then stages them
+ * from L2.  This schedules memory traffic only: results are identical with or
+ * without it.  The page has no counterpart; it serves its T = 1 decode path.
+ *   next: a handle on the same device, h itself, or NULL to remove the link.
+ * Applies to handles with k <= 256 (the one-barrier decode kernel); operands
+ * above 64 MiB are not prefetched.  A CUDA graph captured before a change
+ * keeps the link it was captured with.  Destroying either handle removes the
+ * link.  Not thread-safe against concurrent gsi_set_prefetch or gsi_destroy
+ * on the same handles.  Synchronous, host only. */
+gsi_status_t gsi_set_prefetch(gsi_handle_t h, gsi_handle_t next);
+
 /* Release the handle and its workspace (not W, V_k or M).  Synchronises the
  * device.  NULL is ignored. */
 void gsi_destroy(gsi_handle_t h);

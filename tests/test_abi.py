@@ -75,5 +75,6 @@ def test_host_argument_checks(cl):
     assert cl.gsi_reserve(None, 8) == 1
     assert cl.gsi_device_status(None, None) == 1
     assert cl.gsi_forward_launch_count(None, 1) == 0
+    assert cl.gsi_set_prefetch(None, None) == 1
     cl.gsi_destroy(None)
     del h

@@ -238,3 +238,53 @@ def test_handles_of_one_k_with_different_sizes(gsi, orc):
     check_against_oracle(orc, small, X2, y, g, r, what="small")
     big.close()
     small.close()
+
+
+def test_prefetch_links(gsi, orc):
+    """gsi_set_prefetch schedules L2 traffic only: linked handles (a chain, a
+    self link, a link into a k = 512 handle, inside a CUDA graph) keep
+    parity, and destroying a link target leaves its source working."""
+    import torch
+    eps = 0.1
+    cases = [make_case(2304, 768, 256, eps, 6, 71), make_case(512, 1024, 128, eps, 6, 72),
+             make_case(136, 1024, 512, eps, 6, 73)]
+    lins = [GpuLinear(gsi, orc, W, b.V_bits, eps) for (W, b, X) in cases]
+    gsi.gsi_set_prefetch(lins[0].h, lins[1].h)
+    gsi.gsi_set_prefetch(lins[1].h, lins[2].h)
+    gsi.gsi_set_prefetch(lins[2].h, lins[0].h)
+    for lin, (W, b, X) in zip(lins, cases):
+        y, g, r = lin.forward(X, one_by_one=True)
+        check_against_oracle(orc, lin, X, y, g, r, what="linked")
+    # the chain inside a graph, interleaved call by call
+    xs = [to_dev(X) for (_, _, X) in cases]
+    ys = [torch.zeros((6, lin.d_out), dtype=torch.float32, device="cuda") for lin in lins]
+    gs = [torch.zeros((6,), dtype=torch.uint8, device="cuda") for _ in lins]
+    rs = [torch.zeros((6,), dtype=torch.float32, device="cuda") for _ in lins]
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            for t in range(6):
+                for i, lin in enumerate(lins):
+                    gsi.gsi_forward(lin.h, xs[i][t:t + 1], ys[i][t:t + 1], gs[i][t:t + 1],
+                                    rs[i][t:t + 1], s)
+    for rep in range(2):
+        graph.replay()
+        torch.cuda.synchronize()
+        for i, (lin, (W, b, X)) in enumerate(zip(lins, cases)):
+            assert gsi.gsi_device_status(lin.h) == 0
+            check_against_oracle(orc, lin, X, ys[i].cpu().numpy(), gs[i].cpu().numpy(),
+                                 rs[i].cpu().numpy(), what=f"linked graph {rep}")
+    del graph
+    # a self link, then removing a link target
+    gsi.gsi_set_prefetch(lins[0].h, lins[0].h)
+    W, b, X = cases[0]
+    y, g, r = lins[0].forward(X, one_by_one=True)
+    check_against_oracle(orc, lins[0], X, y, g, r, what="self link")
+    gsi.gsi_set_prefetch(lins[0].h, lins[1].h)
+    lins[1].close()
+    y, g, r = lins[0].forward(X, one_by_one=True)
+    check_against_oracle(orc, lins[0], X, y, g, r, what="target destroyed")
+    gsi.gsi_set_prefetch(lins[2].h, None)
+    lins[0].close()
+    lins[2].close()
