@@ -450,6 +450,128 @@ def run_gsi(args, world, rank, local):
         print(json.dumps(out), flush=True)
 
 
+def run_batched(args, world, rank, local):
+    """The batched prefill-style gated linear: T = 512 tokens per call through
+    one 4096 -> 16384 linear (k = 256, eps = 0.10, 154 slow tokens at seeded
+    positions): projection, gate, compaction, gather and the two tcgen05
+    GEMMs.  R replicas of (W, V_k, M) cycle so that the calls stream more than
+    L2 holds."""
+    import torch
+
+    import gsi_inputs as gi
+    from gated_rank_subspace_gsi_gb300 import lib
+    torch.cuda.set_device(local)
+    lib.library()
+    wl = gi.batched_prefill()
+    spec = wl.linears[0]
+    T, n_slow = wl.T, wl.extra["n_slow"]
+    inp = gi.make_linear_inputs(spec, T, n_slow, wl.seed, w_device="cuda")
+    V = torch.from_numpy(inp.basis.V_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    M = torch.empty((spec.d_out, spec.k), dtype=torch.bfloat16, device="cuda")
+    lib.gsi_precompute_M(inp.W, V, M)
+    props = torch.cuda.get_device_properties(local)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
+    w_bytes = spec.d_out * spec.d * 2
+    replicas = max(2, int(math.ceil(4 * l2 / w_bytes)))
+    reps = []
+    for r in range(replicas):
+        Wr = inp.W if r == 0 else inp.W.clone()
+        Vr = V if r == 0 else V.clone()
+        Mr = M if r == 0 else M.clone()
+        torch.cuda.synchronize()
+        reps.append((Wr, Vr, Mr, lib.gsi_create(Wr, Vr, Mr, spec.eps)))
+    x = torch.from_numpy(inp.X_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    y = torch.zeros((T, spec.d_out), dtype=torch.float32, device="cuda")
+    gate = torch.zeros((T,), dtype=torch.uint8, device="cuda")
+    rho = torch.zeros((T,), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+    calls = 2 * replicas
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            for c in range(calls):
+                lib.gsi_forward(reps[c % replicas][3], x, y, gate, rho, stream)
+    replay(graph, stream, max(args.warmup, 3))
+    stream.synchronize()
+    st = lib.gsi_device_status(reps[0][3], stream)
+    if st != 0:
+        raise RuntimeError(f"device status: {lib.gsi_status_string(st)}")
+    if not np.array_equal(gate.cpu().numpy().astype(bool), inp.slow_mask):
+        raise RuntimeError("gates differ from the generated slow/fast mix")
+    steps = max(1, args.steps // 10)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    replay(graph, stream, steps)
+    e1.record(stream)
+    e1.synchronize()
+    torch.cuda.synchronize()
+    barrier(world)
+    ms_local = e0.elapsed_time(e1) / steps
+    clk = clocks.stop()
+    ms = max_over_ranks(ms_local, world)
+    us_call = ms * 1e3 / calls
+    n_fast = T - n_slow
+    nbytes = (T * spec.d * 2 + spec.d * spec.k * 2 + spec.k * spec.k * 4 + spec.d_out * spec.k * 2
+              + w_bytes + T * spec.d_out * 4 + T * 5)
+    flops = 2.0 * (T * spec.d * spec.k + n_fast * spec.k * spec.d_out * 2
+                   + n_slow * spec.d * spec.d_out)
+    peak, peak_kind = hbm_peak()
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            tpk = float(json.load(f)["bf16_tflops"])
+        tpk_kind = "measured bf16 burst"
+    except Exception:
+        tpk, tpk_kind = 1900.0, "fallback bf16 burst"
+    gbs = nbytes / (us_call * 1e-6) / 1e9
+    tfs = flops / (us_call * 1e-6) / 1e12
+    # end to end: pinned host x in, y / gate / rho out, per call
+    Hx = x.cpu().pin_memory()
+    Hy = torch.empty((T, spec.d_out), dtype=torch.float32).pin_memory()
+    Hg = torch.empty((T,), dtype=torch.uint8).pin_memory()
+    Hr = torch.empty((T,), dtype=torch.float32).pin_memory()
+    ge = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(ge, stream=stream):
+            for c in range(calls):
+                lib.gsi_forward_host(reps[c % replicas][3], Hx, Hy, Hg, Hr, stream)
+    ms_e2e = max_over_ranks(time_graph(ge, stream, reps=max(3, steps), warmup=2), world)
+    launches_per_call = lib.gsi_forward_launch_count(reps[0][3], T)
+    out = {
+        "metric": "µs per gated linear call, batched T=512 prefill (4096 -> 16384, k=256, 30% slow)",
+        "value": round(us_call, 3), "unit": "us per gated linear call", "n_gpus": world,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded Gaussian weights, QR basis, activations with set residual ratios)",
+        "impl": "gsi",
+        "config": {"workload": "batched_T512: T=512 tokens per call, W 16384x4096, k=256, "
+                               "eps=0.10, 154 slow / 358 fast tokens",
+                   "calls_per_step": calls, "replicas": replicas,
+                   "l2": f"inputs larger than L2: {replicas} replicas of W/V_k/M "
+                         f"({w_bytes / 2**20:.0f} MiB W each), L2 {l2 / 2**20:.0f} MiB",
+                   "parallelism": "1 GPU" if world == 1 else f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(gbs / peak, 4), "traffic": None, "kernel": "whole call",
+                     "peak_kind": f"{peak_kind} HBM copy", "bytes_per_call": int(nbytes)},
+        "tensor": {"achieved": round(tfs, 1), "peak": tpk, "unit": "TFLOP/s",
+                   "frac": round(tfs / tpk, 4), "peak_kind": tpk_kind,
+                   "flops_per_call": flops},
+        "e2e": {"value": round(ms_e2e * 1e3 / calls, 3), "unit": "us per gated linear call",
+                "h2d_bytes_per_step": calls * T * spec.d * 2,
+                "d2h_bytes_per_step": calls * T * (spec.d_out * 4 + 5),
+                "how": "gsi_forward_host per call (pinned host buffers), graph-captured"},
+        "gpu_launches": steps * calls * launches_per_call,
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
 def run_reference(args, world, rank):
     """The oracle (fp64 C) on the host cores, each step a bounded sample of the
     decode layer workload: 8 tokens x 3 gated linears, slow token included in
@@ -510,6 +632,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gsi", "reference"], default="gsi")
+    ap.add_argument("--workload", choices=["gptj_layer_decode", "batched_T512"],
+                    default="gptj_layer_decode")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prefetch", type=int, default=1,
@@ -524,6 +648,8 @@ def main(argv=None):
     try:
         if args.impl == "reference":
             run_reference(args, world, rank)
+        elif args.workload == "batched_T512":
+            run_batched(args, world, rank, local)
         else:
             run_gsi(args, world, rank, local)
     finally:
