@@ -106,7 +106,7 @@ gsi_status_t gsi_create(const void* W, const void* V_k, const void* M, int64_t d
   // fixed workspace: Gram matrix, decode accumulators, the packed correction
   // tiles and accumulators of the one-barrier kernel, barrier words, status
   h->dec_acc_stride = int(k + 4);
-  const bool want3 = k <= 256;
+  const bool want3 = k >= 64 && k <= 256;
   const size_t gram_b = size_t(k) * k * 4;
   const size_t acc_b = size_t(2) * h->dec_acc_stride * 4;
   const size_t F_b = want3 ? gsi::corr_tiles_elems(int(k)) * 2 : 0;

@@ -1,5 +1,5 @@
 // gsi_decode3.cu -- the T = 1 (decode) path of the GSI gated linear map as one
-// persistent kernel per call with ONE grid-wide exchange (k <= 256).
+// persistent kernel per call with ONE grid-wide exchange (k in {64, 128, 256}).
 //
 // Page: "Technical summary: Gated Subspace Inference for transformer
 // acceleration" [GSI].  Per token x (section 2.1 eq. 1-2, section 2.2):
@@ -13,49 +13,57 @@
 // once g is known, so unlike the explicit residual it needs no second pass
 // over V_k and no second exchange between CTAs.  E is stored once per handle
 // (made in fp64) as its upper 16 x 16 bf16 tiles in MMA operand order
-// (gsi_internal.h); the form is evaluated with warp-level bf16 MMAs against
-// g split into bf16 high and low parts (g = hi + lo to ~2^-17), accumulated
-// in fp32.
+// (gsi_internal.h).
 //
 // Work split.  G co-resident CTAs (at most one per SM); CTA c owns d / G rows
-// of V_k and d_out / G output rows (of M and of W).  Before it waits on the
-// previous kernel (programmatic dependent launch) each CTA starts 1-D bulk
-// copies of its V_k slice, its M slice and F into shared memory: none depends
-// on x, so these reads overlap the previous kernel's tail.
-//   phase 1   partial g_c = V_c^T x_c and ||x_c||^2, added with vector
-//             red.add into one of kCopies accumulator copies (copy c % 8),
-//             which spreads the atomic traffic over 8 addresses per word;
-//             then the grid barrier (release add / acquire poll)
+// of V_k and d_out / G output rows.  Before it waits on the previous kernel
+// (programmatic dependent launch) each CTA loads, with 2-D TMA tensor copies
+// in the 128-byte swizzled layout, its V_k rows and its M rows (64-column
+// blocks, rows rounded up to 16), plus the correction tiles with a 1-D bulk
+// copy: none depends on x, so these reads overlap the previous kernel's tail.
+// All three contractions run on warp-level bf16 MMAs (m16n8k16, fp32
+// accumulation), their A operands read from the swizzled tiles without bank
+// conflicts:
+//   phase 1   partial g_c = V_c^T x_c: A = V_c^T (ldmatrix.trans), B = x_c
+//             (exact in bf16); warp w owns 16 entries of g over all of the
+//             CTA's rows, and adds them with vector red.add into one of
+//             kCopies accumulator copies (copy c % 8, which spreads the atomic
+//             traffic); ||x_c||^2 in fp32; then the grid barrier (release add,
+//             acquire poll)
 //   phase 2   every CTA sums the copies in a fixed order (the same g, bit for
-//             bit, in every CTA, hence the same gate); half of the warps form
-//             g^T E g and g.g (MMA over the correction tiles) while the others
-//             form the speculative fast-path rows M_c g, 8 rows per warp step
-//             (group_dot)
-//   phase 3   thread 0 forms rho and the gate; the CTA stores M_c g, or, on
-//             the rare slow token, streams its rows of W from HBM for W_c x.
+//             bit, in every CTA, hence the same gate) and writes g's bf16
+//             high part and remainder as the B operand of the MMAs below
+//             (g = hi + lo to ~2^-17); then g^T E g over the correction
+//             tiles, and the speculative fast-path rows M_c g (A = M_c rows
+//             by ldmatrix), spread over all warps
+//   phase 3   thread 0 forms rho and the gate in fp32; the CTA stores M_c g,
+//             or, on the rare slow token, streams its rows of W from HBM for
+//             W_c x.
 // With a prefetch link (gsi_set_prefetch) the last warp also issues, right
 // after the barrier, L2 prefetches of its 1 / G share of the next call's
 // V_k, M and correction tiles, so the next call stages them from L2.
 // The accumulators are double-buffered by a launch epoch kept on the device:
 // CTA 0 zeroes the buffer the next launch uses, so no memset is needed and
 // the kernel replays in a CUDA graph.
+#include <cuda.h>
+
 #include <algorithm>
 #include <cfloat>
 
 #include "gsi_device.cuh"
 #include "gsi_internal.h"
+#include "gsi_tc_gemm.h"
 
 namespace gsi {
 namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kCopies = 8;  // accumulator copies of (g, ||x||^2)
+constexpr int kCopies = 8;        // accumulator copies of (g, ||x||^2)
+constexpr int kMaxBoxRows = 256;  // TMA box limit
 
 struct Decode3Args {
   const __nv_bfloat16* W;
-  const __nv_bfloat16* V;
-  const __nv_bfloat16* M;
   const __nv_bfloat16* F;
   const __nv_bfloat16* x;
   float* y;
@@ -63,27 +71,17 @@ struct Decode3Args {
   float* rho;
   int d_out, d;
   float eps;
-  int rows_M, rows_V;
-  int stage_M;     // M slice staged in shared memory (V_k slice and F always are)
-  float* acc;      // [2][kCopies][acc_stride]
-  int acc_stride;  // >= k + 1, multiple of 4
-  uint32_t* bar;   // [0] arrival counter, [1] launch epoch
+  int rows_M, rows_V;  // rows owned per CTA
+  int box_M, box_V;    // TMA box rows (multiples of 16, <= 256)
+  int nbox_M, nbox_V;  // row boxes per CTA (rows staged = nbox x box)
+  float* acc;          // [2][kCopies][acc_stride]
+  int acc_stride;      // >= k + 1, multiple of 4
+  uint32_t* bar;       // [0] arrival counter, [1] launch epoch
   uint32_t* status;
   // operands of the next call to prefetch into L2 (bytes 0: none), each CTA
   // its 1 / G share
   const char* pf[3];
   uint32_t pf_bytes[3];
-};
-
-// Lane geometry: a row of K bf16 values is K / 8 16-byte chunks, one per lane
-// of a row group of LPR = K / 8 lanes (K <= 256, so LPR <= 32).
-template <int K>
-struct Lanes3 {
-  static_assert(K >= 16 && K <= 256 && (K & (K - 1)) == 0, "k in {16, ..., 256}");
-  static constexpr int LPR = K / 8;             // lanes per row
-  static constexpr int RPI = 32 / LPR;          // row groups per warp
-  static constexpr int NB = LPR < 8 ? LPR : 8;  // rows per row group per step
-  static constexpr int RS = RPI * NB;           // rows per warp step
 };
 
 __device__ __forceinline__ void red_release_u32(uint32_t* p, uint32_t v) {
@@ -101,43 +99,34 @@ __device__ __forceinline__ uint32_t dynamic_smem_bytes() {
   return v;
 }
 
-// Dot products of NB rows at once.  Lane li of a row group of LPR lanes holds
-// v[i], its 8-column partial of row i (i < NB).  A butterfly over sub-groups
-// of NB lanes (offsets NB/2 .. 1; each step a lane keeps one half of its rows
-// and sends the other half) leaves lane li the sub-group sum of row li % NB;
-// xor steps over offsets NB .. LPR/2 then add the sub-groups.  Cost:
-// NB - 1 + log2(LPR / NB) shuffles for NB rows.
-template <int LPR, int NB>
-__device__ __forceinline__ float group_dot(float (&v)[NB], int li) {
-#pragma unroll
-  for (int o = NB / 2; o >= 1; o >>= 1) {
-    const bool up = (li & o) != 0;
-#pragma unroll
-    for (int i = 0; i < o; ++i) {
-      const float send = up ? v[i] : v[i + o];
-      const float keep = up ? v[i + o] : v[i];
-      v[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, o);
-    }
-  }
-  float r = v[0];
-#pragma unroll
-  for (int o = NB; o < LPR; o <<= 1) r += __shfl_xor_sync(0xFFFFFFFFu, r, o);
-  return r;
-}
-
 // D += A B for one 16 x 16 (A, row-major) by 16 x 8 (B, column-major) bf16
 // product with fp32 accumulation (registers in the PTX fragment layout).
-__device__ __forceinline__ void mma_16816(float (&d)[4], const uint4& a, const uint2& b) {
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint4& a, uint32_t b0, uint32_t b1) {
   asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
       "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y));
+      : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  const uint32_t l = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
-  const uint32_t h = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
-  return l | (h << 16);
+// Four 8 x 8 bf16 matrices from shared memory (lane l gives the address of row
+// l % 8 of matrix l / 8); register j holds matrix j, optionally transposed.
+__device__ __forceinline__ uint4 ldsm_x4(uint32_t addr) {
+  uint4 r;
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(addr));
+  return r;
+}
+__device__ __forceinline__ uint4 ldsm_x4_trans(uint32_t addr) {
+  uint4 r;
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(addr));
+  return r;
+}
+
+// Shared address of 16-byte chunk `chunk` (0..7) of row `row` in a block of
+// 128-byte rows written by TMA's 128-byte swizzle (block base 1024-aligned).
+__device__ __forceinline__ uint32_t swz(uint32_t block, int row, int chunk) {
+  return block + uint32_t(row) * 128u + (uint32_t(chunk ^ (row & 7)) << 4);
 }
 
 __device__ __forceinline__ float warp_sum_all(float v) {
@@ -146,31 +135,38 @@ __device__ __forceinline__ float warp_sum_all(float v) {
   return v;
 }
 
-// Dynamic shared-memory layout (byte offsets), identical on host and device.
+// Dynamic shared-memory layout (byte offsets from a 1024-aligned base),
+// identical on host and device.  sM / sV: K / 64 column blocks of
+// rows x 128 bytes each (TMA swizzled).
 struct Smem3 {
-  size_t sM, sV, sF, wpart, xs, g, ys, bfrag, total;
+  size_t sM, sV, sF, xb, g, ys, yp, bfrag, total;
 };
 __host__ __device__ inline size_t al3(size_t v, size_t a) { return (v + a - 1) / a * a; }
-__host__ __device__ inline Smem3 smem3_layout(int K, int rows_M, int rows_V, bool stage_M) {
+__host__ __device__ inline Smem3 smem3_layout(int K, int rowsM, int rowsV) {
   Smem3 s;
   size_t o = 0;
-  s.sM = o;    o = al3(o + (stage_M ? size_t(rows_M) * K * 2 : 0), 128);
-  s.sV = o;    o = al3(o + size_t(rows_V) * K * 2, 128);
+  s.sM = o;    o = al3(o + size_t(K / 64) * rowsM * 128, 1024);
+  s.sV = o;    o = al3(o + size_t(K / 64) * rowsV * 128, 1024);
   s.sF = o;    o = al3(o + corr_tiles_elems(K) * 2, 128);
-  s.wpart = o; o = al3(o + size_t(kWarps) * K * 4, 16);
-  s.xs = o;    o = al3(o + size_t(rows_V) * 4, 16);
+  s.xb = o;    o = al3(o + size_t(rowsV) * 2, 16);
   s.g = o;     o = al3(o + size_t(K) * 4, 16);
-  s.ys = o;    o = al3(o + size_t(rows_M) * 4, 16);
+  s.ys = o;    o = al3(o + size_t(rowsM) * 4, 16);
+  s.yp = o;    o = al3(o + size_t(kWarps) * 16 * 4, 16);
   s.bfrag = o; o = al3(o + size_t(K / 16) * 32 * 8, 128);
   s.total = o;
   return s;
 }
+constexpr size_t kSmemSlack = 1024;  // to align the dynamic base to 1024 bytes
 
-template <int K, bool kStageM>
-__global__ void __launch_bounds__(kThreads, 1) gsi_decode3_kernel(Decode3Args a) {
-  using L = Lanes3<K>;
-  extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ uint64_t s_bar;
+template <int K>
+__global__ void __launch_bounds__(kThreads, 1)
+    gsi_decode3_kernel(const __grid_constant__ CUtensorMap tmV,
+                       const __grid_constant__ CUtensorMap tmM, Decode3Args a) {
+  static_assert(K == 64 || K == 128 || K == 256, "k in {64, 128, 256}");
+  constexpr int T16 = K / 16;  // 16-wide blocks of g
+  constexpr int KC = K / 64;   // 64-column (128-byte) blocks of a row
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  __shared__ uint64_t s_bar[2];  // [0] V_k slice, [1] correction tiles and M slice
   __shared__ uint32_t s_epoch;
   __shared__ int s_ok;
   __shared__ float s_sx;
@@ -178,60 +174,78 @@ __global__ void __launch_bounds__(kThreads, 1) gsi_decode3_kernel(Decode3Args a)
   __shared__ float s_rho;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int grp = lane >> 2, tig = lane & 3;
   const int cta = blockIdx.x, G = gridDim.x;
-  const Smem3 lay = smem3_layout(K, a.rows_M, a.rows_V, kStageM);
+  const int rowsM = a.nbox_M * a.box_M, rowsV = a.nbox_V * a.box_V;
+  const Smem3 lay = smem3_layout(K, rowsM, rowsV);
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
   // Launch self-check (uniform over the grid, before any wait): a launch that
-  // does not cover d and d_out, or got less shared memory than its layout,
+  // does not cover d and d_out or got less shared memory than its layout
   // does nothing and reports it.
   if (blockDim.x != kThreads || int64_t(G) * a.rows_M < a.d_out || int64_t(G) * a.rows_V < a.d ||
-      dynamic_smem_bytes() < lay.total || (a.stage_M != 0) != kStageM) {
+      rowsM < a.rows_M || rowsV < a.rows_V || dynamic_smem_bytes() < lay.total + pad) {
     if (cta == 0 && tid == 0) atomicOr(a.status, kStatusBadLaunch);
     return;
   }
+  unsigned char* smem = smem_raw + pad;
+  const uint32_t sbase = raw + pad;
   const int m0 = cta * a.rows_M;
   const int nM = max(0, min(a.d_out, m0 + a.rows_M) - m0);
   const int v0 = cta * a.rows_V;
   const int nV = max(0, min(a.d, v0 + a.rows_V) - v0);
-  const int slot = lane / L::LPR, li = lane % L::LPR;
 
-  __nv_bfloat16* sM = reinterpret_cast<__nv_bfloat16*>(smem + lay.sM);
-  __nv_bfloat16* sV = reinterpret_cast<__nv_bfloat16*>(smem + lay.sV);
   __nv_bfloat16* sF = reinterpret_cast<__nv_bfloat16*>(smem + lay.sF);
-  float* s_wpart = reinterpret_cast<float*>(smem + lay.wpart);  // [warps][K]
-  float* s_xs = reinterpret_cast<float*>(smem + lay.xs);        // [rows_V]
-  float* s_g = reinterpret_cast<float*>(smem + lay.g);          // [K]
-  float* s_ys = reinterpret_cast<float*>(smem + lay.ys);        // [rows_M]
-  uint2* s_bfrag = reinterpret_cast<uint2*>(smem + lay.bfrag);  // [K / 16][32]
+  __nv_bfloat16* s_xb = reinterpret_cast<__nv_bfloat16*>(smem + lay.xb);  // [rowsV]
+  float* s_g = reinterpret_cast<float*>(smem + lay.g);                    // [K]
+  float* s_ys = reinterpret_cast<float*>(smem + lay.ys);                  // [rowsM]
+  float* s_yp = reinterpret_cast<float*>(smem + lay.yp);                  // [kWarps][16]
+  uint2* s_bfrag = reinterpret_cast<uint2*>(smem + lay.bfrag);            // [T16][32]
 
   // ---- prologue: stage this CTA's weights (independent of x) ------------
-  const uint32_t bytes_M = kStageM ? uint32_t(nM) * K * 2 : 0u;
-  const uint32_t bytes_V = uint32_t(nV) * K * 2;
+  const uint32_t box_bytes_M = uint32_t(a.box_M) * 128, box_bytes_V = uint32_t(a.box_V) * 128;
   const uint32_t bytes_F = uint32_t(corr_tiles_elems(K)) * 2;
+  if (tid == 32) {
+    asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmV)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmM)) : "memory");
+  }
   if (tid == 0) {
-    mbar_init(&s_bar, 1);
+    mbar_init(&s_bar[0], 1);
+    mbar_init(&s_bar[1], 1);
     fence_mbar_init();
   }
   __syncthreads();
-  if (tid == 0) {
-    mbar_arrive_expect_tx(&s_bar, bytes_M + bytes_V + bytes_F);
+  // staging issued by warp 1: fetching a tensor map's descriptor stalls the
+  // issuing thread, and thread 0 must reach the dependent-launch wait first
+  // Two completion groups: phase 1 needs only the V_k slice, so it does not
+  // wait for the correction tiles or the (larger) M slice.
+  if (tid == 32) {
+    mbar_arrive_expect_tx(&s_bar[0], KC * a.nbox_V * box_bytes_V);
+    for (int kc = 0; kc < KC; ++kc)
+      for (int b = 0; b < a.nbox_V; ++b)
+        tma_load_2d(smem + lay.sV + size_t(kc) * rowsV * 128 + size_t(b) * box_bytes_V, &tmV,
+                    kc * 64, v0 + b * a.box_V, &s_bar[0]);
+    mbar_arrive_expect_tx(&s_bar[1], KC * a.nbox_M * box_bytes_M + bytes_F);
     constexpr uint32_t kChunk = 32768;
-    const char* gV = reinterpret_cast<const char*>(a.V + size_t(v0) * K);
-    for (uint32_t off = 0; off < bytes_V; off += kChunk)
-      bulk_g2s(reinterpret_cast<char*>(sV) + off, gV + off, min(kChunk, bytes_V - off), &s_bar);
     const char* gF = reinterpret_cast<const char*>(a.F);
     for (uint32_t off = 0; off < bytes_F; off += kChunk)
-      bulk_g2s(reinterpret_cast<char*>(sF) + off, gF + off, min(kChunk, bytes_F - off), &s_bar);
-    const char* gM = reinterpret_cast<const char*>(a.M + size_t(m0) * K);
-    for (uint32_t off = 0; off < bytes_M; off += kChunk)
-      bulk_g2s(reinterpret_cast<char*>(sM) + off, gM + off, min(kChunk, bytes_M - off), &s_bar);
+      bulk_g2s(reinterpret_cast<char*>(sF) + off, gF + off, min(kChunk, bytes_F - off), &s_bar[1]);
+    for (int kc = 0; kc < KC; ++kc)
+      for (int b = 0; b < a.nbox_M; ++b)
+        tma_load_2d(smem + lay.sM + size_t(kc) * rowsM * 128 + size_t(b) * box_bytes_M, &tmM,
+                    kc * 64, m0 + b * a.box_M, &s_bar[1]);
   }
+  // work that needs neither x nor the previous kernel: the zero part of the
+  // B operands (columns 2..7)
+  for (int t = tid; t < T16 * 24; t += kThreads) s_bfrag[(t / 24) * 32 + 8 + t % 24] = make_uint2(0u, 0u);
   pdl_launch_dependents();
   pdl_wait();  // x and this handle's workspace are now safe to touch
 
   // ---- phase 1: x slice, partial g and ||x_c||^2 ---------------------------
   if (tid == 0) s_epoch = ld_cg_u32(a.bar + 1);
-  for (int i = tid; i < nV; i += kThreads) s_xs[i] = bf16_to_f32(a.x[v0 + i]);
-  bool ok = mbar_wait_bounded(&s_bar, 0, a.status);
+  for (int i = tid; i < rowsV; i += kThreads)
+    s_xb[i] = i < nV ? a.x[v0 + i] : __float2bfloat16_rn(0.f);
+  bool ok = mbar_wait_bounded(&s_bar[0], 0, a.status);
   ok = __syncthreads_and(ok) != 0;
   const uint32_t e = s_epoch;
   float* acc = a.acc + size_t(e & 1u) * kCopies * a.acc_stride;
@@ -240,62 +254,88 @@ __global__ void __launch_bounds__(kThreads, 1) gsi_decode3_kernel(Decode3Args a)
     for (int i = tid; i < kCopies * a.acc_stride; i += kThreads) nxt[i] = 0.f;
   }
   const int nVw = ok ? nV : 0;
-  const int nMw = ok ? nM : 0;
-  const __nv_bfloat16* Vs = sV;
-  const __nv_bfloat16* Ms = kStageM ? sM : a.M + size_t(m0) * K;
-  const __nv_bfloat16* Fs = sF;
-  // B operands of the correction MMAs (filled after the barrier): for column
-  // block J, lane l holds rows 2 (l % 4) + {0, 1, 8, 9} of the 16 x 8 block
-  // whose column 0 is the bf16 high part of g_J, column 1 its remainder and
-  // the other columns zero; the zero part is written here
-  constexpr int T16 = K / 16;
-  for (int t = tid; t < T16 * 24; t += kThreads) s_bfrag[(t / 24) * 32 + 8 + t % 24] = make_uint2(0u, 0u);
-  if (warp == kWarps - 1) {  // ||x_c||^2 (x_i^2 is exact in fp32 for bf16 x_i)
-    float sx = 0.f;
-    for (int i = lane; i < nVw; i += 32) sx = fmaf(s_xs[i], s_xs[i], sx);
-    sx = warp_sum_all(sx);
-    if (lane == 0) s_sx = sx;
-  }
-  {
-    float accg[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) accg[j] = 0.f;
-    for (int r = warp * L::RPI + slot; r < nVw; r += kWarps * L::RPI) {
-      const float xi = s_xs[r];
-      const uint4 v = *reinterpret_cast<const uint4*>(Vs + size_t(r) * K + li * 8);
-      float f[8];
-      bf16x8_to_f32(v, f);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) accg[j] = fmaf(f[j], xi, accg[j]);
-    }
-#pragma unroll
-    for (int o = L::LPR; o < 32; o <<= 1)
-#pragma unroll
-      for (int j = 0; j < 8; ++j) accg[j] += __shfl_xor_sync(0xFFFFFFFFu, accg[j], o);
-    if (slot == 0) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) s_wpart[warp * K + li * 8 + j] = accg[j];
-    }
-  }
-  __syncthreads();
   float* my_copy = acc + size_t(cta % kCopies) * a.acc_stride;
   if (nVw > 0) {
-    for (int t = tid; t < K / 4; t += kThreads) {
-      float s4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) s4[q] += s_wpart[w * K + t * 4 + q];
-      red_add_v4_f32(my_copy + t * 4, s4[0], s4[1], s4[2], s4[3]);
+    // warp w: entries [16 mb, 16 mb + 16) of g over row blocks kb = w / T16,
+    // w / T16 + 16 / T16, ...; rows past nV hold x = 0
+    const int mb = warp % T16, kb0 = warp / T16;
+    constexpr int kStep = kWarps / T16;
+    const int nkb = (nVw + 15) / 16;
+    const int j = lane >> 3, rr = lane & 7;
+    const int col = mb * 16 + (j & 1) * 8;  // A rows m = entries of g
+    const uint32_t blk = sbase + uint32_t(lay.sV) + uint32_t(col / 64) * uint32_t(rowsV) * 128u;
+    const int chunk = (col % 64) / 8;
+    const uint32_t* xw = reinterpret_cast<const uint32_t*>(s_xb);
+    float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+    int kb = kb0;
+    for (; kb + kStep < nkb; kb += 2 * kStep) {
+      const uint4 A0 = ldsm_x4_trans(swz(blk, kb * 16 + rr + (j >> 1) * 8, chunk));
+      const uint4 A1 = ldsm_x4_trans(swz(blk, (kb + kStep) * 16 + rr + (j >> 1) * 8, chunk));
+      const uint32_t b00 = grp == 0 ? xw[kb * 8 + tig] : 0u;
+      const uint32_t b01 = grp == 0 ? xw[kb * 8 + 4 + tig] : 0u;
+      const uint32_t b10 = grp == 0 ? xw[(kb + kStep) * 8 + tig] : 0u;
+      const uint32_t b11 = grp == 0 ? xw[(kb + kStep) * 8 + 4 + tig] : 0u;
+      mma_16816(d0, A0, b00, b01);
+      mma_16816(d1, A1, b10, b11);
     }
-    if (tid == 0) red_add_f32(my_copy + K, s_sx);
+    if (kb < nkb) {
+      const uint4 A0 = ldsm_x4_trans(swz(blk, kb * 16 + rr + (j >> 1) * 8, chunk));
+      mma_16816(d0, A0, grp == 0 ? xw[kb * 8 + tig] : 0u, grp == 0 ? xw[kb * 8 + 4 + tig] : 0u);
+    }
+    // column 0 of D: lanes with tig == 0 hold entries grp and grp + 8
+    const float v0g = d0[0] + d1[0], v8g = d0[2] + d1[2];
+    const int src = lane & 16;
+    float u[4], w4[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      u[q] = __shfl_sync(0xFFFFFFFFu, v0g, src + 4 * q);
+      w4[q] = __shfl_sync(0xFFFFFFFFu, v8g, src + 4 * q);
+    }
+    if (kb0 < nkb && (lane & 15) == 0) {
+      const int a0 = mb * 16 + (lane >> 4) * 4;
+      red_add_v4_f32(my_copy + a0, u[0], u[1], u[2], u[3]);
+      red_add_v4_f32(my_copy + a0 + 8, w4[0], w4[1], w4[2], w4[3]);
+    }
+    if (warp == kWarps - 1) {  // ||x_c||^2 (x_i^2 is exact in fp32 for bf16 x_i)
+      float sx = 0.f;
+      for (int i = lane; i < nVw; i += 32) {
+        const float xv = __bfloat162float(s_xb[i]);
+        sx = fmaf(xv, xv, sx);
+      }
+      sx = warp_sum_all(sx);
+      if (lane == 0) red_add_f32(my_copy + K, sx);
+    }
   }
 
   // ---- the grid barrier ---------------------------------------------------
+  // Thread 0 arrives once every warp's atomics are issued; while the arrival
+  // propagates, all threads load their correction tiles into registers, then
+  // thread 0 polls.
   __syncthreads();
+  const uint32_t target = (e + 1u) * uint32_t(G);
+  if (tid == 0) red_release_u32(a.bar, 1u);
+
+  // Tiles (I, J), I <= J, are taken by column: columns J and T16 - 1 - J pair
+  // up (T16 + 1 tiles), the kWpp warps of a pair split its tiles into
+  // segments of at most kSeg.  Step s of a pair: column J1 = p for s <= p
+  // (row I = s), else column J2 = T16 - 1 - p (row I = s - p - 1).
+  constexpr int kPairs = T16 / 2, kWpp = kWarps / kPairs;
+  constexpr int kSeg = (T16 + 1 + kWpp - 1) / kWpp;
+  const int qp = warp / kWpp, qh = warp % kWpp;
+  const int J1 = qp, J2 = T16 - 1 - qp;
+  uint4 fa[kSeg];
+  const bool staged = mbar_wait_bounded(&s_bar[1], 0, a.status);
+  {
+    const uint4* tiles = reinterpret_cast<const uint4*>(sF);
+#pragma unroll
+    for (int st = 0; st < kSeg; ++st) {
+      const int s = qh * kSeg + st;
+      const bool first = s <= J1;
+      const int I = first ? s : s - J1 - 1, J = first ? J1 : J2;
+      fa[st] = s <= T16 ? tiles[corr_tile_index(I, J, T16) * 32 + lane] : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
   if (tid == 0) {
-    const uint32_t target = (e + 1u) * uint32_t(G);
-    red_release_u32(a.bar, 1u);
     int good = 1;
     if (static_cast<int32_t>(ld_acquire_gpu(a.bar) - target) < 0) {
       const uint64_t t0 = globaltimer_ns();
@@ -309,8 +349,8 @@ __global__ void __launch_bounds__(kThreads, 1) gsi_decode3_kernel(Decode3Args a)
     }
     s_ok = good;
   }
-  __syncthreads();
-  ok = ok && s_ok;
+  ok = (__syncthreads_and(staged) != 0) && ok && s_ok;
+  const int nMw = ok ? nM : 0;
   if (warp == kWarps - 1) {
     // this CTA's share of the next call's operands, into L2.  Issued after
     // the barrier, when the rest of this call works from shared memory: the
@@ -327,19 +367,26 @@ __global__ void __launch_bounds__(kThreads, 1) gsi_decode3_kernel(Decode3Args a)
   }
 
   // ---- phase 2: g (same order in every CTA), g^T E g, g.g, speculative M g --
+  float g2 = 0.f;
   for (int t = tid; t < K; t += kThreads) {
     float gsum = 0.f;
 #pragma unroll
     for (int c = 0; c < kCopies; ++c) gsum += ld_cg_f32(acc + size_t(c) * a.acc_stride + t);
     s_g[t] = gsum;
-    // g_t is row kk = t % 16 of column block J = t / 16: register kk / 8,
-    // lane pair (kk % 8) / 2, half kk % 2 of lanes pair (high) and 4 + pair (low)
+    g2 = fmaf(gsum, gsum, g2);
+    // B operands: g_t is row kk = t % 16 of column block t / 16: register
+    // kk / 8, lane pair (kk % 8) / 2, half kk % 2 of lanes pair (high part)
+    // and 4 + pair (remainder)
     const __nv_bfloat16 hi = __float2bfloat16_rn(gsum);
     const __nv_bfloat16 lo = __float2bfloat16_rn(gsum - __bfloat162float(hi));
     const int kk = t & 15, pos = (kk >> 3) * 2 + (kk & 1), pr = (kk & 7) >> 1;
     __nv_bfloat16* bf = reinterpret_cast<__nv_bfloat16*>(s_bfrag + (t >> 4) * 32);
     bf[pr * 4 + pos] = hi;
     bf[(4 + pr) * 4 + pos] = lo;
+  }
+  if (warp < K / 32) {
+    g2 = warp_sum_all(g2);
+    if (lane == 0) s_ggw[warp] = g2;
   }
   if (tid == 0) {
     float sx = 0.f;
@@ -348,63 +395,65 @@ __global__ void __launch_bounds__(kThreads, 1) gsi_decode3_kernel(Decode3Args a)
     s_sx = sx;
   }
   __syncthreads();
-  constexpr int kQuadWarps = T16 > 1 ? T16 / 2 : 1;
-  if (warp < kQuadWarps) {
-    // g^T E g = sum over tiles I <= J of g_I . (F_IJ g_J); this warp takes
-    // row blocks I1 = warp (T16 - warp tiles) and I2 = T16 - 1 - warp
-    // (warp + 1 tiles), T16 + 1 independent MMAs in all
-    constexpr int kSteps = T16 > 1 ? T16 + 1 : 1;
-    const uint4* tiles = reinterpret_cast<const uint4*>(Fs);
-    const int grp = lane >> 2;
-    const int I1 = warp, I2 = T16 - 1 - warp, n1 = T16 - warp;
-    const float g10 = s_g[I1 * 16 + grp], g11 = s_g[I1 * 16 + grp + 8];
-    const float g20 = s_g[I2 * 16 + grp], g21 = s_g[I2 * 16 + grp + 8];
+  {
+    // g^T E g = sum over tiles I <= J of g_I . (F_IJ g_J), one independent
+    // MMA per tile from the registers loaded before the barrier; B = g_J is
+    // loaded once per column
+    const uint2 bJ1 = s_bfrag[J1 * 32 + lane], bJ2 = s_bfrag[J2 * 32 + lane];
     float qsum = 0.f;
 #pragma unroll
-    for (int st = 0; st < kSteps; ++st) {
-      const bool first = st < n1;
-      const int I = first ? I1 : I2;
-      const int J = first ? I1 + st : I2 + (st - n1);
-      float d[4] = {0.f, 0.f, 0.f, 0.f};
-      mma_16816(d, tiles[corr_tile_index(I, J, T16) * 32 + lane], s_bfrag[J * 32 + lane]);
-      // columns 0 (high) and 1 (low) of rows grp and grp + 8 (lanes with
-      // lane % 4 == 0; the other lanes hold the zero columns)
-      qsum = fmaf(first ? g10 : g20, d[0] + d[1], qsum);
-      qsum = fmaf(first ? g11 : g21, d[2] + d[3], qsum);
-    }
-    float ggsum = fmaf(g10, g10, g11 * g11);
-    if (I2 != I1) ggsum = fmaf(g20, g20, fmaf(g21, g21, ggsum));
-    if ((lane & 3) != 0) qsum = ggsum = 0.f;
-    qsum = warp_sum_all(qsum);
-    ggsum = warp_sum_all(ggsum);
-    if (lane == 0) {
-      s_qw[warp] = qsum;
-      s_ggw[warp] = ggsum;
-    }
-  } else {
-    // speculative fast path: this CTA's rows of M g
-    float gl[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) gl[j] = s_g[li * 8 + j];
-    constexpr int kYWarps = kWarps - kQuadWarps;
-    for (int rb = (warp - kQuadWarps) * L::RS; rb < nMw; rb += kYWarps * L::RS) {
-      float v[L::NB];
-#pragma unroll
-      for (int i = 0; i < L::NB; ++i) {
-        const int r = rb + slot * L::NB + i;
-        float dot = 0.f;
-        if (r < nMw) {
-          const uint4 mv = *reinterpret_cast<const uint4*>(Ms + size_t(r) * K + li * 8);
-          float f[8];
-          bf16x8_to_f32(mv, f);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) dot = fmaf(f[j], gl[j], dot);
-        }
-        v[i] = dot;
+    for (int st = 0; st < kSeg; ++st) {
+      const int s = qh * kSeg + st;
+      if (s <= T16) {
+        const bool first = s <= J1;
+        const int I = first ? s : s - J1 - 1;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_16816(d, fa[st], first ? bJ1.x : bJ2.x, first ? bJ1.y : bJ2.y);
+        // columns 0 (high) and 1 (low) of rows grp and grp + 8 (lanes with
+        // tig == 0; the other lanes hold the zero columns)
+        qsum = fmaf(s_g[I * 16 + grp], d[0] + d[1], qsum);
+        qsum = fmaf(s_g[I * 16 + grp + 8], d[2] + d[3], qsum);
       }
-      const float yr = group_dot<L::LPR, L::NB>(v, li);
-      const int r = rb + slot * L::NB + li % L::NB;
-      if (li < L::NB && r < nMw) s_ys[r] = yr;
+    }
+    if (tig != 0) qsum = 0.f;
+    qsum = warp_sum_all(qsum);
+    if (lane == 0) s_qw[warp] = qsum;
+  }
+  {
+    // speculative fast path: rows of M_c g, A = 16 rows of M_c, B = g (hi,
+    // lo); with fewer than 16 row blocks a row block's K / 16 steps are split
+    // over wpr warps, whose partial sums meet in s_yp[warp]
+    const int RB = (nMw + 15) / 16;
+    if (RB > 0) {
+      const int wpr = RB >= kWarps ? 1 : kWarps / RB;
+      const int j = lane >> 3, rr = lane & 7;
+      const uint32_t blkM = sbase + uint32_t(lay.sM);
+      for (int rb = warp / wpr; rb < RB; rb += kWarps / wpr) {
+        float d0[4] = {0.f, 0.f, 0.f, 0.f}, d1[4] = {0.f, 0.f, 0.f, 0.f};
+        const int row = rb * 16 + rr + (j & 1) * 8;
+        int kb = warp % wpr;
+        for (; kb + wpr < T16; kb += 2 * wpr) {
+          const int c0 = kb * 16 + (j >> 1) * 8, c1 = c0 + wpr * 16;
+          const uint4 A0 = ldsm_x4(swz(blkM + uint32_t(c0 / 64) * uint32_t(rowsM) * 128u, row, (c0 % 64) / 8));
+          const uint4 A1 = ldsm_x4(swz(blkM + uint32_t(c1 / 64) * uint32_t(rowsM) * 128u, row, (c1 % 64) / 8));
+          const uint2 b0 = s_bfrag[kb * 32 + lane], b1 = s_bfrag[(kb + wpr) * 32 + lane];
+          mma_16816(d0, A0, b0.x, b0.y);
+          mma_16816(d1, A1, b1.x, b1.y);
+        }
+        if (kb < T16) {
+          const int c0 = kb * 16 + (j >> 1) * 8;
+          const uint4 A0 = ldsm_x4(swz(blkM + uint32_t(c0 / 64) * uint32_t(rowsM) * 128u, row, (c0 % 64) / 8));
+          const uint2 b0 = s_bfrag[kb * 32 + lane];
+          mma_16816(d0, A0, b0.x, b0.y);
+        }
+        if (tig == 0) {
+          const float y0 = (d0[0] + d0[1]) + (d1[0] + d1[1]);
+          const float y8 = (d0[2] + d0[3]) + (d1[2] + d1[3]);
+          float* dst = wpr == 1 ? s_ys + rb * 16 : s_yp + warp * 16;
+          dst[grp] = y0;
+          dst[grp + 8] = y8;
+        }
+      }
     }
   }
   __syncthreads();
@@ -414,10 +463,8 @@ __global__ void __launch_bounds__(kThreads, 1) gsi_decode3_kernel(Decode3Args a)
     // fp32 throughout: the sums' relative error (~1e-7 of ||x||^2) moves rho by
     // ~1e-6 near any practical eps, and fp64 is slow on this part
     float quad = 0.f, gg = 0.f;
-    for (int w = 0; w < kQuadWarps; ++w) {
-      quad += s_qw[w];
-      gg += s_ggw[w];
-    }
+    for (int w = 0; w < kWarps; ++w) quad += s_qw[w];
+    for (int w = 0; w < K / 32; ++w) gg += s_ggw[w];
     const float sx = s_sx;
     float rho;
     if (!(fabsf(sx) <= FLT_MAX)) {
@@ -441,7 +488,20 @@ __global__ void __launch_bounds__(kThreads, 1) gsi_decode3_kernel(Decode3Args a)
   // ---- phase 3: the branch the gate picked ---------------------------------
   if (ok) {
     if (!slow) {
-      for (int r = tid; r < nMw; r += kThreads) a.y[m0 + r] = s_ys[r];
+      // the split the M g phase used: one warp per row block (rows in s_ys)
+      // or wpr warps per row block (partials in s_yp)
+      const int RB = (nMw + 15) / 16;
+      const int wpr = RB >= kWarps ? 1 : kWarps / max(RB, 1);
+      if (wpr == 1) {
+        for (int r = tid; r < nMw; r += kThreads) a.y[m0 + r] = s_ys[r];
+      } else {
+        for (int r = tid; r < nMw; r += kThreads) {
+          const float* src = s_yp + (r / 16) * wpr * 16 + (r % 16);
+          float v = 0.f;
+          for (int q = 0; q < wpr; ++q) v += src[q * 16];
+          a.y[m0 + r] = v;
+        }
+      }
     } else {
       // W_c x, W streamed from HBM, 4 rows per warp
       const int nch = a.d / 8;
@@ -454,17 +514,17 @@ __global__ void __launch_bounds__(kThreads, 1) gsi_decode3_kernel(Decode3Args a)
           const int r = min(rb + q, nM - 1);
           wr[q] = reinterpret_cast<const uint4*>(a.W + size_t(m0 + r) * a.d);
         }
-        int j = lane;
-        for (; j + 32 < nch; j += 64) {
+        int jj = lane;
+        for (; jj + 32 < nch; jj += 64) {
           uint4 w0[4], w1[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            w0[q] = ld_stream_v4(wr[q] + j);
-            w1[q] = ld_stream_v4(wr[q] + j + 32);
+            w0[q] = ld_stream_v4(wr[q] + jj);
+            w1[q] = ld_stream_v4(wr[q] + jj + 32);
           }
           float xa[8], xb[8];
-          bf16x8_to_f32(x4[j], xa);
-          bf16x8_to_f32(x4[j + 32], xb);
+          bf16x8_to_f32(x4[jj], xa);
+          bf16x8_to_f32(x4[jj + 32], xb);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             float f[8];
@@ -476,13 +536,13 @@ __global__ void __launch_bounds__(kThreads, 1) gsi_decode3_kernel(Decode3Args a)
             for (int t = 0; t < 8; ++t) acc4[q] = fmaf(f[t], xb[t], acc4[q]);
           }
         }
-        for (; j < nch; j += 32) {
+        for (; jj < nch; jj += 32) {
           float xa[8];
-          bf16x8_to_f32(x4[j], xa);
+          bf16x8_to_f32(x4[jj], xa);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             float f[8];
-            bf16x8_to_f32(ld_stream_v4(wr[q] + j), f);
+            bf16x8_to_f32(ld_stream_v4(wr[q] + jj), f);
 #pragma unroll
             for (int t = 0; t < 8; ++t) acc4[q] = fmaf(f[t], xa[t], acc4[q]);
           }
@@ -503,31 +563,31 @@ __global__ void __launch_bounds__(kThreads, 1) gsi_decode3_kernel(Decode3Args a)
   }
 }
 
-template <int K>
-const void* kernel3_ptr(bool stage_M) {
-  return stage_M ? reinterpret_cast<const void*>(&gsi_decode3_kernel<K, true>)
-                 : reinterpret_cast<const void*>(&gsi_decode3_kernel<K, false>);
-}
-
-const void* decode3_kernel_for(int64_t k, bool stage_M) {
+const void* decode3_kernel_for(int64_t k) {
   switch (k) {
-    case 16: return kernel3_ptr<16>(stage_M);
-    case 32: return kernel3_ptr<32>(stage_M);
-    case 64: return kernel3_ptr<64>(stage_M);
-    case 128: return kernel3_ptr<128>(stage_M);
-    case 256: return kernel3_ptr<256>(stage_M);
+    case 64: return reinterpret_cast<const void*>(&gsi_decode3_kernel<64>);
+    case 128: return reinterpret_cast<const void*>(&gsi_decode3_kernel<128>);
+    case 256: return reinterpret_cast<const void*>(&gsi_decode3_kernel<256>);
     default: return nullptr;
   }
 }
 
 int acc3_stride(int64_t k) { return int((k + 1 + 3) / 4 * 4); }
 
+// Row boxes for `rows` owned rows: box rows a multiple of 16 and <= 256.
+void row_boxes(int rows, int* box, int* nbox) {
+  const int padded = (rows + 15) / 16 * 16;
+  *nbox = (padded + kMaxBoxRows - 1) / kMaxBoxRows;
+  *box = ((padded + *nbox - 1) / *nbox + 15) / 16 * 16;
+}
+
 }  // namespace
 
 size_t decode3_acc_floats(int64_t k) { return size_t(2) * kCopies * acc3_stride(k); }
 
 gsi_status_t decode3_configure(gsi_handle* h) {
-  if (!decode3_kernel_for(h->k, true)) return GSI_ERR_UNSUPPORTED_SHAPE;
+  const void* fn = decode3_kernel_for(h->k);
+  if (!fn) return GSI_ERR_UNSUPPORTED_SHAPE;
   int max_optin = 0;
   if (cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device) != cudaSuccess)
     return GSI_ERR_CUDA;
@@ -535,20 +595,17 @@ gsi_status_t decode3_configure(gsi_handle* h) {
   const int G = int(std::max<int64_t>(1, std::min<int64_t>(h->num_sms, rows_hint)));
   const int rows_M = int((h->d_out + G - 1) / G);
   const int rows_V = int((h->d + G - 1) / G);
+  int box_M, nbox_M, box_V, nbox_V;
+  row_boxes(rows_M, &box_M, &nbox_M);
+  row_boxes(rows_V, &box_V, &nbox_V);
   const int K = int(h->k);
-  // Both variants of a k have the same static shared memory.
   cudaFuncAttributes fa;
-  if (cudaFuncGetAttributes(&fa, decode3_kernel_for(h->k, true)) != cudaSuccess) return GSI_ERR_CUDA;
+  if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return GSI_ERR_CUDA;
   const int fn_limit = max_optin - int(fa.sharedSizeBytes);
-  // V_k slice and F are always staged; the M slice too when it fits (else it
-  // is read from global memory after the barrier).
-  const bool stage_M = smem3_layout(K, rows_M, rows_V, true).total <= size_t(fn_limit);
-  const size_t smem = smem3_layout(K, rows_M, rows_V, stage_M).total;
+  const size_t smem = smem3_layout(K, nbox_M * box_M, nbox_V * box_V).total + kSmemSlack;
   if (smem > size_t(fn_limit)) return GSI_ERR_UNSUPPORTED_SHAPE;
-  const void* fn = decode3_kernel_for(h->k, stage_M);
   // The limit belongs to the kernel function, shared by every handle with
   // this k: raise it to the device maximum once, never per handle.
-  if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return GSI_ERR_CUDA;
   if (fa.maxDynamicSharedSizeBytes < fn_limit &&
       cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, fn_limit) != cudaSuccess)
     return GSI_ERR_CUDA;
@@ -557,10 +614,16 @@ gsi_status_t decode3_configure(gsi_handle* h) {
     return GSI_ERR_CUDA;
   // The CTAs wait on one another: all of them must fit at once.
   if (per_sm < 1 || int64_t(per_sm) * h->num_sms < G) return GSI_ERR_UNSUPPORTED_SHAPE;
+  if (!tma_encode_bf16_2d(h->dec3_tmaps[0], h->V, uint64_t(h->d), uint64_t(h->k), uint32_t(box_V), 64) ||
+      !tma_encode_bf16_2d(h->dec3_tmaps[1], h->M, uint64_t(h->d_out), uint64_t(h->k), uint32_t(box_M), 64))
+    return GSI_ERR_CUDA;
   h->dec3_grid = G;
   h->dec3_rows_M = rows_M;
   h->dec3_rows_V = rows_V;
-  h->dec3_stage_M = stage_M;
+  h->dec3_box_M = box_M;
+  h->dec3_nbox_M = nbox_M;
+  h->dec3_box_V = box_V;
+  h->dec3_nbox_V = nbox_V;
   h->dec3_smem = smem;
   return GSI_OK;
 }
@@ -569,8 +632,6 @@ gsi_status_t decode3_launch(gsi_handle* h, const void* x, float* y, uint8_t* gat
                             cudaStream_t s) {
   Decode3Args a;
   a.W = h->W;
-  a.V = h->V;
-  a.M = h->M;
   a.F = h->dec3_F;
   a.x = static_cast<const __nv_bfloat16*>(x);
   a.y = y;
@@ -581,7 +642,10 @@ gsi_status_t decode3_launch(gsi_handle* h, const void* x, float* y, uint8_t* gat
   a.eps = h->eps;
   a.rows_M = h->dec3_rows_M;
   a.rows_V = h->dec3_rows_V;
-  a.stage_M = h->dec3_stage_M ? 1 : 0;
+  a.box_M = h->dec3_box_M;
+  a.box_V = h->dec3_box_V;
+  a.nbox_M = h->dec3_nbox_M;
+  a.nbox_V = h->dec3_nbox_V;
   a.acc = h->dec3_acc;
   a.acc_stride = acc3_stride(h->k);
   a.bar = h->dec3_bar;
@@ -612,10 +676,15 @@ gsi_status_t decode3_launch(gsi_handle* h, const void* x, float* y, uint8_t* gat
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  const void* fn = decode3_kernel_for(h->k, h->dec3_stage_M);
-  if (!fn) return GSI_ERR_UNSUPPORTED_SHAPE;
-  void* args[] = {&a};
-  return cudaLaunchKernelExC(&cfg, fn, args) == cudaSuccess ? GSI_OK : GSI_ERR_CUDA;
+  const CUtensorMap* maps = reinterpret_cast<const CUtensorMap*>(h->dec3_tmaps);
+  cudaError_t err;
+  switch (h->k) {
+    case 64: err = cudaLaunchKernelEx(&cfg, gsi_decode3_kernel<64>, maps[0], maps[1], a); break;
+    case 128: err = cudaLaunchKernelEx(&cfg, gsi_decode3_kernel<128>, maps[0], maps[1], a); break;
+    case 256: err = cudaLaunchKernelEx(&cfg, gsi_decode3_kernel<256>, maps[0], maps[1], a); break;
+    default: return GSI_ERR_UNSUPPORTED_SHAPE;
+  }
+  return err == cudaSuccess ? GSI_OK : GSI_ERR_CUDA;
 }
 
 }  // namespace gsi

@@ -123,6 +123,19 @@ __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem,
       : "memory");
 }
 
+// 2-D tiled TMA load of one box of `map` at coordinates (c0 inner, c1 outer)
+// into shared memory, completing on `bar` via its transaction count.  c0 x the
+// element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* map, int c0, int c1,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];"
+      :: "r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1),
+         "r"(smem_addr(bar))
+      : "memory");
+}
+
 // ---- bf16 helpers ------------------------------------------------------
 __device__ __forceinline__ void bf16x8_to_f32(const uint4& v, float (&f)[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};

@@ -30,11 +30,12 @@ struct gsi_handle {
   size_t dec_smem = 0;       // dynamic shared memory bytes
   bool use_pdl = true;       // programmatic dependent launch between kernels
 
-  // ---- one-barrier decode kernel (k <= 256), used when it configures -----
+  // ---- one-barrier decode kernel (k in {64, 128, 256}), used when it fits --
   bool dec3_ok = false;
   int dec3_grid = 0, dec3_rows_M = 0, dec3_rows_V = 0;
-  bool dec3_stage_M = false;        // M slice staged (V_k slice and F always are)
+  int dec3_box_M = 0, dec3_nbox_M = 0, dec3_box_V = 0, dec3_nbox_V = 0;  // TMA row boxes
   size_t dec3_smem = 0;
+  alignas(64) unsigned char dec3_tmaps[2][128] = {};  // TMA maps of V_k and M (CUtensorMap)
   __nv_bfloat16* dec3_F = nullptr;  // correction tiles (corr_tiles_elems(k))
   float* dec3_acc = nullptr;        // decode3_acc_floats(k) fp32 accumulators
   uint32_t* dec3_bar = nullptr;     // [0] arrival counter, [1] launch epoch
@@ -106,7 +107,7 @@ gsi_status_t decode_configure(gsi_handle* h);
 gsi_status_t decode_launch(gsi_handle* h, const void* x, float* y, uint8_t* gate,
                            float* rho, cudaStream_t s);
 
-// One-barrier decode path (gsi_decode3.cu), k <= 256
+// One-barrier decode path (gsi_decode3.cu), k in {64, 128, 256}
 size_t decode3_acc_floats(int64_t k);
 gsi_status_t decode3_configure(gsi_handle* h);
 gsi_status_t decode3_launch(gsi_handle* h, const void* x, float* y, uint8_t* gate,

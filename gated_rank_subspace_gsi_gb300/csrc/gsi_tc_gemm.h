@@ -25,6 +25,12 @@ struct TcGemmArgs {
   uint32_t* status;
 };
 
+// Encode a TMA map (CUtensorMap, 128 bytes at `map`) of a row-major bf16
+// rows x cols tensor with a box_rows x box_cols box, 128-byte swizzle and zero
+// fill outside the tensor.  False if the driver rejects it.
+bool tma_encode_bf16_2d(void* map, const void* base, uint64_t rows, uint64_t cols,
+                        uint32_t box_rows, uint32_t box_cols);
+
 // Build the TMA tensor maps of a handle (after its workspace is bound).
 gsi_status_t tc_gemm_prepare(gsi_handle* h);
 // One launch computing both GEMMs for T tokens.

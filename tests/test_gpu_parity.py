@@ -20,6 +20,9 @@ pytestmark = pytest.mark.gpu
 # and the decode kernel's per-CTA slices; every supported k.
 SHAPES = [(24, 64, 16), (40, 136, 32), (96, 264, 64), (200, 512, 128), (2304, 768, 256),
           (136, 1024, 512), (1000, 4104, 256)]
+# One-token shapes besides: 10 row blocks of M per CTA (one warp each) and 19
+# row blocks staged as two TMA row boxes.
+DECODE_SHAPES = SHAPES + [(22800, 1024, 256), (45600, 1024, 128)]
 
 
 def spread_rho(eps: float, T: int, seed: int) -> np.ndarray:
@@ -59,7 +62,7 @@ def test_precompute_M(gsi, orc, d_out, d, k):
     lin.close()
 
 
-@pytest.mark.parametrize("d_out,d,k", SHAPES)
+@pytest.mark.parametrize("d_out,d,k", DECODE_SHAPES)
 def test_decode_T1(gsi, orc, d_out, d, k):
     eps = 0.10
     W, basis, X = make_case(d_out, d, k, eps, 14, 2)
