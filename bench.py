@@ -168,12 +168,12 @@ def kernel_traffic():
 # the workload
 # --------------------------------------------------------------------------
 
-def build_layer(n_tokens: int, replicas: int, prefetch: int = 1):
-    """Device tensors and handles of the GPT-J decode layer workload.  With
-    prefetch = p > 0, each handle names the handle of the call p places after
-    it in the step's order (linear i of replica r, then linear i + 1, the
-    last linear then the first of replica r + 1), so each call streams that
-    call's operands into L2."""
+def build_layer(n_tokens: int, replicas: int):
+    """Device tensors, handles and groups of the GPT-J decode layer workload:
+    per replica r the three handles and one group of out_proj and fc_out
+    (their inputs, the attention output and the GELU of fc_in, do not depend
+    on each other: GPT-J's parallel residual).  Prefetch links are set by
+    link_schedule()."""
     import torch
 
     import gsi_inputs as gi
@@ -202,12 +202,33 @@ def build_layer(n_tokens: int, replicas: int, prefetch: int = 1):
                           y=torch.zeros((n_tokens, spec.d_out), dtype=torch.float32, device="cuda"),
                           gate=torch.zeros((n_tokens,), dtype=torch.uint8, device="cuda"),
                           rho=torch.zeros((n_tokens,), dtype=torch.float32, device="cuda")))
-    if prefetch > 0:
+    groups = [lib.gsi_group_create([layer[1]["reps"][r][2], layer[2]["reps"][r][2]])
+              for r in range(replicas)]
+    torch.cuda.synchronize()
+    return wl, slow, layer, groups
+
+
+def link_schedule(layer, groups, replicas, schedule: str, prefetch: int):
+    """Prefetch links in the order the schedule issues its launches: each
+    launch streams the operands of the launch `prefetch` places later into
+    L2 (0: no links).  sequential: linear 0, 1, 2 of replica r, then replica
+    r + 1; grouped: linear 0 of replica r, then the group of replica r."""
+    from gated_rank_subspace_gsi_gb300 import lib
+    for L in layer:
+        for (_, _, h) in L["reps"]:
+            lib.gsi_set_prefetch(h, None)
+    for g in groups:
+        lib.gsi_group_set_prefetch(g, None)
+    if prefetch <= 0:
+        return
+    if schedule == "sequential":
         order = [layer[li]["reps"][r][2] for r in range(replicas) for li in range(len(layer))]
         for i, h in enumerate(order):
             lib.gsi_set_prefetch(h, order[(i + prefetch) % len(order)])
-    torch.cuda.synchronize()
-    return wl, slow, layer
+        return
+    for r in range(replicas):
+        lib.gsi_set_prefetch_group(layer[0]["reps"][r][2], groups[r])
+        lib.gsi_group_set_prefetch(groups[r], layer[0]["reps"][(r + 1) % replicas][2])
 
 
 def correction_bytes(k: int) -> int:
@@ -232,7 +253,12 @@ def step_bytes(layer, slow) -> float:
     return float(sum(linear_bytes(L["spec"], len(slow), n_slow) for L in layer))
 
 
-def capture_step(layer, n_tokens, replicas, stream, handles_subset=None, host=None):
+def capture_step(layer, n_tokens, replicas, stream, handles_subset=None, host=None,
+                 groups=None):
+    """One step in a CUDA graph.  With `groups` (the grouped schedule) each
+    token is a call on linear 0 and one launch of its replica's group;
+    otherwise one call per linear in `handles_subset` (all by default), in
+    order, on device buffers or (host) through gsi_forward_host."""
     import torch
 
     from gated_rank_subspace_gsi_gb300 import lib
@@ -242,6 +268,18 @@ def capture_step(layer, n_tokens, replicas, stream, handles_subset=None, host=No
         with torch.cuda.graph(g, stream=stream):
             for t in range(n_tokens):
                 r = t % replicas
+                if groups is not None:
+                    sl = slice(t, t + 1)
+                    if 0 in idx:
+                        L0 = layer[0]
+                        lib.gsi_forward(L0["reps"][r][2], L0["x"][sl], L0["y"][sl], L0["gate"][sl],
+                                        L0["rho"][sl], stream)
+                    if 1 in idx or 2 in idx:
+                        m = layer[1:]
+                        lib.gsi_group_forward(groups[r], [L["x"][sl] for L in m],
+                                              [L["y"][sl] for L in m], [L["gate"][sl] for L in m],
+                                              [L["rho"][sl] for L in m], stream)
+                    continue
                 for li in idx:
                     L = layer[li]
                     h = L["reps"][r][2]
@@ -319,12 +357,19 @@ def run_gsi(args, world, rank, local):
     l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
     per_token = 32.44e6
     replicas = max(16, int(math.ceil(4 * l2 / per_token)))
-    wl, slow, layer = build_layer(n_tokens, replicas, prefetch=args.prefetch)
+    wl, slow, layer, groups = build_layer(n_tokens, replicas)
     nbytes = step_bytes(layer, slow)
     n_lin = n_tokens * len(layer)
     stream = torch.cuda.Stream()
+    grouped = args.schedule == "grouped"
+    other = "sequential" if grouped else "grouped"
 
-    graph = capture_step(layer, n_tokens, replicas, stream)
+    # the other schedule's graph first (links are captured with the graph)
+    link_schedule(layer, groups, replicas, other, args.prefetch)
+    graph_other = None if args.no_extras else capture_step(
+        layer, n_tokens, replicas, stream, groups=groups if not grouped else None)
+    link_schedule(layer, groups, replicas, args.schedule, args.prefetch)
+    graph = capture_step(layer, n_tokens, replicas, stream, groups=groups if grouped else None)
     for L in layer:
         L["gate"].fill_(7)
     torch.cuda.synchronize()
@@ -358,16 +403,24 @@ def run_gsi(args, world, rank, local):
     us_per_lin = ms * 1e3 / n_lin
     gbs = nbytes / (ms * 1e-3) / 1e9
     peak, peak_kind = hbm_peak()
+    schedules = {args.schedule: round(us_per_lin, 4)}
+    if graph_other is not None:
+        ms_o = max_over_ranks(time_graph(graph_other, stream, reps=max(3, args.steps // 10),
+                                         warmup=2), world)
+        schedules[other] = round(ms_o * 1e3 / n_lin, 4)
+        del graph_other
 
-    # ---- per-linear breakdown (each linear alone, 512 calls per graph) ----
+    # ---- per-launch breakdown: each linear (or the group) alone ----------
     per = {}
-    for li, L in enumerate(layer if not args.no_extras else []):
-        g1 = capture_step(layer, n_tokens, replicas, stream, handles_subset=[li])
+    parts = [([0], "qkv_fc_in"), ([1, 2], "out_proj+fc_out (one grouped launch)")] if grouped \
+        else [([li], L["spec"].name) for li, L in enumerate(layer)]
+    for subset, name in (parts if not args.no_extras else []):
+        g1 = capture_step(layer, n_tokens, replicas, stream, handles_subset=subset,
+                          groups=groups if grouped else None)
         ms1 = time_graph(g1, stream, reps=5, warmup=2)
-        s = L["spec"]
-        b1 = linear_bytes(s, n_tokens, int(slow.sum()))
-        per[s.name] = dict(us_per_call=round(ms1 * 1e3 / n_tokens, 3),
-                           gbs=round(b1 / (ms1 * 1e-3) / 1e9, 1))
+        b1 = sum(linear_bytes(layer[li]["spec"], n_tokens, int(slow.sum())) for li in subset)
+        per[name] = dict(us_per_launch=round(ms1 * 1e3 / n_tokens, 3),
+                         gbs=round(b1 / (ms1 * 1e-3) / 1e9, 1))
         del g1
 
     # ---- end to end: host buffers through gsi_forward_host ---------------
@@ -384,13 +437,14 @@ def run_gsi(args, world, rank, local):
         h2d += n_tokens * s.d * 2
         d2h += n_tokens * (s.d_out * 4 + 1 + 4)
     if host:
+        link_schedule(layer, groups, replicas, "sequential", args.prefetch)
         ge = capture_step(layer, n_tokens, replicas, stream, host=host)
         ms_e2e = max_over_ranks(time_graph(ge, stream, reps=max(3, args.steps // 10), warmup=2),
                                 world)
         if not np.array_equal(host[0]["gate"].numpy().astype(bool), slow):
             raise RuntimeError("end-to-end gates differ from the generated mix")
 
-    launches = args.steps * n_lin
+    launches = args.steps * n_tokens * (2 if grouped else len(layer))
     out = {
         "metric": METRIC,
         "value": round(us_per_lin, 4),
@@ -409,6 +463,9 @@ def run_gsi(args, world, rank, local):
             "workload": "gptj_layer_decode: 512 sequential T=1 tokens x 3 gated linears "
                         "(4096->28672 stacked qkv+fc_in, 4096->4096 out_proj, 16384->4096 fc_out), "
                         "k=256, eps=0.10, 1 slow token (0.2%)",
+            "schedule": ("grouped: per token the qkv+fc_in call, then out_proj and fc_out in "
+                         "one launch (independent inputs: parallel residual)") if grouped
+                        else "sequential: three launches per token",
             "gated_linears_per_step": n_lin,
             "replicas": replicas,
             "l2": f"inputs larger than L2: {replicas} replicas x 32.4 MB per token, "
@@ -420,7 +477,8 @@ def run_gsi(args, world, rank, local):
         "frac_of_measured_hbm": round(gbs / peak, 4),
         "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4),
         "us_per_layer": round(ms * 1e3 / n_tokens, 3),
-        "per_linear": per,
+        "per_launch": per,
+        "schedules_us_per_linear": schedules,
         "algorithmic_bytes_per_step": int(nbytes),
         "roofline": {
             "bound": "hbm",
@@ -439,7 +497,8 @@ def run_gsi(args, world, rank, local):
             "unit": UNIT,
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
-            "how": "gsi_forward_host per call (pinned host x in, y/gate/rho out), graph-captured step",
+            "how": "gsi_forward_host per call (pinned host x in, y/gate/rho out), three calls per "
+                   "token, graph-captured step",
         },
         "gpu_launches": launches,
         "clocks": clk,
@@ -636,6 +695,8 @@ def main(argv=None):
                     default="gptj_layer_decode")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--schedule", choices=["grouped", "sequential"], default="grouped",
+                    help="grouped: out_proj and fc_out of a token in one launch")
     ap.add_argument("--prefetch", type=int, default=1,
                     help="each call prefetches into L2 the operands of the call this many "
                          "places later (0: none)")

@@ -223,16 +223,97 @@ gsi_status_t gsi_device_status(gsi_handle_t h, cudaStream_t stream) {
   return (word & gsi::kStatusTimeout) ? GSI_ERR_TIMEOUT : GSI_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+template <typename T>
+void erase_value(std::vector<T*>& v, T* x) {
+  v.erase(std::remove(v.begin(), v.end(), x), v.end());
+}
+
+// Remove h's prefetch target (a handle or a group), both directions.
+void unlink_target(gsi_handle* h) {
+  if (h->pf_next) erase_value(h->pf_next->pf_from, h);
+  if (h->pf_group) erase_value(h->pf_group->pf_from, h);
+  h->pf_next = nullptr;
+  h->pf_group = nullptr;
+}
+
+}  // namespace
+
+extern "C" {
+
 gsi_status_t gsi_set_prefetch(gsi_handle_t h, gsi_handle_t next) {
   if (!h) return GSI_ERR_INVALID_ARG;
   if (next && next->device != h->device) return GSI_ERR_INVALID_ARG;
-  if (h->pf_next) {
-    auto& from = h->pf_next->pf_from;
-    from.erase(std::remove(from.begin(), from.end(), h), from.end());
-  }
+  unlink_target(h);
   h->pf_next = next;
   if (next) next->pf_from.push_back(h);
   return GSI_OK;
+}
+
+gsi_status_t gsi_set_prefetch_group(gsi_handle_t h, gsi_group_t next) {
+  if (!h) return GSI_ERR_INVALID_ARG;
+  if (next && next->device != h->device) return GSI_ERR_INVALID_ARG;
+  unlink_target(h);
+  h->pf_group = next;
+  if (next) next->pf_from.push_back(h);
+  return GSI_OK;
+}
+
+gsi_status_t gsi_group_create(int n, const gsi_handle_t* handles, gsi_group_t* out) {
+  if (!out) return GSI_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!handles || n < 1 || n > gsi::kMaxGroup) return GSI_ERR_INVALID_ARG;
+  for (int m = 0; m < n; ++m) {
+    if (!handles[m]) return GSI_ERR_INVALID_ARG;
+    for (int j = 0; j < m; ++j)
+      if (handles[j] == handles[m]) return GSI_ERR_INVALID_ARG;  // one workspace, one call
+  }
+  for (int m = 0; m < n; ++m)
+    if (!handles[m]->dec3_ok || handles[m]->k != handles[0]->k ||
+        handles[m]->device != handles[0]->device)
+      return GSI_ERR_UNSUPPORTED_SHAPE;
+  gsi_group* g = new (std::nothrow) gsi_group();
+  if (!g) return GSI_ERR_NOMEM;
+  g->n = n;
+  g->k = int(handles[0]->k);
+  g->device = handles[0]->device;
+  for (int m = 0; m < n; ++m) g->h[m] = handles[m];
+  const gsi_status_t st = gsi::group_configure(g);
+  if (st != GSI_OK) {
+    delete g;
+    return st;
+  }
+  *out = g;
+  return GSI_OK;
+}
+
+gsi_status_t gsi_group_forward(gsi_group_t g, const void* const* x, float* const* y,
+                               uint8_t* const* gate, float* const* rho, cudaStream_t stream) {
+  if (!g || !x || !y) return GSI_ERR_INVALID_ARG;
+  for (int m = 0; m < g->n; ++m)
+    if (!x[m] || !y[m] || !gsi::aligned16(x[m]) || !gsi::aligned16(y[m])) return GSI_ERR_INVALID_ARG;
+  return gsi::group_launch(g, x, y, gate, rho, stream);
+}
+
+gsi_status_t gsi_group_set_prefetch(gsi_group_t g, gsi_handle_t next) {
+  if (!g) return GSI_ERR_INVALID_ARG;
+  if (next && next->device != g->device) return GSI_ERR_INVALID_ARG;
+  if (g->pf_next) erase_value(g->pf_next->pf_from_groups, g);
+  g->pf_next = next;
+  if (next) next->pf_from_groups.push_back(g);
+  return GSI_OK;
+}
+
+void gsi_group_destroy(gsi_group_t g) {
+  if (!g) return;
+  cudaDeviceSynchronize();
+  for (gsi_handle* p : g->pf_from)
+    if (p->pf_group == g) p->pf_group = nullptr;
+  if (g->pf_next) erase_value(g->pf_next->pf_from_groups, g);
+  delete g;
 }
 
 void gsi_destroy(gsi_handle_t h) {
@@ -241,10 +322,10 @@ void gsi_destroy(gsi_handle_t h) {
   // unlink prefetch links in both directions before the memory goes away
   for (gsi_handle* p : h->pf_from)
     if (p->pf_next == h) p->pf_next = nullptr;
-  if (h->pf_next && h->pf_next != h) {
-    auto& from = h->pf_next->pf_from;
-    from.erase(std::remove(from.begin(), from.end(), h), from.end());
-  }
+  for (gsi_group* g : h->pf_from_groups)
+    if (g->pf_next == h) g->pf_next = nullptr;
+  if (h->pf_next && h->pf_next != h) erase_value(h->pf_next->pf_from, h);
+  if (h->pf_group) erase_value(h->pf_group->pf_from, h);
   if (h->ws) cudaFree(h->ws);
   if (h->bws) cudaFree(h->bws);
   if (h->st_dev) cudaFree(h->st_dev);

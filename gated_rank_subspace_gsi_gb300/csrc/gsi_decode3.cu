@@ -49,6 +49,7 @@
 
 #include <algorithm>
 #include <cfloat>
+#include <cstring>
 
 #include "gsi_device.cuh"
 #include "gsi_internal.h"
@@ -61,6 +62,7 @@ constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kCopies = 8;        // accumulator copies of (g, ||x||^2)
 constexpr int kMaxBoxRows = 256;  // TMA box limit
+constexpr int kMaxPf = 12;        // prefetch ranges (3 per handle, up to 4 handles)
 
 struct Decode3Args {
   const __nv_bfloat16* W;
@@ -76,12 +78,24 @@ struct Decode3Args {
   int nbox_M, nbox_V;  // row boxes per CTA (rows staged = nbox x box)
   float* acc;          // [2][kCopies][acc_stride]
   int acc_stride;      // >= k + 1, multiple of 4
-  uint32_t* bar;       // [0] arrival counter, [1] launch epoch
+  uint32_t* bar;       // [0] arrival counter, [1] launch epoch, [2] counter base
   uint32_t* status;
-  // operands of the next call to prefetch into L2 (bytes 0: none), each CTA
-  // its 1 / G share
-  const char* pf[3];
-  uint32_t pf_bytes[3];
+  // operands of the next call to prefetch into L2 (bytes 0: none); CTA
+  // pf_part0 + c of pf_parts prefetches its share of each range
+  const char* pf[kMaxPf];
+  uint32_t pf_bytes[kMaxPf];
+  int pf_part0, pf_parts;
+};
+
+// Up to kMaxGroup one-token calls in one launch (gsi_group_forward): member m
+// owns CTAs [cta0[m], cta0[m + 1]).
+struct GroupMaps {
+  CUtensorMap m[2 * kMaxGroup];  // V_k and M maps of each member
+};
+struct GroupArgs {
+  Decode3Args a[kMaxGroup];
+  int cta0[kMaxGroup + 1];
+  int n;
 };
 
 __device__ __forceinline__ void red_release_u32(uint32_t* p, uint32_t v) {
@@ -158,16 +172,16 @@ __host__ __device__ inline Smem3 smem3_layout(int K, int rowsM, int rowsV) {
 }
 constexpr size_t kSmemSlack = 1024;  // to align the dynamic base to 1024 bytes
 
+// One one-token call on CTAs 0..G-1 of its own (cta = this CTA's index).
 template <int K>
-__global__ void __launch_bounds__(kThreads, 1)
-    gsi_decode3_kernel(const __grid_constant__ CUtensorMap tmV,
-                       const __grid_constant__ CUtensorMap tmM, Decode3Args a) {
+__device__ __forceinline__ void decode3_body(const CUtensorMap* tmV, const CUtensorMap* tmM,
+                                             const Decode3Args& a, const int cta, const int G) {
   static_assert(K == 64 || K == 128 || K == 256, "k in {64, 128, 256}");
   constexpr int T16 = K / 16;  // 16-wide blocks of g
   constexpr int KC = K / 64;   // 64-column (128-byte) blocks of a row
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   __shared__ uint64_t s_bar[2];  // [0] V_k slice, [1] correction tiles and M slice
-  __shared__ uint32_t s_epoch;
+  __shared__ uint32_t s_epoch, s_base;
   __shared__ int s_ok;
   __shared__ float s_sx;
   __shared__ float s_qw[kWarps], s_ggw[kWarps];
@@ -175,7 +189,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int grp = lane >> 2, tig = lane & 3;
-  const int cta = blockIdx.x, G = gridDim.x;
   const int rowsM = a.nbox_M * a.box_M, rowsV = a.nbox_V * a.box_V;
   const Smem3 lay = smem3_layout(K, rowsM, rowsV);
   const uint32_t raw = smem_addr(smem_raw);
@@ -206,8 +219,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t box_bytes_M = uint32_t(a.box_M) * 128, box_bytes_V = uint32_t(a.box_V) * 128;
   const uint32_t bytes_F = uint32_t(corr_tiles_elems(K)) * 2;
   if (tid == 32) {
-    asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmV)) : "memory");
-    asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmM)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(tmV)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(tmM)) : "memory");
   }
   if (tid == 0) {
     mbar_init(&s_bar[0], 1);
@@ -223,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_arrive_expect_tx(&s_bar[0], KC * a.nbox_V * box_bytes_V);
     for (int kc = 0; kc < KC; ++kc)
       for (int b = 0; b < a.nbox_V; ++b)
-        tma_load_2d(smem + lay.sV + size_t(kc) * rowsV * 128 + size_t(b) * box_bytes_V, &tmV,
+        tma_load_2d(smem + lay.sV + size_t(kc) * rowsV * 128 + size_t(b) * box_bytes_V, tmV,
                     kc * 64, v0 + b * a.box_V, &s_bar[0]);
     mbar_arrive_expect_tx(&s_bar[1], KC * a.nbox_M * box_bytes_M + bytes_F);
     constexpr uint32_t kChunk = 32768;
@@ -232,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bulk_g2s(reinterpret_cast<char*>(sF) + off, gF + off, min(kChunk, bytes_F - off), &s_bar[1]);
     for (int kc = 0; kc < KC; ++kc)
       for (int b = 0; b < a.nbox_M; ++b)
-        tma_load_2d(smem + lay.sM + size_t(kc) * rowsM * 128 + size_t(b) * box_bytes_M, &tmM,
+        tma_load_2d(smem + lay.sM + size_t(kc) * rowsM * 128 + size_t(b) * box_bytes_M, tmM,
                     kc * 64, m0 + b * a.box_M, &s_bar[1]);
   }
   // work that needs neither x nor the previous kernel: the zero part of the
@@ -242,7 +255,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_wait();  // x and this handle's workspace are now safe to touch
 
   // ---- phase 1: x slice, partial g and ||x_c||^2 ---------------------------
-  if (tid == 0) s_epoch = ld_cg_u32(a.bar + 1);
+  if (tid == 0) {
+    s_epoch = ld_cg_u32(a.bar + 1);
+    s_base = ld_cg_u32(a.bar + 2);
+  }
   for (int i = tid; i < rowsV; i += kThreads)
     s_xb[i] = i < nV ? a.x[v0 + i] : __float2bfloat16_rn(0.f);
   bool ok = mbar_wait_bounded(&s_bar[0], 0, a.status);
@@ -312,7 +328,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // propagates, all threads load their correction tiles into registers, then
   // thread 0 polls.
   __syncthreads();
-  const uint32_t target = (e + 1u) * uint32_t(G);
+  // the counter stood at s_base when this launch started (launches of one
+  // handle may use different CTA counts)
+  const uint32_t target = s_base + uint32_t(G);
   if (tid == 0) red_release_u32(a.bar, 1u);
 
   // Tiles (I, J), I <= J, are taken by column: columns J and T16 - 1 - J pair
@@ -355,11 +373,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // this CTA's share of the next call's operands, into L2.  Issued after
     // the barrier, when the rest of this call works from shared memory: the
     // stream then does not delay this call's x read, atomics or barrier.
-#pragma unroll
-    for (int o = 0; o < 3; ++o) {
+    const uint32_t part = uint32_t(a.pf_part0 + cta), parts = uint32_t(a.pf_parts);
+#pragma unroll 1
+    for (int o = 0; o < kMaxPf; ++o) {
       const uint32_t bytes = a.pf_bytes[o];
-      const uint32_t share = (bytes / 16 + G - 1) / G * 16;
-      const uint32_t lo = min(bytes, uint32_t(cta) * share), hi = min(bytes, lo + share);
+      if (bytes == 0) continue;
+      const uint32_t share = (bytes / 16 + parts - 1) / parts * 16;
+      const uint32_t lo = min(bytes, part * share), hi = min(bytes, lo + share);
       constexpr uint32_t kPiece = 16384;
       for (uint32_t off = lo + uint32_t(lane) * kPiece; off < hi; off += 32u * kPiece)
         prefetch_l2(a.pf[o] + off, min(kPiece, hi - off));
@@ -559,15 +579,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (cta == 0 && tid == 0) {
     __threadfence();
-    a.bar[1] = e + 1u;  // every CTA read the epoch before the barrier
+    a.bar[2] = s_base + uint32_t(G);
+    a.bar[1] = e + 1u;  // every CTA read the epoch and base before the barrier
   }
 }
 
-const void* decode3_kernel_for(int64_t k) {
+template <int K>
+__global__ void __launch_bounds__(kThreads, 1)
+    gsi_decode3_kernel(const __grid_constant__ CUtensorMap tmV,
+                       const __grid_constant__ CUtensorMap tmM, const __grid_constant__ Decode3Args a) {
+  decode3_body<K>(&tmV, &tmM, a, int(blockIdx.x), int(gridDim.x));
+}
+
+template <int K>
+__global__ void __launch_bounds__(kThreads, 1)
+    gsi_decode3_group_kernel(const __grid_constant__ GroupMaps maps,
+                             const __grid_constant__ GroupArgs g) {
+  int m = 0;
+  while (m + 1 < g.n && int(blockIdx.x) >= g.cta0[m + 1]) ++m;
+  decode3_body<K>(&maps.m[2 * m], &maps.m[2 * m + 1], g.a[m], int(blockIdx.x) - g.cta0[m],
+                  g.cta0[m + 1] - g.cta0[m]);
+}
+
+const void* decode3_kernel_for(int64_t k, bool group) {
   switch (k) {
-    case 64: return reinterpret_cast<const void*>(&gsi_decode3_kernel<64>);
-    case 128: return reinterpret_cast<const void*>(&gsi_decode3_kernel<128>);
-    case 256: return reinterpret_cast<const void*>(&gsi_decode3_kernel<256>);
+    case 64: return group ? reinterpret_cast<const void*>(&gsi_decode3_group_kernel<64>)
+                          : reinterpret_cast<const void*>(&gsi_decode3_kernel<64>);
+    case 128: return group ? reinterpret_cast<const void*>(&gsi_decode3_group_kernel<128>)
+                           : reinterpret_cast<const void*>(&gsi_decode3_kernel<128>);
+    case 256: return group ? reinterpret_cast<const void*>(&gsi_decode3_group_kernel<256>)
+                           : reinterpret_cast<const void*>(&gsi_decode3_kernel<256>);
     default: return nullptr;
   }
 }
@@ -581,107 +622,225 @@ void row_boxes(int rows, int* box, int* nbox) {
   *box = ((padded + *nbox - 1) / *nbox + 15) / 16 * 16;
 }
 
+// Largest dynamic shared memory a kernel of this k may use on this device
+// (raised to that limit once: the limit belongs to the function).
+gsi_status_t smem_limit(const void* fn, int device, int* limit) {
+  int max_optin = 0;
+  if (cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) != cudaSuccess)
+    return GSI_ERR_CUDA;
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return GSI_ERR_CUDA;
+  *limit = max_optin - int(fa.sharedSizeBytes);
+  if (fa.maxDynamicSharedSizeBytes < *limit &&
+      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, *limit) != cudaSuccess)
+    return GSI_ERR_CUDA;
+  return GSI_OK;
+}
+
+// Rows, TMA boxes, shared memory and tensor maps of handle h run on G CTAs.
+gsi_status_t plan_member(const gsi_handle* h, int G, int limit, Dec3Plan* p, void* tmV, void* tmM) {
+  p->G = G;
+  p->rows_M = int((h->d_out + G - 1) / G);
+  p->rows_V = int((h->d + G - 1) / G);
+  row_boxes(p->rows_M, &p->box_M, &p->nbox_M);
+  row_boxes(p->rows_V, &p->box_V, &p->nbox_V);
+  p->smem = smem3_layout(int(h->k), p->nbox_M * p->box_M, p->nbox_V * p->box_V).total + kSmemSlack;
+  if (p->smem > size_t(limit)) return GSI_ERR_UNSUPPORTED_SHAPE;
+  if (!tma_encode_bf16_2d(tmV, h->V, uint64_t(h->d), uint64_t(h->k), uint32_t(p->box_V), 64) ||
+      !tma_encode_bf16_2d(tmM, h->M, uint64_t(h->d_out), uint64_t(h->k), uint32_t(p->box_M), 64))
+    return GSI_ERR_CUDA;
+  return GSI_OK;
+}
+
+// Prefetch ranges of a target handle or group (operands above 64 MiB are
+// not prefetched: a large share of L2).  Returns the number of ranges.
+int prefetch_ranges(const gsi_handle* nh, const gsi_group* ng, const char** p, uint32_t* b) {
+  const gsi_handle* list[kMaxGroup];
+  int nl = 0;
+  if (nh) list[nl++] = nh;
+  if (ng)
+    for (int m = 0; m < ng->n && nl < kMaxGroup; ++m) list[nl++] = ng->h[m];
+  const int64_t kMaxPrefetch = int64_t(64) << 20;
+  int n = 0;
+  for (int i = 0; i < nl; ++i) {
+    const gsi_handle* t = list[i];
+    const int64_t bytes[3] = {t->d * t->k * 2, t->d_out * t->k * 2,
+                              t->dec3_F ? int64_t(corr_tiles_elems(int(t->k))) * 2 : 0};
+    const void* ptr[3] = {t->V, t->M, t->dec3_F};
+    for (int o = 0; o < 3; ++o)
+      if (bytes[o] > 0 && bytes[o] <= kMaxPrefetch && n < kMaxPf) {
+        p[n] = static_cast<const char*>(ptr[o]);
+        b[n] = uint32_t(bytes[o]);
+        ++n;
+      }
+  }
+  for (int i = n; i < kMaxPf; ++i) {
+    p[i] = nullptr;
+    b[i] = 0u;
+  }
+  return n;
+}
+
+void fill_args(Decode3Args* a, const gsi_handle* h, const Dec3Plan& p, const void* x, float* y,
+               uint8_t* gate, float* rho) {
+  a->W = h->W;
+  a->F = h->dec3_F;
+  a->x = static_cast<const __nv_bfloat16*>(x);
+  a->y = y;
+  a->gate = gate;
+  a->rho = rho;
+  a->d_out = int(h->d_out);
+  a->d = int(h->d);
+  a->eps = h->eps;
+  a->rows_M = p.rows_M;
+  a->rows_V = p.rows_V;
+  a->box_M = p.box_M;
+  a->box_V = p.box_V;
+  a->nbox_M = p.nbox_M;
+  a->nbox_V = p.nbox_V;
+  a->acc = h->dec3_acc;
+  a->acc_stride = acc3_stride(h->k);
+  a->bar = h->dec3_bar;
+  a->status = h->status;
+}
+
+cudaLaunchConfig_t launch_config(dim3 grid, size_t smem, cudaStream_t s, bool pdl,
+                                 cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.numAttrs = 0;
+  if (pdl) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 1;
+  }
+  cfg.attrs = attr;
+  return cfg;
+}
+
 }  // namespace
 
 size_t decode3_acc_floats(int64_t k) { return size_t(2) * kCopies * acc3_stride(k); }
 
 gsi_status_t decode3_configure(gsi_handle* h) {
-  const void* fn = decode3_kernel_for(h->k);
-  if (!fn) return GSI_ERR_UNSUPPORTED_SHAPE;
-  int max_optin = 0;
-  if (cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device) != cudaSuccess)
-    return GSI_ERR_CUDA;
+  const void* fn = decode3_kernel_for(h->k, false);
+  const void* fng = decode3_kernel_for(h->k, true);
+  if (!fn || !fng) return GSI_ERR_UNSUPPORTED_SHAPE;
+  int limit = 0;
+  gsi_status_t st = smem_limit(fn, h->device, &limit);
+  if (st == GSI_OK) {
+    int limit_g = 0;
+    st = smem_limit(fng, h->device, &limit_g);
+  }
+  if (st != GSI_OK) return st;
   const int64_t rows_hint = (std::max(h->d_out, h->d) + 7) / 8;
   const int G = int(std::max<int64_t>(1, std::min<int64_t>(h->num_sms, rows_hint)));
-  const int rows_M = int((h->d_out + G - 1) / G);
-  const int rows_V = int((h->d + G - 1) / G);
-  int box_M, nbox_M, box_V, nbox_V;
-  row_boxes(rows_M, &box_M, &nbox_M);
-  row_boxes(rows_V, &box_V, &nbox_V);
-  const int K = int(h->k);
-  cudaFuncAttributes fa;
-  if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return GSI_ERR_CUDA;
-  const int fn_limit = max_optin - int(fa.sharedSizeBytes);
-  const size_t smem = smem3_layout(K, nbox_M * box_M, nbox_V * box_V).total + kSmemSlack;
-  if (smem > size_t(fn_limit)) return GSI_ERR_UNSUPPORTED_SHAPE;
-  // The limit belongs to the kernel function, shared by every handle with
-  // this k: raise it to the device maximum once, never per handle.
-  if (fa.maxDynamicSharedSizeBytes < fn_limit &&
-      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, fn_limit) != cudaSuccess)
-    return GSI_ERR_CUDA;
+  Dec3Plan p;
+  st = plan_member(h, G, limit, &p, h->dec3_tmaps[0], h->dec3_tmaps[1]);
+  if (st != GSI_OK) return st;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, p.smem) != cudaSuccess)
     return GSI_ERR_CUDA;
   // The CTAs wait on one another: all of them must fit at once.
   if (per_sm < 1 || int64_t(per_sm) * h->num_sms < G) return GSI_ERR_UNSUPPORTED_SHAPE;
-  if (!tma_encode_bf16_2d(h->dec3_tmaps[0], h->V, uint64_t(h->d), uint64_t(h->k), uint32_t(box_V), 64) ||
-      !tma_encode_bf16_2d(h->dec3_tmaps[1], h->M, uint64_t(h->d_out), uint64_t(h->k), uint32_t(box_M), 64))
-    return GSI_ERR_CUDA;
-  h->dec3_grid = G;
-  h->dec3_rows_M = rows_M;
-  h->dec3_rows_V = rows_V;
-  h->dec3_box_M = box_M;
-  h->dec3_nbox_M = nbox_M;
-  h->dec3_box_V = box_V;
-  h->dec3_nbox_V = nbox_V;
-  h->dec3_smem = smem;
+  h->dec3_plan = p;
   return GSI_OK;
 }
 
 gsi_status_t decode3_launch(gsi_handle* h, const void* x, float* y, uint8_t* gate, float* rho,
                             cudaStream_t s) {
   Decode3Args a;
-  a.W = h->W;
-  a.F = h->dec3_F;
-  a.x = static_cast<const __nv_bfloat16*>(x);
-  a.y = y;
-  a.gate = gate;
-  a.rho = rho;
-  a.d_out = int(h->d_out);
-  a.d = int(h->d);
-  a.eps = h->eps;
-  a.rows_M = h->dec3_rows_M;
-  a.rows_V = h->dec3_rows_V;
-  a.box_M = h->dec3_box_M;
-  a.box_V = h->dec3_box_V;
-  a.nbox_M = h->dec3_nbox_M;
-  a.nbox_V = h->dec3_nbox_V;
-  a.acc = h->dec3_acc;
-  a.acc_stride = acc3_stride(h->k);
-  a.bar = h->dec3_bar;
-  a.status = h->status;
-  // operands above 64 MiB are not prefetched (a large share of L2)
-  const gsi_handle* n = h->pf_next;
-  const int64_t kMaxPrefetch = int64_t(64) << 20;
-  const int64_t pf_b[3] = {n ? n->d * n->k * 2 : 0, n ? n->d_out * n->k * 2 : 0,
-                           (n && n->dec3_F) ? int64_t(corr_tiles_elems(int(n->k))) * 2 : 0};
-  const void* pf_p[3] = {n ? n->V : nullptr, n ? n->M : nullptr, n ? n->dec3_F : nullptr};
-  for (int o = 0; o < 3; ++o) {
-    const bool on = pf_b[o] > 0 && pf_b[o] <= kMaxPrefetch;
-    a.pf[o] = on ? static_cast<const char*>(pf_p[o]) : nullptr;
-    a.pf_bytes[o] = on ? uint32_t(pf_b[o]) : 0u;
-  }
-
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(h->dec3_grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = h->dec3_smem;
-  cfg.stream = s;
+  fill_args(&a, h, h->dec3_plan, x, y, gate, rho);
+  prefetch_ranges(h->pf_next, h->pf_group, a.pf, a.pf_bytes);
+  a.pf_part0 = 0;
+  a.pf_parts = h->dec3_plan.G;
   cudaLaunchAttribute attr[1];
-  int na = 0;
-  if (h->use_pdl) {
-    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[na].val.programmaticStreamSerializationAllowed = 1;
-    ++na;
-  }
-  cfg.attrs = attr;
-  cfg.numAttrs = na;
+  cudaLaunchConfig_t cfg = launch_config(dim3(h->dec3_plan.G), h->dec3_plan.smem, s, h->use_pdl, attr);
   const CUtensorMap* maps = reinterpret_cast<const CUtensorMap*>(h->dec3_tmaps);
   cudaError_t err;
   switch (h->k) {
     case 64: err = cudaLaunchKernelEx(&cfg, gsi_decode3_kernel<64>, maps[0], maps[1], a); break;
     case 128: err = cudaLaunchKernelEx(&cfg, gsi_decode3_kernel<128>, maps[0], maps[1], a); break;
     case 256: err = cudaLaunchKernelEx(&cfg, gsi_decode3_kernel<256>, maps[0], maps[1], a); break;
+    default: return GSI_ERR_UNSUPPORTED_SHAPE;
+  }
+  return err == cudaSuccess ? GSI_OK : GSI_ERR_CUDA;
+}
+
+gsi_status_t group_configure(gsi_group* g) {
+  const gsi_handle* h0 = g->h[0];
+  const void* fn = decode3_kernel_for(h0->k, true);
+  if (!fn) return GSI_ERR_UNSUPPORTED_SHAPE;
+  int limit = 0;
+  gsi_status_t st = smem_limit(fn, h0->device, &limit);
+  if (st != GSI_OK) return st;
+  // CTAs in proportion to each member's operand bytes (V_k + M), at least one
+  // each, all co-resident (one per SM)
+  const int S = h0->num_sms;
+  if (g->n > S) return GSI_ERR_UNSUPPORTED_SHAPE;
+  double w[kMaxGroup], wsum = 0.0;
+  for (int m = 0; m < g->n; ++m) {
+    w[m] = double(g->h[m]->d + g->h[m]->d_out) * double(g->h[m]->k);
+    wsum += w[m];
+  }
+  int Gm[kMaxGroup], used = 0;
+  for (int m = 0; m < g->n; ++m) {
+    const int64_t rows_hint = (std::max(g->h[m]->d_out, g->h[m]->d) + 7) / 8;
+    Gm[m] = int(std::max<int64_t>(1, std::min<int64_t>(rows_hint, int64_t(S * w[m] / wsum))));
+    used += Gm[m];
+  }
+  for (int m = 0; used > S; m = (m + 1) % g->n)  // rounding never overshoots by much
+    if (Gm[m] > 1) {
+      --Gm[m];
+      --used;
+    }
+  size_t smem = 0;
+  g->cta0[0] = 0;
+  for (int m = 0; m < g->n; ++m) {
+    st = plan_member(g->h[m], Gm[m], limit, &g->plan[m], g->tmaps[2 * m], g->tmaps[2 * m + 1]);
+    if (st != GSI_OK) return st;
+    smem = std::max(smem, g->plan[m].smem);
+    g->cta0[m + 1] = g->cta0[m] + Gm[m];
+  }
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem) != cudaSuccess)
+    return GSI_ERR_CUDA;
+  if (per_sm < 1 || int64_t(per_sm) * S < g->cta0[g->n]) return GSI_ERR_UNSUPPORTED_SHAPE;
+  g->smem = smem;
+  return GSI_OK;
+}
+
+gsi_status_t group_launch(gsi_group* g, const void* const* x, float* const* y,
+                          uint8_t* const* gate, float* const* rho, cudaStream_t s) {
+  GroupMaps maps;
+  GroupArgs ga;
+  std::memset(&maps, 0, sizeof maps);
+  std::memset(&ga, 0, sizeof ga);
+  std::memcpy(maps.m, g->tmaps, size_t(2) * g->n * sizeof(CUtensorMap));
+  ga.n = g->n;
+  const char* pfp[kMaxPf];
+  uint32_t pfb[kMaxPf];
+  prefetch_ranges(g->pf_next, nullptr, pfp, pfb);
+  for (int m = 0; m < g->n; ++m) {
+    fill_args(&ga.a[m], g->h[m], g->plan[m], x[m], y[m], gate ? gate[m] : nullptr,
+              rho ? rho[m] : nullptr);
+    std::memcpy(ga.a[m].pf, pfp, sizeof pfp);
+    std::memcpy(ga.a[m].pf_bytes, pfb, sizeof pfb);
+    ga.a[m].pf_part0 = g->cta0[m];
+    ga.a[m].pf_parts = g->cta0[g->n];
+  }
+  for (int m = 0; m <= g->n; ++m) ga.cta0[m] = g->cta0[m];
+  for (int m = g->n + 1; m <= kMaxGroup; ++m) ga.cta0[m] = g->cta0[g->n];
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = launch_config(dim3(g->cta0[g->n]), g->smem, s, true, attr);
+  cudaError_t err;
+  switch (g->k) {
+    case 64: err = cudaLaunchKernelEx(&cfg, gsi_decode3_group_kernel<64>, maps, ga); break;
+    case 128: err = cudaLaunchKernelEx(&cfg, gsi_decode3_group_kernel<128>, maps, ga); break;
+    case 256: err = cudaLaunchKernelEx(&cfg, gsi_decode3_group_kernel<256>, maps, ga); break;
     default: return GSI_ERR_UNSUPPORTED_SHAPE;
   }
   return err == cudaSuccess ? GSI_OK : GSI_ERR_CUDA;

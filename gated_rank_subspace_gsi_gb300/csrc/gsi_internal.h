@@ -10,6 +10,18 @@
 
 #include "gsi.h"
 
+struct gsi_group;
+
+namespace gsi {
+constexpr int kMaxGroup = 4;  // one-token calls per gsi_group_forward launch
+// Launch plan of the one-barrier decode kernel for one handle on G CTAs.
+struct Dec3Plan {
+  int G = 0, rows_M = 0, rows_V = 0;
+  int box_M = 0, nbox_M = 0, box_V = 0, nbox_V = 0;  // TMA row boxes
+  size_t smem = 0;
+};
+}  // namespace gsi
+
 struct gsi_handle {
   // Borrowed operands (section 2.1 of the GSI summary): W (d_out x d),
   // V_k (d x k), M = W V_k (d_out x k), all bf16 row-major, device memory.
@@ -32,19 +44,21 @@ struct gsi_handle {
 
   // ---- one-barrier decode kernel (k in {64, 128, 256}), used when it fits --
   bool dec3_ok = false;
-  int dec3_grid = 0, dec3_rows_M = 0, dec3_rows_V = 0;
-  int dec3_box_M = 0, dec3_nbox_M = 0, dec3_box_V = 0, dec3_nbox_V = 0;  // TMA row boxes
-  size_t dec3_smem = 0;
+  gsi::Dec3Plan dec3_plan;
   alignas(64) unsigned char dec3_tmaps[2][128] = {};  // TMA maps of V_k and M (CUtensorMap)
   __nv_bfloat16* dec3_F = nullptr;  // correction tiles (corr_tiles_elems(k))
   float* dec3_acc = nullptr;        // decode3_acc_floats(k) fp32 accumulators
-  uint32_t* dec3_bar = nullptr;     // [0] arrival counter, [1] launch epoch
+  uint32_t* dec3_bar = nullptr;     // [0] arrival counter, [1] launch epoch, [2] counter base
 
-  // L2 prefetch link (gsi_set_prefetch): each one-token call on this handle
-  // prefetches pf_next's V_k, M and correction tiles into L2.  pf_from lists
-  // the handles whose link points here, so destroying this handle unlinks them.
+  // L2 prefetch link (gsi_set_prefetch, gsi_set_prefetch_group): each
+  // one-token call on this handle prefetches the V_k, M and correction tiles
+  // of pf_next, or of every member of pf_group, into L2.  pf_from and
+  // pf_from_groups list the handles and groups whose link points here, so
+  // destroying this handle unlinks them.
   gsi_handle* pf_next = nullptr;
+  gsi_group* pf_group = nullptr;
   std::vector<gsi_handle*> pf_from;
+  std::vector<gsi_group*> pf_from_groups;
 
   // ---- device workspace (one allocation) --------------------------------
   void* ws = nullptr;
@@ -76,6 +90,19 @@ struct gsi_handle {
   void* st_dev = nullptr;
   size_t st_bytes = 0;
   int64_t st_T = 0;
+};
+
+// Several one-token calls in one launch (gsi_group_create): members borrow
+// their handles' operands and workspaces.
+struct gsi_group {
+  int n = 0, k = 0, device = 0;
+  gsi_handle* h[gsi::kMaxGroup] = {};
+  gsi::Dec3Plan plan[gsi::kMaxGroup];
+  int cta0[gsi::kMaxGroup + 1] = {};  // member m owns CTAs [cta0[m], cta0[m + 1])
+  size_t smem = 0;
+  alignas(64) unsigned char tmaps[2 * gsi::kMaxGroup][128] = {};
+  gsi_handle* pf_next = nullptr;        // prefetch target of the group's launches
+  std::vector<gsi_handle*> pf_from;     // handles whose pf_group is this group
 };
 
 namespace gsi {
@@ -112,6 +139,9 @@ size_t decode3_acc_floats(int64_t k);
 gsi_status_t decode3_configure(gsi_handle* h);
 gsi_status_t decode3_launch(gsi_handle* h, const void* x, float* y, uint8_t* gate,
                             float* rho, cudaStream_t s);
+gsi_status_t group_configure(gsi_group* g);
+gsi_status_t group_launch(gsi_group* g, const void* const* x, float* const* y,
+                          uint8_t* const* gate, float* const* rho, cudaStream_t s);
 
 // Batched path (gsi_batched.cu)
 gsi_status_t batched_launch(gsi_handle* h, const void* x, int64_t T, float* y,

@@ -26,7 +26,9 @@ GSI_ERR_LAUNCH = 7
 # every function declared in include/gsi.h
 EXPORTS = ("gsi_create", "gsi_forward", "gsi_forward_host", "gsi_precompute_M",
            "gsi_reserve", "gsi_device_status", "gsi_destroy", "gsi_status_string",
-           "gsi_forward_launch_count", "gsi_forward_noalloc", "gsi_set_prefetch")
+           "gsi_forward_launch_count", "gsi_forward_noalloc", "gsi_set_prefetch",
+           "gsi_set_prefetch_group", "gsi_group_create", "gsi_group_forward",
+           "gsi_group_set_prefetch", "gsi_group_destroy")
 
 _lock = threading.Lock()
 _lib = None
@@ -73,6 +75,16 @@ def _load():
         lib.gsi_forward_noalloc.restype = ctypes.c_int
         lib.gsi_set_prefetch.argtypes = [P, P]
         lib.gsi_set_prefetch.restype = ctypes.c_int
+        lib.gsi_set_prefetch_group.argtypes = [P, P]
+        lib.gsi_set_prefetch_group.restype = ctypes.c_int
+        lib.gsi_group_create.argtypes = [ctypes.c_int, P, ctypes.POINTER(P)]
+        lib.gsi_group_create.restype = ctypes.c_int
+        lib.gsi_group_forward.argtypes = [P, P, P, P, P, P]
+        lib.gsi_group_forward.restype = ctypes.c_int
+        lib.gsi_group_set_prefetch.argtypes = [P, P]
+        lib.gsi_group_set_prefetch.restype = ctypes.c_int
+        lib.gsi_group_destroy.argtypes = [P]
+        lib.gsi_group_destroy.restype = None
         _lib = lib
         return lib
 
@@ -163,6 +175,45 @@ def gsi_set_prefetch(h, next_h):
     """Make each one-token call on h prefetch next_h's operands into L2
     (next_h None removes the link)."""
     _check(_load().gsi_set_prefetch(h, next_h), "gsi_set_prefetch")
+
+
+def gsi_set_prefetch_group(h, group):
+    """Make each one-token call on h prefetch every member of `group` into L2
+    (None removes the link)."""
+    _check(_load().gsi_set_prefetch_group(h, group), "gsi_set_prefetch_group")
+
+
+def _ptr_array(items):
+    arr = (ctypes.c_void_p * len(items))()
+    for i, t in enumerate(items):
+        arr[i] = _ptr(t)
+    return arr
+
+
+def gsi_group_create(handles) -> ctypes.c_void_p:
+    """One launch for several independent one-token calls (a group of handles)."""
+    arr = (ctypes.c_void_p * len(handles))(*[h.value if isinstance(h, ctypes.c_void_p) else h
+                                             for h in handles])
+    g = ctypes.c_void_p()
+    _check(_load().gsi_group_create(len(handles), arr, ctypes.byref(g)), "gsi_group_create")
+    return g
+
+
+def gsi_group_forward(g, xs, ys, gates=None, rhos=None, stream=None):
+    """One token through every member of group g (lists of device tensors)."""
+    _check(_load().gsi_group_forward(g, _ptr_array(xs), _ptr_array(ys),
+                                     _ptr_array(gates) if gates is not None else None,
+                                     _ptr_array(rhos) if rhos is not None else None,
+                                     _stream(stream)), "gsi_group_forward")
+
+
+def gsi_group_set_prefetch(g, next_h):
+    _check(_load().gsi_group_set_prefetch(g, next_h), "gsi_group_set_prefetch")
+
+
+def gsi_group_destroy(g):
+    if g is not None:
+        _load().gsi_group_destroy(g)
 
 
 def gsi_forward_launch_count(h, T: int) -> int:

@@ -46,6 +46,7 @@ extern "C" {
 #endif
 
 typedef struct gsi_handle *gsi_handle_t;
+typedef struct gsi_group *gsi_group_t;
 
 typedef enum {
     GSI_OK = 0,
@@ -135,6 +136,46 @@ gsi_status_t gsi_device_status(gsi_handle_t h, cudaStream_t stream);
  * link.  Not thread-safe against concurrent gsi_set_prefetch or gsi_destroy
  * on the same handles.  Synchronous, host only. */
 gsi_status_t gsi_set_prefetch(gsi_handle_t h, gsi_handle_t next);
+
+/* As gsi_set_prefetch, with the operands of every member of a group (below)
+ * as the target: for a call followed by a grouped launch.  Replaces any
+ * previous target of h; NULL removes it. */
+gsi_status_t gsi_set_prefetch_group(gsi_handle_t h, gsi_group_t next);
+
+/* A group of 1 to 4 handles whose one-token calls are independent of one
+ * another, run as ONE kernel launch (gsi_group_forward).  The page has no
+ * counterpart: this schedules calls.  It serves decoder layers whose linears
+ * read different inputs that are ready together.  For example, in a
+ * parallel-residual block (GPT-J) the attention output projection and the
+ * MLP output projection do not depend on each other.  Each member keeps its
+ * own grid exchange on its share of the SMs (shares in proportion to its
+ * V_k + M bytes), so the launch costs one dependent-launch boundary instead
+ * of one per call.
+ *   handles: n distinct handles on one device, all with the same k in
+ *            {64, 128, 256}.  BORROWED: they must outlive the group.  A handle
+ *            may belong to several groups and still be used alone.  All calls
+ *            that involve one handle must be ordered on the GPU.
+ * Computes each member's launch plan and tensor maps once.  Returns
+ * GSI_ERR_UNSUPPORTED_SHAPE if a member's slices do not fit the kernel's
+ * shared memory at its share of the SMs. */
+gsi_status_t gsi_group_create(int n, const gsi_handle_t *handles, gsi_group_t *out);
+
+/* One token through every member: for member m the same result as
+ * gsi_forward(handles[m], x[m], 1, y[m], gate ? gate[m] : NULL,
+ * rho ? rho[m] : NULL, stream).  x, y: arrays of n device pointers (16-byte
+ * aligned); gate, rho: arrays of n device pointers (entries may be NULL) or
+ * NULL.  Asynchronous on `stream`, allocates nothing. */
+gsi_status_t gsi_group_forward(gsi_group_t g, const void *const *x, float *const *y,
+                               uint8_t *const *gate, float *const *rho,
+                               cudaStream_t stream);
+
+/* The group's launches prefetch next's operands into L2 (as gsi_set_prefetch;
+ * NULL removes the link). */
+gsi_status_t gsi_group_set_prefetch(gsi_group_t g, gsi_handle_t next);
+
+/* Release the group (not its handles).  Synchronises the device.  Removes
+ * the prefetch links that point to it.  NULL is ignored. */
+void gsi_group_destroy(gsi_group_t g);
 
 /* Release the handle and its workspace (not W, V_k or M).  Synchronises the
  * device.  NULL is ignored. */

@@ -76,5 +76,14 @@ def test_host_argument_checks(cl):
     assert cl.gsi_device_status(None, None) == 1
     assert cl.gsi_forward_launch_count(None, 1) == 0
     assert cl.gsi_set_prefetch(None, None) == 1
+    assert cl.gsi_set_prefetch_group(None, None) == 1
+    g = ctypes.c_void_p()
+    assert cl.gsi_group_create(0, None, ctypes.byref(g)) == 1
+    assert cl.gsi_group_create(5, (ctypes.c_void_p * 5)(A, B, C, A, B), ctypes.byref(g)) == 1
+    assert cl.gsi_group_create(1, (ctypes.c_void_p * 1)(None), ctypes.byref(g)) == 1
+    assert cl.gsi_group_create(1, (ctypes.c_void_p * 1)(A), None) == 1
+    assert cl.gsi_group_forward(None, None, None, None, None, None) == 1
+    assert cl.gsi_group_set_prefetch(None, None) == 1
+    cl.gsi_group_destroy(None)
     cl.gsi_destroy(None)
     del h
