@@ -58,8 +58,9 @@
 namespace gsi {
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 512;               // compute threads (16 warps)
 constexpr int kWarps = kThreads / 32;
+constexpr int kBlock = kThreads + 32;       // + one warp that issues the L2 prefetches
 constexpr int kCopies = 8;        // accumulator copies of (g, ||x||^2)
 constexpr int kMaxBoxRows = 256;  // TMA box limit
 constexpr int kMaxPf = 12;        // prefetch ranges (3 per handle, up to 4 handles)
@@ -105,6 +106,31 @@ __device__ __forceinline__ void red_release_u32(uint32_t* p, uint32_t v) {
 // Prefetch [p, p + bytes) into L2 (16-byte aligned, bytes a multiple of 16).
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(p), "r"(bytes) : "memory");
+}
+
+// Barriers of the 16 compute warps only (named barrier 1), so that the
+// prefetch warp, whose bulk-prefetch instructions can stall it for a
+// microsecond or more, never holds them up.
+__device__ __forceinline__ void sync_compute() {
+  asm volatile("bar.sync 1, %0;" :: "n"(kThreads) : "memory");
+}
+__device__ __forceinline__ bool sync_compute_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.and.pred p, 1, %2, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r) : "r"(uint32_t(v)), "n"(kThreads) : "memory");
+  return r != 0;
+}
+// Named barrier 2 (all kBlock threads): the compute warps arrive without
+// waiting once the grid exchange is done; the prefetch warp waits for that.
+__device__ __forceinline__ void signal_prefetch_warp() {
+  asm volatile("bar.arrive 2, %0;" :: "n"(kBlock) : "memory");
+}
+__device__ __forceinline__ void wait_for_compute_warps() {
+  asm volatile("bar.sync 2, %0;" :: "n"(kBlock) : "memory");
 }
 
 __device__ __forceinline__ uint32_t dynamic_smem_bytes() {
@@ -196,7 +222,7 @@ __device__ __forceinline__ void decode3_body(const CUtensorMap* tmV, const CUten
   // Launch self-check (uniform over the grid, before any wait): a launch that
   // does not cover d and d_out or got less shared memory than its layout
   // does nothing and reports it.
-  if (blockDim.x != kThreads || int64_t(G) * a.rows_M < a.d_out || int64_t(G) * a.rows_V < a.d ||
+  if (blockDim.x != kBlock || int64_t(G) * a.rows_M < a.d_out || int64_t(G) * a.rows_V < a.d ||
       rowsM < a.rows_M || rowsV < a.rows_V || dynamic_smem_bytes() < lay.total + pad) {
     if (cta == 0 && tid == 0) atomicOr(a.status, kStatusBadLaunch);
     return;
@@ -228,6 +254,26 @@ __device__ __forceinline__ void decode3_body(const CUtensorMap* tmV, const CUten
     fence_mbar_init();
   }
   __syncthreads();
+  if (warp == kWarps) {
+    // The prefetch warp: once the compute warps are past the grid exchange
+    // (the rest of the call works from shared memory), this CTA's share of the
+    // next call's operands, into L2; then it exits.  Weights only: it reads
+    // nothing the previous kernel writes.
+    pdl_launch_dependents();
+    wait_for_compute_warps();
+    const uint32_t part = uint32_t(a.pf_part0 + cta), parts = uint32_t(a.pf_parts);
+#pragma unroll 1
+    for (int o = 0; o < kMaxPf; ++o) {
+      const uint32_t bytes = a.pf_bytes[o];
+      if (bytes == 0) continue;
+      const uint32_t share = (bytes / 16 + parts - 1) / parts * 16;
+      const uint32_t lo = min(bytes, part * share), hi = min(bytes, lo + share);
+      constexpr uint32_t kPiece = 16384;
+      for (uint32_t off = lo + uint32_t(lane) * kPiece; off < hi; off += 32u * kPiece)
+        prefetch_l2(a.pf[o] + off, min(kPiece, hi - off));
+    }
+    return;
+  }
   // staging issued by warp 1: fetching a tensor map's descriptor stalls the
   // issuing thread, and thread 0 must reach the dependent-launch wait first
   // Two completion groups: phase 1 needs only the V_k slice, so it does not
@@ -262,7 +308,7 @@ __device__ __forceinline__ void decode3_body(const CUtensorMap* tmV, const CUten
   for (int i = tid; i < rowsV; i += kThreads)
     s_xb[i] = i < nV ? a.x[v0 + i] : __float2bfloat16_rn(0.f);
   bool ok = mbar_wait_bounded(&s_bar[0], 0, a.status);
-  ok = __syncthreads_and(ok) != 0;
+  ok = sync_compute_and(ok);
   const uint32_t e = s_epoch;
   float* acc = a.acc + size_t(e & 1u) * kCopies * a.acc_stride;
   if (cta == 0) {  // clear the buffers the next launch accumulates into
@@ -327,7 +373,7 @@ __device__ __forceinline__ void decode3_body(const CUtensorMap* tmV, const CUten
   // Thread 0 arrives once every warp's atomics are issued; while the arrival
   // propagates, all threads load their correction tiles into registers, then
   // thread 0 polls.
-  __syncthreads();
+  sync_compute();
   // the counter stood at s_base when this launch started (launches of one
   // handle may use different CTA counts)
   const uint32_t target = s_base + uint32_t(G);
@@ -367,24 +413,9 @@ __device__ __forceinline__ void decode3_body(const CUtensorMap* tmV, const CUten
     }
     s_ok = good;
   }
-  ok = (__syncthreads_and(staged) != 0) && ok && s_ok;
+  ok = sync_compute_and(staged) && ok && s_ok;
   const int nMw = ok ? nM : 0;
-  if (warp == kWarps - 1) {
-    // this CTA's share of the next call's operands, into L2.  Issued after
-    // the barrier, when the rest of this call works from shared memory: the
-    // stream then does not delay this call's x read, atomics or barrier.
-    const uint32_t part = uint32_t(a.pf_part0 + cta), parts = uint32_t(a.pf_parts);
-#pragma unroll 1
-    for (int o = 0; o < kMaxPf; ++o) {
-      const uint32_t bytes = a.pf_bytes[o];
-      if (bytes == 0) continue;
-      const uint32_t share = (bytes / 16 + parts - 1) / parts * 16;
-      const uint32_t lo = min(bytes, part * share), hi = min(bytes, lo + share);
-      constexpr uint32_t kPiece = 16384;
-      for (uint32_t off = lo + uint32_t(lane) * kPiece; off < hi; off += 32u * kPiece)
-        prefetch_l2(a.pf[o] + off, min(kPiece, hi - off));
-    }
-  }
+  signal_prefetch_warp();
 
   // ---- phase 2: g (same order in every CTA), g^T E g, g.g, speculative M g --
   float g2 = 0.f;
@@ -414,7 +445,7 @@ __device__ __forceinline__ void decode3_body(const CUtensorMap* tmV, const CUten
     for (int c = 0; c < kCopies; ++c) sx += ld_cg_f32(acc + size_t(c) * a.acc_stride + K);
     s_sx = sx;
   }
-  __syncthreads();
+  sync_compute();
   {
     // g^T E g = sum over tiles I <= J of g_I . (F_IJ g_J), one independent
     // MMA per tile from the registers loaded before the barrier; B = g_J is
@@ -476,7 +507,7 @@ __device__ __forceinline__ void decode3_body(const CUtensorMap* tmV, const CUten
       }
     }
   }
-  __syncthreads();
+  sync_compute();
 
   // ---- gate ------------------------------------------------------------------
   if (tid == 0) {
@@ -502,7 +533,7 @@ __device__ __forceinline__ void decode3_body(const CUtensorMap* tmV, const CUten
       if (a.rho) a.rho[0] = rho;
     }
   }
-  __syncthreads();
+  sync_compute();
   const bool slow = !(s_rho < a.eps);
 
   // ---- phase 3: the branch the gate picked ---------------------------------
@@ -585,14 +616,14 @@ __device__ __forceinline__ void decode3_body(const CUtensorMap* tmV, const CUten
 }
 
 template <int K>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kBlock, 1)
     gsi_decode3_kernel(const __grid_constant__ CUtensorMap tmV,
                        const __grid_constant__ CUtensorMap tmM, const __grid_constant__ Decode3Args a) {
   decode3_body<K>(&tmV, &tmM, a, int(blockIdx.x), int(gridDim.x));
 }
 
 template <int K>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kBlock, 1)
     gsi_decode3_group_kernel(const __grid_constant__ GroupMaps maps,
                              const __grid_constant__ GroupArgs g) {
   int m = 0;
@@ -708,7 +739,7 @@ cudaLaunchConfig_t launch_config(dim3 grid, size_t smem, cudaStream_t s, bool pd
                                  cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kBlock);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cfg.numAttrs = 0;
@@ -742,7 +773,7 @@ gsi_status_t decode3_configure(gsi_handle* h) {
   st = plan_member(h, G, limit, &p, h->dec3_tmaps[0], h->dec3_tmaps[1]);
   if (st != GSI_OK) return st;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, p.smem) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kBlock, p.smem) != cudaSuccess)
     return GSI_ERR_CUDA;
   // The CTAs wait on one another: all of them must fit at once.
   if (per_sm < 1 || int64_t(per_sm) * h->num_sms < G) return GSI_ERR_UNSUPPORTED_SHAPE;
@@ -806,7 +837,7 @@ gsi_status_t group_configure(gsi_group* g) {
     g->cta0[m + 1] = g->cta0[m] + Gm[m];
   }
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, smem) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kBlock, smem) != cudaSuccess)
     return GSI_ERR_CUDA;
   if (per_sm < 1 || int64_t(per_sm) * S < g->cta0[g->n]) return GSI_ERR_UNSUPPORTED_SHAPE;
   g->smem = smem;
