@@ -41,9 +41,9 @@ METRIC = "µs per gated linear & effective HBM GB/s (GPT-J 4096 shapes, B=1) vs 
 UNIT = "us per gated linear"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-DECODE_KERNEL = "gsi_decode3_kernel<256>"
+DECODE_KERNEL = "gsi_decode3_kernel<256> + gsi_decode3_group_kernel<256>"
 DECODE_SRC = os.path.join(ROOT, "gated_rank_subspace_gsi_gb300", "csrc", "gsi_decode3.cu")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gsi_decode3_kernel__gptj_layer_traffic.txt")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gsi_decode3__gptj_layer_traffic.txt")
 
 
 # --------------------------------------------------------------------------
@@ -146,8 +146,8 @@ class ClockSampler:
 
 
 def kernel_traffic():
-    """DRAM bytes per decode-kernel launch from the committed ncu summary,
-    if it was taken on the decode kernel source as it is now."""
+    """DRAM bytes per gated linear of the decode kernels from the committed ncu
+    summary, if it was taken on the decode kernel source as it is now."""
     try:
         with open(DECODE_SRC, "rb") as f:
             sha = hashlib.sha256(f.read()).hexdigest()[:16]
@@ -159,7 +159,7 @@ def kernel_traffic():
                     vals[k.strip()] = v.strip()
         if vals.get("decode_source_sha256_16") != sha:
             return None
-        return float(vals["dram_bytes_per_launch"])
+        return float(vals["dram_bytes_per_gated_linear"])
     except Exception:
         return None
 
@@ -489,8 +489,9 @@ def run_gsi(args, world, rank, local):
             "traffic": kernel_traffic(),
             "kernel": DECODE_KERNEL,
             "peak_kind": f"{peak_kind} HBM copy",
-            "bytes_per_launch": round(nbytes / n_lin, 1),
-            "us_per_launch": round(us_per_lin, 4),
+            "per": "gated linear (achieved = algorithmic bytes per gated linear / us per gated linear)",
+            "bytes_per_gated_linear": round(nbytes / n_lin, 1),
+            "us_per_gated_linear": round(us_per_lin, 4),
         },
         "e2e": {
             "value": None if math.isnan(ms_e2e) else round(ms_e2e * 1e3 / n_lin, 4),
