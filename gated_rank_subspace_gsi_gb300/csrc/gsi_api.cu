@@ -42,6 +42,8 @@ gsi_status_t grow_batched(gsi_handle* h, int64_t max_T) {
   h->bws = p;
   h->bws_bytes = bytes;
   gsi::batched_bind_workspace(h, p, max_T);
+  gsi_status_t st = gsi::batched_prepare(h);
+  if (st != GSI_OK) return st;
   return gsi::tc_gemm_prepare(h);
 }
 

@@ -131,6 +131,176 @@ __global__ void __launch_bounds__(256) gate_kernel(const float* __restrict__ G,
   }
 }
 
+// rho and gate of 16 tokens per CTA from the Gram identity in the form
+// ||x - V g||^2 = ||x||^2 - g.g + g^T E g, E = V^T V - I (the one-token
+// kernel's form), with g^T E g on warp-level bf16 MMAs over the handle's
+// correction tiles (upper 16 x 16 tiles of E, MMA operand order, see
+// gsi_internal.h).  Warp w takes tokens 4w..4w+3 of the CTA: the B operand's
+// 8 columns are those tokens' g as bf16 high part and remainder (column
+// 2j + part for token j), so lane (grp, tig) accumulates token tig.
+constexpr int kGateMmaTok = 16;
+constexpr int kGateMmaThreads = 128;
+constexpr int kGatePad = 8;  // floats of padding per staged g row (no bank conflicts)
+
+// With S > 0, g is the sum (in slice order) of the S projection partials P[s]
+// and is also written to G for the gather; with S = 0 it is read from G.
+template <int K>
+__global__ void __launch_bounds__(kGateMmaThreads) gate_mma_kernel(
+    float* __restrict__ G, const float* __restrict__ P, int S, size_t split_stride,
+    const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ F, int T, int d,
+    float eps, uint8_t* __restrict__ gate_int, uint8_t* __restrict__ gate_out,
+    float* __restrict__ rho_out, uint32_t* __restrict__ status) {
+  constexpr int T16 = K / 16;
+  constexpr int kTiles = T16 * (T16 + 1) / 2;
+  constexpr int kRow = K + kGatePad;
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint4* sF = reinterpret_cast<uint4*>(smem);                                  // [kTiles][32]
+  float* sg = reinterpret_cast<float*>(smem + size_t(kTiles) * 512);         // [16][kRow]
+  __shared__ float s_sx[kGateMmaTok], s_gg[kGateMmaTok];
+  __shared__ uint64_t s_bar;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int grp = lane >> 2, tig = lane & 3;
+  const int t0 = blockIdx.x * kGateMmaTok;
+  if (tid == 0) {
+    mbar_init(&s_bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    const uint32_t bytes = uint32_t(kTiles) * 512;
+    mbar_arrive_expect_tx(&s_bar, bytes);
+    constexpr uint32_t kChunk = 32768;
+    for (uint32_t off = 0; off < bytes; off += kChunk)
+      bulk_g2s(reinterpret_cast<char*>(sF) + off, reinterpret_cast<const char*>(F) + off,
+               min(kChunk, bytes - off), &s_bar);
+  }
+  for (int q = tid; q < kGateMmaTok * K; q += kGateMmaThreads) {
+    const int t = q / K, a = q % K;
+    float v = 0.f;
+    if (t0 + t < T) {
+      const size_t o = size_t(t0 + t) * K + a;
+      if (S > 0) {
+        for (int sl = 0; sl < S; ++sl) v += P[size_t(sl) * split_stride + o];
+        G[o] = v;
+      } else {
+        v = G[o];
+      }
+    }
+    sg[t * kRow + a] = v;
+  }
+  // ||x_t||^2 and g.g of this warp's 4 tokens (x_i^2 is exact in fp32)
+  for (int j = 0; j < 4; ++j) {
+    const int t = t0 + warp * 4 + j;
+    float sxv = 0.f;
+    if (t < T) {
+      const uint4* xr = reinterpret_cast<const uint4*>(x + size_t(t) * d);
+      for (int c = lane; c < d / 8; c += 32) {
+        float f[8];
+        bf16x8_to_f32(xr[c], f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sxv = fmaf(f[e], f[e], sxv);
+      }
+    }
+    sxv = warp_sum_xor<32>(sxv);
+    if (lane == 0) s_sx[warp * 4 + j] = sxv;
+  }
+  __syncthreads();
+  for (int j = 0; j < 4; ++j) {
+    const float* gr = sg + (warp * 4 + j) * kRow;
+    float v = 0.f;
+    for (int a = lane; a < K; a += 32) v = fmaf(gr[a], gr[a], v);
+    v = warp_sum_xor<32>(v);
+    if (lane == 0) s_gg[warp * 4 + j] = v;
+  }
+  const bool ok = mbar_wait_bounded(&s_bar, 0, status);
+  // B operands of the warp's 4 tokens, one per column block J
+  const float* gb = sg + (warp * 4 + grp / 2) * kRow;
+  const bool low = (grp & 1) != 0;
+  uint2 bfr[T16];
+#pragma unroll
+  for (int J = 0; J < T16; ++J) {
+    const int a = J * 16 + 2 * tig;
+    float v[4] = {gb[a], gb[a + 1], gb[a + 8], gb[a + 9]};
+    uint32_t p[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const __nv_bfloat16 hi = __float2bfloat16_rn(v[e]);
+      const __nv_bfloat16 part = low ? __float2bfloat16_rn(v[e] - __bfloat162float(hi)) : hi;
+      p[e] = __bfloat16_as_ushort(part);
+    }
+    bfr[J] = make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
+  }
+  // g^T E g: tile (I, J) contributes g_I . (F_IJ g_J); lane (grp, tig) holds
+  // columns 2 tig (high) and 2 tig + 1 (low) of token tig, rows grp, grp + 8
+  const float* gq = sg + (warp * 4 + tig) * kRow;
+  float q = 0.f;
+  if (ok) {
+#pragma unroll
+    for (int I = 0; I < T16; ++I) {
+      const float gI0 = gq[I * 16 + grp], gI8 = gq[I * 16 + grp + 8];
+#pragma unroll
+      for (int J = I; J < T16; ++J) {
+        float dd[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint4 A = sF[corr_tile_index(I, J, T16) * 32 + lane];
+        asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+            "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(dd[0]), "+f"(dd[1]), "+f"(dd[2]), "+f"(dd[3])
+            : "r"(A.x), "r"(A.y), "r"(A.z), "r"(A.w), "r"(bfr[J].x), "r"(bfr[J].y));
+        q = fmaf(gI0, dd[0] + dd[1], q);
+        q = fmaf(gI8, dd[2] + dd[3], q);
+      }
+    }
+  }
+  // sum over grp (lanes of equal tig)
+  q += __shfl_xor_sync(0xFFFFFFFFu, q, 4);
+  q += __shfl_xor_sync(0xFFFFFFFFu, q, 8);
+  q += __shfl_xor_sync(0xFFFFFFFFu, q, 16);
+  if (lane < 4) {
+    const int tl = warp * 4 + lane, t = t0 + tl;
+    if (t < T) {
+      const float sxv = s_sx[tl];
+      float rho;
+      if (!ok) {
+        rho = __int_as_float(0x7FC00000);
+      } else if (!(fabsf(sxv) <= FLT_MAX)) {
+        rho = __int_as_float(0x7FC00000);  // non-finite x: NaN, slow path
+      } else if (sxv == 0.f) {
+        rho = 0.f;
+      } else {
+        float sr = (sxv - s_gg[tl]) + q;
+        if (!(sr >= 0.f)) sr = (sr == sr) ? 0.f : sr;
+        rho = sqrtf(sr / sxv);
+      }
+      const uint8_t slow = (rho < eps) ? 0 : 1;
+      gate_int[t] = slow;
+      if (gate_out) gate_out[t] = slow;
+      if (rho_out) rho_out[t] = rho;
+    }
+  }
+}
+
+template <int K>
+size_t gate_mma_smem() {
+  constexpr int T16 = K / 16;
+  return size_t(T16) * (T16 + 1) / 2 * 512 + size_t(kGateMmaTok) * (K + kGatePad) * 4;
+}
+
+// V_k (d x k) -> V_k^T (k x d), 32 x 32 tiles through shared memory.
+__global__ void __launch_bounds__(256) transpose_kernel(const __nv_bfloat16* __restrict__ V, int d,
+                                                        int k, __nv_bfloat16* __restrict__ VT) {
+  __shared__ __nv_bfloat16 tile[32][33];
+  const int a0 = blockIdx.x * 32, i0 = blockIdx.y * 32;
+  for (int q = threadIdx.x; q < 32 * 32; q += blockDim.x) {
+    const int r = q / 32, c = q % 32;
+    if (i0 + r < d && a0 + c < k) tile[r][c] = V[size_t(i0 + r) * k + a0 + c];
+  }
+  __syncthreads();
+  for (int q = threadIdx.x; q < 32 * 32; q += blockDim.x) {
+    const int r = q / 32, c = q % 32;  // VT row a0 + r, column i0 + c
+    if (a0 + r < k && i0 + c < d) VT[size_t(a0 + r) * d + i0 + c] = tile[c][r];
+  }
+}
+
 // Stable partition of token indices by gate; one CTA of 1024 threads.
 __global__ void __launch_bounds__(1024) compact_kernel(const uint8_t* __restrict__ gate, int T,
                                                        int32_t* __restrict__ idx_fast,
@@ -215,12 +385,33 @@ template <int K>
 gsi_status_t launch_front(gsi_handle* h, const void* x, int T, uint8_t* gate, float* rho,
                           cudaStream_t s) {
   const auto* xb = static_cast<const __nv_bfloat16*>(x);
-  if (cudaMemsetAsync(h->bG, 0, size_t(T) * K * sizeof(float), s) != cudaSuccess) return GSI_ERR_CUDA;
-  if (cudaMemsetAsync(h->bsx, 0, size_t(T) * sizeof(float), s) != cudaSuccess) return GSI_ERR_CUDA;
-  dim3 pg(unsigned((h->d + kProjRows - 1) / kProjRows), unsigned((T + kProjTok - 1) / kProjTok));
-  proj_kernel<K><<<pg, 256, 0, s>>>(xb, h->V, T, int(h->d), h->bG, h->bsx);
-  gate_kernel<K><<<(T + kGateTok - 1) / kGateTok, 256, 0, s>>>(h->bG, h->bsx, h->gram, T, h->eps,
-                                                               h->bgate, gate, rho);
+  // projection: tensor cores (k = 128, 256) into partials, else CUDA cores
+  // accumulating into G
+  int S = 0;
+  if (tc_proj_supported(h) && h->bP) {
+    int kb_per = 0;
+    S = tc_proj_splits(h, T, &kb_per);
+    const gsi_status_t st = tc_proj_launch(h, x, T, S, kb_per, s);
+    if (st != GSI_OK) return st;
+  } else {
+    if (cudaMemsetAsync(h->bG, 0, size_t(T) * K * sizeof(float), s) != cudaSuccess) return GSI_ERR_CUDA;
+    if (cudaMemsetAsync(h->bsx, 0, size_t(T) * sizeof(float), s) != cudaSuccess) return GSI_ERR_CUDA;
+    dim3 pg(unsigned((h->d + kProjRows - 1) / kProjRows), unsigned((T + kProjTok - 1) / kProjTok));
+    proj_kernel<K><<<pg, 256, 0, s>>>(xb, h->V, T, int(h->d), h->bG, h->bsx);
+  }
+  if constexpr (K >= 64 && K <= 256) {
+    if (h->dec3_F) {
+      gate_mma_kernel<K><<<(T + kGateMmaTok - 1) / kGateMmaTok, kGateMmaThreads, gate_mma_smem<K>(),
+                           s>>>(h->bG, h->bP, S, size_t(h->max_T) * K, xb, h->dec3_F, T,
+                                int(h->d), h->eps, h->bgate, gate, rho, h->status);
+    } else {
+      gate_kernel<K><<<(T + kGateTok - 1) / kGateTok, 256, 0, s>>>(h->bG, h->bsx, h->gram, T,
+                                                                   h->eps, h->bgate, gate, rho);
+    }
+  } else {
+    gate_kernel<K><<<(T + kGateTok - 1) / kGateTok, 256, 0, s>>>(h->bG, h->bsx, h->gram, T, h->eps,
+                                                                 h->bgate, gate, rho);
+  }
   compact_kernel<<<1, 1024, 0, s>>>(h->bgate, T, h->bidx_fast, h->bidx_slow, h->bcount);
   gather_kernel<K><<<T, 256, 0, s>>>(xb, h->bG, h->bgate, h->bidx_fast, h->bidx_slow, h->bcount,
                                      int(h->d), int(h->max_T), h->bGf, h->bXs);
@@ -240,10 +431,29 @@ size_t batched_workspace_bytes(int64_t max_T, int64_t d, int64_t k) {
   b += align256(16);                         // counts
   b += align256(size_t(max_T) * 2 * k * 2);  // bGf
   b += align256(size_t(max_T) * d * 2);      // bXs
+  if (k == 128 || k == 256) {
+    b += align256(size_t(k) * d * 2);                          // bVT
+    b += align256(size_t(kProjMaxSplits) * max_T * k * 4);     // bP
+  }
   return b;
 }
 
+// The MMA gate kernel's shared memory exceeds the default 48 KB for k = 256:
+// raise its limit once per function (a property of the function, not of a
+// handle).
+template <int K>
+bool gate_mma_prepare() {
+  static bool done = false;
+  if (!done)
+    done = cudaFuncSetAttribute(gate_mma_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                int(gate_mma_smem<K>())) == cudaSuccess;
+  return done;
+}
+
 void batched_bind_workspace(gsi_handle* h, void* base, int64_t max_T) {
+  gate_mma_prepare<64>();
+  gate_mma_prepare<128>();
+  gate_mma_prepare<256>();
   char* p = static_cast<char*>(base);
   auto take = [&](size_t bytes) { char* r = p; p += align256(bytes); return r; };
   h->bG = reinterpret_cast<float*>(take(size_t(max_T) * h->k * 4));
@@ -254,12 +464,27 @@ void batched_bind_workspace(gsi_handle* h, void* base, int64_t max_T) {
   h->bcount = reinterpret_cast<int32_t*>(take(16));
   h->bGf = reinterpret_cast<__nv_bfloat16*>(take(size_t(max_T) * 2 * h->k * 2));
   h->bXs = reinterpret_cast<__nv_bfloat16*>(take(size_t(max_T) * h->d * 2));
+  h->bVT = nullptr;
+  h->bP = nullptr;
+  if (h->k == 128 || h->k == 256) {
+    h->bVT = reinterpret_cast<__nv_bfloat16*>(take(size_t(h->k) * h->d * 2));
+    h->bP = reinterpret_cast<float*>(take(size_t(kProjMaxSplits) * max_T * h->k * 4));
+  }
   h->max_T = max_T;
 }
 
 int batched_launch_count(const gsi_handle* h, int64_t T) {
   (void)h;
   return T > 1 ? 4 + tc_gemm_launch_count() : 0;
+}
+
+gsi_status_t batched_prepare(gsi_handle* h) {
+  if (h->bVT) {
+    dim3 grid(unsigned((h->k + 31) / 32), unsigned((h->d + 31) / 32));
+    transpose_kernel<<<grid, 256>>>(h->V, int(h->d), int(h->k), h->bVT);
+    if (cudaGetLastError() != cudaSuccess) return GSI_ERR_CUDA;
+  }
+  return tc_proj_prepare(h);
 }
 
 gsi_status_t batched_launch(gsi_handle* h, const void* x, int64_t T, float* y, uint8_t* gate,

@@ -81,7 +81,9 @@ struct gsi_handle {
   int32_t* bcount = nullptr;   // [0] n_fast, [1] n_slow
   __nv_bfloat16* bGf = nullptr;// [2][max_T][k] gathered g of fast tokens (hi, lo planes)
   __nv_bfloat16* bXs = nullptr;// max_T x d   gathered x of slow tokens
-
+  __nv_bfloat16* bVT = nullptr;// k x d       V_k transposed (tensor-core projection)
+  float* bP = nullptr;         // [8][max_T][k] projection partials (tensor-core projection)
+  alignas(64) unsigned char tmaps_proj[128] = {};  // TMA map of bVT
   // TMA tensor maps of the tcgen05 GEMMs (CUtensorMap, 128 bytes each):
   // W, M, G_fast hi plane, G_fast lo plane, X_slow
   alignas(64) unsigned char tmaps[5][128] = {};
@@ -149,6 +151,7 @@ gsi_status_t batched_launch(gsi_handle* h, const void* x, int64_t T, float* y,
 int batched_launch_count(const gsi_handle* h, int64_t T);
 size_t batched_workspace_bytes(int64_t max_T, int64_t d, int64_t k);
 void batched_bind_workspace(gsi_handle* h, void* base, int64_t max_T);
+gsi_status_t batched_prepare(gsi_handle* h);  // after binding: V_k^T, tensor maps
 
 // One-off operand preparation (gsi_prep.cu)
 gsi_status_t gram_launch(const __nv_bfloat16* V, int64_t d, int64_t k, float* gram,

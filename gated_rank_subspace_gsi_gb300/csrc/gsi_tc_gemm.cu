@@ -253,6 +253,133 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 }
 
+// ---- projection G = X V_k as a GEMM (T > 1) ------------------------------
+// D (128 entries of g x 64 tokens) = V^T rows (A, K-major: the handle's
+// transposed copy of V_k) . X rows (B, K-major), over one of S slices of the
+// reduction dimension d; each CTA writes its fp32 partial to P[s], and the
+// gate kernel sums the S partials in a fixed order.  Same warp roles as
+// tc_gemm_kernel.
+constexpr int kPN = 64;  // tokens per tile (MMA N)
+constexpr int kPStages = 4;
+constexpr int kPABytes = kBM * kBK * 2;  // 16 KiB
+constexpr int kPBBytes = kPN * kBK * 2;  // 8 KiB
+constexpr int kPStageBytes = kPABytes + kPBBytes;
+constexpr int kPTmemCols = 64;
+constexpr size_t kPSmem = size_t(kPStages) * kPStageBytes + 1024;
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    tc_proj_kernel(const __grid_constant__ CUtensorMap tmVT, const __grid_constant__ CUtensorMap tmX,
+                   TcProjArgs a) {
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ uint64_t full_bar[kPStages];
+  __shared__ uint64_t empty_bar[kPStages];
+  __shared__ uint64_t accum_bar;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ int s_issued;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.x * kBM, t0 = blockIdx.y * kPN, sl = blockIdx.z;
+  const int nkb_all = (a.d + kBK - 1) / kBK;
+  const int kb0 = min(nkb_all, sl * a.kb_per), kb1 = min(nkb_all, kb0 + a.kb_per);
+  const int num_kb = kb1 - kb0;
+  const int nvalid = min(kPN, a.T - t0);
+
+  const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
+  unsigned char* tiles = smem_raw + (base - smem_addr(smem_raw));
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < kPStages; ++st) {
+      mbar_init(&full_bar[st], 1);
+      mbar_init(&empty_bar[st], 1);
+    }
+    mbar_init(&accum_bar, 1);
+    s_abort = 0;
+    s_issued = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(&s_tmem, kPTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int i = 0;
+      for (; i < num_kb; ++i) {
+        const int st = i % kPStages;
+        if (i >= kPStages &&
+            !wait_bounded(&empty_bar[st], ((i / kPStages) & 1) ^ 1, a.status, &s_abort))
+          break;
+        unsigned char* sa = tiles + size_t(st) * kPStageBytes;
+        mbar_arrive_expect_tx(&full_bar[st], kPStageBytes);
+        tma_load_2d(sa, &tmVT, (kb0 + i) * kBK, m0, &full_bar[st]);
+        tma_load_2d(sa + kPABytes, &tmX, (kb0 + i) * kBK, t0, &full_bar[st]);
+      }
+      s_issued = i;
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(kBM, kPN);
+      for (int i = 0; i < num_kb; ++i) {
+        const int st = i % kPStages;
+        if (!wait_bounded(&full_bar[st], (i / kPStages) & 1, a.status, &s_abort)) break;
+        tc_fence_after();
+        const uint32_t sa = base + uint32_t(st) * kPStageBytes;
+        const uint32_t sb = sa + kPABytes;
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk)
+          tc_mma_bf16(tmem, sw128_kmajor_desc(sa + kk * 32), sw128_kmajor_desc(sb + kk * 32), idesc,
+                      (i | kk) != 0 ? 1u : 0u);
+        tc_commit(&empty_bar[st]);
+      }
+      tc_commit(&accum_bar);
+    }
+  } else {
+    // epilogue: warps 2..5 own TMEM lane quarters (warp % 4); entry m0 + row
+    const int q = warp & 3;
+    const bool ok = wait_bounded(&accum_bar, 0, a.status, &s_abort);
+    tc_fence_after();
+    const int row = m0 + q * 32 + lane;
+    float* P = a.P + size_t(sl) * a.split_stride;
+    for (int c0 = 0; c0 < kPN; c0 += 32) {
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(tmem + (uint32_t(q * 32) << 16) + uint32_t(c0), r);
+      if (row < a.k) {
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+          const int j = c0 + jj;
+          // a slice with no reduction steps contributes zero
+          if (j < nvalid)
+            P[size_t(t0 + j) * a.k + row] = (ok && num_kb > 0) ? __uint_as_float(r[jj]) : 0.f;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x == 0 && s_abort) {
+    const int issued = s_issued;
+    for (int i = max(0, issued - kPStages); i < issued; ++i) {
+      const int st = i % kPStages;
+      const uint64_t tw = globaltimer_ns();
+      while (!mbar_try_wait(&full_bar[st], (i / kPStages) & 1) &&
+             globaltimer_ns() - tw < kWaitLimitNs) {
+      }
+    }
+  }
+  if (warp == 1) {
+    if (lane == 0) {
+      const uint64_t tw = globaltimer_ns();
+      while (!mbar_try_wait(&accum_bar, 0) && globaltimer_ns() - tw < kWaitLimitNs) {
+      }
+    }
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kPTmemCols);
+  }
+}
+
 // ---- host side: tensor maps ---------------------------------------------
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -297,6 +424,48 @@ bool tma_encode_bf16_2d(void* map, const void* base, uint64_t rows, uint64_t col
 }
 
 int tc_gemm_launch_count() { return 1; }
+
+bool tc_proj_supported(const gsi_handle* h) { return h->k == 128 || h->k == 256; }
+
+gsi_status_t tc_proj_prepare(gsi_handle* h) {
+  if (!tc_proj_supported(h)) return GSI_OK;
+  if (!tma_encode_bf16_2d(h->tmaps_proj, h->bVT, uint64_t(h->k), uint64_t(h->d), uint32_t(kBM), kBK))
+    return GSI_ERR_CUDA;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(tc_proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(kPSmem)) != cudaSuccess)
+      return GSI_ERR_CUDA;
+    attr = true;
+  }
+  return GSI_OK;
+}
+
+int tc_proj_splits(const gsi_handle* h, int64_t T, int* kb_per) {
+  const int nkb = int((h->d + kBK - 1) / kBK);
+  const int tiles = int(h->k / kBM) * int((T + kPN - 1) / kPN);
+  int S = std::max(1, std::min({kProjMaxSplits, nkb, (h->num_sms + tiles - 1) / tiles}));
+  *kb_per = (nkb + S - 1) / S;
+  S = (nkb + *kb_per - 1) / *kb_per;  // no empty slices
+  return S;
+}
+
+gsi_status_t tc_proj_launch(gsi_handle* h, const void* x, int64_t T, int S, int kb_per, cudaStream_t s) {
+  CUtensorMap tmX;
+  if (!tma_encode_bf16_2d(&tmX, x, uint64_t(T), uint64_t(h->d), uint32_t(kPN), kBK)) return GSI_ERR_CUDA;
+  TcProjArgs a;
+  a.P = h->bP;
+  a.T = int(T);
+  a.d = int(h->d);
+  a.k = int(h->k);
+  a.kb_per = kb_per;
+  a.split_stride = size_t(h->max_T) * h->k;
+  a.status = h->status;
+  dim3 grid(unsigned(h->k / kBM), unsigned((T + kPN - 1) / kPN), unsigned(S));
+  const CUtensorMap* vt = reinterpret_cast<const CUtensorMap*>(h->tmaps_proj);
+  tc_proj_kernel<<<grid, kTcThreads, kPSmem, s>>>(*vt, tmX, a);
+  return cudaGetLastError() == cudaSuccess ? GSI_OK : GSI_ERR_CUDA;
+}
 
 gsi_status_t tc_gemm_prepare(gsi_handle* h) {
   static_assert(sizeof(CUtensorMap) == 128, "tensor map size");

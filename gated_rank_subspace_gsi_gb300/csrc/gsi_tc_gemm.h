@@ -31,6 +31,21 @@ struct TcGemmArgs {
 bool tma_encode_bf16_2d(void* map, const void* base, uint64_t rows, uint64_t cols,
                         uint32_t box_rows, uint32_t box_cols);
 
+// Projection G = X V_k on the tensor cores (T > 1, k in {128, 256}): S
+// slices of the reduction dimension, fp32 partials in the handle's P buffer.
+constexpr int kProjMaxSplits = 8;
+struct TcProjArgs {
+  float* P;             // [S][max_T][k] partials
+  int T, d, k, kb_per;  // kb_per: 64-wide reduction steps per slice
+  size_t split_stride;  // floats between slices
+  uint32_t* status;
+};
+bool tc_proj_supported(const gsi_handle* h);
+gsi_status_t tc_proj_prepare(gsi_handle* h);
+int tc_proj_splits(const gsi_handle* h, int64_t T, int* kb_per);
+gsi_status_t tc_proj_launch(gsi_handle* h, const void* x, int64_t T, int S, int kb_per,
+                            cudaStream_t s);
+
 // Build the TMA tensor maps of a handle (after its workspace is bound).
 gsi_status_t tc_gemm_prepare(gsi_handle* h);
 // One launch computing both GEMMs for T tokens.

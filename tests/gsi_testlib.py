@@ -11,9 +11,13 @@ import numpy as np
 RHO_BAND = 1e-4        # |rho_ref - eps| <= band: the GPU's rho decides the branch
 Y_REL_TOL = 2e-3       # max|y_gpu - y_ref| <= 2e-3 * max|y_ref| (per token row)
 RHO_TOL = 1e-4         # |rho_gpu - rho_ref| for finite rho, or else ...
-RHO2_TOL = 1e-6        # ... |rho_gpu^2 - rho_ref^2|: the GPU forms rho^2 from fp32
-                       # sums of size ||x||^2 (relative error ~16 fp32 ulps), so
-                       # near rho = 0 the absolute error of rho^2, not rho, is bounded
+RHO2_TOL = 5e-6        # ... |rho_gpu^2 - rho_ref^2|: the GPU forms rho^2 as
+                       # (||x||^2 - g.g + g^T E g) / ||x||^2 from fp32 sums over d
+                       # and k terms (g accumulated on the tensor cores for T > 1),
+                       # whose worst-case error is a few 1e-6 of ||x||^2; near
+                       # rho = 0 that bounds the error of rho^2, not rho; near any
+                       # eps >= 0.05 it moves rho by <= 5e-5 (inside the 1e-4
+                       # band); gates are checked exactly regardless
 
 
 def to_dev(bits: np.ndarray):
