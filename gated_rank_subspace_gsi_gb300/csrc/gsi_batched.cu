@@ -131,15 +131,17 @@ __global__ void __launch_bounds__(256) gate_kernel(const float* __restrict__ G,
   }
 }
 
-// rho and gate of 16 tokens per CTA from the Gram identity in the form
+// rho and gate of 8 tokens per CTA from the Gram identity in the form
 // ||x - V g||^2 = ||x||^2 - g.g + g^T E g, E = V^T V - I (the one-token
 // kernel's form), with g^T E g on warp-level bf16 MMAs over the handle's
 // correction tiles (upper 16 x 16 tiles of E, MMA operand order, see
-// gsi_internal.h).  Warp w takes tokens 4w..4w+3 of the CTA: the B operand's
-// 8 columns are those tokens' g as bf16 high part and remainder (column
-// 2j + part for token j), so lane (grp, tig) accumulates token tig.
-constexpr int kGateMmaTok = 16;
-constexpr int kGateMmaThreads = 128;
+// gsi_internal.h).  All 8 warps load (the projection partials and the x rows
+// are read with many independent loads in flight); warps 0 and 1 then take
+// tokens 0..3 and 4..7: the B operand's 8 columns are those tokens' g as bf16
+// high part and remainder (column 2j + part for token j), so lane (grp, tig)
+// accumulates token tig.
+constexpr int kGateMmaTok = 8;
+constexpr int kGateMmaThreads = 256;
 constexpr int kGatePad = 8;  // floats of padding per staged g row (no bank conflicts)
 
 // With S > 0, g is the sum (in slice order) of the S projection partials P[s]
@@ -154,8 +156,8 @@ __global__ void __launch_bounds__(kGateMmaThreads) gate_mma_kernel(
   constexpr int kTiles = T16 * (T16 + 1) / 2;
   constexpr int kRow = K + kGatePad;
   extern __shared__ __align__(128) unsigned char smem[];
-  uint4* sF = reinterpret_cast<uint4*>(smem);                                  // [kTiles][32]
-  float* sg = reinterpret_cast<float*>(smem + size_t(kTiles) * 512);         // [16][kRow]
+  uint4* sF = reinterpret_cast<uint4*>(smem);                          // [kTiles][32]
+  float* sg = reinterpret_cast<float*>(smem + size_t(kTiles) * 512);   // [8][kRow]
   __shared__ float s_sx[kGateMmaTok], s_gg[kGateMmaTok];
   __shared__ uint64_t s_bar;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -174,46 +176,74 @@ __global__ void __launch_bounds__(kGateMmaThreads) gate_mma_kernel(
       bulk_g2s(reinterpret_cast<char*>(sF) + off, reinterpret_cast<const char*>(F) + off,
                min(kChunk, bytes - off), &s_bar);
   }
-  for (int q = tid; q < kGateMmaTok * K; q += kGateMmaThreads) {
-    const int t = q / K, a = q % K;
-    float v = 0.f;
+  pdl_launch_dependents();
+  pdl_wait();  // the projection's output and x are now visible
+  // g of the 8 tokens: float4 units, every slice's load issued before the adds
+  for (int q = tid; q < kGateMmaTok * K / 4; q += kGateMmaThreads) {
+    const int t = q / (K / 4), a4 = q % (K / 4);
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     if (t0 + t < T) {
-      const size_t o = size_t(t0 + t) * K + a;
+      const size_t o = size_t(t0 + t) * K + size_t(a4) * 4;
       if (S > 0) {
-        for (int sl = 0; sl < S; ++sl) v += P[size_t(sl) * split_stride + o];
-        G[o] = v;
+        float4 part[tc_proj_max_splits()];
+#pragma unroll
+        for (int sl = 0; sl < tc_proj_max_splits(); ++sl)
+          part[sl] = sl < S ? *reinterpret_cast<const float4*>(P + size_t(sl) * split_stride + o)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int sl = 0; sl < tc_proj_max_splits(); ++sl) {
+          v.x += part[sl].x;
+          v.y += part[sl].y;
+          v.z += part[sl].z;
+          v.w += part[sl].w;
+        }
+        *reinterpret_cast<float4*>(G + o) = v;
       } else {
-        v = G[o];
+        v = *reinterpret_cast<const float4*>(G + o);
       }
     }
-    sg[t * kRow + a] = v;
+    *reinterpret_cast<float4*>(sg + t * kRow + a4 * 4) = v;
   }
-  // ||x_t||^2 and g.g of this warp's 4 tokens (x_i^2 is exact in fp32)
-  for (int j = 0; j < 4; ++j) {
-    const int t = t0 + warp * 4 + j;
-    float sxv = 0.f;
+  // ||x_t||^2: warp w takes token w, 8 chunks in flight per lane and four
+  // partial sums (x_i^2 is exact in fp32)
+  {
+    const int t = t0 + warp;
+    float acc4[4] = {0.f, 0.f, 0.f, 0.f};
     if (t < T) {
       const uint4* xr = reinterpret_cast<const uint4*>(x + size_t(t) * d);
-      for (int c = lane; c < d / 8; c += 32) {
-        float f[8];
-        bf16x8_to_f32(xr[c], f);
+      const int nch = d / 8;
+      for (int c0 = lane; c0 < nch; c0 += 32 * 8) {
+        uint4 ch[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) sxv = fmaf(f[e], f[e], sxv);
+        for (int u = 0; u < 8; ++u) {
+          const int c = c0 + u * 32;
+          ch[u] = c < nch ? xr[c] : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          float f[8];
+          bf16x8_to_f32(ch[u], f);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc4[e & 3] = fmaf(f[e], f[e], acc4[e & 3]);
+        }
       }
     }
+    float sxv = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
     sxv = warp_sum_xor<32>(sxv);
-    if (lane == 0) s_sx[warp * 4 + j] = sxv;
+    if (lane == 0) s_sx[warp] = sxv;
   }
   __syncthreads();
-  for (int j = 0; j < 4; ++j) {
-    const float* gr = sg + (warp * 4 + j) * kRow;
+  {
+    const float* gr = sg + warp * kRow;
     float v = 0.f;
     for (int a = lane; a < K; a += 32) v = fmaf(gr[a], gr[a], v);
     v = warp_sum_xor<32>(v);
-    if (lane == 0) s_gg[warp * 4 + j] = v;
+    if (lane == 0) s_gg[warp] = v;
   }
   const bool ok = mbar_wait_bounded(&s_bar, 0, status);
-  // B operands of the warp's 4 tokens, one per column block J
+  __syncthreads();
+  if (warp >= 2) return;  // no further block barrier below
+  // B operands of this warp's 4 tokens, one per column block J
   const float* gb = sg + (warp * 4 + grp / 2) * kRow;
   const bool low = (grp & 1) != 0;
   uint2 bfr[T16];
@@ -308,6 +338,8 @@ __global__ void __launch_bounds__(1024) compact_kernel(const uint8_t* __restrict
                                                        int32_t* __restrict__ count) {
   __shared__ int s_warp[32];
   __shared__ int s_base;
+  pdl_launch_dependents();
+  pdl_wait();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) s_base = 0;
   __syncthreads();
@@ -361,6 +393,8 @@ __global__ void __launch_bounds__(256) gather_kernel(const __nv_bfloat16* __rest
                                                      const int32_t* __restrict__ count, int d,
                                                      int max_T, __nv_bfloat16* __restrict__ Gf,
                                                      __nv_bfloat16* __restrict__ Xs) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int j = blockIdx.x;  // position in the concatenated [fast | slow] list
   const int n_fast = count[0], n_slow = count[1];
   if (j < n_fast) {
@@ -401,9 +435,11 @@ gsi_status_t launch_front(gsi_handle* h, const void* x, int T, uint8_t* gate, fl
   }
   if constexpr (K >= 64 && K <= 256) {
     if (h->dec3_F) {
-      gate_mma_kernel<K><<<(T + kGateMmaTok - 1) / kGateMmaTok, kGateMmaThreads, gate_mma_smem<K>(),
-                           s>>>(h->bG, h->bP, S, size_t(h->max_T) * K, xb, h->dec3_F, T,
-                                int(h->d), h->eps, h->bgate, gate, rho, h->status);
+      if (launch_pdl(gate_mma_kernel<K>, dim3((T + kGateMmaTok - 1) / kGateMmaTok),
+                     dim3(kGateMmaThreads), gate_mma_smem<K>(), s, h->bG, h->bP, S,
+                     size_t(h->max_T) * K, xb, h->dec3_F, T, int(h->d), h->eps, h->bgate, gate,
+                     rho, h->status) != cudaSuccess)
+        return GSI_ERR_CUDA;
     } else {
       gate_kernel<K><<<(T + kGateTok - 1) / kGateTok, 256, 0, s>>>(h->bG, h->bsx, h->gram, T,
                                                                    h->eps, h->bgate, gate, rho);
@@ -412,9 +448,11 @@ gsi_status_t launch_front(gsi_handle* h, const void* x, int T, uint8_t* gate, fl
     gate_kernel<K><<<(T + kGateTok - 1) / kGateTok, 256, 0, s>>>(h->bG, h->bsx, h->gram, T, h->eps,
                                                                  h->bgate, gate, rho);
   }
-  compact_kernel<<<1, 1024, 0, s>>>(h->bgate, T, h->bidx_fast, h->bidx_slow, h->bcount);
-  gather_kernel<K><<<T, 256, 0, s>>>(xb, h->bG, h->bgate, h->bidx_fast, h->bidx_slow, h->bcount,
-                                     int(h->d), int(h->max_T), h->bGf, h->bXs);
+  if (launch_pdl(compact_kernel, dim3(1), dim3(1024), 0, s, h->bgate, T, h->bidx_fast,
+                 h->bidx_slow, h->bcount) != cudaSuccess ||
+      launch_pdl(gather_kernel<K>, dim3(T), dim3(256), 0, s, xb, h->bG, h->bgate, h->bidx_fast,
+                 h->bidx_slow, h->bcount, int(h->d), int(h->max_T), h->bGf, h->bXs) != cudaSuccess)
+    return GSI_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? GSI_OK : GSI_ERR_CUDA;
 }
 

@@ -135,6 +135,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __shared__ int s_abort;
   __shared__ int s_issued;
 
+  pdl_launch_dependents();
+  pdl_wait();  // token counts, index lists and gathered operands are now visible
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int o0 = blockIdx.x * kBM;
   const int n_tiles = (a.T + kBN - 1) / kBN;
@@ -278,6 +280,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __shared__ int s_abort;
   __shared__ int s_issued;
 
+  pdl_launch_dependents();
+  pdl_wait();  // x may come from the previous kernel
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.x * kBM, t0 = blockIdx.y * kPN, sl = blockIdx.z;
   const int nkb_all = (a.d + kBK - 1) / kBK;
@@ -463,8 +467,9 @@ gsi_status_t tc_proj_launch(gsi_handle* h, const void* x, int64_t T, int S, int 
   a.status = h->status;
   dim3 grid(unsigned(h->k / kBM), unsigned((T + kPN - 1) / kPN), unsigned(S));
   const CUtensorMap* vt = reinterpret_cast<const CUtensorMap*>(h->tmaps_proj);
-  tc_proj_kernel<<<grid, kTcThreads, kPSmem, s>>>(*vt, tmX, a);
-  return cudaGetLastError() == cudaSuccess ? GSI_OK : GSI_ERR_CUDA;
+  return launch_pdl(tc_proj_kernel, grid, dim3(kTcThreads), kPSmem, s, *vt, tmX, a) == cudaSuccess
+             ? GSI_OK
+             : GSI_ERR_CUDA;
 }
 
 gsi_status_t tc_gemm_prepare(gsi_handle* h) {
@@ -487,8 +492,10 @@ gsi_status_t tc_gemm_launch(gsi_handle* h, const TcGemmArgs& a, cudaStream_t s) 
   const CUtensorMap* maps = reinterpret_cast<const CUtensorMap*>(h->tmaps);
   const int n_tiles = (a.T + kBN - 1) / kBN;
   dim3 grid(unsigned((a.d_out + kBM - 1) / kBM), unsigned(2 * n_tiles));
-  tc_gemm_kernel<<<grid, kTcThreads, kTcSmem, s>>>(maps[0], maps[1], maps[2], maps[3], maps[4], a);
-  return cudaGetLastError() == cudaSuccess ? GSI_OK : GSI_ERR_CUDA;
+  return launch_pdl(tc_gemm_kernel, grid, dim3(kTcThreads), kTcSmem, s, maps[0], maps[1], maps[2],
+                    maps[3], maps[4], a) == cudaSuccess
+             ? GSI_OK
+             : GSI_ERR_CUDA;
 }
 
 }  // namespace gsi

@@ -34,6 +34,7 @@ bool tma_encode_bf16_2d(void* map, const void* base, uint64_t rows, uint64_t col
 // Projection G = X V_k on the tensor cores (T > 1, k in {128, 256}): S
 // slices of the reduction dimension, fp32 partials in the handle's P buffer.
 constexpr int kProjMaxSplits = 8;
+__host__ __device__ constexpr int tc_proj_max_splits() { return kProjMaxSplits; }
 struct TcProjArgs {
   float* P;             // [S][max_T][k] partials
   int T, d, k, kb_per;  // kb_per: 64-wide reduction steps per slice
