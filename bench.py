@@ -260,37 +260,41 @@ def capture_step(layer, n_tokens, replicas, stream, handles_subset=None, host=No
     otherwise one call per linear in `handles_subset` (all by default), in
     order, on device buffers or (host) through gsi_forward_host."""
     import torch
-
-    from gated_rank_subspace_gsi_gb300 import lib
     g = torch.cuda.CUDAGraph()
-    idx = range(len(layer)) if handles_subset is None else handles_subset
     with torch.cuda.stream(stream):
         with torch.cuda.graph(g, stream=stream):
-            for t in range(n_tokens):
-                r = t % replicas
-                if groups is not None:
-                    sl = slice(t, t + 1)
-                    if 0 in idx:
-                        L0 = layer[0]
-                        lib.gsi_forward(L0["reps"][r][2], L0["x"][sl], L0["y"][sl], L0["gate"][sl],
-                                        L0["rho"][sl], stream)
-                    if 1 in idx or 2 in idx:
-                        m = layer[1:]
-                        lib.gsi_group_forward(groups[r], [L["x"][sl] for L in m],
-                                              [L["y"][sl] for L in m], [L["gate"][sl] for L in m],
-                                              [L["rho"][sl] for L in m], stream)
-                    continue
-                for li in idx:
-                    L = layer[li]
-                    h = L["reps"][r][2]
-                    if host is None:
-                        lib.gsi_forward(h, L["x"][t:t + 1], L["y"][t:t + 1], L["gate"][t:t + 1],
-                                        L["rho"][t:t + 1], stream)
-                    else:
-                        H = host[li]
-                        lib.gsi_forward_host(h, H["x"][t:t + 1], H["y"][t:t + 1],
-                                             H["gate"][t:t + 1], H["rho"][t:t + 1], stream)
+            record_step(layer, n_tokens, replicas, stream, handles_subset, host, groups)
     return g
+
+
+def record_step(layer, n_tokens, replicas, stream, handles_subset=None, host=None, groups=None):
+    """Issue one step's calls on `stream` (inside a graph capture)."""
+    from gated_rank_subspace_gsi_gb300 import lib
+    idx = range(len(layer)) if handles_subset is None else handles_subset
+    for t in range(n_tokens):
+        r = t % replicas
+        if groups is not None:
+            sl = slice(t, t + 1)
+            if 0 in idx:
+                L0 = layer[0]
+                lib.gsi_forward(L0["reps"][r][2], L0["x"][sl], L0["y"][sl], L0["gate"][sl],
+                                L0["rho"][sl], stream)
+            if 1 in idx or 2 in idx:
+                m = layer[1:]
+                lib.gsi_group_forward(groups[r], [L["x"][sl] for L in m],
+                                      [L["y"][sl] for L in m], [L["gate"][sl] for L in m],
+                                      [L["rho"][sl] for L in m], stream)
+            continue
+        for li in idx:
+            L = layer[li]
+            h = L["reps"][r][2]
+            if host is None:
+                lib.gsi_forward(h, L["x"][t:t + 1], L["y"][t:t + 1], L["gate"][t:t + 1],
+                                L["rho"][t:t + 1], stream)
+            else:
+                H = host[li]
+                lib.gsi_forward_host(h, H["x"][t:t + 1], H["y"][t:t + 1],
+                                     H["gate"][t:t + 1], H["rho"][t:t + 1], stream)
 
 
 def replay(graph, stream, n: int):
@@ -423,10 +427,11 @@ def run_gsi(args, world, rank, local):
                          gbs=round(b1 / (ms1 * 1e-3) / 1e9, 1))
         del g1
 
-    # ---- end to end: host buffers through gsi_forward_host ---------------
+    # ---- end to end: the step's inputs from pinned host memory, its results
+    # back to pinned host memory, the step itself through the public calls ---
     host = []
     h2d = d2h = 0
-    ms_e2e = float("nan")
+    ms_e2e = ms_call = float("nan")
     for L in (layer if not args.no_extras else []):
         s = L["spec"]
         H = dict(x=L["x"].cpu().pin_memory(),
@@ -437,12 +442,29 @@ def run_gsi(args, world, rank, local):
         h2d += n_tokens * s.d * 2
         d2h += n_tokens * (s.d_out * 4 + 1 + 4)
     if host:
-        link_schedule(layer, groups, replicas, "sequential", args.prefetch)
-        ge = capture_step(layer, n_tokens, replicas, stream, host=host)
+        ge = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(ge, stream=stream):
+                for L, H in zip(layer, host):
+                    L["x"].copy_(H["x"], non_blocking=True)
+                record_step(layer, n_tokens, replicas, stream, groups=groups if grouped else None)
+                for L, H in zip(layer, host):
+                    H["y"].copy_(L["y"], non_blocking=True)
+                    H["gate"].copy_(L["gate"], non_blocking=True)
+                    H["rho"].copy_(L["rho"], non_blocking=True)
+        for H in host:
+            H["gate"].fill_(7)
         ms_e2e = max_over_ranks(time_graph(ge, stream, reps=max(3, args.steps // 10), warmup=2),
                                 world)
         if not np.array_equal(host[0]["gate"].numpy().astype(bool), slow):
             raise RuntimeError("end-to-end gates differ from the generated mix")
+        # every call through the host-buffer entry point (three small copies
+        # per call)
+        link_schedule(layer, groups, replicas, "sequential", args.prefetch)
+        gc = capture_step(layer, n_tokens, replicas, stream, host=host)
+        ms_call = max_over_ranks(time_graph(gc, stream, reps=max(3, args.steps // 10), warmup=2),
+                                 world)
+        link_schedule(layer, groups, replicas, args.schedule, args.prefetch)
 
     launches = args.steps * n_tokens * (2 if grouped else len(layer))
     out = {
@@ -498,8 +520,11 @@ def run_gsi(args, world, rank, local):
             "unit": UNIT,
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
-            "how": "gsi_forward_host per call (pinned host x in, y/gate/rho out), three calls per "
-                   "token, graph-captured step",
+            "how": "per step: one copy of every x of the step from pinned host memory, the step "
+                   "through gsi_forward / gsi_group_forward, one copy of every y, gate and rho "
+                   "back to pinned host memory, graph-captured",
+            "per_call_host_api_us_per_linear": None if math.isnan(ms_call)
+            else round(ms_call * 1e3 / n_lin, 4),
         },
         "gpu_launches": launches,
         "clocks": clk,
