@@ -657,6 +657,280 @@ def run_batched(args, world, rank, local):
         print(json.dumps(out), flush=True)
 
 
+def _linear_setup(spec, basis, seed, tag, eps=None):
+    """W (device draw), V_k, M (gsi_precompute_M) and a handle of one linear."""
+    import torch
+
+    import gsi_inputs as gi
+    from gated_rank_subspace_gsi_gb300 import lib
+    W = gi.gaussian_weights(spec.d_out, spec.d, seed, tag, device="cuda")
+    V = torch.from_numpy(basis.V_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    M = torch.empty((spec.d_out, spec.k), dtype=torch.bfloat16, device="cuda")
+    lib.gsi_precompute_M(W, V, M)
+    torch.cuda.synchronize()
+    h = lib.gsi_create(W, V, M, spec.eps if eps is None else eps)
+    return dict(W=W, V=V, M=M, h=h, spec=spec)
+
+
+def _fast_bytes(spec) -> int:
+    return (spec.d * spec.k * 2 + correction_bytes(spec.k) + spec.d_out * spec.k * 2
+            + spec.d * 2 + spec.d_out * 4 + 5)
+
+
+def _timed(graph, stream, steps, warmup, world, local):
+    import torch
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    replay(graph, stream, max(warmup, 3))
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    replay(graph, stream, steps)
+    e1.record(stream)
+    e1.synchronize()
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = max_over_ranks(e0.elapsed_time(e1) / steps, world)
+    return ms, clocks.stop()
+
+
+def _line(metric, value, unit, world, steps, warmup, ms, config, **extra):
+    out = {"metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": steps,
+           "warmup": warmup, "ms_per_step": round(ms, 4), "higher_is_better": False,
+           "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+           "data": "synthetic (seeded Gaussian weights, QR bases, activations with set residual "
+                   "ratios)", "impl": "gsi", "config": config}
+    out.update(extra)
+    return out
+
+
+def run_gpt2(args, world, rank, local):
+    """GPT-2-small-shaped QKV linear (768 -> 2304, k = 256, eps = 0.10), T = 64
+    tokens per call with 6 slow: L2-resident and latency-bound (a parity
+    configuration), timed as calls in a CUDA graph."""
+    import torch
+
+    import gsi_inputs as gi
+    from gated_rank_subspace_gsi_gb300 import lib
+    torch.cuda.set_device(local)
+    wl = gi.gpt2_qkv()
+    spec = wl.linears[0]
+    inp = gi.make_linear_inputs(spec, wl.T, wl.extra["n_slow"], wl.seed)
+    L = _linear_setup(spec, inp.basis, wl.seed, 0)
+    x = torch.from_numpy(inp.X_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    y = torch.zeros((wl.T, spec.d_out), dtype=torch.float32, device="cuda")
+    gate = torch.zeros((wl.T,), dtype=torch.uint8, device="cuda")
+    rho = torch.zeros((wl.T,), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.Stream()
+    calls = 100
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            for _ in range(calls):
+                lib.gsi_forward(L["h"], x, y, gate, rho, stream)
+    steps = max(3, args.steps // 10)
+    ms, clk = _timed(graph, stream, steps, args.warmup, world, local)
+    if not np.array_equal(gate.cpu().numpy().astype(bool), inp.slow_mask):
+        raise RuntimeError("gates differ from the generated mix")
+    us = ms * 1e3 / calls
+    per_call = (spec.d * spec.k * 2 + 2 * spec.d * wl.T + spec.k * spec.k * 4
+                + spec.d_out * spec.k * 2 + spec.d_out * spec.d * 2 + wl.T * spec.d_out * 4)
+    peak, kind = hbm_peak()
+    out = _line("µs per gated linear call, GPT-2 QKV T=64", round(us, 3), "us per call", world,
+                steps, args.warmup, ms,
+                {"workload": "gpt2_qkv_T64: 768 -> 2304, k=256, eps=0.10, T=64 tokens per call, "
+                             "6 slow", "calls_per_step": calls,
+                 "l2": "L2-resident (5 MB working set, as the configuration describes)"},
+                roofline={"bound": "latency", "achieved": round(per_call / (us * 1e-6) / 1e9, 1),
+                          "peak": peak, "unit": "GB/s",
+                          "frac": round(per_call / (us * 1e-6) / 1e9 / peak, 4),
+                          "traffic": None, "bytes_per_call": per_call,
+                          "peak_kind": f"{kind} HBM copy (L2-resident: not the bound)"},
+                gpu_launches=steps * calls * lib.gsi_forward_launch_count(L["h"], wl.T),
+                clocks=clk)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def run_stack(args, world, rank, local):
+    """GPT-J-shaped 28-layer stack at decode: per layer the stacked qkv+fc_in
+    call, then out_proj and fc_out as one grouped launch; depth-coherent bases
+    per input chain; 256 distinct decode steps of synthetic tokens (43 slow
+    draws over step x layer x linear), weights (11 GB) beyond L2 by size.
+    Every launch prefetches the next launch's operands into L2."""
+    import torch
+
+    import gsi_inputs as gi
+    from gated_rank_subspace_gsi_gb300 import lib
+    torch.cuda.set_device(local)
+    wl = gi.gptj_stack()
+    nL, S, specs = wl.extra["n_layers"], wl.extra["n_steps"], wl.linears
+    slow = gi.slow_positions(S * nL * 3, wl.extra["n_slow"], wl.seed).reshape(S, nL, 3)
+    layers = []
+    chain = [None, None, None]
+    for l in range(nL):
+        lay = []
+        for i, sp in enumerate(specs):
+            chain[i] = (gi.random_basis(sp.d, sp.k, wl.seed, tag=i) if l == 0 else
+                        gi.coherent_next_basis(chain[i], wl.seed, tag=1000 * i + l))
+            L = _linear_setup(sp, chain[i], wl.seed, 100 * l + i)
+            rs = gi.rho_targets(S, sp.rho_fast, sp.rho_slow, slow[:, l, i], wl.seed, 100 * l + i)
+            X = gi.tokens(chain[i], rs, wl.seed, 100 * l + i)
+            L["x"] = torch.from_numpy(X.view(np.int16)).view(torch.bfloat16).cuda()
+            L["y"] = torch.zeros((S, sp.d_out), dtype=torch.float32, device="cuda")
+            L["gate"] = torch.zeros((S,), dtype=torch.uint8, device="cuda")
+            L["rho"] = torch.zeros((S,), dtype=torch.float32, device="cuda")
+            lay.append(L)
+        g = lib.gsi_group_create([lay[1]["h"], lay[2]["h"]])
+        layers.append((lay, g))
+    for l, (lay, g) in enumerate(layers):
+        lib.gsi_set_prefetch_group(lay[0]["h"], g)
+        lib.gsi_group_set_prefetch(g, layers[(l + 1) % nL][0][0]["h"])
+    stream = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            for t in range(S):
+                sl = slice(t, t + 1)
+                for lay, g in layers:
+                    A = lay[0]
+                    lib.gsi_forward(A["h"], A["x"][sl], A["y"][sl], A["gate"][sl], A["rho"][sl],
+                                    stream)
+                    m = lay[1:]
+                    lib.gsi_group_forward(g, [L["x"][sl] for L in m], [L["y"][sl] for L in m],
+                                          [L["gate"][sl] for L in m], [L["rho"][sl] for L in m],
+                                          stream)
+    steps = max(1, args.steps // 100)
+    ms, clk = _timed(graph, stream, steps, args.warmup, world, local)
+    for l, (lay, _) in enumerate(layers):
+        for i, L in enumerate(lay):
+            if not np.array_equal(L["gate"].cpu().numpy().astype(bool), slow[:, l, i]):
+                raise RuntimeError(f"gates differ from the generated mix (layer {l}, linear {i})")
+    per_fast = sum(_fast_bytes(sp) for sp in specs) * nL
+    n_slow = int(slow.sum())
+    slow_extra = sum(int(slow[:, :, i].sum()) * (specs[i].d_out * specs[i].d * 2
+                                                  - specs[i].d_out * specs[i].k * 2)
+                     for i in range(3))
+    total = per_fast * S + slow_extra
+    us_token = ms * 1e3 / S
+    gbs = total / (ms * 1e-3) / 1e9
+    peak, kind = hbm_peak()
+    out = _line("µs per decode step through a 28-layer GPT-J stack (3 gated linears per layer)",
+                round(us_token, 2), "us per decode step", world, steps, args.warmup, ms,
+                {"workload": "gptj_stack: 28 layers x (4096->28672 qkv+fc_in, then 4096->4096 "
+                             "out_proj || 16384->4096 fc_out grouped), k=256, eps=0.10, "
+                             f"{S} decode steps, {n_slow} slow draws",
+                 "l2": f"weights {sum(sp.d_out * sp.d * 2 for sp in specs) * nL / 1e9:.1f} GB, "
+                       f"V_k + M {sum((sp.d + sp.d_out) * sp.k * 2 for sp in specs) * nL / 1e9:.2f}"
+                       " GB: beyond L2 by size"},
+                us_per_gated_linear=round(us_token / (3 * nL), 4),
+                roofline={"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                          "frac": round(gbs / peak, 4), "traffic": None,
+                          "bytes_per_fast_step": per_fast, "peak_kind": f"{kind} HBM copy"},
+                gpu_launches=steps * S * nL * 2, clocks=clk)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def run_opt(args, world, rank, local):
+    """OPT-6.7B-shaped MLP (fc1 4096 -> 16384, fc2 16384 -> 4096) x 32 layers at
+    decode, eps = 0.05, over slow fractions 0, 2, 10, 50 and 100% (exact counts
+    over step x layer x linear), with the dense bf16 W x (torch.matmul) on the
+    same weights and inputs beside each point."""
+    import torch
+
+    import gsi_inputs as gi
+    from gated_rank_subspace_gsi_gb300 import lib
+    torch.cuda.set_device(local)
+    S = 32
+    fracs = [0.0, 0.02, 0.10, 0.50, 1.00]
+    wl0 = gi.opt_mlp(n_steps=S, slow_fraction=0.0)
+    nL, specs = wl0.extra["n_layers"], wl0.linears
+    layers = []
+    for l in range(nL):
+        lay = []
+        for i, sp in enumerate(specs):
+            basis = gi.random_basis(sp.d, sp.k, wl0.seed, tag=100 * l + i)
+            L = _linear_setup(sp, basis, wl0.seed, 100 * l + i)
+            L["basis"] = basis
+            L["y"] = torch.zeros((S, sp.d_out), dtype=torch.float32, device="cuda")
+            L["gate"] = torch.zeros((S,), dtype=torch.uint8, device="cuda")
+            L["rho"] = torch.zeros((S,), dtype=torch.float32, device="cuda")
+            L["yd"] = torch.zeros((S, sp.d_out), dtype=torch.bfloat16, device="cuda")
+            lay.append(L)
+        layers.append(lay)
+    order = [L["h"] for lay in layers for L in lay]
+    for i, h in enumerate(order):
+        lib.gsi_set_prefetch(h, order[(i + 1) % len(order)])
+    stream = torch.cuda.Stream()
+    peak, kind = hbm_peak()
+    steps = max(1, args.steps // 30)
+    curve = []
+    clk = None
+    for f in fracs:
+        wl = gi.opt_mlp(n_steps=S, slow_fraction=f)
+        slow = gi.slow_positions(S * nL * 2, wl.extra["n_slow"], wl.seed).reshape(S, nL, 2)
+        for l, lay in enumerate(layers):
+            for i, L in enumerate(lay):
+                sp = L["spec"]
+                rs = gi.rho_targets(S, sp.rho_fast, sp.rho_slow, slow[:, l, i], wl.seed,
+                                    100 * l + i)
+                X = gi.tokens(L["basis"], rs, wl.seed, 100 * l + i)
+                L["x"] = torch.from_numpy(X.view(np.int16)).view(torch.bfloat16).cuda()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(graph, stream=stream):
+                for t in range(S):
+                    sl = slice(t, t + 1)
+                    for lay in layers:
+                        for L in lay:
+                            lib.gsi_forward(L["h"], L["x"][sl], L["y"][sl], L["gate"][sl],
+                                            L["rho"][sl], stream)
+        ms, clk = _timed(graph, stream, steps, args.warmup, world, local)
+        for l, lay in enumerate(layers):
+            for i, L in enumerate(lay):
+                if not np.array_equal(L["gate"].cpu().numpy().astype(bool), slow[:, l, i]):
+                    raise RuntimeError(f"gates differ (f={f}, layer {l}, linear {i})")
+        dense = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            L0 = layers[0][0]  # cuBLAS sets itself up outside the capture
+            torch.matmul(L0["x"][0:1], L0["W"].t(), out=L0["yd"][0:1])
+            stream.synchronize()
+            with torch.cuda.graph(dense, stream=stream):
+                for t in range(S):
+                    for lay in layers:
+                        for L in lay:
+                            torch.matmul(L["x"][t:t + 1], L["W"].t(), out=L["yd"][t:t + 1])
+        ms_d, _ = _timed(dense, stream, steps, args.warmup, world, local)
+        n_slow = int(slow.sum())
+        total = sum(_fast_bytes(L["spec"]) for lay in layers for L in lay) * S + sum(
+            int(slow[:, :, i].sum()) * (specs[i].d_out * specs[i].d * 2
+                                        - specs[i].d_out * specs[i].k * 2) for i in range(2))
+        curve.append({"slow_fraction": f, "n_slow": n_slow,
+                      "us_per_layer": round(ms * 1e3 / (S * nL), 3),
+                      "gbs": round(total / (ms * 1e-3) / 1e9, 1),
+                      "frac_of_measured_hbm": round(total / (ms * 1e-3) / 1e9 / peak, 4),
+                      "dense_us_per_layer": round(ms_d * 1e3 / (S * nL), 3),
+                      "speedup_vs_dense": round(ms_d / ms, 3)})
+        del graph, dense
+    c0 = curve[0]
+    out = _line("µs per OPT-6.7B MLP layer (fc1 + fc2) at decode, slow-fraction sweep",
+                c0["us_per_layer"], "us per layer (f = 0 point)", world, steps, args.warmup,
+                c0["us_per_layer"] * nL * S / 1e3,
+                {"workload": f"opt_mlp: 32 layers x (4096->16384 fc1, 16384->4096 fc2), k=256, "
+                             f"eps=0.05, {S} decode steps per point",
+                 "l2": "weights 8.6 GB: beyond L2 by size"},
+                curve=curve, roofline={"bound": "hbm", "achieved": c0["gbs"], "peak": peak,
+                                       "unit": "GB/s", "frac": c0["frac_of_measured_hbm"],
+                                       "traffic": None, "peak_kind": f"{kind} HBM copy"},
+                gpu_launches=steps * S * nL * 2 * len(fracs), clocks=clk)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
 def run_reference(args, world, rank):
     """The oracle (fp64 C) on the host cores, each step a bounded sample of the
     decode layer workload: 8 tokens x 3 gated linears, slow token included in
@@ -717,7 +991,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gsi", "reference"], default="gsi")
-    ap.add_argument("--workload", choices=["gptj_layer_decode", "batched_T512"],
+    ap.add_argument("--workload", choices=["gptj_layer_decode", "batched_T512", "gpt2_qkv_T64",
+                                           "gptj_stack", "opt_mlp"],
                     default="gptj_layer_decode")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -737,6 +1012,12 @@ def main(argv=None):
             run_reference(args, world, rank)
         elif args.workload == "batched_T512":
             run_batched(args, world, rank, local)
+        elif args.workload == "gpt2_qkv_T64":
+            run_gpt2(args, world, rank, local)
+        elif args.workload == "gptj_stack":
+            run_stack(args, world, rank, local)
+        elif args.workload == "opt_mlp":
+            run_opt(args, world, rank, local)
         else:
             run_gsi(args, world, rank, local)
     finally:
