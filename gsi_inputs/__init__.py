@@ -344,3 +344,74 @@ def make_linear_inputs(spec: LinearSpec, T: int, n_slow: int, seed: int,
     rs = rho_targets(T, spec.rho_fast, spec.rho_slow, slow_mask, seed, tag)
     X = tokens(basis, rs, seed, tag)
     return LinearInputs(spec, W, basis, X, slow_mask)
+
+
+# --------------------------------------------------------------------------
+# Calibration activations
+# --------------------------------------------------------------------------
+
+
+@dataclass
+class CalibrationSet:
+    """n calibration tokens with a planted spectrum.
+
+    X_bits  n x d bf16 bits, the tokens;
+    U       d x r fp64 orthonormal, the planted directions (descending scale);
+    sigma   r planted scales; token t is U (sigma * c_t) + noise, c_t ~ N(0, I),
+            then rescaled, so the population second moment has eigenvectors
+            U with eigenvalues proportional to sigma^2 above an isotropic floor.
+    """
+    X_bits: np.ndarray
+    U: np.ndarray
+    sigma: np.ndarray
+
+
+def planted_scales(r: int, k: int, decay: float = 0.5, gap: float = 0.5) -> np.ndarray:
+    """sigma_j = (1 + j)^-decay for j < k and gap * (1 + j)^-decay for j >= k:
+    a power-law spectrum with a step of gap^2 between the k-th and (k+1)-th
+    eigenvalue of the second moment."""
+    j = np.arange(r, dtype=np.float64)
+    s = (1.0 + j) ** (-decay)
+    s[k:] *= gap
+    return s
+
+
+def calibration_activations(n: int, d: int, k: int, seed: int, tag: int = 0,
+                            r: Optional[int] = None, decay: float = 0.5,
+                            gap: float = 0.5, noise: float = 0.02,
+                            U: Optional[np.ndarray] = None) -> CalibrationSet:
+    """Seeded stand-in for the activations of one calibration sequence.
+
+    x_t = a_t (U (sigma * c_t) + noise * z_t), with c_t ~ N(0, I_r),
+    z_t ~ N(0, I_d / d) (unit expected norm), U d x r orthonormal (QR of a
+    seeded Gaussian, or the given U), sigma from planted_scales(r, k, decay,
+    gap), and a_t = sqrt(d / sum(sigma^2)) * exp(0.25 N(0, 1)) so that entries
+    are O(1) with a log-normal spread of token norms.  r defaults to
+    min(d, 2k).
+    """
+    if r is None:
+        r = min(d, 2 * k) if U is None else U.shape[1]
+    rng = _rng(seed, 0xCA, tag)
+    if U is None:
+        U = _qr_signed(rng.standard_normal((d, r)))
+    sigma = planted_scales(r, k, decay, gap)
+    c = rng.standard_normal((n, r)) * sigma
+    x = c @ U.T
+    if noise > 0:
+        x += (noise / math.sqrt(d)) * rng.standard_normal((n, d))
+    amp = math.sqrt(d / float(np.sum(sigma ** 2))) * np.exp(0.25 * rng.standard_normal(n))
+    return CalibrationSet(X_bits=to_bf16_bits(x * amp[:, None]), U=U, sigma=sigma)
+
+
+def calibration_start(d: int, k: int, seed: int, tag: int = 0) -> np.ndarray:
+    """The random start block of the basis iteration: d x k entries
+    ~ N(0, 1/d), bf16 bits (the layout of V_k)."""
+    rng = _rng(seed, 0xCB, tag)
+    return to_bf16_bits(rng.standard_normal((d, k)) / math.sqrt(d))
+
+
+def calibration_gptj(n: int = 2048) -> Dict:
+    """Calibration of one GPT-J-6B-shaped linear input (d = 4096, k = 256)
+    from one 2048-token sequence (GPT-J's context length); 8 iterations."""
+    return dict(name="calibrate_gptj_d4096", seed=CONFIG_SEED_BASE + 5, n=n, d=4096,
+                k=256, iters=8)

@@ -1,0 +1,101 @@
+"""fp64 reference for calibrating the rank-k basis V_k.
+
+TEST INFRASTRUCTURE ONLY, under the same rules as the rest of ``oracle/``:
+only ``tests/``, ``__graft_entry__.smoke()`` and the CPU legs of ``bench.py``
+use it; the CUDA library never imports or calls it and shares no code with
+it.  Plain numpy in fp64; library primitives (matmul, Householder QR, a
+symmetric eigensolver, an SVD) serve as single steps.
+
+What it follows.  The page "Technical summary: Gated Subspace Inference for
+transformer acceleration", section 2.3 ("calibration"), says the basis is
+computed once from a single forward pass over a representative calibration
+sequence, and gives no algorithm.  The reading taken here: V_k spans the
+top-k eigenvectors of the uncentred second moment C = X^T X of the
+calibration activations X (n tokens x d).  That subspace minimises
+sum_t ||x_t - V V^T x_t||^2 over rank-k orthonormal V, i.e. the residual
+r of section 2.1 (eq. 1) summed over the calibration tokens, which is what
+the gate of section 2.2 measures.  Uncentred, because the gate projects x
+itself, not x minus a mean.
+
+  top_k_subspace(X, k)            the definition, by a symmetric eigensolver
+  subspace_iteration(X, Q0, t)    the algorithm the GPU runs: block power
+                                  iteration Q <- orth(X^T (X Q)), t times,
+                                  from the given start block Q0
+  principal_sines(A, B)           the comparison between two subspaces
+
+Only span(V_k) matters to the gated map: replacing V_k by V_k R for an
+orthogonal k x k R leaves r and rho unchanged and M g = W V_k R R^T V_k^T x
+unchanged.  So the functions return orthonormal bases of subspaces, and
+results are compared through principal angles, never entry by entry.
+
+Every function is pinned in tests/test_oracle_calibration.py (closed forms
+for planted spectra, the exact two-dimensional iteration, invariance of the
+span under a change of start basis, convergence at the rate set by the
+eigenvalue gap), and the same file plants mistakes in a copy of this source
+to check that the pins catch them.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def _f64(a) -> np.ndarray:
+    return np.asarray(a, dtype=np.float64)
+
+
+def orthonormal_basis(Y) -> np.ndarray:
+    """Orthonormal basis (d x k) of span(Y) for a full-column-rank d x k Y:
+    the Q factor of a Householder QR."""
+    Q, _ = np.linalg.qr(_f64(Y))
+    return Q
+
+
+def second_moment(X) -> np.ndarray:
+    """C = X^T X for n tokens x d (the calibration activations' uncentred
+    second moment, unnormalised: the 1/n factor changes no eigenvector)."""
+    X = _f64(X)
+    return X.T @ X
+
+
+def top_k_subspace(X, k: int):
+    """(V, lam): the k eigenvectors of C = X^T X with the largest eigenvalues
+    (d x k, orthonormal columns) and those eigenvalues, descending."""
+    w, U = np.linalg.eigh(second_moment(X))
+    idx = np.argsort(w)[::-1][:k]
+    return U[:, idx], w[idx]
+
+
+def subspace_iteration(X, Q0, iters: int) -> np.ndarray:
+    """Block power iteration on C = X^T X from the start block Q0 (d x k):
+    Q_0 = orth(Q0); Q_{t+1} = orth(X^T (X Q_t)); returns Q_iters.
+
+    C is applied as two products with X (n x k, then d x k) and never formed.
+    span(Q_t) = span(C^t Q0).  When lambda_k > lambda_{k+1} and V_k^T Q0 is
+    nonsingular (true for a generic Q0), the tangents of the principal angles
+    to the top-k eigenspace shrink by lambda_{k+1} / lambda_k per iteration.
+    """
+    X = _f64(X)
+    Q = orthonormal_basis(Q0)
+    for _ in range(int(iters)):
+        Z = X @ Q
+        Q = orthonormal_basis(X.T @ Z)
+    return Q
+
+
+def principal_sines(A, B) -> np.ndarray:
+    """Sines of the principal angles between span(A) and span(B) (both d x k,
+    full column rank), descending.  Taken as the singular values of
+    (I - Qa Qa^T) Qb, which keeps full relative accuracy for small angles."""
+    Qa = orthonormal_basis(A)
+    Qb = orthonormal_basis(B)
+    R = Qb - Qa @ (Qa.T @ Qb)
+    s = np.linalg.svd(R, compute_uv=False)
+    return np.sort(np.clip(s, 0.0, 1.0))[::-1]
+
+
+def captured_energy(X, V) -> float:
+    """Fraction of the calibration tokens' total energy inside span(V):
+    ||X Qv||_F^2 / ||X||_F^2 with Qv an orthonormal basis of span(V)."""
+    X = _f64(X)
+    Qv = orthonormal_basis(V)
+    return float(np.sum((X @ Qv) ** 2) / np.sum(X ** 2))

@@ -72,3 +72,23 @@ def test_depth_coherence():
 def test_weights_scale():
     W = gi.bf16_bits_to_f64(gi.gaussian_weights(256, 1024, seed=3))
     assert abs(W.std() * math.sqrt(1024) - 1.0) < 0.01
+
+
+def test_calibration_activations_planted_spectrum():
+    """The calibration stand-in has its planted top-k directions as the
+    dominant subspace of its second moment (checked through the oracle's
+    eigensolver) and the step of gap^2 in the planted scales."""
+    from oracle import calibration as cal
+    s = gi.planted_scales(40, 16, decay=0.5, gap=0.5)
+    assert np.all(np.diff(s) < 0)
+    assert abs((s[16] / s[15]) ** 2 - 0.25 * (16 / 17)) < 1e-12
+    cs = gi.calibration_activations(4000, 128, 16, seed=5)
+    assert cs.X_bits.shape == (4000, 128) and cs.X_bits.dtype == np.uint16
+    X = gi.bf16_bits_to_f64(cs.X_bits)
+    V, lam = cal.top_k_subspace(X, 16)
+    assert np.max(cal.principal_sines(V, cs.U[:, :16])) < 0.25
+    assert lam[15] > 2.5 * cal.top_k_subspace(X, 17)[1][16]
+    again = gi.calibration_activations(4000, 128, 16, seed=5)
+    assert np.array_equal(again.X_bits, cs.X_bits)
+    Q0 = gi.calibration_start(128, 16, seed=5)
+    assert Q0.shape == (128, 16) and np.array_equal(Q0, gi.calibration_start(128, 16, seed=5))

@@ -1,0 +1,197 @@
+"""Pins of the calibration oracle (oracle/calibration.py), CPU only.
+
+Each pin checks one function against a fact that the mathematics fixes
+independently of the function's own formula:
+
+* top_k_subspace on a planted spectrum X = A diag(s) B^T (A, B orthonormal,
+  s distinct): the eigenvectors are the columns of B up to sign, in the
+  order of s, and the eigenvalues are s^2;
+* subspace_iteration in two dimensions, where t iterations from the angle a
+  give the exact angle atan((s2/s1)^(2t) tan a), and on a diagonal second
+  moment with n != d, where the iterate is the normalised s^(2t) * q0;
+* the span of the iterate does not depend on the basis of the start block;
+* on a gapped planted spectrum, the principal-angle tangents obey the
+  textbook bound tan(theta_t) <= (lambda_{k+1}/lambda_k)^t tan(theta_0) and
+  reach the planted subspace to rounding;
+* principal_sines on hand-built subspaces with known angles, including an
+  angle of 1e-9 (full relative accuracy for small angles);
+* orthonormal_basis: orthonormal columns spanning the input;
+* captured_energy on the planted spectrum: sum of the k largest s^2 over the
+  sum of all.
+
+test_calibration_pins_catch_mutant plants plausible mistakes in a copy of the
+oracle's source and requires that at least one pin rejects each copy.
+"""
+import importlib.util
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle.calibration as cal_mod
+
+ORACLE_SRC = cal_mod.__file__
+
+
+def _orthonormal(rows, cols, seed):
+    rng = np.random.default_rng(seed)
+    Q, R = np.linalg.qr(rng.standard_normal((rows, cols)))
+    return Q * np.sign(np.diag(R))
+
+
+def _planted(n, d, r, s, seed):
+    A = _orthonormal(n, r, seed)
+    B = _orthonormal(d, r, seed + 1)
+    return A @ np.diag(s) @ B.T, A, B
+
+
+def pin_top_k_planted(cal):
+    s = np.array([9.0, 7.0, 5.5, 4.0, 3.0, 2.0, 1.5, 1.0])
+    X, _, B = _planted(30, 20, 8, s, 11)
+    k = 5
+    V, lam = cal.top_k_subspace(X, k)
+    assert V.shape == (20, k)
+    M = np.abs(B[:, :k].T @ V)
+    assert np.max(np.abs(M - np.eye(k))) < 1e-10, "eigenvectors are not the planted columns"
+    assert np.allclose(lam, s[:k] ** 2, rtol=1e-12, atol=0)
+
+
+def pin_iteration_two_dims(cal):
+    s1, s2, a = 2.0, 1.5, 1.0
+    X = np.diag([s1, s2])
+    Q0 = np.array([[math.cos(a)], [math.sin(a)]])
+    for t in range(0, 7):
+        Q = cal.subspace_iteration(X, Q0, t)
+        assert Q.shape == (2, 1)
+        assert abs(np.linalg.norm(Q) - 1.0) < 1e-14
+        want = (s2 / s1) ** (2 * t) * math.tan(a)
+        got = abs(Q[1, 0] / Q[0, 0])
+        assert abs(got - want) <= 1e-12 * want, (t, got, want)
+
+
+def pin_iteration_diagonal_moment(cal):
+    # X = A diag(s) with A (n x d) orthonormal columns: X^T X = diag(s^2),
+    # so t iterations from q0 give +-(s^(2t) * q0) / ||s^(2t) * q0||.
+    n, d = 7, 4
+    s = np.array([1.7, 1.3, 1.1, 0.6])
+    X = _orthonormal(n, d, 21) @ np.diag(s)
+    q0 = np.array([[0.3], [-0.5], [0.7], [0.4]])
+    for t in range(0, 5):
+        Q = cal.subspace_iteration(X, q0, t)
+        v = (s ** (2 * t))[:, None] * q0
+        v /= np.linalg.norm(v)
+        assert min(np.max(np.abs(Q - v)), np.max(np.abs(Q + v))) < 1e-13, t
+
+
+def pin_iteration_span_invariance(cal):
+    rng = np.random.default_rng(31)
+    X = rng.standard_normal((40, 24))
+    Q0 = rng.standard_normal((24, 5))
+    R = rng.standard_normal((5, 5)) + 3 * np.eye(5)
+    for t in (0, 1, 3):
+        Qa = cal.subspace_iteration(X, Q0, t)
+        Qb = cal.subspace_iteration(X, Q0 @ R, t)
+        assert np.max(cal.principal_sines(Qa, Qb)) < 1e-10, t
+
+
+def pin_iteration_rate(cal):
+    k = 4
+    s = np.array([3.0, 2.6, 2.3, 2.0, 1.0, 0.9, 0.7, 0.5, 0.3, 0.2])
+    X, _, B = _planted(50, 16, 10, s, 41)
+    ratio = (s[k] / s[k - 1]) ** 2          # lambda_{k+1} / lambda_k
+    Q0 = np.random.default_rng(42).standard_normal((16, k))
+
+    def tan_max(Q):
+        sn = np.max(cal.principal_sines(Q, B[:, :k]))
+        return sn / math.sqrt(1.0 - sn * sn)
+
+    t0 = tan_max(cal.subspace_iteration(X, Q0, 0))
+    for t in range(1, 8):
+        tt = tan_max(cal.subspace_iteration(X, Q0, t))
+        assert tt <= ratio ** t * t0 * (1 + 1e-9) + 1e-14, (t, tt, ratio ** t * t0)
+    assert tan_max(cal.subspace_iteration(X, Q0, 60)) < 1e-12
+
+
+def pin_principal_sines(cal):
+    e = np.eye(4)
+    for th in (1e-9, 0.3, 0.7, math.pi / 2):
+        A = e[:, :1]
+        B = (math.cos(th) * e[:, 0] + math.sin(th) * e[:, 1])[:, None]
+        got = cal.principal_sines(A, B)
+        assert abs(got[0] - math.sin(th)) <= 1e-15 + 1e-12 * math.sin(th), (th, got)
+    a, b = 0.2, 0.9
+    A = e[:, :2]
+    B = np.stack([math.cos(a) * e[:, 0] + math.sin(a) * e[:, 2],
+                  math.cos(b) * e[:, 1] + math.sin(b) * e[:, 3]], axis=1)
+    rot = np.array([[math.cos(0.4), -math.sin(0.4)], [math.sin(0.4), math.cos(0.4)]])
+    got = cal.principal_sines(A @ rot, B @ rot.T)
+    assert np.allclose(got, [math.sin(b), math.sin(a)], rtol=0, atol=1e-14), got
+    Y = np.random.default_rng(51).standard_normal((9, 3))
+    same = cal.principal_sines(Y, Y @ np.array([[1.0, 2.0, 0.0], [0.0, 1.0, 3.0], [1.0, 0.0, 1.0]]))
+    assert np.max(same) < 1e-14, same
+
+
+def pin_orthonormal_basis(cal):
+    Y = np.random.default_rng(61).standard_normal((12, 4)) @ np.diag([1.0, 1e3, 1e-3, 5.0])
+    Q = cal.orthonormal_basis(Y)
+    assert Q.shape == (12, 4)
+    assert np.max(np.abs(Q.T @ Q - np.eye(4))) < 1e-14
+    assert np.max(np.abs(Q @ (Q.T @ Y) - Y)) < 1e-12 * np.max(np.abs(Y))
+
+
+def pin_captured_energy(cal):
+    s = np.array([4.0, 3.0, 2.0, 1.0, 0.5])
+    X, _, B = _planted(20, 10, 5, s, 71)
+    for k in (1, 2, 5):
+        want = float(np.sum(s[:k] ** 2) / np.sum(s ** 2))
+        assert abs(cal.captured_energy(X, B[:, :k]) - want) < 1e-13, k
+
+
+ALL_PINS = [
+    pin_top_k_planted, pin_iteration_two_dims, pin_iteration_diagonal_moment,
+    pin_iteration_span_invariance, pin_iteration_rate, pin_principal_sines,
+    pin_orthonormal_basis, pin_captured_energy,
+]
+
+
+@pytest.mark.parametrize("pin", ALL_PINS, ids=[p.__name__ for p in ALL_PINS])
+def test_calibration_oracle_pin(pin):
+    pin(cal_mod)
+
+
+MUTANTS = [
+    ("smallest eigenvectors", "idx = np.argsort(w)[::-1][:k]", "idx = np.argsort(w)[:k]"),
+    ("eigenvectors as rows", "return U[:, idx], w[idx]", "return U[idx, :].T[:, :k], w[idx]"),
+    ("token-side moment", "return X.T @ X", "return X @ X.T"),
+    ("one product per iteration", "Q = orthonormal_basis(X.T @ Z)", "Q = orthonormal_basis(Z)"),
+    ("one iteration short", "for _ in range(int(iters)):", "for _ in range(max(0, int(iters) - 1)):"),
+    ("start block not orthonormalised", "Q = orthonormal_basis(Q0)", "Q = _f64(Q0)"),
+    ("projector transposed", "R = Qb - Qa @ (Qa.T @ Qb)", "R = Qb - Qa @ (Qb.T @ Qa)"),
+    ("sines from cosines",
+     "R = Qb - Qa @ (Qa.T @ Qb)\n    s = np.linalg.svd(R, compute_uv=False)",
+     "c = np.linalg.svd(Qa.T @ Qb, compute_uv=False)\n    s = np.sqrt(np.maximum(0.0, 1.0 - c ** 2))"),
+    ("basis not normalised", "Q, _ = np.linalg.qr(_f64(Y))\n    return Q",
+     "Q, Rf = np.linalg.qr(_f64(Y))\n    return Q * np.abs(np.diag(Rf))"),
+    ("energy of the sum", "np.sum((X @ Qv) ** 2)", "np.sum(X @ Qv) ** 2"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_calibration_pins_catch_mutant(tmp_path, name, old, new):
+    with open(ORACLE_SRC) as f:
+        src = f.read()
+    assert src.count(old) == 1, f"mutation site for '{name}' not unique"
+    path = os.path.join(tmp_path, "calibration_mutant.py")
+    with open(path, "w") as f:
+        f.write(src.replace(old, new))
+    spec = importlib.util.spec_from_file_location("calibration_mutant", path)
+    mut = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mut)
+    caught = []
+    for pin in ALL_PINS:
+        try:
+            pin(mut)
+        except (AssertionError, ValueError, np.linalg.LinAlgError, FloatingPointError):
+            caught.append(pin.__name__)
+    assert caught, f"no pin caught the planted mistake '{name}'"
