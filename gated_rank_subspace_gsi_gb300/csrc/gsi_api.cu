@@ -78,6 +78,8 @@ const char* gsi_status_string(gsi_status_t s) {
     case GSI_ERR_TIMEOUT: return "GSI_ERR_TIMEOUT: a bounded device-side wait ran out";
     case GSI_ERR_LAUNCH:
       return "GSI_ERR_LAUNCH: a kernel found its launch configuration inconsistent and did nothing";
+    case GSI_ERR_RANK:
+      return "GSI_ERR_RANK: calibration lost a column of its block (zero or non-finite) or its factorisation broke down";
   }
   return "unknown gsi_status_t";
 }

@@ -1,0 +1,716 @@
+// gsi_calib.cu -- calibration of the rank-k basis V_k on the GPU.
+//
+// Page: "Technical summary: Gated Subspace Inference for transformer
+// acceleration" [GSI], section 2.3: the basis is computed once from one
+// forward pass over a representative calibration sequence; the page names no
+// algorithm.  Here V_k spans the top-k eigenvectors of the uncentred second
+// moment C = X^T X of the n calibration tokens X (n x d) -- the rank-k
+// subspace with the least summed squared residual r of section 2.1 (eq. 1)
+// -- approached by block power iteration from a caller-supplied start block.
+// One iteration, with every block stored transposed (k rows) so that both
+// operands of each GEMM are K-major rows for the tensor maps:
+//
+//   Z^T = Q^T X^T          tcgen05 split-K GEMM: A = X (n x d), B = Q^T, K = d
+//   Y^T = Z^T X            tcgen05 split-K GEMM: A = X^T (d x n), B = Z^T, K = n
+//   Q^T = orth(Y^T)        CholeskyQR in fp32 on the k x d block:
+//                            G = Y^T Y;  D = diag(G)^(-1/2);
+//                            D G D + s I = L L^T;  Q^T = L^-1 D Y^T
+//
+// The orthonormalisation runs twice (CholeskyQR2).  The first pass adds a
+// small shift s to the unit-diagonal Gram matrix, so that it cannot break
+// down on an ill-conditioned block; its triangular transform still preserves
+// the span exactly.  The second, unshifted pass restores orthonormality.  In
+// the middle of the iteration only the span matters, so the second pass runs
+// only when the first one's smallest pivot says its block is far from
+// orthonormal (a device flag; the kernels of a skipped pass return at once).
+// The last iteration always runs both passes and writes V_k (d x k, bf16).
+//
+// Kernels: a bf16 transpose, the tcgen05 GEMM of gsi_tc_gemm.cu, a fixed-order
+// sum of split-K partials, the Gram matrix (fp32 CUDA cores, split over d,
+// deterministic last-CTA reduction), a one-CTA blocked Cholesky with the
+// inverses of its 32 x 32 diagonal blocks (k <= 256: the lower triangle fits
+// in shared memory), and a blocked forward substitution that applies L^-1 D
+// to 32-column slices of the block.
+#include <cuda.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "gsi.h"
+#include "gsi_device.cuh"
+#include "gsi_internal.h"
+#include "gsi_tc_gemm.h"
+
+namespace gsi {
+namespace {
+
+constexpr uint32_t kStatusRank = 4u;      // a vanished column or a pivot below the floor
+constexpr int kCB = 32;                   // Cholesky block edge
+constexpr int kCalMaxK = 256;             // lower triangle of k x k fp32 in shared memory
+constexpr int kCalMaxNb = kCalMaxK / kCB;
+constexpr int kBlk = kCB * (kCB + 1);     // one 32 x 33 block (padded rows)
+constexpr int kPtStride = 36;             // row stride of transposed panel blocks (16-byte rows)
+constexpr int kPtBlk = kCB * kPtStride;
+constexpr float kShift1 = 1.0f / 8192.0f;        // first-pass shift on the unit diagonal
+constexpr float kPivotSkip2 = 1.0f / 4096.0f;    // first-pass pivots all above this: skip pass 2
+constexpr float kPivotFloor = 1.0f / 1048576.0f; // a pivot below this: breakdown (status)
+
+__host__ __device__ constexpr int tri(int n) { return n * (n + 1) / 2; }
+
+// index (I, J), I >= J, of lower block number p in row-major packed order
+__device__ __forceinline__ void unpack_tri(int p, int& I, int& J) {
+  I = 0;
+  while (tri(I + 1) <= p) ++I;
+  J = p - tri(I);
+}
+
+// Control words at the start of the workspace (one 256-byte line each group).
+struct CalCtl {
+  uint32_t status;        // kStatus* bits
+  int32_t need2;          // set by a first pass whose block needs the second pass
+  uint32_t pad[62];
+  uint32_t counters[64];  // Gram last-CTA tickets, one per 32 x 32 tile
+};
+static_assert(sizeof(CalCtl) == 512, "control block layout");
+
+// ---- bf16 transpose: out (cols x rows) = in (rows x cols)^T -----------------
+template <typename OutT>
+__device__ __forceinline__ void store_val(OutT* p, float v);
+template <>
+__device__ __forceinline__ void store_val<float>(float* p, float v) { *p = v; }
+template <>
+__device__ __forceinline__ void store_val<__nv_bfloat16>(__nv_bfloat16* p, float v) {
+  *p = __float2bfloat16_rn(v);
+}
+
+template <typename OutT>
+__global__ void __launch_bounds__(256) cal_transpose_kernel(const __nv_bfloat16* __restrict__ in,
+                                                            int rows, int cols,
+                                                            OutT* __restrict__ out) {
+  __shared__ float tile[32][33];
+  pdl_launch_dependents();
+  pdl_wait();
+  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+  for (int q = threadIdx.x; q < 1024; q += 256) {
+    const int r = q >> 5, c = q & 31;
+    tile[r][c] = (r0 + r < rows && c0 + c < cols)
+                     ? __bfloat162float(in[size_t(r0 + r) * cols + c0 + c])
+                     : 0.f;
+  }
+  __syncthreads();
+  for (int q = threadIdx.x; q < 1024; q += 256) {
+    const int r = q >> 5, c = q & 31;  // out row c0 + r, column r0 + c
+    if (c0 + r < cols && r0 + c < rows) store_val(&out[size_t(c0 + r) * rows + r0 + c], tile[c][r]);
+  }
+}
+
+// ---- sum of S split-K partials, fixed order (count % 4 == 0) ---------------
+template <typename OutT>
+__global__ void __launch_bounds__(256) cal_sum_kernel(const float* __restrict__ P, int S,
+                                                      size_t stride, size_t count,
+                                                      OutT* __restrict__ out) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const size_t n4 = count / 4;
+  for (size_t i = size_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+       i += size_t(gridDim.x) * blockDim.x) {
+    float4 acc = reinterpret_cast<const float4*>(P)[i];
+    for (int s = 1; s < S; ++s) {
+      const float4 v = reinterpret_cast<const float4*>(P + size_t(s) * stride)[i];
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    store_val(&out[4 * i + 0], acc.x);
+    store_val(&out[4 * i + 1], acc.y);
+    store_val(&out[4 * i + 2], acc.z);
+    store_val(&out[4 * i + 3], acc.w);
+  }
+}
+
+// ---- Gram matrix G = Q Q^T of a k x d fp32 block (lower 32 x 32 tiles) -----
+// Grid (tri(nb) tiles, S slices of d).  Each CTA sums one tile over one slice
+// (four groups of 64 threads over interleaved columns, each thread a 4 x 4
+// patch), writes its partial, and the last CTA of the tile to arrive adds the
+// S partials in slice order and stores the tile of G (kp x kp).
+constexpr int kGThreads = 256;
+constexpr int kGChunk = 64;
+
+__global__ void __launch_bounds__(kGThreads) cal_gram_kernel(const float* __restrict__ Q, int k,
+                                                             int d, int cs, float* __restrict__ Gp,
+                                                             float* __restrict__ G, int kp,
+                                                             CalCtl* __restrict__ ctl,
+                                                             int only_if_need2) {
+  __shared__ __align__(16) float As[kGChunk][kPtStride];
+  __shared__ __align__(16) float Bs[kGChunk][kPtStride];
+  __shared__ float red[3][kCB][kCB + 1];
+  __shared__ int s_last;
+  pdl_launch_dependents();
+  pdl_wait();
+  if (only_if_need2 && *reinterpret_cast<volatile int32_t*>(&ctl->need2) == 0) return;
+  const int p = blockIdx.x, sl = blockIdx.y, S = gridDim.y;
+  int I, J;
+  unpack_tri(p, I, J);
+  const int tid = threadIdx.x, g = tid >> 6, u = tid & 63, ty = u >> 3, tx = u & 7;
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  const int c_begin = sl * cs, c_end = min(d, c_begin + cs);
+  for (int c0 = c_begin; c0 < c_end; c0 += kGChunk) {
+    __syncthreads();
+    for (int q = tid; q < kCB * kGChunk; q += kGThreads) {
+      const int r = q / kGChunk, m = q % kGChunk, col = c0 + m;
+      const int ra = I * kCB + r, rb = J * kCB + r;
+      const bool okc = col < c_end;
+      As[m][r] = (okc && ra < k) ? Q[size_t(ra) * d + col] : 0.f;
+      Bs[m][r] = (okc && rb < k) ? Q[size_t(rb) * d + col] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int m = g; m < kGChunk; m += 4) {
+      const float4 a = *reinterpret_cast<const float4*>(&As[m][4 * ty]);
+      const float4 b = *reinterpret_cast<const float4*>(&Bs[m][4 * tx]);
+      const float av[4] = {a.x, a.y, a.z, a.w};
+      const float bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+  }
+  if (g > 0) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) red[g - 1][4 * ty + i][4 * tx + j] = acc[i][j];
+  }
+  __syncthreads();
+  float* part = Gp + (size_t(p) * S + sl) * (kCB * kCB);
+  if (g == 0) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int r = 4 * ty + i, c = 4 * tx + j;
+        part[r * kCB + c] = ((acc[i][j] + red[0][r][c]) + red[1][r][c]) + red[2][r][c];
+      }
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = (atomicAdd(&ctl->counters[p], 1u) == unsigned(S - 1)) ? 1 : 0;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  for (int e = tid; e < kCB * kCB; e += kGThreads) {
+    float v = 0.f;
+    for (int s2 = 0; s2 < S; ++s2) v += __ldcg(&Gp[(size_t(p) * S + s2) * (kCB * kCB) + e]);
+    G[size_t(I * kCB + (e >> 5)) * kp + J * kCB + (e & 31)] = v;
+  }
+  if (tid == 0) ctl->counters[p] = 0;
+}
+
+// ---- one-CTA blocked Cholesky of D G D + shift I -----------------------------
+// Right-looking over 32-wide block columns.  Shared memory holds the lower
+// blocks (32 x 33 rows), the current panel transposed (for the register-tiled
+// trailing update) and the inverse of the current diagonal block.  Outputs:
+// L (kp x kp, lower blocks; rows/cols >= k padded with the identity), the
+// inverses of its diagonal blocks (nb x 32 x 32), D (kp; 0 past k).  Pivots
+// below kPivotFloor (or NaN) are replaced by 1 and raise kStatusRank; a first
+// pass whose pivots are all >= kPivotSkip2 leaves need2 = 0.
+constexpr int kCThreads = 512;
+
+size_t chol_smem_bytes(int nb) {
+  return size_t(tri(nb)) * kBlk * 4 + size_t(std::max(1, nb - 1)) * kPtBlk * 4 + size_t(kBlk) * 4 +
+         size_t(nb) * kCB * 4;
+}
+
+__global__ void __launch_bounds__(kCThreads, 1)
+    cal_chol_kernel(const float* __restrict__ G, int k, int kp, float shift, int first_pass,
+                    float* __restrict__ Lg, float* __restrict__ LIg, float* __restrict__ Dg,
+                    CalCtl* __restrict__ ctl, int only_if_need2) {
+  extern __shared__ __align__(16) float csm[];
+  __shared__ int s_bad;
+  __shared__ int s_small;
+  pdl_launch_dependents();
+  pdl_wait();
+  if (only_if_need2 && *reinterpret_cast<volatile int32_t*>(&ctl->need2) == 0) return;
+  const int nb = kp / kCB, np = tri(nb);
+  float* A = csm;
+  float* PT = A + size_t(np) * kBlk;
+  float* LI = PT + size_t(max(1, nb - 1)) * kPtBlk;
+  float* Ds = LI + kBlk;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  constexpr int kWarps = kCThreads / 32;
+  if (tid == 0) {
+    s_bad = 0;
+    s_small = 0;
+  }
+  __syncthreads();
+  for (int i = tid; i < kp; i += kCThreads) {
+    float dv = 0.f;
+    if (i < k) {
+      const float gii = G[size_t(i) * kp + i];
+      if (gii > 0.f && gii <= 3.0e38f)
+        dv = 1.0f / sqrtf(gii);
+      else
+        s_bad = 1;
+    }
+    Ds[i] = dv;
+    Dg[i] = dv;
+  }
+  __syncthreads();
+  for (int q = tid; q < np * kCB * kCB; q += kCThreads) {
+    const int b = q >> 10, e = q & 1023, r = e >> 5, c = e & 31;
+    int I, J;
+    unpack_tri(b, I, J);
+    const int i = I * kCB + r, j = J * kCB + c;
+    float v;
+    if (i == j)
+      v = (i < k && Ds[i] > 0.f) ? G[size_t(i) * kp + i] * Ds[i] * Ds[i] + shift : 1.f;
+    else if (i < k && j < k)
+      v = G[size_t(max(i, j)) * kp + min(i, j)] * Ds[i] * Ds[j];
+    else
+      v = 0.f;
+    A[size_t(b) * kBlk + r * (kCB + 1) + c] = v;
+  }
+  __syncthreads();
+
+  for (int J = 0; J < nb; ++J) {
+    float* AJJ = A + size_t(tri(J) + J) * kBlk;
+    if (warp == 0) {
+      // lane i holds row i of the diagonal block
+      float a[kCB];
+#pragma unroll
+      for (int m = 0; m < kCB; ++m) a[m] = AJJ[lane * (kCB + 1) + m];
+      bool bad = false, small = false;
+#pragma unroll
+      for (int c = 0; c < kCB; ++c) {
+        float piv = __shfl_sync(0xffffffffu, a[c], c);
+        if (!(piv >= kPivotFloor)) {
+          bad = true;
+          piv = 1.f;
+        }
+        if (piv < kPivotSkip2) small = true;
+        const float sd = sqrtf(piv);
+        const float l = (lane == c) ? sd : ((lane > c) ? a[c] / sd : 0.f);
+        a[c] = l;
+#pragma unroll
+        for (int m = c + 1; m < kCB; ++m) a[m] = fmaf(-l, __shfl_sync(0xffffffffu, l, m), a[m]);
+      }
+#pragma unroll
+      for (int m = 0; m < kCB; ++m) AJJ[lane * (kCB + 1) + m] = (m <= lane) ? a[m] : 0.f;
+      if (lane == 0) {
+        if (bad) s_bad = 1;
+        if (small) s_small = 1;
+      }
+      __syncwarp();
+      // inverse of the diagonal block; lane j holds column j
+      float x[kCB];
+#pragma unroll
+      for (int i = 0; i < kCB; ++i) {
+        float acc = (i == lane) ? 1.f : 0.f;
+#pragma unroll
+        for (int m = 0; m < i; ++m) acc = fmaf(-AJJ[i * (kCB + 1) + m], x[m], acc);
+        x[i] = acc / AJJ[i * (kCB + 1) + i];
+      }
+#pragma unroll
+      for (int i = 0; i < kCB; ++i) {
+        LI[i * (kCB + 1) + lane] = x[i];
+        LIg[size_t(J) * kCB * kCB + i * kCB + lane] = x[i];
+      }
+    }
+    __syncthreads();
+    // panel: L_IJ = A_IJ Linv_JJ^T for the block rows below, kept transposed too
+    const int rows_below = (nb - 1 - J) * kCB;
+    for (int rr = warp; rr < rows_below; rr += kWarps) {
+      const int I = J + 1 + (rr >> 5), r = rr & 31;
+      float* AIJ = A + size_t(tri(I) + J) * kBlk;
+      float acc = 0.f;
+#pragma unroll
+      for (int m = 0; m < kCB; ++m) acc = fmaf(AIJ[r * (kCB + 1) + m], LI[lane * (kCB + 1) + m], acc);
+      __syncwarp();
+      AIJ[r * (kCB + 1) + lane] = acc;
+      PT[size_t(I - J - 1) * kPtBlk + lane * kPtStride + r] = acc;
+    }
+    __syncthreads();
+    // trailing update A_IL -= L_IJ L_LJ^T, J < L <= I; one warp per block pair,
+    // each lane a 4 x 8 patch
+    const int n1 = nb - 1 - J;
+    const int lr = lane >> 2, lc = lane & 3;
+    for (int pp = warp; pp < tri(n1); pp += kWarps) {
+      int Ip, Lp;
+      unpack_tri(pp, Ip, Lp);
+      const float* PI = PT + size_t(Ip) * kPtBlk;
+      const float* PL = PT + size_t(Lp) * kPtBlk;
+      float acc[4][8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+#pragma unroll 4
+      for (int m = 0; m < kCB; ++m) {
+        const float4 av = *reinterpret_cast<const float4*>(PI + m * kPtStride + 4 * lr);
+        const float4 b0 = *reinterpret_cast<const float4*>(PL + m * kPtStride + 8 * lc);
+        const float4 b1 = *reinterpret_cast<const float4*>(PL + m * kPtStride + 8 * lc + 4);
+        const float a4[4] = {av.x, av.y, av.z, av.w};
+        const float b8[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a4[i], b8[j], acc[i][j]);
+      }
+      float* AIL = A + size_t(tri(J + 1 + Ip) + J + 1 + Lp) * kBlk;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) AIL[(4 * lr + i) * (kCB + 1) + 8 * lc + j] -= acc[i][j];
+    }
+    __syncthreads();
+  }
+  for (int q = tid; q < np * kCB * kCB; q += kCThreads) {
+    const int b = q >> 10, e = q & 1023, r = e >> 5, c = e & 31;
+    int I, J;
+    unpack_tri(b, I, J);
+    Lg[size_t(I * kCB + r) * kp + J * kCB + c] = A[size_t(b) * kBlk + r * (kCB + 1) + c];
+  }
+  if (tid == 0) {
+    if (s_bad) atomicOr(&ctl->status, kStatusRank);
+    if (first_pass) ctl->need2 = s_small ? 1 : 0;
+  }
+}
+
+// ---- apply: Q^T[:, slice] = L^-1 D Y^T[:, slice] (blocked forward substitution)
+// One CTA per 32 columns of d.  The slice (kp x 32, D-scaled) sits in shared
+// memory; block row I is updated by the L blocks to its left (staged
+// transposed) and multiplied by the inverse of L_II.  Outputs (any may be
+// null): outF fp32 k x d, outB bf16 k x d, outV bf16 d x k (the basis layout).
+constexpr int kAThreads = 256;
+constexpr int kACols = 32;
+
+size_t apply_smem_bytes(int nb) {
+  return size_t(nb) * kCB * (kACols + 1) * 4            // slice
+         + size_t(std::max(1, nb - 1)) * kCB * kPtStride * 4  // L row panel, transposed
+         + size_t(kCB) * kPtStride * 4                    // inverse of L_II, transposed
+         + size_t(kCB) * (kACols + 1) * 4;                // block row before the inverse
+}
+
+__global__ void __launch_bounds__(kAThreads)
+    cal_apply_kernel(const float* __restrict__ Y, int k, int d, int kp, const float* __restrict__ Dg,
+                     const float* __restrict__ Lg, const float* __restrict__ LIg,
+                     float* __restrict__ outF, __nv_bfloat16* __restrict__ outB,
+                     __nv_bfloat16* __restrict__ outV, const CalCtl* __restrict__ ctl,
+                     int only_if_need2) {
+  extern __shared__ __align__(16) float asm_[];
+  pdl_launch_dependents();
+  pdl_wait();
+  if (only_if_need2 && *reinterpret_cast<const volatile int32_t*>(&ctl->need2) == 0) return;
+  const int nb = kp / kCB;
+  float* Xs = asm_;                                     // kp x 33
+  float* Lp = Xs + size_t(kp) * (kACols + 1);           // (32 (nb-1)) x 36
+  float* LIt = Lp + size_t(max(1, nb - 1)) * kCB * kPtStride;  // 32 x 36
+  float* Ts = LIt + kCB * kPtStride;                    // 32 x 33
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int c0 = blockIdx.x * kACols;
+  const bool col_ok = c0 + lane < d;
+  for (int r = warp; r < kp; r += kAThreads / 32)
+    Xs[r * (kACols + 1) + lane] = (r < k && col_ok) ? Dg[r] * Y[size_t(r) * d + c0 + lane] : 0.f;
+  for (int I = 0; I < nb; ++I) {
+    const int w = 32 * I;  // columns of L left of the diagonal block
+    __syncthreads();
+    for (int q = tid; q < kCB * w; q += kAThreads) {
+      const int r = q / w, m = q % w;
+      Lp[m * kPtStride + r] = Lg[size_t(I * kCB + r) * kp + m];
+    }
+    for (int q = tid; q < kCB * kCB; q += kAThreads) {
+      const int r = q >> 5, m = q & 31;
+      LIt[m * kPtStride + r] = LIg[size_t(I) * kCB * kCB + q];
+    }
+    __syncthreads();
+    float acc[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) acc[q] = Xs[(I * kCB + 4 * warp + q) * (kACols + 1) + lane];
+    for (int m = 0; m < w; ++m) {
+      const float4 l4 = *reinterpret_cast<const float4*>(Lp + m * kPtStride + 4 * warp);
+      const float x = Xs[m * (kACols + 1) + lane];
+      acc[0] = fmaf(-l4.x, x, acc[0]);
+      acc[1] = fmaf(-l4.y, x, acc[1]);
+      acc[2] = fmaf(-l4.z, x, acc[2]);
+      acc[3] = fmaf(-l4.w, x, acc[3]);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) Ts[(4 * warp + q) * (kACols + 1) + lane] = acc[q];
+    __syncthreads();
+    float o[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+    for (int m = 0; m < kCB; ++m) {
+      const float4 l4 = *reinterpret_cast<const float4*>(LIt + m * kPtStride + 4 * warp);
+      const float t = Ts[m * (kACols + 1) + lane];
+      o[0] = fmaf(l4.x, t, o[0]);
+      o[1] = fmaf(l4.y, t, o[1]);
+      o[2] = fmaf(l4.z, t, o[2]);
+      o[3] = fmaf(l4.w, t, o[3]);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) Xs[(I * kCB + 4 * warp + q) * (kACols + 1) + lane] = o[q];
+  }
+  __syncthreads();
+  if (outF || outB) {
+    for (int r = warp; r < k; r += kAThreads / 32) {
+      if (!col_ok) continue;
+      const float v = Xs[r * (kACols + 1) + lane];
+      if (outF) outF[size_t(r) * d + c0 + lane] = v;
+      if (outB) outB[size_t(r) * d + c0 + lane] = __float2bfloat16_rn(v);
+    }
+  }
+  if (outV) {
+    // row c0 + c of V holds column c of the slice; lanes cover pairs of rows r
+    for (int c = warp; c < kACols; c += kAThreads / 32) {
+      if (c0 + c >= d) continue;
+      for (int r = 2 * lane; r < k; r += 64) {
+        __nv_bfloat162 v2;
+        v2.x = __float2bfloat16_rn(Xs[r * (kACols + 1) + c]);
+        v2.y = __float2bfloat16_rn(Xs[(r + 1) * (kACols + 1) + c]);
+        *reinterpret_cast<__nv_bfloat162*>(&outV[size_t(c0 + c) * k + r]) = v2;
+      }
+    }
+  }
+}
+
+// ---- host side ----------------------------------------------------------------
+
+struct CalLayout {
+  size_t ctl, XT, QT, ZT, P1, Y, P2, Q1, Gp, G, L, LI, D, total;
+};
+
+constexpr int kMaxGramSlices = 32;
+
+CalLayout cal_layout(int64_t n, int64_t d, int64_t k) {
+  const int64_t kp = (k + kCB - 1) / kCB * kCB, nb = kp / kCB;
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  CalLayout o{};
+  size_t at = 0;
+  auto take = [&](size_t bytes) {
+    const size_t here = at;
+    at += up(bytes);
+    return here;
+  };
+  o.ctl = take(sizeof(CalCtl));
+  o.XT = take(size_t(d) * n * 2);
+  o.QT = take(size_t(k) * d * 2);
+  o.ZT = take(size_t(k) * n * 2);
+  o.P1 = take(size_t(kProjMaxSplits) * k * n * 4);
+  o.Y = take(size_t(k) * d * 4);
+  o.P2 = take(size_t(kProjMaxSplits) * k * d * 4);
+  o.Q1 = take(size_t(k) * d * 4);
+  o.Gp = take(size_t(kMaxGramSlices) * tri(int(nb)) * kCB * kCB * 4);
+  o.G = take(size_t(kp) * kp * 4);
+  o.L = take(size_t(kp) * kp * 4);
+  o.LI = take(size_t(nb) * kCB * kCB * 4);
+  o.D = take(size_t(kp) * 4);
+  o.total = at;
+  return o;
+}
+
+bool cal_shape_ok(int64_t n, int64_t d, int64_t k) {
+  const bool k_ok = k == 16 || k == 32 || k == 64 || k == 128 || k == 256;
+  return k_ok && d >= k && n >= k && d % 8 == 0 && n % 8 == 0 && d <= (int64_t(1) << 30) &&
+         n <= (int64_t(1) << 30) && size_t(d) * size_t(n) <= (size_t(1) << 40);
+}
+
+struct CalRun {
+  int64_t n, d, k, kp, nb;
+  CalLayout lay;
+  unsigned char* ws;
+  CalCtl* ctl;
+  int sms;
+  cudaStream_t s;
+  template <typename T>
+  T* at(size_t off) const {
+    return reinterpret_cast<T*>(ws + off);
+  }
+};
+
+gsi_status_t orth_pass(const CalRun& r, const float* Yin, bool first, int only_if_need2,
+                       float* outF, __nv_bfloat16* outB, __nv_bfloat16* outV) {
+  const int np = tri(int(r.nb));
+  const int d = int(r.d);
+  int S = std::max(1, std::min(kMaxGramSlices, (2 * r.sms + np - 1) / np));
+  S = std::min(S, std::max(1, d / 256));
+  int cs = (d + S - 1) / S;
+  cs = (cs + kGChunk - 1) / kGChunk * kGChunk;
+  S = (d + cs - 1) / cs;
+  float* Gp = r.at<float>(r.lay.Gp);
+  float* G = r.at<float>(r.lay.G);
+  float* L = r.at<float>(r.lay.L);
+  float* LI = r.at<float>(r.lay.LI);
+  float* D = r.at<float>(r.lay.D);
+  if (launch_pdl(cal_gram_kernel, dim3(unsigned(np), unsigned(S)), dim3(kGThreads), 0, r.s, Yin,
+                 int(r.k), d, cs, Gp, G, int(r.kp), r.ctl, only_if_need2) != cudaSuccess)
+    return GSI_ERR_CUDA;
+  if (launch_pdl(cal_chol_kernel, dim3(1), dim3(kCThreads), chol_smem_bytes(int(r.nb)), r.s,
+                 (const float*)G, int(r.k), int(r.kp), first ? kShift1 : 0.f, first ? 1 : 0, L, LI, D,
+                 r.ctl, only_if_need2) != cudaSuccess)
+    return GSI_ERR_CUDA;
+  const unsigned ncta = unsigned((r.d + kACols - 1) / kACols);
+  if (launch_pdl(cal_apply_kernel, dim3(ncta), dim3(kAThreads), apply_smem_bytes(int(r.nb)), r.s,
+                 Yin, int(r.k), d, int(r.kp), (const float*)D, (const float*)L, (const float*)LI, outF,
+                 outB, outV, (const CalCtl*)r.ctl, only_if_need2) != cudaSuccess)
+    return GSI_ERR_CUDA;
+  return GSI_OK;
+}
+
+gsi_status_t cal_prepare() {
+  static bool done = false;
+  if (done) return GSI_OK;
+  if (cudaFuncSetAttribute(cal_chol_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(chol_smem_bytes(kCalMaxNb))) != cudaSuccess ||
+      cudaFuncSetAttribute(cal_apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(apply_smem_bytes(kCalMaxNb))) != cudaSuccess)
+    return GSI_ERR_CUDA;
+  const gsi_status_t st = tc_nt_prepare();
+  if (st != GSI_OK) return st;
+  done = true;
+  return GSI_OK;
+}
+
+// Launches per call, for the accounting entry point.
+int cal_launches(int64_t n, int64_t d, int64_t k, int iters, int sms) {
+  const int per_pass = 3;
+  if (iters == 0) return 1 + 2 * per_pass;
+  int kb1, kb2;
+  const int S2 = tc_nt_splits(d, k, n, sms, &kb2);
+  (void)tc_nt_splits(n, k, d, sms, &kb1);
+  const int per_iter = 3 + (S2 > 1 ? 1 : 0) + 2 * per_pass;
+  return 2 + iters * per_iter;
+}
+
+}  // namespace
+}  // namespace gsi
+
+using namespace gsi;
+
+extern "C" {
+
+gsi_status_t gsi_calibrate_workspace_size(int64_t n, int64_t d, int64_t k, size_t* bytes) {
+  if (!bytes) return GSI_ERR_INVALID_ARG;
+  *bytes = 0;
+  if (!cal_shape_ok(n, d, k)) return GSI_ERR_UNSUPPORTED_SHAPE;
+  *bytes = cal_layout(n, d, k).total;
+  return GSI_OK;
+}
+
+int gsi_calibrate_launch_count(int64_t n, int64_t d, int64_t k, int iters) {
+  if (!cal_shape_ok(n, d, k) || iters < 0) return 0;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return cal_launches(n, d, k, iters, sms);
+}
+
+gsi_status_t gsi_calibrate(const void* X, int64_t n, int64_t d, int64_t k, const void* Q0,
+                           int iters, void* V_k, void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream) {
+  if (!X || !Q0 || !V_k || !workspace || iters < 0 || iters > 10000) return GSI_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(Q0) || !aligned16(V_k) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return GSI_ERR_INVALID_ARG;
+  if (!cal_shape_ok(n, d, k)) return GSI_ERR_UNSUPPORTED_SHAPE;
+  CalRun r;
+  r.n = n;
+  r.d = d;
+  r.k = k;
+  r.kp = (k + kCB - 1) / kCB * kCB;
+  r.nb = r.kp / kCB;
+  r.lay = cal_layout(n, d, k);
+  if (workspace_bytes < r.lay.total) return GSI_ERR_WORKSPACE;
+  r.ws = static_cast<unsigned char*>(workspace);
+  r.ctl = r.at<CalCtl>(r.lay.ctl);
+  r.s = stream;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&r.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return GSI_ERR_CUDA;
+  gsi_status_t st = cal_prepare();
+  if (st != GSI_OK) return st;
+  if (cudaMemsetAsync(r.ctl, 0, sizeof(CalCtl), stream) != cudaSuccess) return GSI_ERR_CUDA;
+
+  const auto* Xb = static_cast<const __nv_bfloat16*>(X);
+  const auto* Q0b = static_cast<const __nv_bfloat16*>(Q0);
+  auto* XT = r.at<__nv_bfloat16>(r.lay.XT);
+  auto* QT = r.at<__nv_bfloat16>(r.lay.QT);
+  auto* ZT = r.at<__nv_bfloat16>(r.lay.ZT);
+  float* P1 = r.at<float>(r.lay.P1);
+  float* Y = r.at<float>(r.lay.Y);
+  float* P2 = r.at<float>(r.lay.P2);
+  float* Q1 = r.at<float>(r.lay.Q1);
+  auto* V = static_cast<__nv_bfloat16*>(V_k);
+  uint32_t* status = &r.ctl->status;
+  const dim3 tb(256);
+
+  if (iters == 0) {
+    // V_k = orth(Q0): the block itself, in fp32, through both passes
+    const dim3 g(unsigned((k + 31) / 32), unsigned((d + 31) / 32));
+    if (launch_pdl(cal_transpose_kernel<float>, g, tb, 0, stream, Q0b, int(d), int(k), Y) !=
+        cudaSuccess)
+      return GSI_ERR_CUDA;
+    if ((st = orth_pass(r, Y, true, 0, Q1, nullptr, nullptr)) != GSI_OK) return st;
+    return orth_pass(r, Q1, false, 0, nullptr, nullptr, V);
+  }
+
+  {
+    const dim3 gx(unsigned((d + 31) / 32), unsigned((n + 31) / 32));
+    if (launch_pdl(cal_transpose_kernel<__nv_bfloat16>, gx, tb, 0, stream, Xb, int(n), int(d), XT) !=
+        cudaSuccess)
+      return GSI_ERR_CUDA;
+    const dim3 gq(unsigned((k + 31) / 32), unsigned((d + 31) / 32));
+    if (launch_pdl(cal_transpose_kernel<__nv_bfloat16>, gq, tb, 0, stream, Q0b, int(d), int(k), QT) !=
+        cudaSuccess)
+      return GSI_ERR_CUDA;
+  }
+  int kb1, kb2;
+  const int S1 = tc_nt_splits(n, k, d, r.sms, &kb1);
+  const int S2 = tc_nt_splits(d, k, n, r.sms, &kb2);
+  const size_t kn = size_t(k) * n, kd = size_t(k) * d;
+  const unsigned sum_grid1 = unsigned(std::min<size_t>(4 * size_t(r.sms), (kn / 4 + 255) / 256));
+  const unsigned sum_grid2 = unsigned(std::min<size_t>(4 * size_t(r.sms), (kd / 4 + 255) / 256));
+  for (int it = 0; it < iters; ++it) {
+    const bool last = it + 1 == iters;
+    // Z^T = Q^T X^T: P1[s][j][t]
+    if ((st = tc_nt_gemm(Xb, n, QT, k, d, P1, kn, S1, kb1, status, stream)) != GSI_OK) return st;
+    if (launch_pdl(cal_sum_kernel<__nv_bfloat16>, dim3(std::max(1u, sum_grid1)), tb, 0, stream,
+                   (const float*)P1, S1, kn, kn, ZT) != cudaSuccess)
+      return GSI_ERR_CUDA;
+    // Y^T = Z^T X: P2[s][j][i]
+    float* Ydst = (S2 > 1) ? P2 : Y;
+    if ((st = tc_nt_gemm(XT, d, ZT, k, n, Ydst, kd, S2, kb2, status, stream)) != GSI_OK) return st;
+    if (S2 > 1 && launch_pdl(cal_sum_kernel<float>, dim3(std::max(1u, sum_grid2)), tb, 0, stream,
+                             (const float*)P2, S2, kd, kd, Y) != cudaSuccess)
+      return GSI_ERR_CUDA;
+    // CholeskyQR2 (the second pass only where needed, except at the end)
+    if ((st = orth_pass(r, Y, true, 0, Q1, last ? nullptr : QT, nullptr)) != GSI_OK) return st;
+    if ((st = orth_pass(r, Q1, false, last ? 0 : 1, nullptr, last ? nullptr : QT,
+                        last ? V : nullptr)) != GSI_OK)
+      return st;
+  }
+  return GSI_OK;
+}
+
+gsi_status_t gsi_calibrate_status(const void* workspace, cudaStream_t stream) {
+  if (!workspace) return GSI_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return GSI_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, workspace, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return GSI_ERR_CUDA;
+  if (word & kStatusBadLaunch) return GSI_ERR_LAUNCH;
+  if (word & kStatusTimeout) return GSI_ERR_TIMEOUT;
+  return (word & kStatusRank) ? GSI_ERR_RANK : GSI_OK;
+}
+
+}  // extern "C"

@@ -454,6 +454,48 @@ int tc_proj_splits(const gsi_handle* h, int64_t T, int* kb_per) {
   return S;
 }
 
+gsi_status_t tc_nt_prepare() {
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(tc_proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(kPSmem)) != cudaSuccess)
+      return GSI_ERR_CUDA;
+    attr = true;
+  }
+  return GSI_OK;
+}
+
+int tc_nt_splits(int64_t rows_a, int64_t rows_b, int64_t K, int num_sms, int* kb_per) {
+  const int nkb = int((K + kBK - 1) / kBK);
+  const int tiles = int((rows_a + kBM - 1) / kBM) * int((rows_b + kPN - 1) / kPN);
+  int S = std::max(1, std::min({kProjMaxSplits, nkb, (num_sms + tiles - 1) / tiles}));
+  *kb_per = (nkb + S - 1) / S;
+  return (nkb + *kb_per - 1) / *kb_per;  // no empty slices
+}
+
+gsi_status_t tc_nt_gemm(const void* A, int64_t rows_a, const void* B, int64_t rows_b, int64_t K,
+                        float* P, size_t split_stride, int S, int kb_per, uint32_t* status,
+                        cudaStream_t s) {
+  if (rows_a <= 0 || rows_b <= 0 || K <= 0 || K % 8 != 0 || !aligned16(A) || !aligned16(B))
+    return GSI_ERR_UNSUPPORTED_SHAPE;
+  CUtensorMap tmA, tmB;
+  if (!tma_encode_bf16_2d(&tmA, A, uint64_t(rows_a), uint64_t(K), uint32_t(kBM), kBK) ||
+      !tma_encode_bf16_2d(&tmB, B, uint64_t(rows_b), uint64_t(K), uint32_t(kPN), kBK))
+    return GSI_ERR_CUDA;
+  TcProjArgs a;
+  a.P = P;
+  a.T = int(rows_b);
+  a.d = int(K);
+  a.k = int(rows_a);
+  a.kb_per = kb_per;
+  a.split_stride = split_stride;
+  a.status = status;
+  dim3 grid(unsigned((rows_a + kBM - 1) / kBM), unsigned((rows_b + kPN - 1) / kPN), unsigned(S));
+  return launch_pdl(tc_proj_kernel, grid, dim3(kTcThreads), kPSmem, s, tmA, tmB, a) == cudaSuccess
+             ? GSI_OK
+             : GSI_ERR_CUDA;
+}
+
 gsi_status_t tc_proj_launch(gsi_handle* h, const void* x, int64_t T, int S, int kb_per, cudaStream_t s) {
   CUtensorMap tmX;
   if (!tma_encode_bf16_2d(&tmX, x, uint64_t(T), uint64_t(h->d), uint32_t(kPN), kBK)) return GSI_ERR_CUDA;

@@ -47,6 +47,17 @@ int tc_proj_splits(const gsi_handle* h, int64_t T, int* kb_per);
 gsi_status_t tc_proj_launch(gsi_handle* h, const void* x, int64_t T, int S, int kb_per,
                             cudaStream_t s);
 
+// The projection kernel as a general split-K product on the tensor cores:
+// P[s][b][a] = sum over slice s of the K axis of A[a][:] . B[b][:], with A
+// (rows_a x K) and B (rows_b x K) row-major bf16 (16-byte aligned,
+// K % 8 == 0), fp32 partials with slice stride split_stride.  Ragged edges
+// are read as zeros by the tensor maps.  S * kb_per * 64 must cover K.
+gsi_status_t tc_nt_prepare();
+int tc_nt_splits(int64_t rows_a, int64_t rows_b, int64_t K, int num_sms, int* kb_per);
+gsi_status_t tc_nt_gemm(const void* A, int64_t rows_a, const void* B, int64_t rows_b, int64_t K,
+                        float* P, size_t split_stride, int S, int kb_per, uint32_t* status,
+                        cudaStream_t s);
+
 // Build the TMA tensor maps of a handle (after its workspace is bound).
 gsi_status_t tc_gemm_prepare(gsi_handle* h);
 // One launch computing both GEMMs for T tokens.

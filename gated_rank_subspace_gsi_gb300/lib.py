@@ -22,13 +22,15 @@ GSI_ERR_CUDA = 4
 GSI_ERR_WORKSPACE = 5
 GSI_ERR_TIMEOUT = 6
 GSI_ERR_LAUNCH = 7
+GSI_ERR_RANK = 8
 
 # every function declared in include/gsi.h
 EXPORTS = ("gsi_create", "gsi_forward", "gsi_forward_host", "gsi_precompute_M",
            "gsi_reserve", "gsi_device_status", "gsi_destroy", "gsi_status_string",
            "gsi_forward_launch_count", "gsi_forward_noalloc", "gsi_set_prefetch",
            "gsi_set_prefetch_group", "gsi_group_create", "gsi_group_forward",
-           "gsi_group_set_prefetch", "gsi_group_destroy")
+           "gsi_group_set_prefetch", "gsi_group_destroy", "gsi_calibrate_workspace_size",
+           "gsi_calibrate", "gsi_calibrate_status", "gsi_calibrate_launch_count")
 
 _lock = threading.Lock()
 _lib = None
@@ -85,6 +87,14 @@ def _load():
         lib.gsi_group_set_prefetch.restype = ctypes.c_int
         lib.gsi_group_destroy.argtypes = [P]
         lib.gsi_group_destroy.restype = None
+        lib.gsi_calibrate_workspace_size.argtypes = [I64, I64, I64, ctypes.POINTER(ctypes.c_size_t)]
+        lib.gsi_calibrate_workspace_size.restype = ctypes.c_int
+        lib.gsi_calibrate.argtypes = [P, I64, I64, I64, P, ctypes.c_int, P, P, ctypes.c_size_t, P]
+        lib.gsi_calibrate.restype = ctypes.c_int
+        lib.gsi_calibrate_status.argtypes = [P, P]
+        lib.gsi_calibrate_status.restype = ctypes.c_int
+        lib.gsi_calibrate_launch_count.argtypes = [I64, I64, I64, ctypes.c_int]
+        lib.gsi_calibrate_launch_count.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -272,3 +282,36 @@ class GatedLinear:
             self.close()
         except Exception:
             pass
+
+
+# ---- calibration of V_k ---------------------------------------------------
+
+
+def gsi_calibrate_workspace_size(n: int, d: int, k: int) -> int:
+    """Device scratch bytes gsi_calibrate needs for n tokens of width d, rank k."""
+    out = ctypes.c_size_t()
+    _check(_load().gsi_calibrate_workspace_size(int(n), int(d), int(k), ctypes.byref(out)),
+           "gsi_calibrate_workspace_size")
+    return int(out.value)
+
+
+def gsi_calibrate(X, Q0, iters: int, V_k, workspace, stream=None):
+    """V_k (d x k bf16) = orthonormal basis of span((X^T X)^iters Q0), by block
+    power iteration on the GPU.  X (n x d), Q0 (d x k): bf16 CUDA tensors;
+    workspace: a CUDA tensor of at least gsi_calibrate_workspace_size bytes."""
+    n, d = X.shape
+    d2, k = Q0.shape
+    if d2 != d or tuple(V_k.shape) != (d, k):
+        raise ValueError("X, Q0 and V_k shapes disagree")
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(_load().gsi_calibrate(_ptr(X), n, d, k, _ptr(Q0), int(iters), _ptr(V_k),
+                                 _ptr(workspace), nbytes, _stream(stream)), "gsi_calibrate")
+
+
+def gsi_calibrate_status(workspace, stream=None) -> int:
+    """Synchronise the stream; the device-side status of the last gsi_calibrate."""
+    return int(_load().gsi_calibrate_status(_ptr(workspace), _stream(stream)))
+
+
+def gsi_calibrate_launch_count(n: int, d: int, k: int, iters: int) -> int:
+    return int(_load().gsi_calibrate_launch_count(int(n), int(d), int(k), int(iters)))

@@ -56,7 +56,8 @@ typedef enum {
     GSI_ERR_CUDA = 4,              /* a CUDA runtime call or launch failed */
     GSI_ERR_WORKSPACE = 5,         /* T larger than the reserved workspace */
     GSI_ERR_TIMEOUT = 6,           /* a device-side bounded wait ran out */
-    GSI_ERR_LAUNCH = 7             /* a kernel saw an inconsistent launch and did nothing */
+    GSI_ERR_LAUNCH = 7,            /* a kernel saw an inconsistent launch and did nothing */
+    GSI_ERR_RANK = 8               /* calibration: a block column vanished or the factorisation broke down */
 } gsi_status_t;
 
 /* Create a handle for one gated linear (section 2.1: W, V_k and M).
@@ -212,6 +213,59 @@ gsi_status_t gsi_forward_noalloc(const void *W, const void *V_k, const void *M,
                                  int64_t d_out, int64_t d, int64_t k, float eps,
                                  const void *x, float *y, uint8_t *gate,
                                  float *rho, cudaStream_t stream);
+
+/* ---- Calibration of V_k -------------------------------------------------
+ *
+ * Section 2.3 of the page computes the basis once from one forward pass over
+ * a representative calibration sequence, and gives no algorithm.  Here V_k
+ * spans the top-k eigenvectors of the uncentred second moment C = X^T X of
+ * the calibration tokens X (n x d): the rank-k subspace with the least summed
+ * squared residual ||x - V_k V_k^T x||^2 (section 2.1, eq. 1) over those
+ * tokens.  It is approached by block power iteration from a start block Q0:
+ *   Q <- orth(X^T (X Q)),  iters times,
+ * each product a tcgen05 GEMM with fp32 accumulation on bf16 operands (Q and
+ * X Q are rounded to bf16 between the products), orth() a two-pass Cholesky
+ * QR in fp32.  Only span(V_k) is defined: the basis inside the span (its
+ * rotation, the order of its columns) is whatever the orthonormalisation
+ * gives, and every use of V_k in this library depends on the span alone.
+ * The caller computes M = W V_k with gsi_precompute_M afterwards.
+ *
+ *   X          n x d bf16, the calibration tokens (device)
+ *   Q0         d x k bf16, the start block (device), full column rank; a
+ *              seeded Gaussian block is the usual choice.  Its span should
+ *              not be orthogonal to any top-k eigenvector (a random block is
+ *              not, with probability 1)
+ *   iters      number of applications of C (>= 0; 0 orthonormalises Q0)
+ *   V_k        d x k bf16 output (device), orthonormal columns up to bf16
+ *              rounding
+ *   workspace  device scratch of at least gsi_calibrate_workspace_size()
+ *              bytes, 256-byte aligned, owned by the caller, not shared by
+ *              calls that may overlap on the GPU
+ * Shapes: k in {16, 32, 64, 128, 256}, k <= d, k <= n, d % 8 == 0,
+ * n % 8 == 0 (else GSI_ERR_UNSUPPORTED_SHAPE).  A workspace smaller than
+ * required is GSI_ERR_WORKSPACE.  Asynchronous on `stream`; allocates
+ * nothing; the launch sequence does not depend on the data, so a call can be
+ * captured in a CUDA graph.  Each call clears the workspace's status word
+ * first; gsi_calibrate_status() then reports the call's device-side outcome:
+ * GSI_ERR_RANK when a column of the iterated block vanished (zero or
+ * non-finite norm: X Q has a zero column, e.g. X = 0 or a zero column in
+ * Q0) or a pivot of the unshifted Cholesky pass fell below 2^-20 on the
+ * unit-diagonal Gram matrix; V_k is then not valid.  GSI_ERR_TIMEOUT when a
+ * bounded wait of a tensor-core kernel ran out.  Tokens of rank below k are
+ * not an error: the top-k eigenspace is then not unique, and V_k is one of
+ * them up to the rounding that fills the missing directions. */
+gsi_status_t gsi_calibrate_workspace_size(int64_t n, int64_t d, int64_t k,
+                                          size_t *bytes);
+gsi_status_t gsi_calibrate(const void *X, int64_t n, int64_t d, int64_t k,
+                           const void *Q0, int iters, void *V_k,
+                           void *workspace, size_t workspace_bytes,
+                           cudaStream_t stream);
+/* Synchronise `stream` and read the status of the last gsi_calibrate on
+ * this workspace (see above). */
+gsi_status_t gsi_calibrate_status(const void *workspace, cudaStream_t stream);
+/* Kernel launches one gsi_calibrate(n, d, k, iters) issues on the current
+ * device (0 for unsupported shapes). */
+int gsi_calibrate_launch_count(int64_t n, int64_t d, int64_t k, int iters);
 
 #ifdef __cplusplus
 }

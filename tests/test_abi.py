@@ -41,8 +41,9 @@ def test_library_exports_every_declared_symbol(cl):
 
 
 def test_status_strings(cl):
-    for s in range(8):
+    for s in range(9):
         assert cl.gsi_status_string(s)
+    assert b"RANK" in cl.gsi_status_string(8)
     assert b"UNSUPPORTED" in cl.gsi_status_string(2)
 
 
@@ -87,3 +88,31 @@ def test_host_argument_checks(cl):
     cl.gsi_group_destroy(None)
     cl.gsi_destroy(None)
     del h
+
+
+def test_calibrate_argument_checks(cl):
+    """gsi_calibrate's shape, pointer and workspace checks (fake pointers,
+    never dereferenced: each case is rejected before any CUDA call)."""
+    A = ctypes.c_void_p(0x10000)
+    B = ctypes.c_void_p(0x20000)
+    C = ctypes.c_void_p(0x30000)
+    WS = ctypes.c_void_p(0x100000)     # 256-byte aligned
+    size = ctypes.c_size_t()
+    assert cl.gsi_calibrate_workspace_size(2048, 4096, 256, None) == 1
+    assert cl.gsi_calibrate_workspace_size(2048, 4096, 256, ctypes.byref(size)) == 0
+    need = size.value
+    assert need > 2048 * 4096 * 2            # holds X^T at least
+    assert cl.gsi_calibrate_workspace_size(2048, 4096, 512, ctypes.byref(size)) == 2   # k > 256
+    assert cl.gsi_calibrate_workspace_size(2048, 4096, 48, ctypes.byref(size)) == 2    # k not allowed
+    assert cl.gsi_calibrate_workspace_size(200, 4096, 256, ctypes.byref(size)) == 2    # n < k
+    assert cl.gsi_calibrate_workspace_size(2048, 4100, 256, ctypes.byref(size)) == 2   # d % 8
+    assert cl.gsi_calibrate_workspace_size(2044, 4096, 256, ctypes.byref(size)) == 2   # n % 8
+    assert cl.gsi_calibrate_workspace_size(64, 64, 16, ctypes.byref(size)) == 0
+    assert cl.gsi_calibrate(None, 2048, 4096, 256, B, 8, C, WS, need, None) == 1
+    assert cl.gsi_calibrate(A, 2048, 4096, 256, B, -1, C, WS, need, None) == 1
+    assert cl.gsi_calibrate(A, 2048, 4096, 256, B, 8, C, ctypes.c_void_p(0x100010), need, None) == 1
+    assert cl.gsi_calibrate(ctypes.c_void_p(0x10008), 2048, 4096, 256, B, 8, C, WS, need, None) == 1
+    assert cl.gsi_calibrate(A, 2048, 4096, 24, B, 8, C, WS, need, None) == 2
+    assert cl.gsi_calibrate(A, 2048, 4096, 256, B, 8, C, WS, need - 1, None) == 5
+    assert cl.gsi_calibrate_status(None, None) == 1
+    assert cl.gsi_calibrate_launch_count(2048, 4096, 48, 8) == 0
