@@ -162,16 +162,30 @@ __global__ void __launch_bounds__(kGThreads) cal_gram_kernel(const float* __rest
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
   const int c_begin = sl * cs, c_end = min(d, c_begin + cs);
-  for (int c0 = c_begin; c0 < c_end; c0 += kGChunk) {
-    __syncthreads();
-    for (int q = tid; q < kCB * kGChunk; q += kGThreads) {
-      const int r = q / kGChunk, m = q % kGChunk, col = c0 + m;
+  // the next chunk is loaded into registers while the current one is used
+  constexpr int kPer = kCB * kGChunk / kGThreads;  // 8 elements per operand
+  float na[kPer], nbv[kPer];
+  auto fetch = [&](int c0) {
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int q = tid + u * kGThreads, r = q / kGChunk, col = c0 + q % kGChunk;
       const int ra = I * kCB + r, rb = J * kCB + r;
       const bool okc = col < c_end;
-      As[m][r] = (okc && ra < k) ? Q[size_t(ra) * d + col] : 0.f;
-      Bs[m][r] = (okc && rb < k) ? Q[size_t(rb) * d + col] : 0.f;
+      na[u] = (okc && ra < k) ? Q[size_t(ra) * d + col] : 0.f;
+      nbv[u] = (okc && rb < k) ? Q[size_t(rb) * d + col] : 0.f;
+    }
+  };
+  if (c_begin < c_end) fetch(c_begin);
+  for (int c0 = c_begin; c0 < c_end; c0 += kGChunk) {
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int q = tid + u * kGThreads, r = q / kGChunk, m = q % kGChunk;
+      As[m][r] = na[u];
+      Bs[m][r] = nbv[u];
     }
     __syncthreads();
+    if (c0 + kGChunk < c_end) fetch(c0 + kGChunk);
 #pragma unroll 4
     for (int m = g; m < kGChunk; m += 4) {
       const float4 a = *reinterpret_cast<const float4*>(&As[m][4 * ty]);
@@ -226,8 +240,92 @@ __global__ void __launch_bounds__(kGThreads) cal_gram_kernel(const float* __rest
 constexpr int kCThreads = 512;
 
 size_t chol_smem_bytes(int nb) {
-  return size_t(tri(nb)) * kBlk * 4 + size_t(std::max(1, nb - 1)) * kPtBlk * 4 + size_t(kBlk) * 4 +
+  return size_t(tri(nb)) * kBlk * 4 + size_t(std::max(1, nb - 1)) * kPtBlk * 4 + 2 * size_t(kPtBlk) * 4 +
          size_t(nb) * kCB * 4;
+}
+
+// Factor the diagonal block AJJ (in place, lower triangle, zeros above) and
+// write its inverse to LI (shared, rows of kPtStride) and LIg (global); one
+// warp.  Flags pivots below the floor (replaced by 1) and pivots below the
+// skip threshold.
+//
+// Lane i keeps row i (factor) or column i (inverse) in registers as a window
+// that slides one entry per step, so the step loops stay rolled while every
+// register index is static.  Column c of L is published through LR (32 x
+// kPtStride, shared), row c, rotated so that entry c + 1 + m sits at m:
+// every lane then reads the entries its window needs as aligned 16-byte
+// broadcasts -- in the rank-1 update of step c and again in step c of the
+// forward substitution that forms the inverse.
+__device__ __forceinline__ void chol_diag_block(float* AJJ, float* LI, float* LR, float* LIg,
+                                                int lane, int* s_bad, int* s_small) {
+  constexpr unsigned kAll = 0xffffffffu;
+  // Start converged: a warp that arrives here split (after lane-divergent
+  // code) would run every shuffle below as a rendezvous of its splits, which
+  // costs about 25x the converged loop.
+  __syncwarp();
+  float w[kCB];
+#pragma unroll
+  for (int m = 0; m < kCB; ++m) w[m] = AJJ[lane * (kCB + 1) + m];
+  bool bad = false, small = false;
+  float my_inv = 0.f;  // 1 / L_ii of this lane's row
+#pragma unroll 1
+  for (int c = 0; c < kCB; ++c) {
+    // w[m] holds A[lane][c + m]
+    float piv = __shfl_sync(kAll, w[0], c);
+    if (!(piv >= kPivotFloor)) {
+      bad = true;
+      piv = 1.f;
+    }
+    if (piv < kPivotSkip2) small = true;
+    // rsqrtf's error (a few ulp) scales column c of L by 1 + O(1e-7): the
+    // span of the transformed block does not change and its orthonormality
+    // moves by that much, far below the fp32 Gram matrix's own rounding
+    const float inv = rsqrtf(piv);
+    const float l = (lane == c) ? piv * inv : ((lane > c) ? w[0] * inv : 0.f);
+    if (lane == c) my_inv = inv;
+    AJJ[lane * (kCB + 1) + c] = l;
+    float* row = LR + c * kPtStride;
+    row[(lane - c - 1) & (kCB - 1)] = l;  // L[c + 1 + m][c] at m
+    __syncwarp();
+#pragma unroll
+    for (int m4 = 0; m4 < kCB; m4 += 4) {
+      const float4 q = *reinterpret_cast<const float4*>(row + m4);
+      w[m4 + 1] = fmaf(-l, q.x, w[m4 + 1]);
+      if (m4 + 2 < kCB) w[m4 + 2] = fmaf(-l, q.y, w[m4 + 2]);
+      if (m4 + 3 < kCB) w[m4 + 3] = fmaf(-l, q.z, w[m4 + 3]);
+      if (m4 + 4 < kCB) w[m4 + 4] = fmaf(-l, q.w, w[m4 + 4]);
+    }
+#pragma unroll
+    for (int m = 0; m + 1 < kCB; ++m) w[m] = w[m + 1];
+  }
+  if (lane == 0) {
+    if (bad) *s_bad = 1;
+    if (small) *s_small = 1;
+  }
+  __syncwarp();
+  // inverse by forward substitution on the unit vectors; lane j owns column
+  // j, as a sliding window: x[m] holds entry i + m at step i
+  float x[kCB];
+#pragma unroll
+  for (int m = 0; m < kCB; ++m) x[m] = (m == lane) ? 1.f : 0.f;
+#pragma unroll 1
+  for (int i = 0; i < kCB; ++i) {
+    const float xi = x[0] * __shfl_sync(kAll, my_inv, i);
+    LI[i * kPtStride + lane] = xi;
+    LIg[i * kCB + lane] = xi;
+    const float* row = LR + i * kPtStride;
+#pragma unroll
+    for (int m4 = 0; m4 < kCB; m4 += 4) {
+      const float4 q = *reinterpret_cast<const float4*>(row + m4);
+      x[m4 + 1] = fmaf(-q.x, xi, x[m4 + 1]);
+      if (m4 + 2 < kCB) x[m4 + 2] = fmaf(-q.y, xi, x[m4 + 2]);
+      if (m4 + 3 < kCB) x[m4 + 3] = fmaf(-q.z, xi, x[m4 + 3]);
+      if (m4 + 4 < kCB) x[m4 + 4] = fmaf(-q.w, xi, x[m4 + 4]);
+    }
+#pragma unroll
+    for (int m = 0; m + 1 < kCB; ++m) x[m] = x[m + 1];
+  }
+  __syncwarp();
 }
 
 __global__ void __launch_bounds__(kCThreads, 1)
@@ -243,8 +341,9 @@ __global__ void __launch_bounds__(kCThreads, 1)
   const int nb = kp / kCB, np = tri(nb);
   float* A = csm;
   float* PT = A + size_t(np) * kBlk;
-  float* LI = PT + size_t(max(1, nb - 1)) * kPtBlk;
-  float* Ds = LI + kBlk;
+  float* LI = PT + size_t(max(1, nb - 1)) * kPtBlk;  // inverse of the current diagonal block
+  float* LTd = LI + kPtBlk;                            // current diagonal block of L, rotated columns
+  float* Ds = LTd + kPtBlk;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   constexpr int kWarps = kCThreads / 32;
   if (tid == 0) {
@@ -265,119 +364,115 @@ __global__ void __launch_bounds__(kCThreads, 1)
     Dg[i] = dv;
   }
   __syncthreads();
-  for (int q = tid; q < np * kCB * kCB; q += kCThreads) {
-    const int b = q >> 10, e = q & 1023, r = e >> 5, c = e & 31;
-    int I, J;
-    unpack_tri(b, I, J);
-    const int i = I * kCB + r, j = J * kCB + c;
-    float v;
-    if (i == j)
-      v = (i < k && Ds[i] > 0.f) ? G[size_t(i) * kp + i] * Ds[i] * Ds[i] + shift : 1.f;
-    else if (i < k && j < k)
-      v = G[size_t(max(i, j)) * kp + min(i, j)] * Ds[i] * Ds[j];
-    else
-      v = 0.f;
-    A[size_t(b) * kBlk + r * (kCB + 1) + c] = v;
+  // row i of the lower blocks (columns 0 .. 32 (I + 1) - 1, the diagonal
+  // block in full) is contiguous in G: one warp per row, all loads first
+  for (int i0 = warp; i0 < kp; i0 += 2 * kWarps) {
+    float v[2][kCalMaxNb];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int i = i0 + h * kWarps, ncol = ((i >> 5) + 1) * kCB;
+#pragma unroll
+      for (int u = 0; u < kCalMaxNb; ++u) {
+        const int j = u * kCB + lane;
+        v[h][u] = (i < kp && j < ncol && i < k && j < k) ? G[size_t(i) * kp + j] : 0.f;
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int i = i0 + h * kWarps;
+      if (i >= kp) break;
+      const int I = i >> 5, r = i & 31, ncol = (I + 1) * kCB;
+      const float di = Ds[i];
+#pragma unroll
+      for (int u = 0; u < kCalMaxNb; ++u) {
+        const int j = u * kCB + lane;
+        if (j >= ncol) break;
+        float a = v[h][u] * di * Ds[j];
+        if (i == j) a = (i < k && di > 0.f) ? a + shift : 1.f;
+        A[size_t(tri(I) + u) * kBlk + r * (kCB + 1) + lane] = a;
+      }
+    }
   }
   __syncthreads();
 
-  for (int J = 0; J < nb; ++J) {
-    float* AJJ = A + size_t(tri(J) + J) * kBlk;
-    if (warp == 0) {
-      // lane i holds row i of the diagonal block
-      float a[kCB];
+  // step J: the panel below diagonal block J, the trailing update, and (warp
+  // 0, overlapped with the update) the factorisation of diagonal block J + 1;
+  // step -1 only factors block 0
+  for (int J = -1; J < nb; ++J) {
+    if (J >= 0) {
+      // panel: L_IJ = A_IJ Linv_JJ^T for the block rows below.  Lane r keeps
+      // row r of A_IJ in registers; a warp produces 16 of the 32 columns.  The
+      // result goes to L (global) and, transposed, to PT for the trailing
+      // update; A_IJ itself is not needed again.
+      const int n_tasks = (nb - 1 - J) * 2;
+      for (int task = warp; task < n_tasks; task += kWarps) {
+        const int I = J + 1 + (task >> 1), c0 = (task & 1) * (kCB / 2);
+        const float* AIJ = A + size_t(tri(I) + J) * kBlk;
+        float a[kCB];
 #pragma unroll
-      for (int m = 0; m < kCB; ++m) a[m] = AJJ[lane * (kCB + 1) + m];
-      bool bad = false, small = false;
+        for (int m = 0; m < kCB; ++m) a[m] = AIJ[lane * (kCB + 1) + m];
+        float* pt = PT + size_t(I - J - 1) * kPtBlk;
+#pragma unroll 2
+        for (int c = c0; c < c0 + kCB / 2; ++c) {
+          float part[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < kCB; ++c) {
-        float piv = __shfl_sync(0xffffffffu, a[c], c);
-        if (!(piv >= kPivotFloor)) {
-          bad = true;
-          piv = 1.f;
+          for (int m = 0; m < kCB; m += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(LI + c * kPtStride + m);
+            part[0] = fmaf(a[m + 0], l4.x, part[0]);
+            part[1] = fmaf(a[m + 1], l4.y, part[1]);
+            part[2] = fmaf(a[m + 2], l4.z, part[2]);
+            part[3] = fmaf(a[m + 3], l4.w, part[3]);
+          }
+          const float v = (part[0] + part[1]) + (part[2] + part[3]);
+          pt[c * kPtStride + lane] = v;
+          Lg[size_t(I * kCB + lane) * kp + J * kCB + c] = v;
         }
-        if (piv < kPivotSkip2) small = true;
-        const float sd = sqrtf(piv);
-        const float l = (lane == c) ? sd : ((lane > c) ? a[c] / sd : 0.f);
-        a[c] = l;
-#pragma unroll
-        for (int m = c + 1; m < kCB; ++m) a[m] = fmaf(-l, __shfl_sync(0xffffffffu, l, m), a[m]);
       }
-#pragma unroll
-      for (int m = 0; m < kCB; ++m) AJJ[lane * (kCB + 1) + m] = (m <= lane) ? a[m] : 0.f;
-      if (lane == 0) {
-        if (bad) s_bad = 1;
-        if (small) s_small = 1;
-      }
-      __syncwarp();
-      // inverse of the diagonal block; lane j holds column j
-      float x[kCB];
-#pragma unroll
-      for (int i = 0; i < kCB; ++i) {
-        float acc = (i == lane) ? 1.f : 0.f;
-#pragma unroll
-        for (int m = 0; m < i; ++m) acc = fmaf(-AJJ[i * (kCB + 1) + m], x[m], acc);
-        x[i] = acc / AJJ[i * (kCB + 1) + i];
-      }
-#pragma unroll
-      for (int i = 0; i < kCB; ++i) {
-        LI[i * (kCB + 1) + lane] = x[i];
-        LIg[size_t(J) * kCB * kCB + i * kCB + lane] = x[i];
-      }
-    }
-    __syncthreads();
-    // panel: L_IJ = A_IJ Linv_JJ^T for the block rows below, kept transposed too
-    const int rows_below = (nb - 1 - J) * kCB;
-    for (int rr = warp; rr < rows_below; rr += kWarps) {
-      const int I = J + 1 + (rr >> 5), r = rr & 31;
-      float* AIJ = A + size_t(tri(I) + J) * kBlk;
-      float acc = 0.f;
-#pragma unroll
-      for (int m = 0; m < kCB; ++m) acc = fmaf(AIJ[r * (kCB + 1) + m], LI[lane * (kCB + 1) + m], acc);
-      __syncwarp();
-      AIJ[r * (kCB + 1) + lane] = acc;
-      PT[size_t(I - J - 1) * kPtBlk + lane * kPtStride + r] = acc;
-    }
-    __syncthreads();
-    // trailing update A_IL -= L_IJ L_LJ^T, J < L <= I; one warp per block pair,
-    // each lane a 4 x 8 patch
-    const int n1 = nb - 1 - J;
-    const int lr = lane >> 2, lc = lane & 3;
-    for (int pp = warp; pp < tri(n1); pp += kWarps) {
-      int Ip, Lp;
-      unpack_tri(pp, Ip, Lp);
-      const float* PI = PT + size_t(Ip) * kPtBlk;
-      const float* PL = PT + size_t(Lp) * kPtBlk;
-      float acc[4][8];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
-#pragma unroll 4
-      for (int m = 0; m < kCB; ++m) {
-        const float4 av = *reinterpret_cast<const float4*>(PI + m * kPtStride + 4 * lr);
-        const float4 b0 = *reinterpret_cast<const float4*>(PL + m * kPtStride + 8 * lc);
-        const float4 b1 = *reinterpret_cast<const float4*>(PL + m * kPtStride + 8 * lc + 4);
-        const float a4[4] = {av.x, av.y, av.z, av.w};
-        const float b8[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+      __syncthreads();
+      // trailing update A_IL -= L_IJ L_LJ^T, J < L <= I; one warp per block pair,
+      // each lane a 4 x 8 patch
+      const int n1 = nb - 1 - J;
+      const int lr = lane >> 2, lc = lane & 3;
+      // warp 0 updates block (J+1, J+1) first and factors it while the other
+      // warps update the rest (pairs 1.. over warps 1..)
+      for (int pp = (warp == 0) ? 0 : warp; pp < tri(n1); pp += (warp == 0) ? tri(n1) : kWarps - 1) {
+        int Ip, Lp;
+        unpack_tri(pp, Ip, Lp);
+        const float* PI = PT + size_t(Ip) * kPtBlk;
+        const float* PL = PT + size_t(Lp) * kPtBlk;
+        float acc[4][8];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
-          for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a4[i], b8[j], acc[i][j]);
+          for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+#pragma unroll 4
+        for (int m = 0; m < kCB; ++m) {
+          const float4 av = *reinterpret_cast<const float4*>(PI + m * kPtStride + 4 * lr);
+          const float4 b0 = *reinterpret_cast<const float4*>(PL + m * kPtStride + 8 * lc);
+          const float4 b1 = *reinterpret_cast<const float4*>(PL + m * kPtStride + 8 * lc + 4);
+          const float a4[4] = {av.x, av.y, av.z, av.w};
+          const float b8[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a4[i], b8[j], acc[i][j]);
+        }
+        float* AIL = A + size_t(tri(J + 1 + Ip) + J + 1 + Lp) * kBlk;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) AIL[(4 * lr + i) * (kCB + 1) + 8 * lc + j] -= acc[i][j];
       }
-      float* AIL = A + size_t(tri(J + 1 + Ip) + J + 1 + Lp) * kBlk;
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) AIL[(4 * lr + i) * (kCB + 1) + 8 * lc + j] -= acc[i][j];
     }
+    if (warp == 0 && J + 1 < nb)
+      chol_diag_block(A + size_t(tri(J + 1) + J + 1) * kBlk, LI, LTd,
+                      LIg + size_t(J + 1) * kCB * kCB, lane, &s_bad, &s_small);
     __syncthreads();
   }
-  for (int q = tid; q < np * kCB * kCB; q += kCThreads) {
-    const int b = q >> 10, e = q & 1023, r = e >> 5, c = e & 31;
-    int I, J;
-    unpack_tri(b, I, J);
-    Lg[size_t(I * kCB + r) * kp + J * kCB + c] = A[size_t(b) * kBlk + r * (kCB + 1) + c];
+  // the diagonal blocks of L (the panels went to Lg as they were formed)
+  for (int q = tid; q < nb * kCB * kCB; q += kCThreads) {
+    const int J = q >> 10, e = q & 1023, r = e >> 5, c = e & 31;
+    Lg[size_t(J * kCB + r) * kp + J * kCB + c] = A[size_t(tri(J) + J) * kBlk + r * (kCB + 1) + c];
   }
   if (tid == 0) {
     if (s_bad) atomicOr(&ctl->status, kStatusRank);
@@ -386,18 +481,21 @@ __global__ void __launch_bounds__(kCThreads, 1)
 }
 
 // ---- apply: Q^T[:, slice] = L^-1 D Y^T[:, slice] (blocked forward substitution)
-// One CTA per 32 columns of d.  The slice (kp x 32, D-scaled) sits in shared
-// memory; block row I is updated by the L blocks to its left (staged
-// transposed) and multiplied by the inverse of L_II.  Outputs (any may be
-// null): outF fp32 k x d, outB bf16 k x d, outV bf16 d x k (the basis layout).
+// One CTA per 32 columns of d.  The CTA first stages all of L it needs in
+// shared memory -- the panels left of each diagonal block, transposed, and
+// the inverses of the diagonal blocks, transposed -- with every load in
+// flight at once, then runs the substitution from shared memory only: block
+// row I of the D-scaled slice is updated by the blocks to its left and
+// multiplied by the inverse of L_II.  Outputs (any may be null): outF fp32
+// k x d, outB bf16 k x d, outV bf16 d x k (the basis layout).
 constexpr int kAThreads = 256;
 constexpr int kACols = 32;
 
 size_t apply_smem_bytes(int nb) {
-  return size_t(nb) * kCB * (kACols + 1) * 4            // slice
-         + size_t(std::max(1, nb - 1)) * kCB * kPtStride * 4  // L row panel, transposed
-         + size_t(kCB) * kPtStride * 4                    // inverse of L_II, transposed
-         + size_t(kCB) * (kACols + 1) * 4;                // block row before the inverse
+  return size_t(nb) * kCB * (kACols + 1) * 4        // slice
+         + size_t(tri(nb - 1)) * kPtBlk * 4         // panels left of the diagonal, transposed
+         + size_t(nb) * kPtBlk * 4                  // inverses of the diagonal blocks, transposed
+         + size_t(kCB) * (kACols + 1) * 4;          // block row before its inverse
 }
 
 __global__ void __launch_bounds__(kAThreads)
@@ -412,29 +510,46 @@ __global__ void __launch_bounds__(kAThreads)
   if (only_if_need2 && *reinterpret_cast<const volatile int32_t*>(&ctl->need2) == 0) return;
   const int nb = kp / kCB;
   float* Xs = asm_;                                     // kp x 33
-  float* Lp = Xs + size_t(kp) * (kACols + 1);           // (32 (nb-1)) x 36
-  float* LIt = Lp + size_t(max(1, nb - 1)) * kCB * kPtStride;  // 32 x 36
-  float* Ts = LIt + kCB * kPtStride;                    // 32 x 33
+  float* LT = Xs + size_t(kp) * (kACols + 1);           // panel I at kPtBlk * tri(I - 1): [32 I][36]
+  float* LIt = LT + size_t(tri(nb - 1)) * kPtBlk;       // nb x [32][36]
+  float* Ts = LIt + size_t(nb) * kPtBlk;                // 32 x 33
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c0 = blockIdx.x * kACols;
   const bool col_ok = c0 + lane < d;
   for (int r = warp; r < kp; r += kAThreads / 32)
     Xs[r * (kACols + 1) + lane] = (r < k && col_ok) ? Dg[r] * Y[size_t(r) * d + c0 + lane] : 0.f;
+  // L panels: row r of block row I, columns 0 .. 32 I - 1, as float4
+  for (int I = 1; I < nb; ++I) {
+    float* dst = LT + size_t(tri(I - 1)) * kPtBlk;
+    const int w4 = I * kCB / 4;
+#pragma unroll 4
+    for (int q = tid; q < kCB * w4; q += kAThreads) {
+      const int r = q / w4, m = 4 * (q % w4);
+      const float4 l4 = *reinterpret_cast<const float4*>(&Lg[size_t(I * kCB + r) * kp + m]);
+      dst[(m + 0) * kPtStride + r] = l4.x;
+      dst[(m + 1) * kPtStride + r] = l4.y;
+      dst[(m + 2) * kPtStride + r] = l4.z;
+      dst[(m + 3) * kPtStride + r] = l4.w;
+    }
+  }
+#pragma unroll 4
+  for (int q = tid; q < nb * kCB * kCB / 4; q += kAThreads) {
+    const int I = q >> 8, e = 4 * (q & 255), r = e >> 5, m = e & 31;
+    const float4 l4 = *reinterpret_cast<const float4*>(&LIg[size_t(I) * kCB * kCB + e]);
+    float* dst = LIt + size_t(I) * kPtBlk;
+    dst[(m + 0) * kPtStride + r] = l4.x;
+    dst[(m + 1) * kPtStride + r] = l4.y;
+    dst[(m + 2) * kPtStride + r] = l4.z;
+    dst[(m + 3) * kPtStride + r] = l4.w;
+  }
+  __syncthreads();
   for (int I = 0; I < nb; ++I) {
-    const int w = 32 * I;  // columns of L left of the diagonal block
-    __syncthreads();
-    for (int q = tid; q < kCB * w; q += kAThreads) {
-      const int r = q / w, m = q % w;
-      Lp[m * kPtStride + r] = Lg[size_t(I * kCB + r) * kp + m];
-    }
-    for (int q = tid; q < kCB * kCB; q += kAThreads) {
-      const int r = q >> 5, m = q & 31;
-      LIt[m * kPtStride + r] = LIg[size_t(I) * kCB * kCB + q];
-    }
-    __syncthreads();
+    const int w = kCB * I;  // columns of L left of the diagonal block
+    const float* Lp = LT + size_t(tri(I - 1)) * kPtBlk;
     float acc[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) acc[q] = Xs[(I * kCB + 4 * warp + q) * (kACols + 1) + lane];
+#pragma unroll 8
     for (int m = 0; m < w; ++m) {
       const float4 l4 = *reinterpret_cast<const float4*>(Lp + m * kPtStride + 4 * warp);
       const float x = Xs[m * (kACols + 1) + lane];
@@ -446,10 +561,11 @@ __global__ void __launch_bounds__(kAThreads)
 #pragma unroll
     for (int q = 0; q < 4; ++q) Ts[(4 * warp + q) * (kACols + 1) + lane] = acc[q];
     __syncthreads();
+    const float* Li = LIt + size_t(I) * kPtBlk;
     float o[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 8
     for (int m = 0; m < kCB; ++m) {
-      const float4 l4 = *reinterpret_cast<const float4*>(LIt + m * kPtStride + 4 * warp);
+      const float4 l4 = *reinterpret_cast<const float4*>(Li + m * kPtStride + 4 * warp);
       const float t = Ts[m * (kACols + 1) + lane];
       o[0] = fmaf(l4.x, t, o[0]);
       o[1] = fmaf(l4.y, t, o[1]);
@@ -458,8 +574,8 @@ __global__ void __launch_bounds__(kAThreads)
     }
 #pragma unroll
     for (int q = 0; q < 4; ++q) Xs[(I * kCB + 4 * warp + q) * (kACols + 1) + lane] = o[q];
+    __syncthreads();
   }
-  __syncthreads();
   if (outF || outB) {
     for (int r = warp; r < k; r += kAThreads / 32) {
       if (!col_ok) continue;
