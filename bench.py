@@ -657,6 +657,185 @@ def run_batched(args, world, rank, local):
         print(json.dumps(out), flush=True)
 
 
+CAL_METRIC = ("ms per calibration of V_k, GPT-J-shaped linear input (n=2048 calibration tokens, "
+              "d=4096, k=256, 8 block power iterations)")
+CAL_UNIT = "ms per calibration"
+
+
+def _cal_inputs():
+    import gsi_inputs as gi
+    c = gi.calibration_gptj()
+    cs = gi.calibration_activations(c["n"], c["d"], c["k"], seed=c["seed"])
+    Q0 = gi.calibration_start(c["d"], c["k"], seed=c["seed"])
+    return c, cs, Q0
+
+
+def cal_cpu_baseline(c, cs, Q0, budget_s: float = 12.0):
+    """The oracle's subspace iteration (numpy fp64, the host BLAS threads) on
+    the same inputs: whole calibrations until the budget is spent."""
+    import gsi_inputs as gi
+    from oracle import calibration as cal
+    X = gi.bf16_bits_to_f64(cs.X_bits)
+    Q = gi.bf16_bits_to_f64(Q0)
+    n_done = 0
+    t0 = time.perf_counter()
+    while True:
+        cal.subspace_iteration(X, Q, c["iters"])
+        n_done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return dict(value=round(dt / n_done * 1e3, 3), unit=CAL_UNIT, cores=os.cpu_count(),
+                kind="oracle",
+                sample=f"{n_done} whole calibrations (fp64 numpy subspace iteration, "
+                       f"Householder QR per iteration), {dt:.1f} s")
+
+
+def run_calibrate(args, world, rank, local):
+    """Calibration of one GPT-J-shaped linear's basis: n = 2048 tokens (one
+    GPT-J context), d = 4096, k = 256, 8 iterations of block power iteration
+    with CholeskyQR2, through gsi_calibrate.  R replicas of the calibration
+    tokens cycle so that the inputs stream from HBM (more than L2 holds)."""
+    import torch
+
+    from gated_rank_subspace_gsi_gb300 import lib
+    torch.cuda.set_device(local)
+    lib.library()
+    c, cs, Q0b = _cal_inputs()
+    n, d, k, iters = c["n"], c["d"], c["k"], c["iters"]
+    props = torch.cuda.get_device_properties(local)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
+    x_bytes = n * d * 2
+    replicas = max(2, int(math.ceil(1.5 * l2 / x_bytes)))
+    X0 = torch.from_numpy(cs.X_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    Xs = [X0] + [X0.clone() for _ in range(replicas - 1)]
+    Q0 = torch.from_numpy(Q0b.view(np.int16)).view(torch.bfloat16).cuda()
+    V = torch.empty((d, k), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(lib.gsi_calibrate_workspace_size(n, d, k), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+    calls = replicas
+    with torch.cuda.stream(stream):
+        lib.gsi_calibrate(Xs[0], Q0, iters, V, ws, stream)   # attributes, first-use setup
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            for r in range(calls):
+                lib.gsi_calibrate(Xs[r], Q0, iters, V, ws, stream)
+    replay(graph, stream, max(args.warmup, 3))
+    st = lib.gsi_calibrate_status(ws, stream)
+    if st != 0:
+        raise RuntimeError(f"calibration status: {lib.gsi_status_string(st)}")
+    steps = max(1, args.steps // 30)
+    ms, clk = _timed(graph, stream, steps, args.warmup, world, local)
+    ms_cal = ms / calls
+    # end to end: pinned host X and Q0 in, V out, per calibration
+    Hx = torch.from_numpy(cs.X_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+    Hq = torch.from_numpy(Q0b.view(np.int16)).view(torch.bfloat16).pin_memory()
+    Hv = torch.empty((d, k), dtype=torch.bfloat16).pin_memory()
+    Xd = torch.empty_like(X0)
+    Qd = torch.empty_like(Q0)
+    ge = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(ge, stream=stream):
+            for r in range(calls):
+                Xd.copy_(Hx, non_blocking=True)
+                Qd.copy_(Hq, non_blocking=True)
+                lib.gsi_calibrate(Xd, Qd, iters, V, ws, stream)
+                Hv.copy_(V, non_blocking=True)
+    ms_e2e = max_over_ranks(time_graph(ge, stream, reps=max(3, steps), warmup=2), world)
+    launches = lib.gsi_calibrate_launch_count(n, d, k, iters)
+    flops_gemm = 2 * 2.0 * n * d * k * iters          # Z = X Q and Y = X^T Z per iteration
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cal_cpu_baseline(c, cs, Q0b, budget_s=args.cpu_budget)
+    rl = cal_roofline(lib, Xs[0], Q0, iters, V, ws, stream, k)
+    out = _line(CAL_METRIC, round(ms_cal, 4), CAL_UNIT, world, steps, args.warmup, ms,
+                {"workload": f"calibrate_gptj: n={n} calibration tokens (seeded planted-spectrum "
+                             f"activations), d={d}, k={k}, {iters} iterations, Q0 seeded Gaussian",
+                 "calls_per_step": calls, "replicas": replicas,
+                 "l2": f"inputs larger than L2: {replicas} replicas of X "
+                       f"({x_bytes / 2**20:.0f} MiB each), L2 {l2 / 2**20:.0f} MiB",
+                 "parallelism": "1 GPU" if world == 1 else f"replicas x{world}"},
+                roofline=rl,
+                tensor_gemm_tflops=round(flops_gemm / (ms_cal * 1e-3) / 1e12, 2),
+                e2e={"value": round(ms_e2e / calls, 4), "unit": CAL_UNIT,
+                     "h2d_bytes_per_step": calls * (n * d * 2 + d * k * 2),
+                     "d2h_bytes_per_step": calls * d * k * 2,
+                     "how": "pinned X, Q0 copied in and V_k copied out around each "
+                            "gsi_calibrate, graph-captured"},
+                gpu_launches=steps * calls * launches, clocks=clk)
+    out["data"] = ("synthetic (seeded planted-spectrum calibration activations, seeded "
+                   "Gaussian start block)")
+    out["dtype"] = "bf16 GEMMs, fp32 orthonormalisation"
+    if cpu is not None:
+        out["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+CAL_SRC = os.path.join(ROOT, "gated_rank_subspace_gsi_gb300", "csrc", "gsi_calib.cu")
+CAL_TRAFFIC_FILE = os.path.join(ROOT, "profiles", "cal_chol_kernel__calibrate_gptj.md")
+
+
+def cal_chol_traffic():
+    """DRAM bytes per launch of the Cholesky kernel from the committed ncu
+    summary, if it was taken on the calibration source as it is now."""
+    try:
+        with open(CAL_SRC, "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()[:16]
+        vals = {}
+        with open(CAL_TRAFFIC_FILE) as f:
+            for line in f:
+                if ":" in line:
+                    key, v = line.split(":", 1)
+                    vals[key.strip().lstrip("- ")] = v.strip()
+        if vals.get("calib_source_sha256_16") != sha:
+            return None
+        return float(vals["dram_bytes_per_active_launch"])
+    except Exception:
+        return None
+
+
+def cal_roofline(lib, X, Q0, iters, V, ws, stream, k, reps=3):
+    """Per-launch durations from gsi_calibrate_timed (CUDA events on the
+    launching stream, around each launch) over a few calibrations; the
+    dominant kind by total time gets the roofline.  For the Cholesky the
+    algorithmic work is k^3/3 flops per launch that factors (the second-pass
+    launches that find their pass not needed return at once and count as no
+    work), against the fp32 FMA rate of the GPU (152 SMs x 128 FMA/clk x
+    2 flops at the 2.07 GHz maximum SM clock) and of the one SM it runs on."""
+    totals, counts, chol = {}, {}, []
+    for _ in range(reps):
+        for kind, ms in lib.gsi_calibrate_timed(X, Q0, iters, V, ws, stream):
+            totals[kind] = totals.get(kind, 0.0) + ms
+            counts[kind] = counts.get(kind, 0) + 1
+            if kind == "Cholesky":
+                chol.append(ms)
+    dom = max(totals, key=totals.get)
+    share = {kd: round(t / sum(totals.values()), 4) for kd, t in totals.items()}
+    info = {"kernel": {"Cholesky": "cal_chol_kernel"}.get(dom, dom), "shares": share,
+            "avg_ms_by_kind": {kd: round(totals[kd] / counts[kd], 5) for kd in totals},
+            "source": "gsi_calibrate_timed: CUDA events around each launch on its stream"}
+    if dom == "Cholesky":
+        top = max(chol)
+        active = [t for t in chol if t > 0.2 * top]
+        flops = k ** 3 / 3.0
+        peak_gpu = 152 * 128 * 2 * 2.07e9 / 1e12
+        ach = flops * len(active) / (sum(chol) * 1e-3) / 1e12
+        traffic = cal_chol_traffic()
+        info.update(bound="alu", unit="TFLOP/s", achieved=round(ach, 4), peak=round(peak_gpu, 1),
+                    frac=round(ach / peak_gpu, 6), frac_of_one_sm=round(ach / (peak_gpu / 152), 4),
+                    traffic=traffic, traffic_per="active launch (ncu)",
+                    active_launch_avg_ms=round(sum(active) / len(active), 5),
+                    flops_per_active_launch=flops,
+                    peak_kind="derived fp32 FMA rate: 152 SMs x 128 FMA/clk x 2 x 2.07 GHz; "
+                              "the kernel is one CTA on one SM")
+    else:
+        info.update(bound=None, achieved=None, peak=None, frac=None, traffic=None)
+    return info
+
+
 def _linear_setup(spec, basis, seed, tag, eps=None):
     """W (device draw), V_k, M (gsi_precompute_M) and a handle of one linear."""
     import torch
@@ -985,6 +1164,41 @@ def run_reference(args, world, rank):
     print(json.dumps(out), flush=True)
 
 
+
+def run_reference_calibrate(args, world, rank):
+    """The oracle's subspace iteration (numpy fp64) on the host cores: each
+    step one whole GPT-J-shaped calibration on the same inputs."""
+    if rank != 0:
+        return
+    c, cs, Q0b = _cal_inputs()
+    import gsi_inputs as gi
+    from oracle import calibration as cal
+    X = gi.bf16_bits_to_f64(cs.X_bits)
+    Q = gi.bf16_bits_to_f64(Q0b)
+    steps = max(1, min(args.steps, 8))
+    warm = min(args.warmup, 1)
+    for _ in range(warm):
+        cal.subspace_iteration(X, Q, c["iters"])
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        cal.subspace_iteration(X, Q, c["iters"])
+    dt = time.perf_counter() - t0
+    v = dt / steps * 1e3
+    out = {
+        "metric": CAL_METRIC, "value": round(v, 3), "unit": CAL_UNIT, "n_gpus": world,
+        "steps": steps, "warmup": warm, "ms_per_step": round(v, 3), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference",
+        "config": {"workload": "calibrate_gptj (oracle: numpy fp64 subspace iteration, one "
+                               "whole calibration per step)"},
+        "cpu_baseline": {"value": round(v, 3), "unit": CAL_UNIT, "cores": os.cpu_count(),
+                         "kind": "oracle", "sample": f"{steps} whole calibrations"},
+        "e2e": {"value": round(v, 3), "unit": CAL_UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -992,7 +1206,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gsi", "reference"], default="gsi")
     ap.add_argument("--workload", choices=["gptj_layer_decode", "batched_T512", "gpt2_qkv_T64",
-                                           "gptj_stack", "opt_mlp"],
+                                           "gptj_stack", "opt_mlp", "calibrate_gptj"],
                     default="gptj_layer_decode")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -1008,8 +1222,12 @@ def main(argv=None):
         args.warmup = 3
     world, rank, local = dist_setup(args.gpus)
     try:
-        if args.impl == "reference":
+        if args.impl == "reference" and args.workload == "calibrate_gptj":
+            run_reference_calibrate(args, world, rank)
+        elif args.impl == "reference":
             run_reference(args, world, rank)
+        elif args.workload == "calibrate_gptj":
+            run_calibrate(args, world, rank, local)
         elif args.workload == "batched_T512":
             run_batched(args, world, rank, local)
         elif args.workload == "gpt2_qkv_T64":

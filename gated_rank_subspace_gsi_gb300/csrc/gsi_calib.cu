@@ -36,6 +36,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
+#include <vector>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -639,7 +640,35 @@ bool cal_shape_ok(int64_t n, int64_t d, int64_t k) {
          n <= (int64_t(1) << 30) && size_t(d) * size_t(n) <= (size_t(1) << 40);
 }
 
+// Optional per-launch timing (gsi_calibrate_timed): an event pair around
+// every kernel launch, on the launching stream.
+enum CalKind { kKindTranspose = 0, kKindGemm, kKindSum, kKindGram, kKindChol, kKindApply };
+struct CalTimer {
+  std::vector<cudaEvent_t> ev;  // start, stop per launch
+  std::vector<int> kind;
+  bool failed = false;
+  void begin(int kd, cudaStream_t s) {
+    cudaEvent_t a = nullptr, b = nullptr;
+    if (cudaEventCreate(&a) != cudaSuccess || cudaEventCreate(&b) != cudaSuccess) {
+      failed = true;
+      return;
+    }
+    ev.push_back(a);
+    ev.push_back(b);
+    kind.push_back(kd);
+    if (cudaEventRecord(a, s) != cudaSuccess) failed = true;
+  }
+  void end(cudaStream_t s) {
+    if (!ev.empty() && cudaEventRecord(ev.back(), s) != cudaSuccess) failed = true;
+  }
+  ~CalTimer() {
+    for (cudaEvent_t e : ev)
+      if (e) cudaEventDestroy(e);
+  }
+};
+
 struct CalRun {
+  CalTimer* tm = nullptr;
   int64_t n, d, k, kp, nb;
   CalLayout lay;
   unsigned char* ws;
@@ -649,6 +678,12 @@ struct CalRun {
   template <typename T>
   T* at(size_t off) const {
     return reinterpret_cast<T*>(ws + off);
+  }
+  void tb(int kd) const {
+    if (tm) tm->begin(kd, s);
+  }
+  void te() const {
+    if (tm) tm->end(s);
   }
 };
 
@@ -666,19 +701,24 @@ gsi_status_t orth_pass(const CalRun& r, const float* Yin, bool first, int only_i
   float* L = r.at<float>(r.lay.L);
   float* LI = r.at<float>(r.lay.LI);
   float* D = r.at<float>(r.lay.D);
-  if (launch_pdl(cal_gram_kernel, dim3(unsigned(np), unsigned(S)), dim3(kGThreads), 0, r.s, Yin,
-                 int(r.k), d, cs, Gp, G, int(r.kp), r.ctl, only_if_need2) != cudaSuccess)
-    return GSI_ERR_CUDA;
-  if (launch_pdl(cal_chol_kernel, dim3(1), dim3(kCThreads), chol_smem_bytes(int(r.nb)), r.s,
+  r.tb(kKindGram);
+  cudaError_t e = launch_pdl(cal_gram_kernel, dim3(unsigned(np), unsigned(S)), dim3(kGThreads), 0,
+                             r.s, Yin, int(r.k), d, cs, Gp, G, int(r.kp), r.ctl, only_if_need2);
+  r.te();
+  if (e != cudaSuccess) return GSI_ERR_CUDA;
+  r.tb(kKindChol);
+  e = launch_pdl(cal_chol_kernel, dim3(1), dim3(kCThreads), chol_smem_bytes(int(r.nb)), r.s,
                  (const float*)G, int(r.k), int(r.kp), first ? kShift1 : 0.f, first ? 1 : 0, L, LI, D,
-                 r.ctl, only_if_need2) != cudaSuccess)
-    return GSI_ERR_CUDA;
+                 r.ctl, only_if_need2);
+  r.te();
+  if (e != cudaSuccess) return GSI_ERR_CUDA;
   const unsigned ncta = unsigned((r.d + kACols - 1) / kACols);
-  if (launch_pdl(cal_apply_kernel, dim3(ncta), dim3(kAThreads), apply_smem_bytes(int(r.nb)), r.s,
+  r.tb(kKindApply);
+  e = launch_pdl(cal_apply_kernel, dim3(ncta), dim3(kAThreads), apply_smem_bytes(int(r.nb)), r.s,
                  Yin, int(r.k), d, int(r.kp), (const float*)D, (const float*)L, (const float*)LI, outF,
-                 outB, outV, (const CalCtl*)r.ctl, only_if_need2) != cudaSuccess)
-    return GSI_ERR_CUDA;
-  return GSI_OK;
+                 outB, outV, (const CalCtl*)r.ctl, only_if_need2);
+  r.te();
+  return e == cudaSuccess ? GSI_OK : GSI_ERR_CUDA;
 }
 
 gsi_status_t cal_prepare() {
@@ -730,15 +770,21 @@ int gsi_calibrate_launch_count(int64_t n, int64_t d, int64_t k, int iters) {
   return cal_launches(n, d, k, iters, sms);
 }
 
-gsi_status_t gsi_calibrate(const void* X, int64_t n, int64_t d, int64_t k, const void* Q0,
-                           int iters, void* V_k, void* workspace, size_t workspace_bytes,
-                           cudaStream_t stream) {
+}  // extern "C"
+
+namespace gsi {
+namespace {
+
+gsi_status_t calibrate_impl(const void* X, int64_t n, int64_t d, int64_t k, const void* Q0,
+                            int iters, void* V_k, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream, CalTimer* tm) {
   if (!X || !Q0 || !V_k || !workspace || iters < 0 || iters > 10000) return GSI_ERR_INVALID_ARG;
   if (!aligned16(X) || !aligned16(Q0) || !aligned16(V_k) ||
       (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
     return GSI_ERR_INVALID_ARG;
   if (!cal_shape_ok(n, d, k)) return GSI_ERR_UNSUPPORTED_SHAPE;
   CalRun r;
+  r.tm = tm;
   r.n = n;
   r.d = d;
   r.k = k;
@@ -773,22 +819,27 @@ gsi_status_t gsi_calibrate(const void* X, int64_t n, int64_t d, int64_t k, const
   if (iters == 0) {
     // V_k = orth(Q0): the block itself, in fp32, through both passes
     const dim3 g(unsigned((k + 31) / 32), unsigned((d + 31) / 32));
-    if (launch_pdl(cal_transpose_kernel<float>, g, tb, 0, stream, Q0b, int(d), int(k), Y) !=
-        cudaSuccess)
-      return GSI_ERR_CUDA;
+    r.tb(kKindTranspose);
+    const cudaError_t e = launch_pdl(cal_transpose_kernel<float>, g, tb, 0, stream, Q0b, int(d),
+                                     int(k), Y);
+    r.te();
+    if (e != cudaSuccess) return GSI_ERR_CUDA;
     if ((st = orth_pass(r, Y, true, 0, Q1, nullptr, nullptr)) != GSI_OK) return st;
     return orth_pass(r, Q1, false, 0, nullptr, nullptr, V);
   }
 
   {
     const dim3 gx(unsigned((d + 31) / 32), unsigned((n + 31) / 32));
-    if (launch_pdl(cal_transpose_kernel<__nv_bfloat16>, gx, tb, 0, stream, Xb, int(n), int(d), XT) !=
-        cudaSuccess)
-      return GSI_ERR_CUDA;
+    r.tb(kKindTranspose);
+    cudaError_t e = launch_pdl(cal_transpose_kernel<__nv_bfloat16>, gx, tb, 0, stream, Xb, int(n),
+                               int(d), XT);
+    r.te();
+    if (e != cudaSuccess) return GSI_ERR_CUDA;
     const dim3 gq(unsigned((k + 31) / 32), unsigned((d + 31) / 32));
-    if (launch_pdl(cal_transpose_kernel<__nv_bfloat16>, gq, tb, 0, stream, Q0b, int(d), int(k), QT) !=
-        cudaSuccess)
-      return GSI_ERR_CUDA;
+    r.tb(kKindTranspose);
+    e = launch_pdl(cal_transpose_kernel<__nv_bfloat16>, gq, tb, 0, stream, Q0b, int(d), int(k), QT);
+    r.te();
+    if (e != cudaSuccess) return GSI_ERR_CUDA;
   }
   int kb1, kb2;
   const int S1 = tc_nt_splits(n, k, d, r.sms, &kb1);
@@ -799,22 +850,67 @@ gsi_status_t gsi_calibrate(const void* X, int64_t n, int64_t d, int64_t k, const
   for (int it = 0; it < iters; ++it) {
     const bool last = it + 1 == iters;
     // Z^T = Q^T X^T: P1[s][j][t]
-    if ((st = tc_nt_gemm(Xb, n, QT, k, d, P1, kn, S1, kb1, status, stream)) != GSI_OK) return st;
-    if (launch_pdl(cal_sum_kernel<__nv_bfloat16>, dim3(std::max(1u, sum_grid1)), tb, 0, stream,
-                   (const float*)P1, S1, kn, kn, ZT) != cudaSuccess)
-      return GSI_ERR_CUDA;
+    r.tb(kKindGemm);
+    st = tc_nt_gemm(Xb, n, QT, k, d, P1, kn, S1, kb1, status, stream);
+    r.te();
+    if (st != GSI_OK) return st;
+    r.tb(kKindSum);
+    cudaError_t e = launch_pdl(cal_sum_kernel<__nv_bfloat16>, dim3(std::max(1u, sum_grid1)), tb, 0,
+                               stream, (const float*)P1, S1, kn, kn, ZT);
+    r.te();
+    if (e != cudaSuccess) return GSI_ERR_CUDA;
     // Y^T = Z^T X: P2[s][j][i]
     float* Ydst = (S2 > 1) ? P2 : Y;
-    if ((st = tc_nt_gemm(XT, d, ZT, k, n, Ydst, kd, S2, kb2, status, stream)) != GSI_OK) return st;
-    if (S2 > 1 && launch_pdl(cal_sum_kernel<float>, dim3(std::max(1u, sum_grid2)), tb, 0, stream,
-                             (const float*)P2, S2, kd, kd, Y) != cudaSuccess)
-      return GSI_ERR_CUDA;
+    r.tb(kKindGemm);
+    st = tc_nt_gemm(XT, d, ZT, k, n, Ydst, kd, S2, kb2, status, stream);
+    r.te();
+    if (st != GSI_OK) return st;
+    if (S2 > 1) {
+      r.tb(kKindSum);
+      e = launch_pdl(cal_sum_kernel<float>, dim3(std::max(1u, sum_grid2)), tb, 0, stream,
+                     (const float*)P2, S2, kd, kd, Y);
+      r.te();
+      if (e != cudaSuccess) return GSI_ERR_CUDA;
+    }
     // CholeskyQR2 (the second pass only where needed, except at the end)
     if ((st = orth_pass(r, Y, true, 0, Q1, last ? nullptr : QT, nullptr)) != GSI_OK) return st;
     if ((st = orth_pass(r, Q1, false, last ? 0 : 1, nullptr, last ? nullptr : QT,
                         last ? V : nullptr)) != GSI_OK)
       return st;
   }
+  return GSI_OK;
+}
+
+}  // namespace
+}  // namespace gsi
+
+extern "C" {
+
+gsi_status_t gsi_calibrate(const void* X, int64_t n, int64_t d, int64_t k, const void* Q0,
+                           int iters, void* V_k, void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream) {
+  return calibrate_impl(X, n, d, k, Q0, iters, V_k, workspace, workspace_bytes, stream, nullptr);
+}
+
+gsi_status_t gsi_calibrate_timed(const void* X, int64_t n, int64_t d, int64_t k, const void* Q0,
+                                 int iters, void* V_k, void* workspace, size_t workspace_bytes,
+                                 cudaStream_t stream, float* launch_ms, int* launch_kind,
+                                 int max_launches, int* n_launches) {
+  if (!launch_ms || !launch_kind || !n_launches || max_launches < 0) return GSI_ERR_INVALID_ARG;
+  *n_launches = 0;
+  CalTimer tm;
+  const gsi_status_t st =
+      calibrate_impl(X, n, d, k, Q0, iters, V_k, workspace, workspace_bytes, stream, &tm);
+  if (st != GSI_OK) return st;
+  if (tm.failed || cudaStreamSynchronize(stream) != cudaSuccess) return GSI_ERR_CUDA;
+  const int cnt = int(tm.kind.size());
+  for (int i = 0; i < cnt && i < max_launches; ++i) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, tm.ev[2 * i], tm.ev[2 * i + 1]) != cudaSuccess) return GSI_ERR_CUDA;
+    launch_ms[i] = ms;
+    launch_kind[i] = tm.kind[i];
+  }
+  *n_launches = std::min(cnt, max_launches);
   return GSI_OK;
 }
 

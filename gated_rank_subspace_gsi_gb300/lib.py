@@ -30,7 +30,8 @@ EXPORTS = ("gsi_create", "gsi_forward", "gsi_forward_host", "gsi_precompute_M",
            "gsi_forward_launch_count", "gsi_forward_noalloc", "gsi_set_prefetch",
            "gsi_set_prefetch_group", "gsi_group_create", "gsi_group_forward",
            "gsi_group_set_prefetch", "gsi_group_destroy", "gsi_calibrate_workspace_size",
-           "gsi_calibrate", "gsi_calibrate_status", "gsi_calibrate_launch_count")
+           "gsi_calibrate", "gsi_calibrate_status", "gsi_calibrate_launch_count",
+           "gsi_calibrate_timed")
 
 _lock = threading.Lock()
 _lib = None
@@ -91,6 +92,9 @@ def _load():
         lib.gsi_calibrate_workspace_size.restype = ctypes.c_int
         lib.gsi_calibrate.argtypes = [P, I64, I64, I64, P, ctypes.c_int, P, P, ctypes.c_size_t, P]
         lib.gsi_calibrate.restype = ctypes.c_int
+        lib.gsi_calibrate_timed.argtypes = [P, I64, I64, I64, P, ctypes.c_int, P, P, ctypes.c_size_t,
+                                            P, P, P, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
+        lib.gsi_calibrate_timed.restype = ctypes.c_int
         lib.gsi_calibrate_status.argtypes = [P, P]
         lib.gsi_calibrate_status.restype = ctypes.c_int
         lib.gsi_calibrate_launch_count.argtypes = [I64, I64, I64, ctypes.c_int]
@@ -315,3 +319,22 @@ def gsi_calibrate_status(workspace, stream=None) -> int:
 
 def gsi_calibrate_launch_count(n: int, d: int, k: int, iters: int) -> int:
     return int(_load().gsi_calibrate_launch_count(int(n), int(d), int(k), int(iters)))
+
+
+CAL_KINDS = ("transpose", "tensor-core GEMM", "split-K sum", "Gram matrix", "Cholesky",
+             "forward substitution")
+
+
+def gsi_calibrate_timed(X, Q0, iters: int, V_k, workspace, stream=None, max_launches: int = 4096):
+    """gsi_calibrate with an event pair around every launch; returns a list of
+    (kind name, ms) in launch order (synchronises the stream)."""
+    n, d = X.shape
+    _, k = Q0.shape
+    ms = (ctypes.c_float * max_launches)()
+    kinds = (ctypes.c_int * max_launches)()
+    cnt = ctypes.c_int()
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(_load().gsi_calibrate_timed(_ptr(X), n, d, k, _ptr(Q0), int(iters), _ptr(V_k),
+                                       _ptr(workspace), nbytes, _stream(stream), ms, kinds,
+                                       max_launches, ctypes.byref(cnt)), "gsi_calibrate_timed")
+    return [(CAL_KINDS[kinds[i]], float(ms[i])) for i in range(cnt.value)]

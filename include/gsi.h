@@ -260,6 +260,20 @@ gsi_status_t gsi_calibrate(const void *X, int64_t n, int64_t d, int64_t k,
                            const void *Q0, int iters, void *V_k,
                            void *workspace, size_t workspace_bytes,
                            cudaStream_t stream);
+/* gsi_calibrate with a CUDA event pair recorded on `stream` around every
+ * kernel launch, for measurement: synchronises the stream, then writes each
+ * launch's duration (ms) and kind to launch_ms[i] / launch_kind[i] (host
+ * arrays of max_launches entries, launch order) and the number written to
+ * *n_launches.  Kinds: 0 transpose, 1 tensor-core GEMM, 2 split-K sum,
+ * 3 Gram matrix, 4 Cholesky, 5 forward substitution.  The events keep
+ * neighbouring launches from overlapping, so the durations add up to a bit
+ * more than a gsi_calibrate call takes. */
+gsi_status_t gsi_calibrate_timed(const void *X, int64_t n, int64_t d, int64_t k,
+                                 const void *Q0, int iters, void *V_k,
+                                 void *workspace, size_t workspace_bytes,
+                                 cudaStream_t stream, float *launch_ms,
+                                 int *launch_kind, int max_launches,
+                                 int *n_launches);
 /* Synchronise `stream` and read the status of the last gsi_calibrate on
  * this workspace (see above). */
 gsi_status_t gsi_calibrate_status(const void *workspace, cudaStream_t stream);
