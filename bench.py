@@ -1199,6 +1199,155 @@ def run_reference_calibrate(args, world, rank):
     print(json.dumps(out), flush=True)
 
 
+CASC_METRIC = ("ms per layer, depth cascade of 28 GPT-J-shaped layers (n=2048 calibration tokens, "
+               "d=4096, k=256; 8 iterations for layer 0, 2 from the previous layer's basis after)")
+
+
+def _casc_inputs(layers):
+    import gsi_inputs as gi
+    c = gi.calibration_gptj()
+    sets = gi.calibration_cascade(layers, c["n"], c["d"], c["k"], seed=c["seed"] + 100)
+    Q0 = gi.calibration_start(c["d"], c["k"], seed=c["seed"] + 100)
+    return c, sets, Q0
+
+
+def run_cascade(args, world, rank, local):
+    """Depth cascade (section 2.3) over 28 GPT-J-shaped layers through
+    gsi_calibrate_cascade, against per-layer calibration from a random start
+    (8 iterations each) on the same tokens: time per layer, the cost cut, and
+    the energy each basis captures (measured on the device)."""
+    import torch
+
+    from gated_rank_subspace_gsi_gb300 import lib
+    torch.cuda.set_device(local)
+    lib.library()
+    L, it_first, it_next = 28, 8, 2
+    c, sets, Q0b = _casc_inputs(L)
+    n, d, k = c["n"], c["d"], c["k"]
+    Xs = [torch.from_numpy(s.X_bits.view(np.int16)).view(torch.bfloat16).cuda() for s in sets]
+    Q0 = torch.from_numpy(Q0b.view(np.int16)).view(torch.bfloat16).cuda()
+    Vc = [torch.empty((d, k), dtype=torch.bfloat16, device="cuda") for _ in range(L)]
+    Vp = [torch.empty((d, k), dtype=torch.bfloat16, device="cuda") for _ in range(L)]
+    ws = torch.empty(lib.gsi_calibrate_workspace_size(n, d, k), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        lib.gsi_calibrate(Xs[0], Q0, 1, Vp[0], ws, stream)
+    stream.synchronize()
+    g_casc = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g_casc, stream=stream):
+            lib.gsi_calibrate_cascade(Xs, Q0, it_first, it_next, Vc, ws, stream)
+    g_cold = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g_cold, stream=stream):
+            for layer in range(L):
+                lib.gsi_calibrate(Xs[layer], Q0, it_first, Vp[layer], ws, stream)
+    replay(g_casc, stream, 1)
+    replay(g_cold, stream, 1)
+    st = lib.gsi_calibrate_status(ws, stream)
+    if st != 0:
+        raise RuntimeError(f"calibration status: {lib.gsi_status_string(st)}")
+    steps = max(1, args.steps // 100)
+    ms, clk = _timed(g_casc, stream, steps, args.warmup, world, local)
+    ms_cold = max_over_ranks(time_graph(g_cold, stream, reps=steps, warmup=1), world)
+    # captured energy ||X V||_F^2 / ||X||_F^2 of each basis (device matmuls:
+    # measurement, not part of the calibration)
+    e_c, e_p = [], []
+    for layer in range(L):
+        X = Xs[layer].float()
+        tot = float((X * X).sum())
+        e_c.append(float((X @ Vc[layer].float()).pow(2).sum()) / tot)
+        e_p.append(float((X @ Vp[layer].float()).pow(2).sum()) / tot)
+    rl = cal_roofline(lib, Xs[1], Vc[0], it_next, Vp[1], ws, stream, k)
+    launches = (lib.gsi_calibrate_launch_count(n, d, k, it_first)
+                + (L - 1) * lib.gsi_calibrate_launch_count(n, d, k, it_next))
+    out = _line(CASC_METRIC, round(ms / L, 4), "ms per layer", world, steps, args.warmup, ms,
+                {"workload": f"cascade_gptj: {L} layers of depth-coherent planted-spectrum "
+                             f"calibration tokens (adjacent planted subspaces: mean principal "
+                             f"cosine ~0.96), n={n}, d={d}, k={k}, iterations {it_first} then "
+                             f"{it_next}",
+                 "l2": f"inputs larger than L2: {L} layers x {n * d * 2 / 2**20:.0f} MiB of tokens",
+                 "parallelism": "1 GPU" if world == 1 else f"replicas x{world}"},
+                roofline=rl,
+                per_layer_cold_ms=round(ms_cold / L, 4),
+                cost_cut_vs_per_layer=round(1.0 - ms / ms_cold, 4),
+                captured_energy={"cascade_mean": round(float(np.mean(e_c)), 6),
+                                 "per_layer_cold_mean": round(float(np.mean(e_p)), 6),
+                                 "max_shortfall": round(float(np.max(np.array(e_p) - np.array(e_c))), 6)},
+                gpu_launches=steps * launches, clocks=clk)
+    out["data"] = ("synthetic (seeded depth-coherent planted-spectrum calibration activations, "
+                   "seeded Gaussian start block)")
+    out["dtype"] = "bf16 GEMMs, fp32 orthonormalisation"
+    # end to end: the layers' tokens from pinned host memory, the bases back
+    Hx = [x.cpu().pin_memory() for x in Xs]
+    Hv = [torch.empty((d, k), dtype=torch.bfloat16).pin_memory() for _ in range(L)]
+    Hq = Q0.cpu().pin_memory()
+    Xd = [torch.empty_like(x) for x in Xs]
+    Qd = torch.empty_like(Q0)
+    ge = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(ge, stream=stream):
+            for layer in range(L):
+                Xd[layer].copy_(Hx[layer], non_blocking=True)
+            Qd.copy_(Hq, non_blocking=True)
+            lib.gsi_calibrate_cascade(Xd, Qd, it_first, it_next, Vc, ws, stream)
+            for layer in range(L):
+                Hv[layer].copy_(Vc[layer], non_blocking=True)
+    ms_e2e = max_over_ranks(time_graph(ge, stream, reps=steps, warmup=1), world)
+    out["e2e"] = {"value": round(ms_e2e / L, 4), "unit": "ms per layer",
+                  "h2d_bytes_per_step": L * n * d * 2 + d * k * 2,
+                  "d2h_bytes_per_step": L * d * k * 2,
+                  "how": "pinned tokens of every layer and Q0 copied in, every basis copied out, "
+                         "around one gsi_calibrate_cascade, graph-captured"}
+    if rank == 0 and not args.no_cpu_baseline:
+        import gsi_inputs as gi
+        from oracle import calibration as cal
+        t0 = time.perf_counter()
+        done = 0
+        V = cal.subspace_iteration(gi.bf16_bits_to_f64(sets[0].X_bits), gi.bf16_bits_to_f64(Q0b),
+                                   it_first)
+        done = 1
+        while done < L and time.perf_counter() - t0 < args.cpu_budget:
+            V = cal.subspace_iteration(gi.bf16_bits_to_f64(sets[done].X_bits), V, it_next)
+            done += 1
+        dt = time.perf_counter() - t0
+        out["cpu_baseline"] = {"value": round(dt / done * 1e3, 3), "unit": "ms per layer",
+                               "cores": os.cpu_count(), "kind": "oracle",
+                               "sample": f"the oracle's cascade over the first {done} layers "
+                                         f"(fp64 numpy), {dt:.1f} s"}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def run_reference_cascade(args, world, rank):
+    """The oracle's cascade (numpy fp64) over the 28 layers, one whole cascade
+    per step."""
+    if rank != 0:
+        return
+    import gsi_inputs as gi
+    from oracle import calibration as cal
+    L = 28
+    c, sets, Q0b = _casc_inputs(L)
+    Xs = [gi.bf16_bits_to_f64(s.X_bits) for s in sets]
+    Q = gi.bf16_bits_to_f64(Q0b)
+    steps = max(1, min(args.steps, 3))
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        cal.cascade(Xs, Q, 8, 2)
+    dt = time.perf_counter() - t0
+    v = dt / steps / L * 1e3
+    out = {"metric": CASC_METRIC, "value": round(v, 3), "unit": "ms per layer", "n_gpus": world,
+           "steps": steps, "warmup": 0, "ms_per_step": round(dt / steps * 1e3, 3),
+           "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic", "impl": "reference",
+           "config": {"workload": "cascade_gptj (oracle: numpy fp64 cascade, 28 layers per step)"},
+           "cpu_baseline": {"value": round(v, 3), "unit": "ms per layer", "cores": os.cpu_count(),
+                            "kind": "oracle", "sample": f"{steps} whole cascades"},
+           "e2e": {"value": round(v, 3), "unit": "ms per layer", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -1206,7 +1355,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["gsi", "reference"], default="gsi")
     ap.add_argument("--workload", choices=["gptj_layer_decode", "batched_T512", "gpt2_qkv_T64",
-                                           "gptj_stack", "opt_mlp", "calibrate_gptj"],
+                                           "gptj_stack", "opt_mlp", "calibrate_gptj",
+                                           "cascade_gptj"],
                     default="gptj_layer_decode")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -1224,6 +1374,10 @@ def main(argv=None):
     try:
         if args.impl == "reference" and args.workload == "calibrate_gptj":
             run_reference_calibrate(args, world, rank)
+        elif args.impl == "reference" and args.workload == "cascade_gptj":
+            run_reference_cascade(args, world, rank)
+        elif args.workload == "cascade_gptj":
+            run_cascade(args, world, rank, local)
         elif args.impl == "reference":
             run_reference(args, world, rank)
         elif args.workload == "calibrate_gptj":

@@ -777,7 +777,7 @@ namespace {
 
 gsi_status_t calibrate_impl(const void* X, int64_t n, int64_t d, int64_t k, const void* Q0,
                             int iters, void* V_k, void* workspace, size_t workspace_bytes,
-                            cudaStream_t stream, CalTimer* tm) {
+                            cudaStream_t stream, CalTimer* tm, bool clear_status = true) {
   if (!X || !Q0 || !V_k || !workspace || iters < 0 || iters > 10000) return GSI_ERR_INVALID_ARG;
   if (!aligned16(X) || !aligned16(Q0) || !aligned16(V_k) ||
       (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
@@ -801,7 +801,10 @@ gsi_status_t calibrate_impl(const void* X, int64_t n, int64_t d, int64_t k, cons
     return GSI_ERR_CUDA;
   gsi_status_t st = cal_prepare();
   if (st != GSI_OK) return st;
-  if (cudaMemsetAsync(r.ctl, 0, sizeof(CalCtl), stream) != cudaSuccess) return GSI_ERR_CUDA;
+  // the Gram tickets return to zero after every use; the status word is
+  // cleared at the start of a call (of a cascade)
+  if (clear_status && cudaMemsetAsync(r.ctl, 0, sizeof(CalCtl), stream) != cudaSuccess)
+    return GSI_ERR_CUDA;
 
   const auto* Xb = static_cast<const __nv_bfloat16*>(X);
   const auto* Q0b = static_cast<const __nv_bfloat16*>(Q0);
@@ -890,6 +893,25 @@ gsi_status_t gsi_calibrate(const void* X, int64_t n, int64_t d, int64_t k, const
                            int iters, void* V_k, void* workspace, size_t workspace_bytes,
                            cudaStream_t stream) {
   return calibrate_impl(X, n, d, k, Q0, iters, V_k, workspace, workspace_bytes, stream, nullptr);
+}
+
+gsi_status_t gsi_calibrate_cascade(const void* const* X, int layers, int64_t n, int64_t d,
+                                   int64_t k, const void* Q0, int iters_first, int iters_next,
+                                   void* const* V, void* workspace, size_t workspace_bytes,
+                                   cudaStream_t stream) {
+  if (!X || !V || layers < 1 || iters_next < 0) return GSI_ERR_INVALID_ARG;
+  for (int l = 0; l < layers; ++l) {
+    if (!X[l] || !V[l]) return GSI_ERR_INVALID_ARG;
+    for (int m = 0; m < l; ++m)
+      if (V[m] == V[l]) return GSI_ERR_INVALID_ARG;  // each layer keeps its own basis
+  }
+  for (int l = 0; l < layers; ++l) {
+    const gsi_status_t st =
+        calibrate_impl(X[l], n, d, k, l == 0 ? Q0 : V[l - 1], l == 0 ? iters_first : iters_next,
+                       V[l], workspace, workspace_bytes, stream, nullptr, l == 0);
+    if (st != GSI_OK) return st;
+  }
+  return GSI_OK;
 }
 
 gsi_status_t gsi_calibrate_timed(const void* X, int64_t n, int64_t d, int64_t k, const void* Q0,

@@ -31,7 +31,7 @@ EXPORTS = ("gsi_create", "gsi_forward", "gsi_forward_host", "gsi_precompute_M",
            "gsi_set_prefetch_group", "gsi_group_create", "gsi_group_forward",
            "gsi_group_set_prefetch", "gsi_group_destroy", "gsi_calibrate_workspace_size",
            "gsi_calibrate", "gsi_calibrate_status", "gsi_calibrate_launch_count",
-           "gsi_calibrate_timed")
+           "gsi_calibrate_timed", "gsi_calibrate_cascade")
 
 _lock = threading.Lock()
 _lib = None
@@ -95,6 +95,9 @@ def _load():
         lib.gsi_calibrate_timed.argtypes = [P, I64, I64, I64, P, ctypes.c_int, P, P, ctypes.c_size_t,
                                             P, P, P, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
         lib.gsi_calibrate_timed.restype = ctypes.c_int
+        lib.gsi_calibrate_cascade.argtypes = [P, ctypes.c_int, I64, I64, I64, P, ctypes.c_int,
+                                              ctypes.c_int, P, P, ctypes.c_size_t, P]
+        lib.gsi_calibrate_cascade.restype = ctypes.c_int
         lib.gsi_calibrate_status.argtypes = [P, P]
         lib.gsi_calibrate_status.restype = ctypes.c_int
         lib.gsi_calibrate_launch_count.argtypes = [I64, I64, I64, ctypes.c_int]
@@ -338,3 +341,19 @@ def gsi_calibrate_timed(X, Q0, iters: int, V_k, workspace, stream=None, max_laun
                                        _ptr(workspace), nbytes, _stream(stream), ms, kinds,
                                        max_launches, ctypes.byref(cnt)), "gsi_calibrate_timed")
     return [(CAL_KINDS[kinds[i]], float(ms[i])) for i in range(cnt.value)]
+
+
+def gsi_calibrate_cascade(Xs, Q0, iters_first: int, iters_next: int, Vs, workspace, stream=None):
+    """Depth cascade: V_0 from Q0 with iters_first iterations on Xs[0]; V_l
+    from V_{l-1} with iters_next iterations on Xs[l].  Xs: list of n x d bf16
+    CUDA tensors; Vs: list of d x k bf16 CUDA tensors (outputs)."""
+    if len(Xs) != len(Vs) or not Xs:
+        raise ValueError("one output basis per layer")
+    n, d = Xs[0].shape
+    _, k = Q0.shape
+    xa = _ptr_array(Xs)
+    va = _ptr_array(Vs)
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(_load().gsi_calibrate_cascade(xa, len(Xs), n, d, k, _ptr(Q0), int(iters_first),
+                                         int(iters_next), va, _ptr(workspace), nbytes,
+                                         _stream(stream)), "gsi_calibrate_cascade")

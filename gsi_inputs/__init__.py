@@ -415,3 +415,23 @@ def calibration_gptj(n: int = 2048) -> Dict:
     from one 2048-token sequence (GPT-J's context length); 8 iterations."""
     return dict(name="calibrate_gptj_d4096", seed=CONFIG_SEED_BASE + 5, n=n, d=4096,
                 k=256, iters=8)
+
+
+def calibration_cascade(n_layers: int, n: int, d: int, k: int, seed: int, mix: float = 0.3,
+                        **kw) -> List[CalibrationSet]:
+    """Calibration tokens of n_layers consecutive layers whose planted
+    directions are depth-coherent: U_{l+1} = QR(U_l + mix * E_l), E_l ~
+    N(0, 1/d) per entry (relative to unit columns, as coherent_next_basis),
+    each layer's tokens drawn by calibration_activations with its own U and
+    seed tag.  With mix = 0.3 adjacent layers' planted subspaces have mean
+    principal-angle cosines near 0.96, in line with the page's observation of
+    > 0.90 in deeper layers (section 2.3)."""
+    r = kw.pop("r", None) or min(d, 2 * k)
+    rng = _rng(seed, 0xCC)
+    U = _qr_signed(rng.standard_normal((d, r)))
+    out = []
+    for layer in range(n_layers):
+        out.append(calibration_activations(n, d, k, seed, tag=layer, U=U, **kw))
+        E = rng.standard_normal((d, r)) / math.sqrt(d)
+        U = _qr_signed(U + mix * E)
+    return out

@@ -260,6 +260,23 @@ gsi_status_t gsi_calibrate(const void *X, int64_t n, int64_t d, int64_t k,
                            const void *Q0, int iters, void *V_k,
                            void *workspace, size_t workspace_bytes,
                            cudaStream_t stream);
+/* The depth cascade of section 2.3: the basis of each layer starts from the
+ * basis just computed for the layer before it.  Layer 0 is
+ * gsi_calibrate(X[0], ..., Q0, iters_first, V[0]); layer l > 0 is
+ * gsi_calibrate(X[l], ..., V[l - 1], iters_next, V[l]).
+ *   X  array of `layers` device pointers, each n x d bf16 (that layer's
+ *      calibration tokens)
+ *   V  array of `layers` distinct device pointers, each d x k bf16 (output)
+ * The host arrays X and V are read during the call only.  One workspace
+ * serves all layers; the status word is cleared once, at the start, and
+ * gsi_calibrate_status() afterwards reports any layer's device-side error.
+ * Shapes and errors as gsi_calibrate; layers < 1, a null entry or a
+ * repeated V entry is GSI_ERR_INVALID_ARG.  Asynchronous on `stream`. */
+gsi_status_t gsi_calibrate_cascade(const void *const *X, int layers, int64_t n,
+                                   int64_t d, int64_t k, const void *Q0,
+                                   int iters_first, int iters_next,
+                                   void *const *V, void *workspace,
+                                   size_t workspace_bytes, cudaStream_t stream);
 /* gsi_calibrate with a CUDA event pair recorded on `stream` around every
  * kernel launch, for measurement: synchronises the stream, then writes each
  * launch's duration (ms) and kind to launch_ms[i] / launch_kind[i] (host

@@ -21,6 +21,9 @@ itself, not x minus a mean.
   subspace_iteration(X, Q0, t)    the algorithm the GPU runs: block power
                                   iteration Q <- orth(X^T (X Q)), t times,
                                   from the given start block Q0
+  cascade(Xs, Q0, t0, t1)         the depth cascade of section 2.3: layer 0
+                                  from Q0 with t0 iterations, layer l + 1
+                                  started from layer l's basis with t1
   principal_sines(A, B)           the comparison between two subspaces
 
 Only span(V_k) matters to the gated map: replacing V_k by V_k R for an
@@ -80,6 +83,21 @@ def subspace_iteration(X, Q0, iters: int) -> np.ndarray:
         Z = X @ Q
         Q = orthonormal_basis(X.T @ Z)
     return Q
+
+
+def cascade(Xs, Q0, iters_first: int, iters_next: int):
+    """Depth cascade (section 2.3: a layer's basis starts from the previous
+    layer's).  Xs: the calibration tokens of consecutive layers.  Layer 0 is
+    subspace_iteration(Xs[0], Q0, iters_first); layer l + 1 is
+    subspace_iteration(Xs[l + 1], V_l, iters_next) with V_l the basis just
+    computed for layer l.  Returns the list of bases."""
+    out = []
+    start, t = Q0, iters_first
+    for X in Xs:
+        V = subspace_iteration(X, start, t)
+        out.append(V)
+        start, t = V, iters_next
+    return out
 
 
 def principal_sines(A, B) -> np.ndarray:

@@ -116,3 +116,16 @@ def test_calibrate_argument_checks(cl):
     assert cl.gsi_calibrate(A, 2048, 4096, 256, B, 8, C, WS, need - 1, None) == 5
     assert cl.gsi_calibrate_status(None, None) == 1
     assert cl.gsi_calibrate_launch_count(2048, 4096, 48, 8) == 0
+
+
+def test_calibrate_cascade_argument_checks(cl):
+    A = ctypes.c_void_p(0x10000)
+    WS = ctypes.c_void_p(0x100000)
+    xs = (ctypes.c_void_p * 2)(0x20000, 0x30000)
+    vs_same = (ctypes.c_void_p * 2)(0x40000, 0x40000)
+    vs_null = (ctypes.c_void_p * 2)(0x40000, None)
+    assert cl.gsi_calibrate_cascade(None, 2, 64, 64, 16, A, 4, 2, vs_same, WS, 1 << 30, None) == 1
+    assert cl.gsi_calibrate_cascade(xs, 0, 64, 64, 16, A, 4, 2, vs_same, WS, 1 << 30, None) == 1
+    assert cl.gsi_calibrate_cascade(xs, 2, 64, 64, 16, A, 4, 2, vs_same, WS, 1 << 30, None) == 1
+    assert cl.gsi_calibrate_cascade(xs, 2, 64, 64, 16, A, 4, 2, vs_null, WS, 1 << 30, None) == 1
+    assert cl.gsi_calibrate_cascade(xs, 2, 64, 64, 16, A, 4, -1, vs_same, WS, 1 << 30, None) == 1

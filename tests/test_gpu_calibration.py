@@ -194,3 +194,34 @@ def test_calibrated_basis_drives_the_gated_map(gsi, orc, cal):
     assert 0.4 < f_ref < 0.6, f_ref
     assert abs(f_gpu - f_ref) <= 0.02, (f_gpu, f_ref)
     assert abs(np.mean(rho) - np.mean(rho_ref)) <= 1e-2 * np.mean(rho_ref)
+
+
+def test_cascade_matches_oracle(gsi, cal):
+    """Depth cascade over 4 depth-coherent layers (8 iterations for layer 0,
+    2 for each later layer from the previous basis) against the oracle's
+    cascade; the result equals gsi_calibrate called layer by layer."""
+    import torch
+    L, n, d, k = 4, 512, 256, 32
+    sets = gi.calibration_cascade(L, n, d, k, seed=361)
+    Q0b = gi.calibration_start(d, k, seed=361)
+    Xs = [to_dev(s.X_bits) for s in sets]
+    Q0 = to_dev(Q0b)
+    Vs = [torch.full((d, k), float("nan"), dtype=torch.bfloat16, device="cuda") for _ in range(L)]
+    ws = torch.empty(gsi.gsi_calibrate_workspace_size(n, d, k), dtype=torch.uint8, device="cuda")
+    gsi.gsi_calibrate_cascade(Xs, Q0, 8, 2, Vs, ws)
+    assert gsi.gsi_calibrate_status(ws) == 0
+    ref = cal.cascade([gi.bf16_bits_to_f64(s.X_bits) for s in sets],
+                      gi.bf16_bits_to_f64(Q0b), 8, 2)
+    for layer, (V, R, s) in enumerate(zip(Vs, ref, sets)):
+        Vf = gi.bf16_bits_to_f64(to_bits(V))
+        X = gi.bf16_bits_to_f64(s.X_bits)
+        assert np.max(cal.principal_sines(Vf, R)) <= SIN_TOL, layer
+        e_gpu, e_ref = cal.captured_energy(X, Vf), cal.captured_energy(X, R)
+        assert abs(e_gpu - e_ref) <= ENERGY_RTOL * e_ref, layer
+    # layer by layer through gsi_calibrate: the same bits
+    prev = Q0
+    for layer in range(L):
+        V = torch.empty((d, k), dtype=torch.bfloat16, device="cuda")
+        gsi.gsi_calibrate(Xs[layer], prev, 8 if layer == 0 else 2, V, ws)
+        assert np.array_equal(to_bits(V), to_bits(Vs[layer])), layer
+        prev = V

@@ -17,7 +17,11 @@ independently of the function's own formula:
   angle of 1e-9 (full relative accuracy for small angles);
 * orthonormal_basis: orthonormal columns spanning the input;
 * captured_energy on the planted spectrum: sum of the k largest s^2 over the
-  sum of all.
+  sum of all;
+* cascade: with no refinement every layer keeps layer 0's subspace; with
+  enough refinement each planted layer reaches its own top-k eigenspace; one
+  refinement step is one product with the next layer's second moment applied
+  to the previous layer's basis.
 
 test_calibration_pins_catch_mutant plants plausible mistakes in a copy of the
 oracle's source and requires that at least one pin rejects each copy.
@@ -148,10 +152,40 @@ def pin_captured_energy(cal):
         assert abs(cal.captured_energy(X, B[:, :k]) - want) < 1e-13, k
 
 
+def pin_cascade(cal):
+    # (i) no refinement past layer 0: every layer keeps layer 0's subspace,
+    # which is the plain iteration on layer 0 (not the start block)
+    rng = np.random.default_rng(81)
+    Xs = [rng.standard_normal((30, 12)) @ np.diag(np.linspace(3.0, 0.5, 12)) for _ in range(3)]
+    Q0 = rng.standard_normal((12, 4))
+    Vs = cal.cascade(Xs, Q0, 5, 0)
+    assert len(Vs) == 3
+    assert np.max(cal.principal_sines(Vs[0], Q0)) > 1e-3
+    for V in Vs[1:]:
+        assert np.max(cal.principal_sines(V, Vs[0])) < 1e-12
+    # (ii) planted layers whose top-4 subspaces differ: enough refinement
+    # reaches each layer's own top-4 eigenspace
+    s = np.array([3.0, 2.6, 2.3, 2.0, 0.9, 0.7, 0.5, 0.3])
+    Xp, Bs = [], []
+    for i in range(3):
+        X, _, B = _planted(40, 16, 8, s, 90 + 3 * i)
+        Xp.append(X)
+        Bs.append(B)
+    Vs = cal.cascade(Xp, Q0=np.random.default_rng(91).standard_normal((16, 4)),
+                     iters_first=40, iters_next=40)
+    for V, B in zip(Vs, Bs):
+        assert np.max(cal.principal_sines(V, B[:, :4])) < 1e-10
+    # (iii) one refinement step from the previous basis: exactly one product
+    # with layer 1's second moment applied to layer 0's result
+    Vs = cal.cascade(Xp[:2], np.random.default_rng(92).standard_normal((16, 4)), 3, 1)
+    want = Xp[1].T @ (Xp[1] @ Vs[0])
+    assert np.max(cal.principal_sines(Vs[1], want)) < 1e-10
+
+
 ALL_PINS = [
     pin_top_k_planted, pin_iteration_two_dims, pin_iteration_diagonal_moment,
     pin_iteration_span_invariance, pin_iteration_rate, pin_principal_sines,
-    pin_orthonormal_basis, pin_captured_energy,
+    pin_orthonormal_basis, pin_captured_energy, pin_cascade,
 ]
 
 
@@ -174,6 +208,8 @@ MUTANTS = [
     ("basis not normalised", "Q, _ = np.linalg.qr(_f64(Y))\n    return Q",
      "Q, Rf = np.linalg.qr(_f64(Y))\n    return Q * np.abs(np.diag(Rf))"),
     ("energy of the sum", "np.sum((X @ Qv) ** 2)", "np.sum(X @ Qv) ** 2"),
+    ("cascade restarts from Q0", "        start, t = V, iters_next", "        start, t = Q0, iters_next"),
+    ("cascade keeps the first count", "        start, t = V, iters_next", "        start, t = V, iters_first"),
 ]
 
 
