@@ -1348,6 +1348,174 @@ def run_reference_cascade(args, world, rank):
     print(json.dumps(out), flush=True)
 
 
+SWEEP_KS = (128, 256, 512)
+SWEEP_EPS = (0.02, 0.05, 0.10, 0.20, math.inf)
+
+
+def run_sweep(args, world, rank, local):
+    """Operating points of the GPT-J-shaped stacked qkv+fc_in linear (4096 ->
+    28672) at decode: k in {128, 256, 512} x eps in {0.02, 0.05, 0.10, 0.20,
+    inf}; eps = inf is the static projection (no residual path), the page's
+    negative control.  512 sequential one-token calls per point on tokens with
+    a gapless power-law spectrum; V_k = the population top-k basis.  Per point:
+    the fast fraction, the algorithmic bytes per call, the relative output
+    error against W x (the same kernel at eps = 0), the largest ratio of a
+    fast token's error to Theorem 4's bound ||W||_2 eps ||x||, and the time
+    per call.  Replicas of (V_k, M) per k cycle so that the fast path streams
+    from HBM."""
+    import torch
+
+    import gsi_inputs as gi
+    from gated_rank_subspace_gsi_gb300 import lib
+    torch.cuda.set_device(local)
+    lib.library()
+    seed = gi.CONFIG_SEED_BASE + 7
+    d_out, d, T = 28672, 4096, 512
+    cs = gi.sweep_activations(T, d, seed)
+    W = gi.gaussian_weights(d_out, d, seed, device="cuda")
+    x = torch.from_numpy(cs.X_bits.view(np.int16)).view(torch.bfloat16).cuda()
+    props = torch.cuda.get_device_properties(local)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
+    stream = torch.cuda.Stream()
+    steps = max(1, args.steps // 60)
+    peak, pkind = hbm_peak()
+    # ||W||_2 by power iteration (fp32 on the device; measurement only)
+    v = torch.randn(d, device="cuda", generator=torch.Generator(device="cuda").manual_seed(seed))
+    Wf = W.float()
+    for _ in range(60):
+        v = Wf.t() @ (Wf @ v)
+        v = v / v.norm()
+    w_norm = float((Wf @ v).norm())
+    del Wf
+    xnorm = x.float().norm(dim=1)
+
+    def run_point(handles, eps_is_inf):
+        y = torch.zeros((T, d_out), dtype=torch.float32, device="cuda")
+        gate = torch.zeros((T,), dtype=torch.uint8, device="cuda")
+        rho = torch.zeros((T,), dtype=torch.float32, device="cuda")
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(graph, stream=stream):
+                for t in range(T):
+                    sl = slice(t, t + 1)
+                    lib.gsi_forward(handles[t % len(handles)], x[sl], y[sl], gate[sl], rho[sl],
+                                    stream)
+        ms, clk = _timed(graph, stream, steps, args.warmup, world, local)
+        st = lib.gsi_device_status(handles[0], stream)
+        if st != 0:
+            raise RuntimeError(f"device status: {lib.gsi_status_string(st)}")
+        del graph
+        return y, gate, rho, ms, clk
+
+    # exact W x: the slow path everywhere (eps = 0), any basis
+    V0 = torch.from_numpy(gi.to_bf16_bits(cs.U[:, :128]).view(np.int16)).view(torch.bfloat16).cuda()
+    M0 = torch.empty((d_out, 128), dtype=torch.bfloat16, device="cuda")
+    lib.gsi_precompute_M(W, V0, M0)
+    torch.cuda.synchronize()
+    h0 = lib.gsi_create(W, V0, M0, 0.0)
+    y_exact, g0, _, ms_dense, clk = run_point([h0], False)
+    lib.gsi_destroy(h0)
+    ynorm = y_exact.norm(dim=1)
+    points = []
+    for k in SWEEP_KS:
+        V = torch.from_numpy(gi.to_bf16_bits(cs.U[:, :k]).view(np.int16)).view(torch.bfloat16).cuda()
+        M = torch.empty((d_out, k), dtype=torch.bfloat16, device="cuda")
+        lib.gsi_precompute_M(W, V, M)
+        torch.cuda.synchronize()
+        op_bytes = d * k * 2 + d_out * k * 2
+        R = max(2, int(math.ceil(1.5 * l2 / op_bytes)))
+        Vs = [V] + [V.clone() for _ in range(R - 1)]
+        Ms = [M] + [M.clone() for _ in range(R - 1)]
+        torch.cuda.synchronize()
+        for eps in SWEEP_EPS:
+            hs = [lib.gsi_create(W, Vs[r], Ms[r], eps) for r in range(R)]
+            for r in range(R):
+                lib.gsi_set_prefetch(hs[r], hs[(r + 1) % R])
+            y, gate, rho, ms, clk = run_point(hs, math.isinf(eps))
+            fast = gate == 0
+            err = (y - y_exact).norm(dim=1)
+            rel = err / ynorm
+            n_fast = int(fast.sum())
+            fast_b = _fast_bytes(gi.LinearSpec("qkv_fc_in", d_out, d, k, eps, 0, 0))
+            if k > 256:  # the k = 512 kernel forms the residual explicitly: no correction tiles
+                fast_b -= correction_bytes(k)
+            bytes_call = fast_b + (T - n_fast) / T * (d_out * d * 2)
+            us = ms * 1e3 / T
+            pt = {"k": k, "eps": "inf" if math.isinf(eps) else eps, "fast_fraction": n_fast / T,
+                  "us_per_call": round(us, 3), "bytes_per_call": int(bytes_call),
+                  "gbs": round(bytes_call / (us * 1e-6) / 1e9, 1),
+                  "rel_err_mean": float(rel.mean()), "rel_err_max": float(rel.max()),
+                  "weight_read_speedup": round(d_out * d * 2 / bytes_call, 2),
+                  "time_speedup_vs_eps0": round(ms_dense / ms, 3), "replicas": R}
+            if n_fast and not math.isinf(eps):
+                bound = w_norm * eps * xnorm
+                pt["theorem4_max_ratio"] = float((err[fast] / bound[fast]).max())
+            points.append(pt)
+            for h in hs:
+                lib.gsi_destroy(h)
+        del Vs, Ms
+    main_pt = next(p for p in points if p["k"] == 256 and p["eps"] == 0.10)
+    out = _line("µs per gated linear at k=256, eps=0.10 (GPT-J qkv+fc_in 4096 -> 28672, decode), "
+                "operating-point sweep", main_pt["us_per_call"], "us per gated linear", world,
+                steps, args.warmup, main_pt["us_per_call"] * T / 1e3,
+                {"workload": f"sweep_gptj: W 28672x4096, k in {list(SWEEP_KS)}, eps in "
+                             f"[0.02, 0.05, 0.10, 0.20, inf], {T} sequential decode tokens per "
+                             f"point (gapless power-law spectrum, r=1024), V_k = population "
+                             f"top-k basis",
+                 "l2": "replicas of (V_k, M) per k exceed L2 (1.5x); W 235 MB beyond L2 by size"},
+                sweep=points, w_spectral_norm=round(w_norm, 4),
+                eps0_us_per_call=round(ms_dense * 1e3 / T, 3),
+                roofline={"bound": "hbm", "achieved": main_pt["gbs"], "peak": peak, "unit": "GB/s",
+                          "frac": round(main_pt["gbs"] / peak, 4), "traffic": None,
+                          "kernel": "gsi_decode3_kernel<256> (whole call)",
+                          "peak_kind": f"{pkind} HBM copy"},
+                gpu_launches=steps * T * (1 + len(points)), clocks=clk)
+    out["data"] = ("synthetic (seeded Gaussian W, power-law activations, planted population "
+                   "basis)")
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def run_reference_sweep(args, world, rank):
+    """The oracle (fp64 C) at the sweep's main operating point (k = 256,
+    eps = 0.10) on the host cores: each step 4 of the sweep's tokens through
+    the 4096 -> 28672 linear."""
+    if rank != 0:
+        return
+    import oracle
+
+    import gsi_inputs as gi
+    orc = oracle.default()
+    seed = gi.CONFIG_SEED_BASE + 7
+    d_out, d, T, k = 28672, 4096, 512, 256
+    cs = gi.sweep_activations(T, d, seed)
+    Wd = orc.bf16_decode(gi.gaussian_weights(d_out, d, seed))
+    Vb = gi.to_bf16_bits(cs.U[:, :k])
+    Vd = orc.bf16_decode(Vb)
+    Md = orc.bf16_decode(orc.bf16_encode(orc.precompute_M(Wd, Vd)))
+    per_step = 4
+    steps = max(1, min(args.steps, 10))
+    t0 = time.perf_counter()
+    for st in range(steps):
+        toks = [(st * per_step + i) % T for i in range(per_step)]
+        orc.forward(Wd, Vd, Md, 0.10, orc.bf16_decode(cs.X_bits[toks]))
+    dt = time.perf_counter() - t0
+    v = dt / (steps * per_step) * 1e6
+    out = {"metric": "µs per gated linear at k=256, eps=0.10 (GPT-J qkv+fc_in 4096 -> 28672, "
+                     "decode), operating-point sweep", "value": round(v, 3),
+           "unit": "us per gated linear", "n_gpus": world, "steps": steps, "warmup": 0,
+           "ms_per_step": round(dt / steps * 1e3, 3), "higher_is_better": False,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "impl": "reference",
+           "config": {"workload": f"sweep_gptj main point (oracle: {per_step} tokens per step)"},
+           "cpu_baseline": {"value": round(v, 3), "unit": "us per gated linear",
+                            "cores": orc.num_threads(), "kind": "oracle",
+                            "sample": f"{steps * per_step} tokens at k=256, eps=0.10"},
+           "e2e": {"value": round(v, 3), "unit": "us per gated linear", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -1356,7 +1524,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["gsi", "reference"], default="gsi")
     ap.add_argument("--workload", choices=["gptj_layer_decode", "batched_T512", "gpt2_qkv_T64",
                                            "gptj_stack", "opt_mlp", "calibrate_gptj",
-                                           "cascade_gptj"],
+                                           "cascade_gptj", "sweep_gptj"],
                     default="gptj_layer_decode")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -1376,8 +1544,12 @@ def main(argv=None):
             run_reference_calibrate(args, world, rank)
         elif args.impl == "reference" and args.workload == "cascade_gptj":
             run_reference_cascade(args, world, rank)
+        elif args.impl == "reference" and args.workload == "sweep_gptj":
+            run_reference_sweep(args, world, rank)
         elif args.workload == "cascade_gptj":
             run_cascade(args, world, rank, local)
+        elif args.workload == "sweep_gptj":
+            run_sweep(args, world, rank, local)
         elif args.impl == "reference":
             run_reference(args, world, rank)
         elif args.workload == "calibrate_gptj":

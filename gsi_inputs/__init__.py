@@ -435,3 +435,15 @@ def calibration_cascade(n_layers: int, n: int, d: int, k: int, seed: int, mix: f
         E = rng.standard_normal((d, r)) / math.sqrt(d)
         U = _qr_signed(U + mix * E)
     return out
+
+
+def sweep_activations(T: int, d: int, seed: int, r: int = 1024, decay: float = 1.0,
+                      noise: float = 0.02, tag: int = 0) -> CalibrationSet:
+    """Tokens for operating-point sweeps: a gapless power-law spectrum
+    sigma_j = (1 + j)^-decay over r planted directions (decay 1 puts about
+    0.6 / k of a token's energy outside the top k directions, so rho ~ 0.05 at
+    k = 256: the concentration the page reports for GPT-J, 99.8% of tokens
+    below eps = 0.10), plus the isotropic noise floor of
+    calibration_activations.  U[:, :k] is the population top-k basis."""
+    return calibration_activations(T, d, r, seed, tag=tag, r=r, decay=decay, gap=1.0,
+                                   noise=noise)

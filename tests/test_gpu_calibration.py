@@ -15,6 +15,8 @@ Tolerances, from the arithmetic:
   span, GPU vs oracle: first-order insensitive to the span's error (the
   oracle's span is near-stationary for it), so 1e-4 relative.
 """
+import math
+
 import numpy as np
 import pytest
 
@@ -225,3 +227,36 @@ def test_cascade_matches_oracle(gsi, cal):
         gsi.gsi_calibrate(Xs[layer], prev, 8 if layer == 0 else 2, V, ws)
         assert np.array_equal(to_bits(V), to_bits(Vs[layer])), layer
         prev = V
+
+
+@pytest.mark.parametrize("k", [64, 128])
+@pytest.mark.parametrize("T", [1, 96])
+def test_theorem4_holds_on_gpu_outputs(gsi, orc, k, T):
+    """Operating points (N4): on power-law tokens with the population top-k
+    basis, every token the GPU sends down the fast path has
+    ||y - W x|| <= ||W||_2 eps ||x|| (Theorem 4, section 2.2), with W x and
+    ||W||_2 from the oracle in fp64; eps = inf (static projection) sends every
+    token fast.  The GPU's extra error (bf16 M, fp32 sums) is a few 1e-3 of
+    ||y|| and leaves the bound with room at these shapes."""
+    d_out, d, n_tok = 2048, 1024, 96
+    cs = gi.sweep_activations(n_tok, d, seed=371, r=512)
+    W = gi.gaussian_weights(d_out, d, seed=372)
+    Vb = gi.to_bf16_bits(cs.U[:, :k])
+    w2 = orc.spectral_norm(gi.bf16_bits_to_f64(W)) * (1 + 1e-6)
+    Xf = gi.bf16_bits_to_f64(cs.X_bits)
+    y_exact = Xf @ gi.bf16_bits_to_f64(W).T
+    xn = np.linalg.norm(Xf, axis=1)
+    for eps in (0.05, 0.1, float("inf")):
+        lin = GpuLinear(gsi, orc, W, Vb, eps, max_T=n_tok)
+        try:
+            y, gate, rho = lin.forward(cs.X_bits, one_by_one=(T == 1))
+        finally:
+            lin.close()
+        fast = gate == 0
+        if math.isinf(eps):
+            assert fast.all()
+            continue
+        assert 0 < fast.sum() < n_tok, (k, eps, fast.sum())
+        err = np.linalg.norm(y - y_exact, axis=1)
+        ratio = err[fast] / (w2 * eps * xn[fast])
+        assert ratio.max() <= 1.0, (k, eps, ratio.max())
