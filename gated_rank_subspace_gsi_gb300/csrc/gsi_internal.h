@@ -86,7 +86,7 @@ struct gsi_handle {
   alignas(64) unsigned char tmaps_proj[128] = {};  // TMA map of bVT
   // TMA tensor maps of the tcgen05 GEMMs (CUtensorMap, 128 bytes each):
   // W, M, G_fast hi plane, G_fast lo plane, X_slow
-  alignas(64) unsigned char tmaps[5][128] = {};
+  alignas(64) unsigned char tmaps[14][128] = {};  // the batched GEMM's tensor maps
 
   // host staging for gsi_forward_host
   void* st_dev = nullptr;

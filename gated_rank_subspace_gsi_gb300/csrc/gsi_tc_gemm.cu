@@ -40,6 +40,17 @@ constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kTcThreads = 192;
 constexpr int kTmemCols = 256;
 constexpr size_t kTcSmem = size_t(kStages) * kStageBytes + 1024;  // + alignment slack
+// The ring of the GEMM kernel: its bytes are fixed (4 stages of the largest
+// tiles); a CTA whose token tile is shorter loads B as one or two boxes of
+// 32, 64, 128 or 256 rows that just cover it, and fits more, smaller stages.
+constexpr int kRingBytes = kStages * kStageBytes;
+constexpr int kMaxStages = 6;
+constexpr int kBoxRows[4] = {256, 128, 64, 32};  // host: the maps' box heights
+__host__ __device__ constexpr int box_rows(int i) { return 256 >> i; }  // = kBoxRows[i]
+struct TcMaps {
+  CUtensorMap W, M;
+  CUtensorMap Xs[4], Ghi[4], Glo[4];  // B operands, box heights kBoxRows[]
+};
 
 // ---- tcgen05 wrappers ------------------------------------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
@@ -122,14 +133,16 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, uin
   return true;
 }
 
+// index into kBoxRows of the smallest box of at least r rows (r <= 128), and
+// the two boxes that cover a tile of N rows: a 256-row box for N > 192, else
+// a 128-row box followed by the smallest box that covers the rest
+__device__ __forceinline__ int box_index(int r) { return r <= 32 ? 3 : (r <= 64 ? 2 : 1); }
+
 __global__ void __launch_bounds__(kTcThreads, 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmM,
-                   const __grid_constant__ CUtensorMap tmGhi,
-                   const __grid_constant__ CUtensorMap tmGlo,
-                   const __grid_constant__ CUtensorMap tmXs, TcGemmArgs a) {
+    tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs a) {
   extern __shared__ unsigned char smem_raw[];
-  __shared__ uint64_t full_bar[kStages];
-  __shared__ uint64_t empty_bar[kStages];
+  __shared__ uint64_t full_bar[kMaxStages];
+  __shared__ uint64_t empty_bar[kMaxStages];
   __shared__ uint64_t accum_bar;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
@@ -147,6 +160,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (j0 >= n) return;  // uniform: this token tile is empty
   const int nvalid = min(kBN, n - j0);
   const int N = (nvalid + 15) & ~15;
+  // B boxes covering the N token rows, and the ring depth they leave room for
+  const int bx1 = N > 192 ? 0 : box_index(N);
+  const int bx2 = (N > 128 && N <= 192) ? box_index(N - 128) : -1;
+  const int b_rows = box_rows(bx1) + (bx2 >= 0 ? box_rows(bx2) : 0);
+  const int st_bytes = kABytes + b_rows * kBK * 2;
+  const int stages = min(kMaxStages, kRingBytes / st_bytes);
   const int kb_half = (a.k + kBK - 1) / kBK;
   const int num_kb = is_slow ? (a.d + kBK - 1) / kBK : 2 * kb_half;
   const int32_t* idx = is_slow ? a.idx_slow : a.idx_fast;
@@ -155,7 +174,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   unsigned char* tiles = smem_raw + (base - smem_addr(smem_raw));
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < stages; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
@@ -174,21 +193,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       int kb = 0;
       for (; kb < num_kb; ++kb) {
-        const int s = kb % kStages;
-        if (kb >= kStages &&
-            !wait_bounded(&empty_bar[s], ((kb / kStages) & 1) ^ 1, a.status, &s_abort))
+        const int s = kb % stages;
+        if (kb >= stages &&
+            !wait_bounded(&empty_bar[s], ((kb / stages) & 1) ^ 1, a.status, &s_abort))
           break;
-        unsigned char* sa = tiles + size_t(s) * kStageBytes;
+        unsigned char* sa = tiles + size_t(s) * st_bytes;
         unsigned char* sb = sa + kABytes;
-        mbar_arrive_expect_tx(&full_bar[s], kStageBytes);
-        if (is_slow) {
-          tma_load_2d(sa, &tmW, kb * kBK, o0, &full_bar[s]);
-          tma_load_2d(sb, &tmXs, kb * kBK, j0, &full_bar[s]);
-        } else {
-          const int plane = kb / kb_half, kk = kb % kb_half;
-          tma_load_2d(sa, &tmM, kk * kBK, o0, &full_bar[s]);
-          tma_load_2d(sb, plane ? &tmGlo : &tmGhi, kk * kBK, j0, &full_bar[s]);
-        }
+        mbar_arrive_expect_tx(&full_bar[s], uint32_t(st_bytes));
+        const int plane = is_slow ? 0 : kb / kb_half;
+        const int kc = (is_slow ? kb : kb % kb_half) * kBK;
+        const CUtensorMap* bm = is_slow ? maps.Xs : (plane ? maps.Glo : maps.Ghi);
+        tma_load_2d(sa, is_slow ? &maps.W : &maps.M, kc, o0, &full_bar[s]);
+        tma_load_2d(sb, &bm[bx1], kc, j0, &full_bar[s]);
+        if (bx2 >= 0)
+          tma_load_2d(sb + box_rows(bx1) * kBK * 2, &bm[bx2], kc, j0 + box_rows(bx1), &full_bar[s]);
       }
       s_issued = kb;
     }
@@ -196,10 +214,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(kBM, N);
       for (int kb = 0; kb < num_kb; ++kb) {
-        const int s = kb % kStages;
-        if (!wait_bounded(&full_bar[s], (kb / kStages) & 1, a.status, &s_abort)) break;
+        const int s = kb % stages;
+        if (!wait_bounded(&full_bar[s], (kb / stages) & 1, a.status, &s_abort)) break;
         tc_fence_after();
-        const uint32_t sa = base + uint32_t(s) * kStageBytes;
+        const uint32_t sa = base + uint32_t(s) * uint32_t(st_bytes);
         const uint32_t sb = sa + kABytes;
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk)
@@ -235,10 +253,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (threadIdx.x == 0 && s_abort) {
     // make sure no bulk copy is still writing into this CTA's shared memory
     const int issued = s_issued;
-    for (int kb = max(0, issued - kStages); kb < issued; ++kb) {
-      const int s = kb % kStages;
+    for (int kb = max(0, issued - stages); kb < issued; ++kb) {
+      const int s = kb % stages;
       const uint64_t t0 = globaltimer_ns();
-      while (!mbar_try_wait(&full_bar[s], (kb / kStages) & 1) &&
+      while (!mbar_try_wait(&full_bar[s], (kb / stages) & 1) &&
              globaltimer_ns() - t0 < kWaitLimitNs) {
       }
     }
@@ -516,13 +534,17 @@ gsi_status_t tc_proj_launch(gsi_handle* h, const void* x, int64_t T, int S, int 
 
 gsi_status_t tc_gemm_prepare(gsi_handle* h) {
   static_assert(sizeof(CUtensorMap) == 128, "tensor map size");
-  CUtensorMap* maps = reinterpret_cast<CUtensorMap*>(h->tmaps);
+  static_assert(sizeof(TcMaps) <= sizeof(h->tmaps), "tensor map storage");
+  TcMaps* maps = reinterpret_cast<TcMaps*>(h->tmaps);
   const uint64_t mt = uint64_t(h->max_T);
-  bool ok = encode_2d(&maps[0], h->W, uint64_t(h->d_out), uint64_t(h->d), kBM) &&
-            encode_2d(&maps[1], h->M, uint64_t(h->d_out), uint64_t(h->k), kBM) &&
-            encode_2d(&maps[2], h->bGf, mt, uint64_t(h->k), kBN) &&
-            encode_2d(&maps[3], h->bGf + size_t(mt) * h->k, mt, uint64_t(h->k), kBN) &&
-            encode_2d(&maps[4], h->bXs, mt, uint64_t(h->d), kBN);
+  bool ok = encode_2d(&maps->W, h->W, uint64_t(h->d_out), uint64_t(h->d), kBM) &&
+            encode_2d(&maps->M, h->M, uint64_t(h->d_out), uint64_t(h->k), kBM);
+  for (int b = 0; b < 4 && ok; ++b) {
+    const uint32_t rows = uint32_t(kBoxRows[b]);
+    ok = encode_2d(&maps->Xs[b], h->bXs, mt, uint64_t(h->d), rows) &&
+         encode_2d(&maps->Ghi[b], h->bGf, mt, uint64_t(h->k), rows) &&
+         encode_2d(&maps->Glo[b], h->bGf + size_t(mt) * h->k, mt, uint64_t(h->k), rows);
+  }
   if (!ok) return GSI_ERR_CUDA;
   if (cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            int(kTcSmem)) != cudaSuccess)
@@ -531,11 +553,10 @@ gsi_status_t tc_gemm_prepare(gsi_handle* h) {
 }
 
 gsi_status_t tc_gemm_launch(gsi_handle* h, const TcGemmArgs& a, cudaStream_t s) {
-  const CUtensorMap* maps = reinterpret_cast<const CUtensorMap*>(h->tmaps);
+  const TcMaps* maps = reinterpret_cast<const TcMaps*>(h->tmaps);
   const int n_tiles = (a.T + kBN - 1) / kBN;
   dim3 grid(unsigned((a.d_out + kBM - 1) / kBM), unsigned(2 * n_tiles));
-  return launch_pdl(tc_gemm_kernel, grid, dim3(kTcThreads), kTcSmem, s, maps[0], maps[1], maps[2],
-                    maps[3], maps[4], a) == cudaSuccess
+  return launch_pdl(tc_gemm_kernel, grid, dim3(kTcThreads), kTcSmem, s, *maps, a) == cudaSuccess
              ? GSI_OK
              : GSI_ERR_CUDA;
 }
