@@ -378,6 +378,7 @@ __global__ void __launch_bounds__(1024) compact_kernel(const uint8_t* __restrict
   if (tid == 0) {
     count[0] = T - s_base;  // n_fast
     count[1] = s_base;      // n_slow
+    count[2] = 0;           // the GEMM's tile queue starts empty
   }
 }
 
@@ -546,6 +547,7 @@ gsi_status_t batched_launch(gsi_handle* h, const void* x, int64_t T, float* y, u
   g.idx_fast = h->bidx_fast;
   g.idx_slow = h->bidx_slow;
   g.count = h->bcount;
+  g.tile_counter = h->bcount + 2;
   g.y = y;
   g.T = int(T);
   g.d_out = int(h->d_out);

@@ -13,11 +13,13 @@
 // bf16 planes hi = bf16(g), lo = bf16(g - hi); both accumulate into the same
 // TMEM tile, which keeps g to ~2^-16 relative although the operands are bf16.
 //
-// CTA layout (192 threads): warp 0 issues TMA loads (one elected lane),
-// warp 1 allocates TMEM and issues tcgen05.mma (one elected lane), warps 2-5
-// drain the fp32 accumulator from TMEM (tcgen05.ld 32x32b) and scatter each
-// token column to its row of y.  A 4-stage mbarrier ring of 128x64 (A) and
-// 256x64 (B) bf16 tiles, 128-byte swizzled, feeds the MMAs.
+// Persistent CTAs (192 threads, one per SM) take 128-row x 256-token tiles of
+// both GEMMs from a device-side queue, slow tiles first: warp 0 issues TMA
+// loads (one elected lane), warp 1 allocates TMEM and issues tcgen05.mma (one
+// elected lane) into one of two 256-column accumulators, warps 2-5 drain the
+// other (tcgen05.ld 32x32b) and scatter each token column to its row of y.
+// A 4-stage mbarrier ring of 128x64 (A) and up to 256x64 (B) bf16 tiles,
+// 128-byte swizzled, runs on across a CTA's tiles.
 #include <cuda.h>
 
 #include <algorithm>
@@ -38,13 +40,11 @@ constexpr int kABytes = kBM * kBK * 2;   // 16 KiB
 constexpr int kBBytes = kBN * kBK * 2;   // 32 KiB
 constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kTcThreads = 192;
-constexpr int kTmemCols = 256;
+constexpr int kTmemCols = 512;  // two 256-column accumulators
 constexpr size_t kTcSmem = size_t(kStages) * kStageBytes + 1024;  // + alignment slack
-// The ring of the GEMM kernel: its bytes are fixed (4 stages of the largest
-// tiles); a CTA whose token tile is shorter loads B as one or two boxes of
-// 32, 64, 128 or 256 rows that just cover it, and fits more, smaller stages.
-constexpr int kRingBytes = kStages * kStageBytes;
-constexpr int kMaxStages = 6;
+// The GEMM kernel's ring has 4 stages of the largest tiles (A 128 x 64,
+// B 256 x 64); a shorter token tile loads B as one or two boxes of 32, 64,
+// 128 or 256 rows that just cover it.
 constexpr int kBoxRows[4] = {256, 128, 64, 32};  // host: the maps' box heights
 __host__ __device__ constexpr int box_rows(int i) { return 256 >> i; }  // = kBoxRows[i]
 struct TcMaps {
@@ -138,47 +138,78 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, uin
 // a 128-row box followed by the smallest box that covers the rest
 __device__ __forceinline__ int box_index(int r) { return r <= 32 ? 3 : (r <= 64 ? 2 : 1); }
 
+__device__ __forceinline__ void mbar_arrive_cta(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_addr(bar)) : "memory");
+}
+
+// One tile of the two GEMMs: 128 output rows (o0) x up to 256 tokens (j0).
+// Slow tiles come first in the numbering (the long ones start first), then
+// fast tiles; within a kind, consecutive tiles share a token tile and walk the
+// output rows, so their B operand stays in L2.
+struct Tile {
+  bool slow;
+  int o0, j0, nvalid, N, num_kb, bx1, bx2, b_bytes;
+};
+
+__device__ __forceinline__ Tile decode_tile(int t, int n_slow_tiles, int n_mt, int n_fast,
+                                            int n_slow, const TcGemmArgs& a) {
+  Tile u;
+  u.slow = t < n_slow_tiles;
+  const int tt = u.slow ? t : t - n_slow_tiles;
+  const int mt = tt % n_mt, jt = tt / n_mt;
+  u.o0 = mt * kBM;
+  u.j0 = jt * kBN;
+  u.nvalid = min(kBN, (u.slow ? n_slow : n_fast) - u.j0);
+  u.N = (u.nvalid + 15) & ~15;
+  u.num_kb = u.slow ? (a.d + kBK - 1) / kBK : 2 * ((a.k + kBK - 1) / kBK);
+  u.bx1 = u.N > 192 ? 0 : box_index(u.N);
+  u.bx2 = (u.N > 128 && u.N <= 192) ? box_index(u.N - 128) : -1;
+  u.b_bytes = (box_rows(u.bx1) + (u.bx2 >= 0 ? box_rows(u.bx2) : 0)) * kBK * 2;
+  return u;
+}
+
+// Persistent: one CTA per SM takes tiles from a device-wide counter (zeroed
+// by the compaction kernel) until none are left.  Warp 0 (one lane) takes
+// each tile, publishes it to the other roles through a two-slot queue in
+// shared memory, and streams its operands through a 4-stage TMA ring that runs
+// on across tiles; warp 1 (one lane) issues the tile's MMAs into one of two
+// TMEM accumulators; warps 2-5 drain the other accumulator of the previous
+// tile meanwhile and scatter it to y.  Every wait is bounded.
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs a) {
+  constexpr int kQ = 2;  // tiles in flight: queue slots and TMEM accumulators
   extern __shared__ unsigned char smem_raw[];
-  __shared__ uint64_t full_bar[kMaxStages];
-  __shared__ uint64_t empty_bar[kMaxStages];
-  __shared__ uint64_t accum_bar;
+  __shared__ uint64_t full_bar[kStages];
+  __shared__ uint64_t empty_bar[kStages];
+  __shared__ uint64_t tq_full[kQ], tq_empty[kQ], acc_full[kQ], acc_empty[kQ];
+  __shared__ int s_tile[kQ];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int s_issued;
 
   pdl_launch_dependents();
-  pdl_wait();  // token counts, index lists and gathered operands are now visible
+  pdl_wait();  // token counts, index lists, gathered operands and the tile counter are visible
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int o0 = blockIdx.x * kBM;
-  const int n_tiles = (a.T + kBN - 1) / kBN;
-  const bool is_slow = int(blockIdx.y) < n_tiles;
-  const int jt = is_slow ? int(blockIdx.y) : int(blockIdx.y) - n_tiles;
-  const int n = is_slow ? a.count[1] : a.count[0];
-  const int j0 = jt * kBN;
-  if (j0 >= n) return;  // uniform: this token tile is empty
-  const int nvalid = min(kBN, n - j0);
-  const int N = (nvalid + 15) & ~15;
-  // B boxes covering the N token rows, and the ring depth they leave room for
-  const int bx1 = N > 192 ? 0 : box_index(N);
-  const int bx2 = (N > 128 && N <= 192) ? box_index(N - 128) : -1;
-  const int b_rows = box_rows(bx1) + (bx2 >= 0 ? box_rows(bx2) : 0);
-  const int st_bytes = kABytes + b_rows * kBK * 2;
-  const int stages = min(kMaxStages, kRingBytes / st_bytes);
+  const int n_fast = a.count[0], n_slow = a.count[1];
+  const int n_mt = (a.d_out + kBM - 1) / kBM;
+  const int n_slow_tiles = n_mt * ((n_slow + kBN - 1) / kBN);
+  const int total = n_slow_tiles + n_mt * ((n_fast + kBN - 1) / kBN);
   const int kb_half = (a.k + kBK - 1) / kBK;
-  const int num_kb = is_slow ? (a.d + kBK - 1) / kBK : 2 * kb_half;
-  const int32_t* idx = is_slow ? a.idx_slow : a.idx_fast;
 
   const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
   unsigned char* tiles = smem_raw + (base - smem_addr(smem_raw));
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < stages; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
-    mbar_init(&accum_bar, 1);
+    for (int q = 0; q < kQ; ++q) {
+      mbar_init(&tq_full[q], 1);
+      mbar_init(&tq_empty[q], 5);   // the MMA lane and the 4 epilogue warps
+      mbar_init(&acc_full[q], 1);
+      mbar_init(&acc_empty[q], 4);  // the 4 epilogue warps
+    }
     s_abort = 0;
     s_issued = 0;
     fence_mbar_init();
@@ -191,61 +222,109 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      int kb = 0;
-      for (; kb < num_kb; ++kb) {
-        const int s = kb % stages;
-        if (kb >= stages &&
-            !wait_bounded(&empty_bar[s], ((kb / stages) & 1) ^ 1, a.status, &s_abort))
-          break;
-        unsigned char* sa = tiles + size_t(s) * st_bytes;
-        unsigned char* sb = sa + kABytes;
-        mbar_arrive_expect_tx(&full_bar[s], uint32_t(st_bytes));
-        const int plane = is_slow ? 0 : kb / kb_half;
-        const int kc = (is_slow ? kb : kb % kb_half) * kBK;
-        const CUtensorMap* bm = is_slow ? maps.Xs : (plane ? maps.Glo : maps.Ghi);
-        tma_load_2d(sa, is_slow ? &maps.W : &maps.M, kc, o0, &full_bar[s]);
-        tma_load_2d(sb, &bm[bx1], kc, j0, &full_bar[s]);
-        if (bx2 >= 0)
-          tma_load_2d(sb + box_rows(bx1) * kBK * 2, &bm[bx2], kc, j0 + box_rows(bx1), &full_bar[s]);
+      int g = 0;  // K steps issued over all tiles: stage g % kStages
+      for (int i = 0;; ++i) {
+        const int q = i % kQ;
+        if (i >= kQ && !wait_bounded(&tq_empty[q], ((i / kQ) & 1) ^ 1, a.status, &s_abort)) break;
+        int t = atomicAdd(a.tile_counter, 1);
+        if (t >= total) t = -1;
+        s_tile[q] = t;
+        mbar_arrive_cta(&tq_full[q]);
+        if (t < 0) break;
+        const Tile u = decode_tile(t, n_slow_tiles, n_mt, n_fast, n_slow, a);
+        bool ok = true;
+        for (int kb = 0; kb < u.num_kb; ++kb, ++g) {
+          const int s = g % kStages;
+          if (g >= kStages &&
+              !wait_bounded(&empty_bar[s], ((g / kStages) & 1) ^ 1, a.status, &s_abort)) {
+            ok = false;
+            break;
+          }
+          unsigned char* sa = tiles + size_t(s) * kStageBytes;
+          unsigned char* sb = sa + kABytes;
+          mbar_arrive_expect_tx(&full_bar[s], uint32_t(kABytes + u.b_bytes));
+          const int plane = u.slow ? 0 : kb / kb_half;
+          const int kc = (u.slow ? kb : kb % kb_half) * kBK;
+          const CUtensorMap* bm = u.slow ? maps.Xs : (plane ? maps.Glo : maps.Ghi);
+          tma_load_2d(sa, u.slow ? &maps.W : &maps.M, kc, u.o0, &full_bar[s]);
+          tma_load_2d(sb, &bm[u.bx1], kc, u.j0, &full_bar[s]);
+          if (u.bx2 >= 0)
+            tma_load_2d(sb + box_rows(u.bx1) * kBK * 2, &bm[u.bx2], kc, u.j0 + box_rows(u.bx1),
+                        &full_bar[s]);
+        }
+        if (!ok) break;
       }
-      s_issued = kb;
+      s_issued = g;
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(kBM, N);
-      for (int kb = 0; kb < num_kb; ++kb) {
-        const int s = kb % stages;
-        if (!wait_bounded(&full_bar[s], (kb / stages) & 1, a.status, &s_abort)) break;
+      int g = 0;
+      for (int i = 0;; ++i) {
+        const int q = i % kQ;
+        if (!wait_bounded(&tq_full[q], (i / kQ) & 1, a.status, &s_abort)) break;
+        const int t = s_tile[q];
+        mbar_arrive_cta(&tq_empty[q]);
+        if (t < 0) break;
+        const Tile u = decode_tile(t, n_slow_tiles, n_mt, n_fast, n_slow, a);
+        if (i >= kQ && !wait_bounded(&acc_empty[q], ((i / kQ) & 1) ^ 1, a.status, &s_abort)) break;
         tc_fence_after();
-        const uint32_t sa = base + uint32_t(s) * uint32_t(st_bytes);
-        const uint32_t sb = sa + kABytes;
+        const uint32_t acc = tmem + uint32_t(q * kBN);
+        const uint32_t idesc = idesc_bf16_f32(kBM, u.N);
+        bool ok = true;
+        for (int kb = 0; kb < u.num_kb; ++kb, ++g) {
+          const int s = g % kStages;
+          if (!wait_bounded(&full_bar[s], (g / kStages) & 1, a.status, &s_abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = base + uint32_t(s) * kStageBytes;
+          const uint32_t sb = sa + kABytes;
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk)
-          tc_mma_bf16(tmem, sw128_kmajor_desc(sa + kk * 32), sw128_kmajor_desc(sb + kk * 32), idesc,
-                      (kb | kk) != 0 ? 1u : 0u);
-        tc_commit(&empty_bar[s]);
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            tc_mma_bf16(acc, sw128_kmajor_desc(sa + kk * 32), sw128_kmajor_desc(sb + kk * 32), idesc,
+                        (kb | kk) != 0 ? 1u : 0u);
+          tc_commit(&empty_bar[s]);
+        }
+        if (!ok) break;
+        tc_commit(&acc_full[q]);
       }
-      tc_commit(&accum_bar);
     }
   } else {
     // epilogue: warps 2..5 own TMEM lane quarters (warp % 4)
-    const int q = warp & 3;
-    const bool ok = wait_bounded(&accum_bar, 0, a.status, &s_abort);
-    tc_fence_after();
-    const int o = o0 + q * 32 + lane;
-    for (int c0 = 0; c0 < N; c0 += 32) {
-      uint32_t r[32];
-      tmem_ld_32x32b_x32(tmem + (uint32_t(q * 32) << 16) + uint32_t(c0), r);
-      if (ok && o < a.d_out) {
+    const int qw = warp & 3;
+    for (int i = 0;; ++i) {
+      const int q = i % kQ;
+      if (!wait_bounded(&tq_full[q], (i / kQ) & 1, a.status, &s_abort)) break;
+      const int t = s_tile[q];
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cta(&tq_empty[q]);
+      if (t < 0) break;
+      const Tile u = decode_tile(t, n_slow_tiles, n_mt, n_fast, n_slow, a);
+      const bool ok = wait_bounded(&acc_full[q], (i / kQ) & 1, a.status, &s_abort);
+      tc_fence_after();
+      const int o = u.o0 + qw * 32 + lane;
+      const int32_t* idx = u.slow ? a.idx_slow : a.idx_fast;
+      if (ok) {
+        for (int c0 = 0; c0 < u.N; c0 += 32) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(tmem + (uint32_t(qw * 32) << 16) + uint32_t(q * kBN + c0), r);
+          if (o < a.d_out) {
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          const int j = c0 + jj;
-          if (j < nvalid) {
-            const int tok = __ldg(idx + j0 + j);
-            a.y[size_t(tok) * a.d_out + o] = __uint_as_float(r[jj]);
+            for (int jj = 0; jj < 32; ++jj) {
+              const int j = c0 + jj;
+              if (j < u.nvalid) {
+                const int tok = __ldg(idx + u.j0 + j);
+                a.y[size_t(tok) * a.d_out + o] = __uint_as_float(r[jj]);
+              }
+            }
           }
         }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cta(&acc_empty[q]);
+      if (!ok) break;
     }
   }
   tc_fence_before();
@@ -253,20 +332,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (threadIdx.x == 0 && s_abort) {
     // make sure no bulk copy is still writing into this CTA's shared memory
     const int issued = s_issued;
-    for (int kb = max(0, issued - stages); kb < issued; ++kb) {
-      const int s = kb % stages;
+    for (int g = max(0, issued - kStages); g < issued; ++g) {
+      const int s = g % kStages;
       const uint64_t t0 = globaltimer_ns();
-      while (!mbar_try_wait(&full_bar[s], (kb / stages) & 1) &&
-             globaltimer_ns() - t0 < kWaitLimitNs) {
+      while (!mbar_try_wait(&full_bar[s], (g / kStages) & 1) && globaltimer_ns() - t0 < kWaitLimitNs) {
       }
     }
   }
   if (warp == 1) {
-    if (lane == 0) {  // all MMAs done before the accumulator is released
-      const uint64_t t0 = globaltimer_ns();
-      while (!mbar_try_wait(&accum_bar, 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
-      }
-    }
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -554,8 +627,18 @@ gsi_status_t tc_gemm_prepare(gsi_handle* h) {
 
 gsi_status_t tc_gemm_launch(gsi_handle* h, const TcGemmArgs& a, cudaStream_t s) {
   const TcMaps* maps = reinterpret_cast<const TcMaps*>(h->tmaps);
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return GSI_ERR_CUDA;
+  }
+  // at most one CTA per SM (the ring takes most of shared memory), and no more
+  // CTAs than tiles could exist
   const int n_tiles = (a.T + kBN - 1) / kBN;
-  dim3 grid(unsigned((a.d_out + kBM - 1) / kBM), unsigned(2 * n_tiles));
+  const int max_tiles = ((a.d_out + kBM - 1) / kBM) * (n_tiles + 1);
+  dim3 grid(unsigned(std::max(1, std::min(sms, max_tiles))));
   return launch_pdl(tc_gemm_kernel, grid, dim3(kTcThreads), kTcSmem, s, *maps, a) == cudaSuccess
              ? GSI_OK
              : GSI_ERR_CUDA;

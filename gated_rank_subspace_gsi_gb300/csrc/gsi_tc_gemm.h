@@ -20,6 +20,7 @@ struct TcGemmArgs {
   const int32_t* idx_fast;  // fast token indices (count[0] of them)
   const int32_t* idx_slow;  // slow token indices (count[1] of them)
   const int32_t* count;     // [0] n_fast, [1] n_slow (device)
+  int32_t* tile_counter;    // device, zero at launch: the GEMM's tile queue
   float* y;                 // T x d_out
   int T, d_out, d, k;
   uint32_t* status;
