@@ -242,23 +242,22 @@ constexpr int kCThreads = 512;
 
 size_t chol_smem_bytes(int nb) {
   return size_t(tri(nb)) * kBlk * 4 + size_t(std::max(1, nb - 1)) * kPtBlk * 4 + 2 * size_t(kPtBlk) * 4 +
-         size_t(nb) * kCB * 4;
+         size_t(nb) * kCB * 4 + size_t(kCB) * 4;
 }
 
-// Factor the diagonal block AJJ (in place, lower triangle, zeros above) and
-// write its inverse to LI (shared, rows of kPtStride) and LIg (global); one
-// warp.  Flags pivots below the floor (replaced by 1) and pivots below the
-// skip threshold.
+// Factor the diagonal block AJJ in place (lower triangle, zeros above); one
+// warp.  Also writes L_JJ with 16-byte rows to LN (32 x kPtStride, shared) and
+// 1 / L_ii to Dinv (32, shared) for the panel's forward substitution, and
+// flags pivots below the floor (replaced by 1) and below the skip threshold.
 //
-// Lane i keeps row i (factor) or column i (inverse) in registers as a window
-// that slides one entry per step, so the step loops stay rolled while every
-// register index is static.  Column c of L is published through LR (32 x
-// kPtStride, shared), row c, rotated so that entry c + 1 + m sits at m:
-// every lane then reads the entries its window needs as aligned 16-byte
-// broadcasts -- in the rank-1 update of step c and again in step c of the
-// forward substitution that forms the inverse.
-__device__ __forceinline__ void chol_diag_block(float* AJJ, float* LI, float* LR, float* LIg,
-                                                int lane, int* s_bad, int* s_small) {
+// Lane i keeps row i in registers as a window that slides one column per
+// step (w[0] is always the current pivot column), so the step loop stays
+// rolled while every register index is static.  Column c of L is published
+// through LR (32 x kPtStride, shared), row c, rotated so that entry c + 1 + m
+// sits at m: every lane then reads the entries its window needs as aligned
+// 16-byte broadcasts.
+__device__ __forceinline__ void chol_diag_factor(float* AJJ, float* LN, float* Dinv, float* LR,
+                                                 int lane, int* s_bad, int* s_small) {
   constexpr unsigned kAll = 0xffffffffu;
   // Start converged: a warp that arrives here split (after lane-divergent
   // code) would run every shuffle below as a rendezvous of its splits, which
@@ -268,7 +267,6 @@ __device__ __forceinline__ void chol_diag_block(float* AJJ, float* LI, float* LR
 #pragma unroll
   for (int m = 0; m < kCB; ++m) w[m] = AJJ[lane * (kCB + 1) + m];
   bool bad = false, small = false;
-  float my_inv = 0.f;  // 1 / L_ii of this lane's row
 #pragma unroll 1
   for (int c = 0; c < kCB; ++c) {
     // w[m] holds A[lane][c + m]
@@ -283,8 +281,9 @@ __device__ __forceinline__ void chol_diag_block(float* AJJ, float* LI, float* LR
     // moves by that much, far below the fp32 Gram matrix's own rounding
     const float inv = rsqrtf(piv);
     const float l = (lane == c) ? piv * inv : ((lane > c) ? w[0] * inv : 0.f);
-    if (lane == c) my_inv = inv;
+    if (lane == c) Dinv[c] = inv;
     AJJ[lane * (kCB + 1) + c] = l;
+    LN[lane * kPtStride + c] = l;
     float* row = LR + c * kPtStride;
     row[(lane - c - 1) & (kCB - 1)] = l;  // L[c + 1 + m][c] at m
     __syncwarp();
@@ -304,17 +303,29 @@ __device__ __forceinline__ void chol_diag_block(float* AJJ, float* LI, float* LR
     if (small) *s_small = 1;
   }
   __syncwarp();
-  // inverse by forward substitution on the unit vectors; lane j owns column
-  // j, as a sliding window: x[m] holds entry i + m at step i
+}
+
+// Inverse of a factored 32 x 32 diagonal block (AJJ, rows of 33) by forward
+// substitution on the unit vectors, written to LIg (row-major 32 x 32); one
+// warp, lane j owning column j as a sliding window (x[m] holds entry i + m at
+// step i).  The block's columns are first copied to R (32 x kPtStride,
+// shared scratch) rotated as in chol_diag_factor, so that each step reads
+// them as 16-byte broadcasts.  Off the factorisation's critical path: only
+// the forward substitution kernel that follows reads these.
+__device__ __forceinline__ void chol_diag_inverse(const float* AJJ, float* R, float* LIg, int lane) {
+  constexpr unsigned kAll = 0xffffffffu;
+  __syncwarp();
+  for (int c = 0; c < kCB; ++c) R[c * kPtStride + ((lane - c - 1) & (kCB - 1))] = AJJ[lane * (kCB + 1) + c];
+  const float my_inv = 1.0f / AJJ[lane * (kCB + 1) + lane];
+  __syncwarp();
   float x[kCB];
 #pragma unroll
   for (int m = 0; m < kCB; ++m) x[m] = (m == lane) ? 1.f : 0.f;
 #pragma unroll 1
   for (int i = 0; i < kCB; ++i) {
     const float xi = x[0] * __shfl_sync(kAll, my_inv, i);
-    LI[i * kPtStride + lane] = xi;
     LIg[i * kCB + lane] = xi;
-    const float* row = LR + i * kPtStride;
+    const float* row = R + i * kPtStride;
 #pragma unroll
     for (int m4 = 0; m4 < kCB; m4 += 4) {
       const float4 q = *reinterpret_cast<const float4*>(row + m4);
@@ -326,7 +337,6 @@ __device__ __forceinline__ void chol_diag_block(float* AJJ, float* LI, float* LR
 #pragma unroll
     for (int m = 0; m + 1 < kCB; ++m) x[m] = x[m + 1];
   }
-  __syncwarp();
 }
 
 __global__ void __launch_bounds__(kCThreads, 1)
@@ -342,9 +352,10 @@ __global__ void __launch_bounds__(kCThreads, 1)
   const int nb = kp / kCB, np = tri(nb);
   float* A = csm;
   float* PT = A + size_t(np) * kBlk;
-  float* LI = PT + size_t(max(1, nb - 1)) * kPtBlk;  // inverse of the current diagonal block
-  float* LTd = LI + kPtBlk;                            // current diagonal block of L, rotated columns
-  float* Ds = LTd + kPtBlk;
+  float* LN = PT + size_t(max(1, nb - 1)) * kPtBlk;  // current diagonal block of L, 16-byte rows
+  float* LTd = LN + kPtBlk;                            // the same block's columns, rotated
+  float* Ds = LTd + kPtBlk;                            // D (kp), then 1 / L_ii of the block (32)
+  float* Dinv = Ds + kp;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   constexpr int kWarps = kCThreads / 32;
   if (tid == 0) {
@@ -401,33 +412,36 @@ __global__ void __launch_bounds__(kCThreads, 1)
   // step -1 only factors block 0
   for (int J = -1; J < nb; ++J) {
     if (J >= 0) {
-      // panel: L_IJ = A_IJ Linv_JJ^T for the block rows below.  Lane r keeps
-      // row r of A_IJ in registers; a warp produces 16 of the 32 columns.  The
-      // result goes to L (global) and, transposed, to PT for the trailing
-      // update; A_IJ itself is not needed again.
-      const int n_tasks = (nb - 1 - J) * 2;
-      for (int task = warp; task < n_tasks; task += kWarps) {
-        const int I = J + 1 + (task >> 1), c0 = (task & 1) * (kCB / 2);
+      // panel: L_IJ solves L_IJ L_JJ^T = A_IJ for the block rows below, by
+      // forward substitution: one warp per block row, lane r holding row r
+      // (a, then the solution x) in registers, row c of L_JJ read as 16-byte
+      // broadcasts.  The result goes to L (global) and, transposed, to PT
+      // for the trailing update; A_IJ itself is not needed again.
+      for (int I = J + 1 + warp; I < nb; I += kWarps) {
         const float* AIJ = A + size_t(tri(I) + J) * kBlk;
-        float a[kCB];
+        float x[kCB];
 #pragma unroll
-        for (int m = 0; m < kCB; ++m) a[m] = AIJ[lane * (kCB + 1) + m];
-        float* pt = PT + size_t(I - J - 1) * kPtBlk;
-#pragma unroll 2
-        for (int c = c0; c < c0 + kCB / 2; ++c) {
-          float part[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int m = 0; m < kCB; ++m) x[m] = AIJ[lane * (kCB + 1) + m];
 #pragma unroll
-          for (int m = 0; m < kCB; m += 4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(LI + c * kPtStride + m);
-            part[0] = fmaf(a[m + 0], l4.x, part[0]);
-            part[1] = fmaf(a[m + 1], l4.y, part[1]);
-            part[2] = fmaf(a[m + 2], l4.z, part[2]);
-            part[3] = fmaf(a[m + 3], l4.w, part[3]);
+        for (int c = 0; c < kCB; ++c) {
+          float part[4] = {x[c], 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int m4 = 0; m4 < c; m4 += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(LN + c * kPtStride + m4);
+            part[0] = fmaf(-x[m4], l4.x, part[0]);
+            if (m4 + 1 < c) part[1] = fmaf(-x[m4 + 1], l4.y, part[1]);
+            if (m4 + 2 < c) part[2] = fmaf(-x[m4 + 2], l4.z, part[2]);
+            if (m4 + 3 < c) part[3] = fmaf(-x[m4 + 3], l4.w, part[3]);
           }
-          const float v = (part[0] + part[1]) + (part[2] + part[3]);
-          pt[c * kPtStride + lane] = v;
-          Lg[size_t(I * kCB + lane) * kp + J * kCB + c] = v;
+          x[c] = ((part[0] + part[1]) + (part[2] + part[3])) * Dinv[c];
         }
+        float* pt = PT + size_t(I - J - 1) * kPtBlk;
+#pragma unroll
+        for (int c = 0; c < kCB; ++c) pt[c * kPtStride + lane] = x[c];
+        __syncwarp();
+        // the block to L in global memory, one coalesced row per step
+        for (int r = 0; r < kCB; ++r)
+          Lg[size_t(I * kCB + r) * kp + J * kCB + lane] = pt[lane * kPtStride + r];
       }
       __syncthreads();
       // trailing update A_IL -= L_IJ L_LJ^T, J < L <= I; one warp per block pair,
@@ -466,10 +480,16 @@ __global__ void __launch_bounds__(kCThreads, 1)
       }
     }
     if (warp == 0 && J + 1 < nb)
-      chol_diag_block(A + size_t(tri(J + 1) + J + 1) * kBlk, LI, LTd,
-                      LIg + size_t(J + 1) * kCB * kCB, lane, &s_bad, &s_small);
+      chol_diag_factor(A + size_t(tri(J + 1) + J + 1) * kBlk, LN, Dinv, LTd, lane, &s_bad,
+                       &s_small);
     __syncthreads();
   }
+  // the inverses of the diagonal blocks, one warp each, for the forward
+  // substitution kernel
+  // (scratch: the panel buffer PT, then LN and LTd, contiguous: nb + 1 blocks)
+  for (int J = warp; J < nb; J += kWarps)
+    chol_diag_inverse(A + size_t(tri(J) + J) * kBlk, PT + size_t(J) * kPtBlk,
+                      LIg + size_t(J) * kCB * kCB, lane);
   // the diagonal blocks of L (the panels went to Lg as they were formed)
   for (int q = tid; q < nb * kCB * kCB; q += kCThreads) {
     const int J = q >> 10, e = q & 1023, r = e >> 5, c = e & 31;
