@@ -203,6 +203,7 @@ template <int K>
 __device__ __forceinline__ void decode3_body(const CUtensorMap* tmV, const CUtensorMap* tmM,
                                              const Decode3Args& a, const int cta, const int G) {
   static_assert(K == 64 || K == 128 || K == 256, "k in {64, 128, 256}");
+  static_assert(K < kThreads, "one compute thread is free to read ||x||^2 beside the g loads");
   constexpr int T16 = K / 16;  // 16-wide blocks of g
   constexpr int KC = K / 64;   // 64-column (128-byte) blocks of a row
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -439,7 +440,7 @@ __device__ __forceinline__ void decode3_body(const CUtensorMap* tmV, const CUten
     g2 = warp_sum_all(g2);
     if (lane == 0) s_ggw[warp] = g2;
   }
-  if (tid == 0) {
+  if (tid == kThreads - 1) {  // idle in the loop above (K < kThreads): the loads overlap
     float sx = 0.f;
 #pragma unroll
     for (int c = 0; c < kCopies; ++c) sx += ld_cg_f32(acc + size_t(c) * a.acc_stride + K);
