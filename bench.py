@@ -165,6 +165,32 @@ def kernel_traffic():
 
 
 # --------------------------------------------------------------------------
+# workload names (one string per workload, shared by both arms of the bench)
+# --------------------------------------------------------------------------
+
+DECODE_WORKLOAD = ("gptj_layer_decode: 512 sequential T=1 tokens x 3 gated linears "
+                   "(4096->28672 stacked qkv+fc_in, 4096->4096 out_proj, 16384->4096 fc_out), "
+                   "k=256, eps=0.10, 1 slow token (0.2%)")
+
+
+def cal_workload(n, d, k, iters):
+    return (f"calibrate_gptj: n={n} calibration tokens (seeded planted-spectrum activations), "
+            f"d={d}, k={k}, {iters} iterations, Q0 seeded Gaussian")
+
+
+def casc_workload(L, n, d, k, it_first, it_next):
+    return (f"cascade_gptj: {L} layers of depth-coherent planted-spectrum calibration tokens "
+            f"(adjacent planted subspaces: mean principal cosine ~0.96), n={n}, d={d}, k={k}, "
+            f"iterations {it_first} then {it_next}")
+
+
+def sweep_workload(T):
+    return (f"sweep_gptj: W 28672x4096, k in {list(SWEEP_KS)}, eps in "
+            f"[0.02, 0.05, 0.10, 0.20, inf], {T} sequential decode tokens per point (gapless "
+            f"power-law spectrum, r=1024), V_k = population top-k basis")
+
+
+# --------------------------------------------------------------------------
 # the workload
 # --------------------------------------------------------------------------
 
@@ -482,9 +508,7 @@ def run_gsi(args, world, rank, local):
         "data": "synthetic (seeded Gaussian weights, QR bases, activations with set residual ratios)",
         "impl": "gsi",
         "config": {
-            "workload": "gptj_layer_decode: 512 sequential T=1 tokens x 3 gated linears "
-                        "(4096->28672 stacked qkv+fc_in, 4096->4096 out_proj, 16384->4096 fc_out), "
-                        "k=256, eps=0.10, 1 slow token (0.2%)",
+            "workload": DECODE_WORKLOAD,
             "schedule": ("grouped: per token the qkv+fc_in call, then out_proj and fc_out in "
                          "one launch (independent inputs: parallel residual)") if grouped
                         else "sequential: three launches per token",
@@ -751,8 +775,7 @@ def run_calibrate(args, world, rank, local):
         cpu = cal_cpu_baseline(c, cs, Q0b, budget_s=args.cpu_budget)
     rl = cal_roofline(lib, Xs[0], Q0, iters, V, ws, stream, k)
     out = _line(CAL_METRIC, round(ms_cal, 4), CAL_UNIT, world, steps, args.warmup, ms,
-                {"workload": f"calibrate_gptj: n={n} calibration tokens (seeded planted-spectrum "
-                             f"activations), d={d}, k={k}, {iters} iterations, Q0 seeded Gaussian",
+                {"workload": cal_workload(n, d, k, iters),
                  "calls_per_step": calls, "replicas": replicas,
                  "l2": f"inputs larger than L2: {replicas} replicas of X "
                        f"({x_bytes / 2**20:.0f} MiB each), L2 {l2 / 2**20:.0f} MiB",
@@ -1153,7 +1176,7 @@ def run_reference(args, world, rank):
         "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "impl": "reference",
-        "config": {"workload": "gptj_layer_decode (oracle sample: 8 tokens x 3 gated linears per step)"},
+        "config": {"workload": DECODE_WORKLOAD},
         "cpu_baseline": {"value": round(v, 3), "unit": UNIT, "cores": orc.num_threads(),
                          "kind": "oracle",
                          "sample": f"{per_step} decode tokens x 3 gated linears per step, "
@@ -1189,10 +1212,10 @@ def run_reference_calibrate(args, world, rank):
         "steps": steps, "warmup": warm, "ms_per_step": round(v, 3), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "impl": "reference",
-        "config": {"workload": "calibrate_gptj (oracle: numpy fp64 subspace iteration, one "
-                               "whole calibration per step)"},
+        "config": {"workload": cal_workload(c["n"], c["d"], c["k"], c["iters"])},
         "cpu_baseline": {"value": round(v, 3), "unit": CAL_UNIT, "cores": os.cpu_count(),
-                         "kind": "oracle", "sample": f"{steps} whole calibrations"},
+                         "kind": "oracle",
+                         "sample": f"{steps} whole calibrations (numpy fp64 subspace iteration)"},
         "e2e": {"value": round(v, 3), "unit": CAL_UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -1262,10 +1285,7 @@ def run_cascade(args, world, rank, local):
     launches = (lib.gsi_calibrate_launch_count(n, d, k, it_first)
                 + (L - 1) * lib.gsi_calibrate_launch_count(n, d, k, it_next))
     out = _line(CASC_METRIC, round(ms / L, 4), "ms per layer", world, steps, args.warmup, ms,
-                {"workload": f"cascade_gptj: {L} layers of depth-coherent planted-spectrum "
-                             f"calibration tokens (adjacent planted subspaces: mean principal "
-                             f"cosine ~0.96), n={n}, d={d}, k={k}, iterations {it_first} then "
-                             f"{it_next}",
+                {"workload": casc_workload(L, n, d, k, it_first, it_next),
                  "l2": f"inputs larger than L2: {L} layers x {n * d * 2 / 2**20:.0f} MiB of tokens",
                  "parallelism": "1 GPU" if world == 1 else f"replicas x{world}"},
                 roofline=rl,
@@ -1340,9 +1360,10 @@ def run_reference_cascade(args, world, rank):
            "steps": steps, "warmup": 0, "ms_per_step": round(dt / steps * 1e3, 3),
            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic", "impl": "reference",
-           "config": {"workload": "cascade_gptj (oracle: numpy fp64 cascade, 28 layers per step)"},
+           "config": {"workload": casc_workload(L, c["n"], c["d"], c["k"], 8, 2)},
            "cpu_baseline": {"value": round(v, 3), "unit": "ms per layer", "cores": os.cpu_count(),
-                            "kind": "oracle", "sample": f"{steps} whole cascades"},
+                            "kind": "oracle",
+                            "sample": f"{steps} whole cascades of {L} layers (numpy fp64)"},
            "e2e": {"value": round(v, 3), "unit": "ms per layer", "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
@@ -1458,10 +1479,7 @@ def run_sweep(args, world, rank, local):
     out = _line("µs per gated linear at k=256, eps=0.10 (GPT-J qkv+fc_in 4096 -> 28672, decode), "
                 "operating-point sweep", main_pt["us_per_call"], "us per gated linear", world,
                 steps, args.warmup, main_pt["us_per_call"] * T / 1e3,
-                {"workload": f"sweep_gptj: W 28672x4096, k in {list(SWEEP_KS)}, eps in "
-                             f"[0.02, 0.05, 0.10, 0.20, inf], {T} sequential decode tokens per "
-                             f"point (gapless power-law spectrum, r=1024), V_k = population "
-                             f"top-k basis",
+                {"workload": sweep_workload(T),
                  "l2": "replicas of (V_k, M) per k exceed L2 (1.5x); W 235 MB beyond L2 by size"},
                 sweep=points, w_spectral_norm=round(w_norm, 4),
                 eps0_us_per_call=round(ms_dense * 1e3 / T, 3),
@@ -1507,7 +1525,7 @@ def run_reference_sweep(args, world, rank):
            "ms_per_step": round(dt / steps * 1e3, 3), "higher_is_better": False,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
            "impl": "reference",
-           "config": {"workload": f"sweep_gptj main point (oracle: {per_step} tokens per step)"},
+           "config": {"workload": sweep_workload(T)},
            "cpu_baseline": {"value": round(v, 3), "unit": "us per gated linear",
                             "cores": orc.num_threads(), "kind": "oracle",
                             "sample": f"{steps * per_step} tokens at k=256, eps=0.10"},
