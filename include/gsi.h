@@ -193,7 +193,7 @@ int gsi_forward_launch_count(gsi_handle_t h, int64_t T);
  * for callers that cannot call cudaMalloc -- code running inside a framework
  * or server whose allocator owns all device memory (a pooling or caching
  * allocator that must see every allocation), or a fixed-memory deployment
- * where the first call must not fail for lack of memory.  The paper has no
+ * where the first call must not fail for lack of memory.  The pages have no
  * counterpart to this entry point; it is an interface convenience.
  *   W, V_k, M, x, y, gate, rho, d_out, d, k, eps: as in gsi_create and
  *   gsi_forward (device pointers, 16-byte aligned; gate, rho may be NULL).
