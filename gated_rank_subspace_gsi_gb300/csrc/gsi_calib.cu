@@ -250,12 +250,14 @@ size_t chol_smem_bytes(int nb) {
 // 1 / L_ii to Dinv (32, shared) for the panel's forward substitution, and
 // flags pivots below the floor (replaced by 1) and below the skip threshold.
 //
-// Lane i keeps row i in registers as a window that slides one column per
-// step (w[0] is always the current pivot column), so the step loop stays
-// rolled while every register index is static.  Column c of L is published
-// through LR (32 x kPtStride, shared), row c, rotated so that entry c + 1 + m
-// sits at m: every lane then reads the entries its window needs as aligned
-// 16-byte broadcasts.
+// Lane i keeps row i in registers; the 32 steps are unrolled, so step c
+// updates only the columns m > c that are still live.  Column c of L is
+// published through row c of LR (32 x kPtStride, shared scratch) and read
+// back as 16-byte broadcasts.  The next pivot is lane c + 1's diagonal entry
+// after step c, which needs only that lane's own new entry of L: its
+// broadcast and square root start before the column broadcast and overlap
+// it.  The arithmetic (each entry's updates, in step order) is that of plain
+// right-looking elimination.
 __device__ __forceinline__ void chol_diag_factor(float* AJJ, float* LN, float* Dinv, float* LR,
                                                  int lane, int* s_bad, int* s_small) {
   constexpr unsigned kAll = 0xffffffffu;
@@ -263,14 +265,14 @@ __device__ __forceinline__ void chol_diag_factor(float* AJJ, float* LN, float* D
   // code) would run every shuffle below as a rendezvous of its splits, which
   // costs about 25x the converged loop.
   __syncwarp();
-  float w[kCB];
+  float a[kCB];
 #pragma unroll
-  for (int m = 0; m < kCB; ++m) w[m] = AJJ[lane * (kCB + 1) + m];
+  for (int m = 0; m < kCB; ++m) a[m] = AJJ[lane * (kCB + 1) + m];
   bool bad = false, small = false;
-#pragma unroll 1
+  float piv = __shfl_sync(kAll, a[0], 0);
+#pragma unroll
   for (int c = 0; c < kCB; ++c) {
-    // w[m] holds A[lane][c + m]
-    float piv = __shfl_sync(kAll, w[0], c);
+    // piv: A[c][c] after the updates of steps 0 .. c - 1
     if (!(piv >= kPivotFloor)) {
       bad = true;
       piv = 1.f;
@@ -280,23 +282,27 @@ __device__ __forceinline__ void chol_diag_factor(float* AJJ, float* LN, float* D
     // span of the transformed block does not change and its orthonormality
     // moves by that much, far below the fp32 Gram matrix's own rounding
     const float inv = rsqrtf(piv);
-    const float l = (lane == c) ? piv * inv : ((lane > c) ? w[0] * inv : 0.f);
+    const float l = (lane == c) ? piv * inv : ((lane > c) ? a[c] * inv : 0.f);
     if (lane == c) Dinv[c] = inv;
     AJJ[lane * (kCB + 1) + c] = l;
     LN[lane * kPtStride + c] = l;
-    float* row = LR + c * kPtStride;
-    row[(lane - c - 1) & (kCB - 1)] = l;  // L[c + 1 + m][c] at m
-    __syncwarp();
+    if (c + 1 < kCB) {
+      // lane c + 1: its entry c + 1 after this step (the same fma as below)
+      const float pn = fmaf(-l, l, a[c + 1]);
+      const float piv_next = __shfl_sync(kAll, pn, c + 1);
+      float* row = LR + c * kPtStride;  // row c: L[m][c] at m
+      row[lane] = l;
+      __syncwarp();
 #pragma unroll
-    for (int m4 = 0; m4 < kCB; m4 += 4) {
-      const float4 q = *reinterpret_cast<const float4*>(row + m4);
-      w[m4 + 1] = fmaf(-l, q.x, w[m4 + 1]);
-      if (m4 + 2 < kCB) w[m4 + 2] = fmaf(-l, q.y, w[m4 + 2]);
-      if (m4 + 3 < kCB) w[m4 + 3] = fmaf(-l, q.z, w[m4 + 3]);
-      if (m4 + 4 < kCB) w[m4 + 4] = fmaf(-l, q.w, w[m4 + 4]);
+      for (int m4 = ((c + 1) / 4) * 4; m4 < kCB; m4 += 4) {
+        const float4 q = *reinterpret_cast<const float4*>(row + m4);
+        if (m4 + 0 > c) a[m4 + 0] = fmaf(-l, q.x, a[m4 + 0]);
+        if (m4 + 1 > c) a[m4 + 1] = fmaf(-l, q.y, a[m4 + 1]);
+        if (m4 + 2 > c) a[m4 + 2] = fmaf(-l, q.z, a[m4 + 2]);
+        if (m4 + 3 > c) a[m4 + 3] = fmaf(-l, q.w, a[m4 + 3]);
+      }
+      piv = piv_next;
     }
-#pragma unroll
-    for (int m = 0; m + 1 < kCB; ++m) w[m] = w[m + 1];
   }
   if (lane == 0) {
     if (bad) *s_bad = 1;
