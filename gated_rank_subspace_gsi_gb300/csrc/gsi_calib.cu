@@ -246,9 +246,9 @@ size_t chol_smem_bytes(int nb) {
 }
 
 // Factor the diagonal block AJJ in place (lower triangle, zeros above); one
-// warp.  Also writes L_JJ with 16-byte rows to LN (32 x kPtStride, shared) and
-// 1 / L_ii to Dinv (32, shared) for the panel's forward substitution, and
-// flags pivots below the floor (replaced by 1) and below the skip threshold.
+// warp.  Also writes 1 / L_ii to Dinv (32, shared) and the columns of L_JJ to
+// LR (below) for the panel's forward substitution, and flags pivots below
+// the floor (replaced by 1) and below the skip threshold.
 //
 // Lane i keeps row i in registers; the 32 steps are unrolled, so step c
 // updates only the columns m > c that are still live.  Column c of L is
@@ -258,8 +258,8 @@ size_t chol_smem_bytes(int nb) {
 // broadcast and square root start before the column broadcast and overlap
 // it.  The arithmetic (each entry's updates, in step order) is that of plain
 // right-looking elimination.
-__device__ __forceinline__ void chol_diag_factor(float* AJJ, float* LN, float* Dinv, float* LR,
-                                                 int lane, int* s_bad, int* s_small) {
+__device__ __forceinline__ void chol_diag_factor(float* AJJ, float* Dinv, float* LR, int lane,
+                                                 int* s_bad, int* s_small) {
   constexpr unsigned kAll = 0xffffffffu;
   // Start converged: a warp that arrives here split (after lane-divergent
   // code) would run every shuffle below as a rendezvous of its splits, which
@@ -285,7 +285,6 @@ __device__ __forceinline__ void chol_diag_factor(float* AJJ, float* LN, float* D
     const float l = (lane == c) ? piv * inv : ((lane > c) ? a[c] * inv : 0.f);
     if (lane == c) Dinv[c] = inv;
     AJJ[lane * (kCB + 1) + c] = l;
-    LN[lane * kPtStride + c] = l;
     if (c + 1 < kCB) {
       // lane c + 1: its entry c + 1 after this step (the same fma as below)
       const float pn = fmaf(-l, l, a[c + 1]);
@@ -358,8 +357,8 @@ __global__ void __launch_bounds__(kCThreads, 1)
   const int nb = kp / kCB, np = tri(nb);
   float* A = csm;
   float* PT = A + size_t(np) * kBlk;
-  float* LN = PT + size_t(max(1, nb - 1)) * kPtBlk;  // current diagonal block of L, 16-byte rows
-  float* LTd = LN + kPtBlk;                            // the same block's columns, rotated
+  float* LN = PT + size_t(max(1, nb - 1)) * kPtBlk;  // scratch for the diagonal-block inverses
+  float* LTd = LN + kPtBlk;                            // current diagonal block of L: row c = column c
   float* Ds = LTd + kPtBlk;                            // D (kp), then 1 / L_ii of the block (32)
   float* Dinv = Ds + kp;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -420,9 +419,13 @@ __global__ void __launch_bounds__(kCThreads, 1)
     if (J >= 0) {
       // panel: L_IJ solves L_IJ L_JJ^T = A_IJ for the block rows below, by
       // forward substitution: one warp per block row, lane r holding row r
-      // (a, then the solution x) in registers, row c of L_JJ read as 16-byte
-      // broadcasts.  The result goes to L (global) and, transposed, to PT
-      // for the trailing update; A_IJ itself is not needed again.
+      // (a, then the solution x) in registers.  Right-looking and unrolled:
+      // x[c] is final once columns 0 .. c - 1 are eliminated, and then updates
+      // the live columns m > c with column c of L_JJ (row c of LTd, 16-byte
+      // broadcasts), so each step is a few independent FMAs rather than a
+      // dot product over all earlier columns.  The result goes to L (global)
+      // and, transposed, to PT for the trailing update; A_IJ itself is not
+      // needed again.
       for (int I = J + 1 + warp; I < nb; I += kWarps) {
         const float* AIJ = A + size_t(tri(I) + J) * kBlk;
         float x[kCB];
@@ -430,16 +433,18 @@ __global__ void __launch_bounds__(kCThreads, 1)
         for (int m = 0; m < kCB; ++m) x[m] = AIJ[lane * (kCB + 1) + m];
 #pragma unroll
         for (int c = 0; c < kCB; ++c) {
-          float part[4] = {x[c], 0.f, 0.f, 0.f};
+          x[c] *= Dinv[c];
+          if (c + 1 < kCB) {
+            const float* col = LTd + c * kPtStride;  // L_JJ[m][c] at m
 #pragma unroll
-          for (int m4 = 0; m4 < c; m4 += 4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(LN + c * kPtStride + m4);
-            part[0] = fmaf(-x[m4], l4.x, part[0]);
-            if (m4 + 1 < c) part[1] = fmaf(-x[m4 + 1], l4.y, part[1]);
-            if (m4 + 2 < c) part[2] = fmaf(-x[m4 + 2], l4.z, part[2]);
-            if (m4 + 3 < c) part[3] = fmaf(-x[m4 + 3], l4.w, part[3]);
+            for (int m4 = ((c + 1) / 4) * 4; m4 < kCB; m4 += 4) {
+              const float4 q = *reinterpret_cast<const float4*>(col + m4);
+              if (m4 + 0 > c) x[m4 + 0] = fmaf(-x[c], q.x, x[m4 + 0]);
+              if (m4 + 1 > c) x[m4 + 1] = fmaf(-x[c], q.y, x[m4 + 1]);
+              if (m4 + 2 > c) x[m4 + 2] = fmaf(-x[c], q.z, x[m4 + 2]);
+              if (m4 + 3 > c) x[m4 + 3] = fmaf(-x[c], q.w, x[m4 + 3]);
+            }
           }
-          x[c] = ((part[0] + part[1]) + (part[2] + part[3])) * Dinv[c];
         }
         float* pt = PT + size_t(I - J - 1) * kPtBlk;
 #pragma unroll
@@ -486,7 +491,7 @@ __global__ void __launch_bounds__(kCThreads, 1)
       }
     }
     if (warp == 0 && J + 1 < nb)
-      chol_diag_factor(A + size_t(tri(J + 1) + J + 1) * kBlk, LN, Dinv, LTd, lane, &s_bad,
+      chol_diag_factor(A + size_t(tri(J + 1) + J + 1) * kBlk, Dinv, LTd, lane, &s_bad,
                        &s_small);
     __syncthreads();
   }
