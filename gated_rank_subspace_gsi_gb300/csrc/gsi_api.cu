@@ -158,6 +158,7 @@ gsi_status_t gsi_forward(gsi_handle_t h, const void* x, int64_t T, float* y, uin
   if (!h || T < 0) return GSI_ERR_INVALID_ARG;
   if (T == 0) return GSI_OK;
   if (!x || !y || !gsi::aligned16(x) || !gsi::aligned16(y)) return GSI_ERR_INVALID_ARG;
+  if (rho && (reinterpret_cast<uintptr_t>(rho) & 3u)) return GSI_ERR_INVALID_ARG;  // fp32 stores
   if (T == 1)
     return h->dec3_ok ? gsi::decode3_launch(h, x, y, gate, rho, stream)
                       : gsi::decode_launch(h, x, y, gate, rho, stream);
@@ -298,7 +299,9 @@ gsi_status_t gsi_group_forward(gsi_group_t g, const void* const* x, float* const
                                uint8_t* const* gate, float* const* rho, cudaStream_t stream) {
   if (!g || !x || !y) return GSI_ERR_INVALID_ARG;
   for (int m = 0; m < g->n; ++m)
-    if (!x[m] || !y[m] || !gsi::aligned16(x[m]) || !gsi::aligned16(y[m])) return GSI_ERR_INVALID_ARG;
+    if (!x[m] || !y[m] || !gsi::aligned16(x[m]) || !gsi::aligned16(y[m]) ||
+        (rho && rho[m] && (reinterpret_cast<uintptr_t>(rho[m]) & 3u)))
+      return GSI_ERR_INVALID_ARG;
   return gsi::group_launch(g, x, y, gate, rho, stream);
 }
 

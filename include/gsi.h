@@ -76,10 +76,11 @@ gsi_status_t gsi_create(const void *W, const void *V_k, const void *M,
                         gsi_handle_t *out);
 
 /* The gated map of sections 2.1-2.2 on T tokens.
- *   x     : T x d bf16 (device).
- *   y     : T x d_out fp32 (device), written in token order.
+ *   x     : T x d bf16 (device), 16-byte aligned.
+ *   y     : T x d_out fp32 (device), 16-byte aligned, written in token order.
  *   gate  : T uint8 (device) or NULL.
- *   rho   : T fp32 (device) or NULL.
+ *   rho   : T fp32 (device, 4-byte aligned) or NULL.
+ * A null x or y, or a misaligned x, y or rho -> GSI_ERR_INVALID_ARG.
  *   stream: CUDA stream; the call is asynchronous, allocates nothing, never
  *           synchronises, and may be captured in a CUDA graph.
  * T == 0 is a no-op.  T > reserved workspace -> GSI_ERR_WORKSPACE.

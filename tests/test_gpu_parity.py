@@ -168,6 +168,14 @@ def test_T0_workspace_and_reserve(gsi, orc):
     check_against_oracle(orc, lin, X, y2, g2, r2, what="after reserve")
     assert gsi.gsi_forward_launch_count(lin.h, 1) == 1
     assert gsi.gsi_forward_launch_count(lin.h, 600) >= 2
+    # a misaligned rho is refused on the host, before any launch (fp32 stores)
+    rb = torch.zeros(2 * 600 + 4, dtype=torch.float32, device="cuda")
+    rho_bad = rb.view(torch.uint8)[1:1 + 4 * 600]
+    for T in (1, 600):
+        with pytest.raises(gsi.GsiError) as ei:
+            gsi.gsi_forward(lin.h, x[:T], y[:T], rho=rho_bad, T=T)
+        assert ei.value.status == gsi.GSI_ERR_INVALID_ARG
+    assert gsi.gsi_device_status(lin.h) == gsi.GSI_OK
     lin.close()
 
 
