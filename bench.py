@@ -184,6 +184,29 @@ def casc_workload(L, n, d, k, it_first, it_next):
             f"iterations {it_first} then {it_next}")
 
 
+BATCHED_METRIC = "µs per gated linear call, batched T=512 prefill (4096 -> 16384, k=256, 30% slow)"
+BATCHED_UNIT = "us per gated linear call"
+BATCHED_WORKLOAD = ("batched_T512: T=512 tokens per call, W 16384x4096, k=256, eps=0.10, "
+                    "154 slow / 358 fast tokens")
+GPT2_METRIC = "µs per gated linear call, GPT-2 QKV T=64"
+GPT2_UNIT = "us per call"
+GPT2_WORKLOAD = "gpt2_qkv_T64: 768 -> 2304, k=256, eps=0.10, T=64 tokens per call, 6 slow"
+STACK_METRIC = "µs per decode step through a 28-layer GPT-J stack (3 gated linears per layer)"
+STACK_UNIT = "us per decode step"
+OPT_METRIC = "µs per OPT-6.7B MLP layer (fc1 + fc2) at decode, slow-fraction sweep"
+OPT_UNIT = "us per layer (f = 0 point)"
+
+
+def stack_workload(S, n_slow):
+    return ("gptj_stack: 28 layers x (4096->28672 qkv+fc_in, then 4096->4096 out_proj || "
+            f"16384->4096 fc_out grouped), k=256, eps=0.10, {S} decode steps, {n_slow} slow draws")
+
+
+def opt_workload(S):
+    return (f"opt_mlp: 32 layers x (4096->16384 fc1, 16384->4096 fc2), k=256, eps=0.05, "
+            f"{S} decode steps per point")
+
+
 def sweep_workload(T):
     return (f"sweep_gptj: W 28672x4096, k in {list(SWEEP_KS)}, eps in "
             f"[0.02, 0.05, 0.10, 0.20, inf], {T} sequential decode tokens per point (gapless "
@@ -652,14 +675,13 @@ def run_batched(args, world, rank, local):
     ms_e2e = max_over_ranks(time_graph(ge, stream, reps=max(3, steps), warmup=2), world)
     launches_per_call = lib.gsi_forward_launch_count(reps[0][3], T)
     out = {
-        "metric": "µs per gated linear call, batched T=512 prefill (4096 -> 16384, k=256, 30% slow)",
-        "value": round(us_call, 3), "unit": "us per gated linear call", "n_gpus": world,
+        "metric": BATCHED_METRIC,
+        "value": round(us_call, 3), "unit": BATCHED_UNIT, "n_gpus": world,
         "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded Gaussian weights, QR basis, activations with set residual ratios)",
         "impl": "gsi",
-        "config": {"workload": "batched_T512: T=512 tokens per call, W 16384x4096, k=256, "
-                               "eps=0.10, 154 slow / 358 fast tokens",
+        "config": {"workload": BATCHED_WORKLOAD,
                    "calls_per_step": calls, "replicas": replicas,
                    "l2": f"inputs larger than L2: {replicas} replicas of W/V_k/M "
                          f"({w_bytes / 2**20:.0f} MiB W each), L2 {l2 / 2**20:.0f} MiB",
@@ -941,10 +963,9 @@ def run_gpt2(args, world, rank, local):
     per_call = (spec.d * spec.k * 2 + 2 * spec.d * wl.T + spec.k * spec.k * 4
                 + spec.d_out * spec.k * 2 + spec.d_out * spec.d * 2 + wl.T * spec.d_out * 4)
     peak, kind = hbm_peak()
-    out = _line("µs per gated linear call, GPT-2 QKV T=64", round(us, 3), "us per call", world,
+    out = _line(GPT2_METRIC, round(us, 3), GPT2_UNIT, world,
                 steps, args.warmup, ms,
-                {"workload": "gpt2_qkv_T64: 768 -> 2304, k=256, eps=0.10, T=64 tokens per call, "
-                             "6 slow", "calls_per_step": calls,
+                {"workload": GPT2_WORKLOAD, "calls_per_step": calls,
                  "l2": "L2-resident (5 MB working set, as the configuration describes)"},
                 roofline={"bound": "latency", "achieved": round(per_call / (us * 1e-6) / 1e9, 1),
                           "peak": peak, "unit": "GB/s",
@@ -1020,11 +1041,8 @@ def run_stack(args, world, rank, local):
     us_token = ms * 1e3 / S
     gbs = total / (ms * 1e-3) / 1e9
     peak, kind = hbm_peak()
-    out = _line("µs per decode step through a 28-layer GPT-J stack (3 gated linears per layer)",
-                round(us_token, 2), "us per decode step", world, steps, args.warmup, ms,
-                {"workload": "gptj_stack: 28 layers x (4096->28672 qkv+fc_in, then 4096->4096 "
-                             "out_proj || 16384->4096 fc_out grouped), k=256, eps=0.10, "
-                             f"{S} decode steps, {n_slow} slow draws",
+    out = _line(STACK_METRIC, round(us_token, 2), STACK_UNIT, world, steps, args.warmup, ms,
+                {"workload": stack_workload(S, n_slow),
                  "l2": f"weights {sum(sp.d_out * sp.d * 2 for sp in specs) * nL / 1e9:.1f} GB, "
                        f"V_k + M {sum((sp.d + sp.d_out) * sp.k * 2 for sp in specs) * nL / 1e9:.2f}"
                        " GB: beyond L2 by size"},
@@ -1119,11 +1137,9 @@ def run_opt(args, world, rank, local):
                       "speedup_vs_dense": round(ms_d / ms, 3)})
         del graph, dense
     c0 = curve[0]
-    out = _line("µs per OPT-6.7B MLP layer (fc1 + fc2) at decode, slow-fraction sweep",
-                c0["us_per_layer"], "us per layer (f = 0 point)", world, steps, args.warmup,
+    out = _line(OPT_METRIC, c0["us_per_layer"], OPT_UNIT, world, steps, args.warmup,
                 c0["us_per_layer"] * nL * S / 1e3,
-                {"workload": f"opt_mlp: 32 layers x (4096->16384 fc1, 16384->4096 fc2), k=256, "
-                             f"eps=0.05, {S} decode steps per point",
+                {"workload": opt_workload(S),
                  "l2": "weights 8.6 GB: beyond L2 by size"},
                 curve=curve, roofline={"bound": "hbm", "achieved": c0["gbs"], "peak": peak,
                                        "unit": "GB/s", "frac": c0["frac_of_measured_hbm"],
@@ -1186,6 +1202,99 @@ def run_reference(args, world, rank):
     }
     print(json.dumps(out), flush=True)
 
+
+
+def _ref_token_seconds(orc, spec, seed, tag, steps, n_fast=2, n_slow=1, batch=False):
+    """Seconds per token of the oracle's gated linear on one shape, fast and
+    slow tokens apart: `steps` x (n_fast fast + n_slow slow) tokens of the
+    workload's token mix, one forward call per token (decode) or one call
+    for all fast and one for all slow tokens (batch: the call carries T
+    tokens in the workload too)."""
+    import gsi_inputs as gi
+    T = (n_fast + n_slow) * steps
+    inp = gi.make_linear_inputs(spec, T, n_slow * steps, seed, tag=tag)
+    W = orc.bf16_decode(inp.W)
+    V = orc.bf16_decode(inp.V_bits)
+    M = orc.bf16_decode(orc.bf16_encode(orc.precompute_M(W, V)))
+    eps = float(np.float32(spec.eps))
+    fast = [t for t in range(T) if not inp.slow_mask[t]]
+    slow = [t for t in range(T) if inp.slow_mask[t]]
+
+    def per_token(toks):
+        t0 = time.perf_counter()
+        if batch:
+            orc.forward(W, V, M, eps, orc.bf16_decode(inp.X_bits[toks]))
+        else:
+            for t in toks:
+                orc.forward(W, V, M, eps, orc.bf16_decode(inp.X_bits[t:t + 1]))
+        return (time.perf_counter() - t0) / len(toks)
+
+    per_token(fast[:1])  # warm-up
+    return per_token(fast), per_token(slow)
+
+
+def run_reference_linear(args, world, rank):
+    """The oracle (fp64 C) on the host cores for the workloads made of gated
+    linears of fixed shapes (batched_T512, gpt2_qkv_T64, gptj_stack, opt_mlp):
+    per shape, fast and slow tokens are timed one by one on a bounded sample,
+    and the metric's unit is composed from the workload's exact fast and slow
+    counts."""
+    if rank != 0:
+        return
+    import oracle
+
+    import gsi_inputs as gi
+    orc = oracle.default()
+    steps = max(1, min(args.steps, 4))
+    wname = args.workload
+    batched = wname in ("batched_T512", "gpt2_qkv_T64")
+    if wname == "batched_T512":
+        wl = gi.batched_prefill()
+        sp, n_slow = wl.linears[0], wl.extra["n_slow"]
+        tf, ts = _ref_token_seconds(orc, sp, wl.seed, 0, steps, n_fast=4, n_slow=2, batch=True)
+        v = ((wl.T - n_slow) * tf + n_slow * ts) * 1e6
+        metric, unit, workload = BATCHED_METRIC, BATCHED_UNIT, BATCHED_WORKLOAD
+        how = f"{wl.T - n_slow} fast x t_fast + {n_slow} slow x t_slow per call"
+    elif wname == "gpt2_qkv_T64":
+        wl = gi.gpt2_qkv()
+        sp, n_slow = wl.linears[0], wl.extra["n_slow"]
+        tf, ts = _ref_token_seconds(orc, sp, wl.seed, 0, steps, n_fast=16, n_slow=4, batch=True)
+        v = ((wl.T - n_slow) * tf + n_slow * ts) * 1e6
+        metric, unit, workload = GPT2_METRIC, GPT2_UNIT, GPT2_WORKLOAD
+        how = f"{wl.T - n_slow} fast x t_fast + {n_slow} slow x t_slow per call"
+    elif wname == "gptj_stack":
+        wl = gi.gptj_stack()
+        nL, S, n_slow = wl.extra["n_layers"], wl.extra["n_steps"], wl.extra["n_slow"]
+        per_lin = n_slow / (S * 3)  # expected slow draws per linear per decode step
+        v = 0.0
+        for i, sp in enumerate(wl.linears):
+            tf, ts = _ref_token_seconds(orc, sp, wl.seed, i, steps)
+            v += ((nL - per_lin) * tf + per_lin * ts) * 1e6
+        metric, unit, workload = STACK_METRIC, STACK_UNIT, stack_workload(S, n_slow)
+        how = (f"per linear shape: {nL} layers x t_fast, with {n_slow} slow draws over {S} steps "
+               f"x {nL} layers x 3 linears taken at their mean rate")
+    elif wname == "opt_mlp":
+        wl = gi.opt_mlp(n_steps=32, slow_fraction=0.0)
+        v = 0.0
+        for i, sp in enumerate(wl.linears):
+            tf, _ = _ref_token_seconds(orc, sp, wl.seed, i, steps, n_fast=3, n_slow=1)
+            v += tf * 1e6
+        metric, unit, workload = OPT_METRIC, OPT_UNIT, opt_workload(32)
+        how = "t_fast(fc1) + t_fast(fc2): the f = 0 point"
+    else:
+        raise ValueError(wname)
+    out = {"metric": metric, "value": round(v, 3), "unit": unit, "n_gpus": world,
+           "steps": steps, "warmup": 1, "ms_per_step": round(v / 1e3, 3),
+           "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic", "impl": "reference",
+           "config": {"workload": workload},
+           "cpu_baseline": {"value": round(v, 3), "unit": unit, "cores": orc.num_threads(),
+                            "kind": "oracle",
+                            "sample": f"per linear shape, fast and slow tokens of {steps} steps "
+                                      f"timed apart ({'in one call each' if batched else 'one call per token'}); {how}"},
+           "e2e": {"value": round(v, 3), "unit": unit, "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
 
 
 def run_reference_calibrate(args, world, rank):
@@ -1564,6 +1673,9 @@ def main(argv=None):
             run_reference_cascade(args, world, rank)
         elif args.impl == "reference" and args.workload == "sweep_gptj":
             run_reference_sweep(args, world, rank)
+        elif args.impl == "reference" and args.workload in ("batched_T512", "gpt2_qkv_T64",
+                                                             "gptj_stack", "opt_mlp"):
+            run_reference_linear(args, world, rank)
         elif args.workload == "cascade_gptj":
             run_cascade(args, world, rank, local)
         elif args.workload == "sweep_gptj":

@@ -36,3 +36,17 @@ def test_reference_arm_prints_the_contract_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["value"] == d["value"] and d["e2e"]["unit"] == d["unit"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_reference_arm_of_a_batched_workload():
+    """A workload of T-token calls (GPT-2 QKV, T = 64): the oracle arm reports
+    the GPU arm's metric, unit and workload name, composed per call."""
+    import bench
+    d = _reference_line("--workload", "gpt2_qkv_T64")
+    for key in CONTRACT:
+        assert key in d, key
+    assert d["impl"] == "reference"
+    assert d["metric"] == bench.GPT2_METRIC and d["unit"] == bench.GPT2_UNIT
+    assert d["config"]["workload"] == bench.GPT2_WORKLOAD
+    assert d["value"] > 0 and d["cpu_baseline"]["value"] == d["value"]
+    assert "58 fast" in d["cpu_baseline"]["sample"] and "6 slow" in d["cpu_baseline"]["sample"]
