@@ -259,8 +259,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) gsi_decode_kernel(DecodeArgs a
   }
   const bool slow = !(rho < a.eps);
   if (cta == 0 && tid == 0) {
-    if (a.gate) a.gate[0] = slow ? 1 : 0;
-    if (a.rho) a.rho[0] = rho;
+    // a CTA whose bounded wait ran out reports NaN (rho, and its rows of y
+    // below), so that a caller without a status word can still see it
+    if (a.gate) a.gate[0] = (slow || !ok) ? 1 : 0;
+    if (a.rho) a.rho[0] = ok ? rho : __int_as_float(0x7FC00000);
   }
 
   if (ok) {
@@ -334,6 +336,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) gsi_decode_kernel(DecodeArgs a
         }
       }
     }
+  } else {
+    for (int r = tid; r < nM; r += kDecThreads) a.y[m0 + r] = __int_as_float(0x7FC00000);
   }
   if (cta == 0 && tid == 0) {
     __threadfence();
@@ -476,20 +480,73 @@ constexpr size_t kNoAllocBytes = kNoAllocBarOffset + 128;  // + counter, epoch, 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 
 constexpr int kMaxDevices = 64;
+// the largest k of the one-token path fits the fixed scratch
+static_assert(kNoAllocMaxK >= 512, "scratch must hold the largest supported k");
+
 std::mutex g_noalloc_mutex;
 unsigned char* g_noalloc_ptr[kMaxDevices] = {};
+int g_noalloc_sms[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device, looked up once
-// per device (the host-side symbol is only a stand-in, never a device address).
-gsi_status_t noalloc_scratch(int dev, unsigned char** out) {
+// Launch plans of earlier calls, by device and shape, so that a repeated shape
+// skips the attribute and occupancy queries of decode_configure.
+struct NoAllocPlan {
+  int device = -1;
+  int64_t d_out = 0, d = 0, k = 0;
+  int grid = 0, rows_M = 0, rows_V = 0;
+  bool stage_M = false, stage_V = false;
+  size_t smem = 0;
+};
+constexpr int kNoAllocPlans = 32;
+NoAllocPlan g_noalloc_plans[kNoAllocPlans];
+int g_noalloc_next_plan = 0;
+
+// Device address of the scratch array on device `dev` (current), looked up
+// once per device (the host-side symbol is only a stand-in, never a device
+// address), and the device's SM count.
+gsi_status_t noalloc_scratch(int dev, unsigned char** out, int* num_sms) {
   if (dev < 0 || dev >= kMaxDevices) return GSI_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
   if (!g_noalloc_ptr[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return GSI_ERR_CUDA;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return GSI_ERR_CUDA;
+    g_noalloc_sms[dev] = sms;
     g_noalloc_ptr[dev] = static_cast<unsigned char*>(p);
   }
   *out = g_noalloc_ptr[dev];
+  *num_sms = g_noalloc_sms[dev];
+  return GSI_OK;
+}
+
+// decode_configure for h, or the plan an earlier call on the same device and
+// shape computed.
+gsi_status_t noalloc_configure(gsi_handle* h) {
+  for (const NoAllocPlan& p : g_noalloc_plans) {
+    if (p.device == h->device && p.d_out == h->d_out && p.d == h->d && p.k == h->k) {
+      h->dec_grid = p.grid;
+      h->dec_rows_M = p.rows_M;
+      h->dec_rows_V = p.rows_V;
+      h->dec_stage_M = p.stage_M;
+      h->dec_stage_V = p.stage_V;
+      h->dec_smem = p.smem;
+      return GSI_OK;
+    }
+  }
+  const gsi_status_t st = decode_configure(h);
+  if (st != GSI_OK) return st;
+  NoAllocPlan& p = g_noalloc_plans[g_noalloc_next_plan];
+  g_noalloc_next_plan = (g_noalloc_next_plan + 1) % kNoAllocPlans;
+  p.device = h->device;
+  p.d_out = h->d_out;
+  p.d = h->d;
+  p.k = h->k;
+  p.grid = h->dec_grid;
+  p.rows_M = h->dec_rows_M;
+  p.rows_V = h->dec_rows_V;
+  p.stage_M = h->dec_stage_M;
+  p.stage_V = h->dec_stage_V;
+  p.smem = h->dec_smem;
   return GSI_OK;
 }
 
@@ -504,11 +561,12 @@ extern "C" gsi_status_t gsi_forward_noalloc(const void* W, const void* V_k, cons
   if (!W || !V_k || !M || !x || !y || eps != eps) return GSI_ERR_INVALID_ARG;
   if (!aligned16(W) || !aligned16(V_k) || !aligned16(M) || !aligned16(x) || !aligned16(y))
     return GSI_ERR_INVALID_ARG;
+  if (rho && (reinterpret_cast<uintptr_t>(rho) & 3u)) return GSI_ERR_INVALID_ARG;  // fp32 store
+  // k above 512 fails this shape check, before any use of the scratch
   if (d_out <= 0 || d <= 0 || d % 8 != 0 || d_out % 8 != 0 || k > d ||
       (k != 16 && k != 32 && k != 64 && k != 128 && k != 256 && k != 512) ||
       d_out > (int64_t(1) << 30) || d > (int64_t(1) << 24))
     return GSI_ERR_UNSUPPORTED_SHAPE;
-  if (k > kNoAllocMaxK) return GSI_ERR_WORKSPACE;  // beyond the fixed scratch
   gsi_handle h;  // configuration only: no memory is allocated for it
   h.W = static_cast<const __nv_bfloat16*>(W);
   h.V = static_cast<const __nv_bfloat16*>(V_k);
@@ -517,14 +575,15 @@ extern "C" gsi_status_t gsi_forward_noalloc(const void* W, const void* V_k, cons
   h.d = d;
   h.k = k;
   h.eps = eps;
-  if (cudaGetDevice(&h.device) != cudaSuccess ||
-      cudaDeviceGetAttribute(&h.num_sms, cudaDevAttrMultiProcessorCount, h.device) != cudaSuccess)
-    return GSI_ERR_CUDA;
+  if (cudaGetDevice(&h.device) != cudaSuccess) return GSI_ERR_CUDA;
   unsigned char* scratch = nullptr;
-  gsi_status_t st = noalloc_scratch(h.device, &scratch);
-  if (st != GSI_OK) return st;
-  st = decode_configure(&h);
-  if (st != GSI_OK) return st;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    gsi_status_t st = noalloc_scratch(h.device, &scratch, &h.num_sms);
+    if (st != GSI_OK) return st;
+    st = noalloc_configure(&h);
+    if (st != GSI_OK) return st;
+  }
   h.dec_acc = reinterpret_cast<float*>(scratch);
   h.dec_acc_stride = kNoAllocAccStride;
   h.dec_bar = reinterpret_cast<uint32_t*>(scratch + kNoAllocBarOffset);

@@ -197,19 +197,24 @@ int gsi_forward_launch_count(gsi_handle_t h, int64_t T);
  * where the first call must not fail for lack of memory.  The pages have no
  * counterpart to this entry point; it is an interface convenience.
  *   W, V_k, M, x, y, gate, rho, d_out, d, k, eps: as in gsi_create and
- *   gsi_forward (device pointers, 16-byte aligned; gate, rho may be NULL).
+ *   gsi_forward (device pointers, 16-byte aligned, rho 4-byte aligned; gate,
+ *   rho may be NULL).  Shapes as gsi_create: k in {16, ..., 512}, anything
+ *   else is GSI_ERR_UNSUPPORTED_SHAPE.
  * The kernel's scratch (about 4.4 KB: two reduction buffers of up to
  * k + 4 = 516 floats, an arrival counter, a launch epoch and a status word)
  * lives in a fixed array that every GPU loading this library holds until
- * the process exits; k above 512 is rejected with GSI_ERR_WORKSPACE.  No
- * cudaMalloc, cudaFree or allocating library routine is called.  The first
- * call on a device looks up that array's device address (once per device,
- * with the device current); make that first call before any stream capture.
- * Each call clears the scratch on `stream` before its kernel; all calls share
- * the one array, so calls that overlap on the GPU (different streams, no
- * ordering) race and give wrong results.  Device-side timeouts of this
- * entry point are not reported (there is no handle to read them from).
- * Asynchronous on `stream`. */
+ * the process exits.  No cudaMalloc, cudaFree or allocating library routine
+ * is called.  The first call on a device looks up that array's device
+ * address (once per device, with the device current); make that first call
+ * before any stream capture.  The launch plan of each (device, shape) is
+ * kept on the host after its first call, so later calls of that shape make
+ * no attribute or occupancy queries.
+ * Each call clears the scratch on `stream` (one memset node) before its
+ * kernel; all calls share the one array, so calls that overlap on the GPU
+ * (different streams, no ordering) race and give wrong results.  There is no
+ * status word to read a device-side timeout from: a call whose bounded wait
+ * ran out writes NaN into rho (with gate = 1) and into the rows of y its
+ * stalled CTAs own, so the outputs show it.  Asynchronous on `stream`. */
 gsi_status_t gsi_forward_noalloc(const void *W, const void *V_k, const void *M,
                                  int64_t d_out, int64_t d, int64_t k, float eps,
                                  const void *x, float *y, uint8_t *gate,

@@ -152,6 +152,36 @@ def test_threshold_band(gsi, orc, path):
     lin.close()
 
 
+@pytest.mark.parametrize("path", ["decode", "batched"])
+@pytest.mark.parametrize("eps", [0.02, 0.05])
+def test_threshold_band_small_eps(gsi, orc, path, eps):
+    """Small thresholds (the sweep's eps = 0.02 and 0.05) at the GPT-J input
+    shape d = 4096, k = 256: tokens whose oracle rho lies 1.5e-4 to 1e-3 on
+    either side of eps.  No token is in the 1e-4 band, so every gate must
+    equal the oracle's, and rho itself must be within 1e-4 (near a small eps
+    an error of 5e-6 in rho^2 alone would be 1.25e-4 in rho)."""
+    d_out, d, k = 256, 4096, 256
+    seed = 23 + int(eps * 1000)
+    W = gi.gaussian_weights(d_out, d, seed)
+    basis = gi.random_basis(d, k, seed, n_sub=200)
+    V = gi.bf16_bits_to_f64(basis.V_bits)
+    rng = np.random.default_rng(seed)
+    targets = eps + rng.uniform(-1.2e-3, 1.2e-3, size=160)
+    Xc = gi.tokens(basis, targets, seed)
+    rho_c = orc.forward(None, V, None, eps, gi.bf16_bits_to_f64(Xc))["rho"]
+    off = rho_c - np.float64(np.float32(eps))
+    keep = np.nonzero((np.abs(off) >= 1.5e-4) & (np.abs(off) <= 1e-3))[0][:48]
+    assert (off[keep] < 0).sum() >= 8 and (off[keep] > 0).sum() >= 8
+    Xb = Xc[keep]
+    lin = GpuLinear(gsi, orc, W, basis.V_bits, eps)
+    y, g, r = lin.forward(Xb, one_by_one=(path == "decode"))
+    rep = check_against_oracle(orc, lin, Xb, y, g, r, what=f"eps={eps} {path}")
+    assert rep["n_band"] == 0
+    assert np.array_equal(g.astype(bool), off[keep] >= 0)
+    assert np.abs(r.astype(np.float64) - rho_c[keep]).max() <= 1e-4
+    lin.close()
+
+
 def test_T0_workspace_and_reserve(gsi, orc):
     import torch
     d_out, d, k = 128, 256, 32

@@ -16,8 +16,39 @@ import gsi_inputs as gi
 from gsi_testlib import RHO2_TOL, RHO_TOL, Y_REL_TOL, GpuLinear, to_dev
 
 
+NOALLOC_SHAPES = [(2304, 768, 256), (200, 512, 128), (4096, 16384, 256)]
+
+
 @pytest.mark.gpu
-@pytest.mark.parametrize("d_out,d,k", [(2304, 768, 256), (200, 512, 128), (4096, 16384, 256)])
+@pytest.mark.parametrize("d_out,d,k", NOALLOC_SHAPES)
+def test_noalloc_matches_oracle(gsi, orc, d_out, d, k):
+    """The entry point on its own against the fp64 oracle (gates exact outside
+    the 1e-4 band, rho within 1e-4, y within 2e-3 of max|y| per token), two
+    calls in a row on each token."""
+    import torch
+    from gsi_testlib import check_against_oracle
+    eps = 0.1
+    spec = gi.LinearSpec("noalloc", d_out, d, k, eps, 0.05, 0.3)
+    inp = gi.make_linear_inputs(spec, 4, 2, seed=91 + k)
+    lin = GpuLinear(gsi, orc, inp.W, inp.V_bits, eps)
+    x = to_dev(inp.X_bits)
+    stream = torch.cuda.current_stream()
+    for call in range(2):
+        y = torch.full((4, d_out), float("nan"), dtype=torch.float32, device="cuda")
+        g = torch.full((4,), 7, dtype=torch.uint8, device="cuda")
+        r = torch.full((4,), -1.0, dtype=torch.float32, device="cuda")
+        for t in range(4):
+            gsi.gsi_forward_noalloc(lin.W_dev, lin.V_dev, lin.M_dev, eps, x[t:t + 1],
+                                    y[t:t + 1], g[t:t + 1], r[t:t + 1], stream)
+        stream.synchronize()
+        rep = check_against_oracle(orc, lin, inp.X_bits, y.cpu().numpy(), g.cpu().numpy(),
+                                   r.cpu().numpy(), what=f"noalloc call {call}")
+        assert rep["n_slow"] == 2
+    lin.close()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("d_out,d,k", NOALLOC_SHAPES)
 def test_noalloc_matches_handle_path(gsi, orc, d_out, d, k):
     import torch
     eps = 0.1
@@ -61,3 +92,6 @@ def test_noalloc_rejects_bad_arguments():
                                   None) == 1
     assert cl.gsi_forward_noalloc(A, B, C, 64, 60, 16, f(0.1), X, Y, None, None, None) == 2
     assert cl.gsi_forward_noalloc(A, B, C, 64, 2048, 1024, f(0.1), X, Y, None, None, None) == 2
+    # a misaligned rho is refused on the host (the kernel stores it as fp32)
+    assert cl.gsi_forward_noalloc(A, B, C, 64, 64, 16, f(0.1), X, Y, None,
+                                  ctypes.c_void_p(0x60001), None) == 1
