@@ -41,9 +41,9 @@ METRIC = "µs per gated linear & effective HBM GB/s (GPT-J 4096 shapes, B=1) vs 
 UNIT = "us per gated linear"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-DECODE_KERNEL = "gsi_decode3_kernel<256> + gsi_decode3_group_kernel<256>"
-DECODE_SRC = os.path.join(ROOT, "gated_rank_subspace_gsi_gb300", "csrc", "gsi_decode3.cu")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gsi_decode3__gptj_layer_traffic.txt")
+DECODE_KERNEL = "gsi_decode_cr_kernel<256> + gsi_decode_cr_group_kernel<256>"
+DECODE_SRC = os.path.join(ROOT, "gated_rank_subspace_gsi_gb300", "csrc", "gsi_decode_cr.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gsi_decode_cr__gptj_layer_traffic.txt")
 
 
 # --------------------------------------------------------------------------
@@ -1594,7 +1594,7 @@ def run_sweep(args, world, rank, local):
                 eps0_us_per_call=round(ms_dense * 1e3 / T, 3),
                 roofline={"bound": "hbm", "achieved": main_pt["gbs"], "peak": peak, "unit": "GB/s",
                           "frac": round(main_pt["gbs"] / peak, 4), "traffic": None,
-                          "kernel": "gsi_decode3_kernel<256> (whole call)",
+                          "kernel": "gsi_decode_cr_kernel<256> (whole call)",
                           "peak_kind": f"{pkind} HBM copy"},
                 gpu_launches=steps * T * (1 + len(points)), clocks=clk)
     out["data"] = ("synthetic (seeded Gaussian W, power-law activations, planted population "
@@ -1657,9 +1657,10 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--schedule", choices=["grouped", "sequential"], default="grouped",
                     help="grouped: out_proj and fc_out of a token in one launch")
-    ap.add_argument("--prefetch", type=int, default=1,
+    ap.add_argument("--prefetch", type=int, default=0,
                     help="each call prefetches into L2 the operands of the call this many "
-                         "places later (0: none)")
+                         "places later (0: none; the one-token kernel's next call already "
+                         "stages its operands while the current call runs)")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the per-linear breakdown and the end-to-end leg (profiling runs)")
     args = ap.parse_args(argv)

@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libgsi.so")
 
-SOURCES = ["gsi_api.cu", "gsi_decode.cu", "gsi_decode3.cu", "gsi_batched.cu", "gsi_tc_gemm.cu",
+SOURCES = ["gsi_api.cu", "gsi_decode.cu", "gsi_decode_cr.cu", "gsi_batched.cu", "gsi_tc_gemm.cu",
            "gsi_prep.cu", "gsi_calib.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",

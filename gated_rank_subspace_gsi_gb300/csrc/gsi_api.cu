@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstring>
 #include <new>
+#include <vector>
 
 #include "gsi_device.cuh"
 #include "gsi_internal.h"
@@ -114,7 +115,7 @@ gsi_status_t gsi_create(const void* W, const void* V_k, const void* M, int64_t d
   const size_t gram_b = size_t(k) * k * 4;
   const size_t acc_b = size_t(2) * h->dec_acc_stride * 4;
   const size_t F_b = want3 ? gsi::corr_tiles_elems(int(k)) * 2 : 0;
-  const size_t acc3_b = want3 ? gsi::decode3_acc_floats(k) * 4 : 0;
+  const size_t acc3_b = want3 ? gsi::decode_cr_acc_floats(k) * 4 : 0;
   auto r256 = [](size_t v) { return (v + 255) / 256 * 256; };
   const size_t ws = r256(gram_b) + r256(acc_b) + r256(F_b) + r256(acc3_b) + 256;
   if (cudaMalloc(&h->ws, ws) != cudaSuccess) {
@@ -128,20 +129,37 @@ gsi_status_t gsi_create(const void* W, const void* V_k, const void* M, int64_t d
   h->dec_acc = reinterpret_cast<float*>(p);
   p += r256(acc_b);
   if (want3) {
-    h->dec3_F = reinterpret_cast<__nv_bfloat16*>(p);
+    h->cr_F = reinterpret_cast<__nv_bfloat16*>(p);
     p += r256(F_b);
-    h->dec3_acc = reinterpret_cast<float*>(p);
+    h->cr_acc = reinterpret_cast<float*>(p);
     p += r256(acc3_b);
   }
   h->dec_bar = reinterpret_cast<uint32_t*>(p);
   h->status = reinterpret_cast<uint32_t*>(p + 64);
-  h->dec3_bar = reinterpret_cast<uint32_t*>(p + 128);
+  h->cr_bar = reinterpret_cast<uint32_t*>(p + 128);
   st = GSI_OK;
   if (cudaMemset(h->ws, 0, ws) != cudaSuccess) st = GSI_ERR_CUDA;
   if (st == GSI_OK) st = gsi::decode_configure(h);
-  // the one-barrier kernel serves T = 1 whenever its shape fits
-  if (st == GSI_OK && want3) h->dec3_ok = gsi::decode3_configure(h) == GSI_OK;
-  if (st == GSI_OK) st = gsi::gram_launch(h->V, d, k, h->gram, h->dec3_F, nullptr);
+  if (st == GSI_OK) st = gsi::gram_launch(h->V, d, k, h->gram, h->cr_F, nullptr);
+  // the one-exchange kernel serves T = 1 whenever its shape fits; it needs the
+  // largest column norm of V_k and a bound of ||E||_2, both from the Gram step
+  if (st == GSI_OK && want3) {
+    std::vector<float> gram(size_t(k) * k);
+    std::vector<uint16_t> tiles(gsi::corr_tiles_elems(int(k)));
+    if (cudaMemcpy(gram.data(), h->gram, gram.size() * 4, cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemcpy(tiles.data(), h->cr_F, tiles.size() * 2, cudaMemcpyDeviceToHost) != cudaSuccess) {
+      st = GSI_ERR_CUDA;
+    } else {
+      double vmax2 = 0.0;
+      for (int64_t j = 0; j < k; ++j) vmax2 = std::max(vmax2, double(gram[size_t(j) * k + j]));
+      h->cr_vmax = float(std::sqrt(vmax2) * (1.0 + 1e-6));
+      const double nb = gsi::corr_norm_bound(tiles.data(), int(k));
+      float f = float(nb);
+      if (double(f) < nb) f = std::nextafter(f, INFINITY);
+      h->cr_normE = f;
+      h->cr_ok = std::isfinite(f) && gsi::decode_cr_configure(h) == GSI_OK;
+    }
+  }
   if (st == GSI_OK) st = grow_batched(h, kDefaultMaxT);
   if (st == GSI_OK) st = grow_staging(h, kDefaultMaxT);
   if (st == GSI_OK && cudaDeviceSynchronize() != cudaSuccess) st = GSI_ERR_CUDA;
@@ -160,8 +178,8 @@ gsi_status_t gsi_forward(gsi_handle_t h, const void* x, int64_t T, float* y, uin
   if (!x || !y || !gsi::aligned16(x) || !gsi::aligned16(y)) return GSI_ERR_INVALID_ARG;
   if (rho && (reinterpret_cast<uintptr_t>(rho) & 3u)) return GSI_ERR_INVALID_ARG;  // fp32 stores
   if (T == 1)
-    return h->dec3_ok ? gsi::decode3_launch(h, x, y, gate, rho, stream)
-                      : gsi::decode_launch(h, x, y, gate, rho, stream);
+    return h->cr_ok ? gsi::decode_cr_launch(h, x, y, gate, rho, stream)
+                    : gsi::decode_launch(h, x, y, gate, rho, stream);
   if (T > h->max_T) return GSI_ERR_WORKSPACE;
   return gsi::batched_launch(h, x, T, y, gate, rho, stream);
 }
@@ -277,7 +295,7 @@ gsi_status_t gsi_group_create(int n, const gsi_handle_t* handles, gsi_group_t* o
       if (handles[j] == handles[m]) return GSI_ERR_INVALID_ARG;  // one workspace, one call
   }
   for (int m = 0; m < n; ++m)
-    if (!handles[m]->dec3_ok || handles[m]->k != handles[0]->k ||
+    if (!handles[m]->cr_ok || handles[m]->k != handles[0]->k ||
         handles[m]->device != handles[0]->device)
       return GSI_ERR_UNSUPPORTED_SHAPE;
   gsi_group* g = new (std::nothrow) gsi_group();
@@ -346,3 +364,62 @@ int gsi_forward_launch_count(gsi_handle_t h, int64_t T) {
 }
 
 }  // extern "C"
+
+namespace gsi {
+
+// Upper bound of ||A||_2 for the symmetric matrix A whose quadratic form the
+// correction tiles compute: g^T A g = sum over tiles I <= J of g_I^T F_IJ g_J,
+// i.e. A_II = sym(F_II), A_IJ = F_IJ / 2, A_JI = F_IJ^T / 2.  For symmetric A,
+// ||A^(2^p)||_F^(1 / 2^p) = (sum_i lambda_i^(2^(p+1)))^(1 / 2^(p+1)) is at
+// least max |lambda_i| = ||A||_2 and at most k^(1 / 2^(p+1)) times it; four
+// squarings (p = 4) give a bound within a factor 256^(1/32) = 1.19 at k = 256.
+// fp64 throughout, with each power renormalised to unit Frobenius norm.
+double corr_norm_bound(const uint16_t* tiles, int k) {
+  const int t16 = k / 16;
+  std::vector<double> A(size_t(k) * k, 0.0), B(size_t(k) * k, 0.0);
+  auto bf = [](uint16_t b) {
+    uint32_t u = uint32_t(b) << 16;
+    float f;
+    std::memcpy(&f, &u, 4);
+    return double(f);
+  };
+  for (int I = 0; I < t16; ++I)
+    for (int J = I; J < t16; ++J) {
+      const uint16_t* t = tiles + size_t(corr_tile_index(I, J, t16)) * 256;
+      for (int r = 0; r < 16; ++r)
+        for (int c = 0; c < 16; ++c) {
+          const double v = 0.5 * bf(t[corr_tile_pos(r, c)]);
+          A[size_t(16 * I + r) * k + 16 * J + c] += v;
+          A[size_t(16 * J + c) * k + 16 * I + r] += v;
+        }
+    }
+  auto fro = [k](const std::vector<double>& M) {
+    double s = 0.0;
+    for (size_t i = 0; i < size_t(k) * k; ++i) s += M[i] * M[i];
+    return std::sqrt(s);
+  };
+  double f = fro(A);
+  if (!(f > 0.0)) return 0.0;
+  if (!std::isfinite(f)) return f;
+  for (double& v : A) v /= f;
+  double log_norm = std::log(f);  // log ||A^(2^j)||_F
+  for (int p = 1; p <= 4; ++p) {
+    std::fill(B.begin(), B.end(), 0.0);
+    for (int i = 0; i < k; ++i)
+      for (int l = 0; l < k; ++l) {
+        const double a = A[size_t(i) * k + l];
+        if (a == 0.0) continue;
+        const double* row = &A[size_t(l) * k];
+        double* out = &B[size_t(i) * k];
+        for (int j = 0; j < k; ++j) out[j] += a * row[j];
+      }
+    const double n = fro(B);
+    if (!(n > 0.0)) return 0.0;
+    for (double& v : B) v /= n;
+    log_norm = 2.0 * log_norm + std::log(n);
+    A.swap(B);
+  }
+  return std::exp(log_norm / 16.0) * (1.0 + 1e-9);
+}
+
+}  // namespace gsi

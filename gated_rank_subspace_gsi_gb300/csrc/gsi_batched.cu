@@ -435,10 +435,10 @@ gsi_status_t launch_front(gsi_handle* h, const void* x, int T, uint8_t* gate, fl
     proj_kernel<K><<<pg, 256, 0, s>>>(xb, h->V, T, int(h->d), h->bG, h->bsx);
   }
   if constexpr (K >= 64 && K <= 256) {
-    if (h->dec3_F) {
+    if (h->cr_F) {
       if (launch_pdl(gate_mma_kernel<K>, dim3((T + kGateMmaTok - 1) / kGateMmaTok),
                      dim3(kGateMmaThreads), gate_mma_smem<K>(), s, h->bG, h->bP, S,
-                     size_t(h->max_T) * K, xb, h->dec3_F, T, int(h->d), h->eps, h->bgate, gate,
+                     size_t(h->max_T) * K, xb, h->cr_F, T, int(h->d), h->eps, h->bgate, gate,
                      rho, h->status) != cudaSuccess)
         return GSI_ERR_CUDA;
     } else {

@@ -14,11 +14,15 @@ struct gsi_group;
 
 namespace gsi {
 constexpr int kMaxGroup = 4;  // one-token calls per gsi_group_forward launch
-// Launch plan of the one-barrier decode kernel for one handle on G CTAs.
-struct Dec3Plan {
+// Launch plan of the one-exchange decode kernel for one handle on G CTAs
+// (CTA 0 decides the gate; CTAs 1..G-1 own rows_V rows of V_k and rows_M
+// output rows each).
+struct CrPlan {
   int G = 0, rows_M = 0, rows_V = 0;
   int box_M = 0, nbox_M = 0, box_V = 0, nbox_V = 0;  // TMA row boxes
+  int vbits = 0;            // bound of a CTA's partial projection, in powers of two of max|x|
   size_t smem = 0;
+  bool coresident = false;  // two CTAs (of consecutive calls) fit on one SM
 };
 }  // namespace gsi
 
@@ -42,13 +46,16 @@ struct gsi_handle {
   size_t dec_smem = 0;       // dynamic shared memory bytes
   bool use_pdl = true;       // programmatic dependent launch between kernels
 
-  // ---- one-barrier decode kernel (k in {64, 128, 256}), used when it fits --
-  bool dec3_ok = false;
-  gsi::Dec3Plan dec3_plan;
-  alignas(64) unsigned char dec3_tmaps[2][128] = {};  // TMA maps of V_k and M (CUtensorMap)
-  __nv_bfloat16* dec3_F = nullptr;  // correction tiles (corr_tiles_elems(k))
-  float* dec3_acc = nullptr;        // decode3_acc_floats(k) fp32 accumulators
-  uint32_t* dec3_bar = nullptr;     // [0] arrival counter, [1] launch epoch, [2] counter base
+  // ---- one-exchange decode kernel (k in {64, 128, 256}), used when it fits --
+  bool cr_ok = false;
+  gsi::CrPlan cr_plan;
+  alignas(64) unsigned char cr_tmaps[2][128] = {};  // TMA maps of V_k and M (CUtensorMap)
+  __nv_bfloat16* cr_F = nullptr;  // correction tiles (corr_tiles_elems(k))
+  float* cr_acc = nullptr;        // decode_cr_acc_floats(k) fp32 digit accumulators
+  uint32_t* cr_bar = nullptr;     // [0] arrival counter, [1] launch epoch, [2] counter base,
+                                  // [4..5] published gate (64-bit)
+  float cr_vmax = 0.f;            // largest column norm of V_k (from the Gram matrix)
+  float cr_normE = 0.f;           // upper bound of ||E||_2 for the correction tiles
 
   // L2 prefetch link (gsi_set_prefetch, gsi_set_prefetch_group): each
   // one-token call on this handle prefetches the V_k, M and correction tiles
@@ -99,7 +106,7 @@ struct gsi_handle {
 struct gsi_group {
   int n = 0, k = 0, device = 0;
   gsi_handle* h[gsi::kMaxGroup] = {};
-  gsi::Dec3Plan plan[gsi::kMaxGroup];
+  gsi::CrPlan plan[gsi::kMaxGroup];
   int cta0[gsi::kMaxGroup + 1] = {};  // member m owns CTAs [cta0[m], cta0[m + 1])
   size_t smem = 0;
   alignas(64) unsigned char tmaps[2 * gsi::kMaxGroup][128] = {};
@@ -136,11 +143,14 @@ gsi_status_t decode_configure(gsi_handle* h);
 gsi_status_t decode_launch(gsi_handle* h, const void* x, float* y, uint8_t* gate,
                            float* rho, cudaStream_t s);
 
-// One-barrier decode path (gsi_decode3.cu), k in {64, 128, 256}
-size_t decode3_acc_floats(int64_t k);
-gsi_status_t decode3_configure(gsi_handle* h);
-gsi_status_t decode3_launch(gsi_handle* h, const void* x, float* y, uint8_t* gate,
-                            float* rho, cudaStream_t s);
+// One-exchange decode path (gsi_decode_cr.cu), k in {64, 128, 256}
+size_t decode_cr_acc_floats(int64_t k);
+gsi_status_t decode_cr_configure(gsi_handle* h);
+gsi_status_t decode_cr_launch(gsi_handle* h, const void* x, float* y, uint8_t* gate,
+                              float* rho, cudaStream_t s);
+// Upper bound of the spectral norm of the symmetric matrix that the
+// correction tiles (bf16, corr_tiles_elems(k) values) represent.
+double corr_norm_bound(const uint16_t* tiles, int k);
 gsi_status_t group_configure(gsi_group* g);
 gsi_status_t group_launch(gsi_group* g, const void* const* x, float* const* y,
                           uint8_t* const* gate, float* const* rho, cudaStream_t s);
