@@ -582,6 +582,100 @@ def run_gsi(args, world, rank, local):
         print(json.dumps(out), flush=True)
 
 
+def run_gsi_rowshard(args, world, rank, local):
+    """The decode layer split by rows over the ranks (one GPU each): rank r
+    holds rows row_ranges(d_out, N)[r] of every linear's W and M and the full
+    V_k, computes g, rho and the gate itself, and the y parts of each call are
+    gathered (NCCL all_gather) before the next call.  Strong scaling: the N
+    ranks share one layer.  Calls are issued one by one (no CUDA graph)."""
+    import torch
+
+    import gsi_inputs as gi
+    from gated_rank_subspace_gsi_gb300 import lib, shard
+    torch.cuda.set_device(local)
+    lib.library()
+    n_tokens = 512
+    props = torch.cuda.get_device_properties(local)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
+    replicas = max(16, int(math.ceil(4 * l2 * world / 32.44e6)))
+    wl = gi.gptj_layer(n_tokens)
+    slow = gi.slow_positions(n_tokens, wl.extra["n_slow"], wl.seed)
+    layer = []
+    for li, spec in enumerate(wl.linears):
+        W = gi.gaussian_weights(spec.d_out, spec.d, wl.seed, li, device="cuda")
+        basis = gi.random_basis(spec.d, spec.k, wl.seed, li)
+        rs = gi.rho_targets(n_tokens, spec.rho_fast, spec.rho_slow, slow, wl.seed, li)
+        X = gi.tokens(basis, rs, wl.seed, li)
+        V = torch.from_numpy(basis.V_bits.view(np.int16)).view(torch.bfloat16).cuda()
+        M = torch.empty((spec.d_out, spec.k), dtype=torch.bfloat16, device="cuda")
+        lib.gsi_precompute_M(W, V, M)
+        torch.cuda.synchronize()
+        parts = []
+        for r in range(replicas):
+            Vr = V if r == 0 else V.clone()
+            Mr = M if r == 0 else M.clone()
+            parts.append((Vr, Mr, shard.RowShard(W, Vr, Mr, spec.eps, rank, world)))
+        x = torch.from_numpy(X.view(np.int16)).view(torch.bfloat16).cuda()
+        layer.append(dict(spec=spec, W=W, parts=parts, x=x,
+                          y=torch.zeros((n_tokens, spec.d_out), dtype=torch.float32, device="cuda"),
+                          gate=torch.zeros((n_tokens,), dtype=torch.uint8, device="cuda")))
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for t in range(n_tokens):
+            r = t % replicas
+            for L in layer:
+                p = L["parts"][r][2]
+                y, g, _ = p.forward(L["x"][t:t + 1], stream=stream)
+                L["y"][t:t + 1].copy_(y)
+                L["gate"][t:t + 1].copy_(g)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    for L in layer:
+        if not np.array_equal(L["gate"].cpu().numpy().astype(bool), slow):
+            raise RuntimeError("gates differ from the generated slow/fast mix")
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    e1.synchronize()
+    barrier(world)
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+    clk = clocks.stop()
+    n_lin = n_tokens * len(layer)
+    nbytes = step_bytes([dict(spec=L["spec"]) for L in layer], slow)
+    peak, peak_kind = hbm_peak()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    out = {
+        "metric": METRIC, "value": round(ms * 1e3 / n_lin, 4), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": False, "scaling": "strong", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded Gaussian weights, QR bases, activations with set residual ratios)",
+        "impl": "gsi",
+        "config": {"workload": DECODE_WORKLOAD,
+                   "parallelism": f"rows x{world}: W and M split by output rows, V_k and the gate "
+                                  f"replicated, y parts all-gathered after every call",
+                   "schedule": "sequential, calls issued one by one (no CUDA graph)",
+                   "replicas": replicas},
+        "effective_hbm_gbs": round(gbs, 1),
+        "roofline": {"bound": "hbm", "achieved": round(gbs / world, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(gbs / world / peak, 4), "traffic": None,
+                     "kernel": DECODE_KERNEL + " (per GPU)", "peak_kind": f"{peak_kind} HBM copy"},
+        "gpu_launches": args.steps * n_tokens * len(layer),
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
 def run_batched(args, world, rank, local):
     """The batched prefill-style gated linear: T = 512 tokens per call through
     one 4096 -> 16384 linear (k = 256, eps = 0.10, 154 slow tokens at seeded
@@ -1661,6 +1755,9 @@ def main(argv=None):
                     help="each call prefetches into L2 the operands of the call this many "
                          "places later (0: none; the one-token kernel's next call already "
                          "stages its operands while the current call runs)")
+    ap.add_argument("--shard", choices=["none", "rows"], default="none",
+                    help="rows: split the decode layer's linears by output rows over the GPUs "
+                         "(NCCL all_gather of y after every call) instead of running replicas")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the per-linear breakdown and the end-to-end leg (profiling runs)")
     args = ap.parse_args(argv)
@@ -1693,6 +1790,8 @@ def main(argv=None):
             run_stack(args, world, rank, local)
         elif args.workload == "opt_mlp":
             run_opt(args, world, rank, local)
+        elif args.shard == "rows":
+            run_gsi_rowshard(args, world, rank, local)
         else:
             run_gsi(args, world, rank, local)
     finally:
