@@ -14,8 +14,11 @@ streams ~17 GB and no replica is reused within R x 32 MB >= 4 x L2.
 Reported (one JSON line on rank 0): us per gated linear (the metric), the
 effective HBM GB/s and its fraction of the measured copy peak (and of
 8 TB/s), a roofline object for the decode kernel, an end-to-end number
-through the host-buffer entry point, the oracle timed on the host cores,
-and the SM clocks sampled during the timed region.
+through the C ABI's host-buffer entry point, the oracle timed on the host
+cores, the SM clocks sampled during the timed region, and under "configs"
+the other configurations (GPT-2 QKV call, 28-layer GPT-J stack, OPT MLP
+slow-fraction sweep, batched T = 512 call), each with its own metric,
+roofline fraction and oracle baseline.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gsi|reference]
 """
@@ -342,8 +345,18 @@ def record_step(layer, n_tokens, replicas, stream, handles_subset=None, host=Non
                                 L["rho"][t:t + 1], stream)
             else:
                 H = host[li]
-                lib.gsi_forward_host(h, H["x"][t:t + 1], H["y"][t:t + 1],
-                                     H["gate"][t:t + 1], H["rho"][t:t + 1], stream)
+                lib.gsi_forward_host(h, H["x"][t:t + 1], H["yp"][t], H["gp"][t], H["rp"][t],
+                                     stream)
+
+
+def _release():
+    """Return freed device memory to the driver between workloads."""
+    import gc
+
+    import torch
+    gc.collect()
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
 
 
 def replay(graph, stream, n: int):
@@ -476,44 +489,54 @@ def run_gsi(args, world, rank, local):
                          gbs=round(b1 / (ms1 * 1e-3) / 1e9, 1))
         del g1
 
-    # ---- end to end: the step's inputs from pinned host memory, its results
-    # back to pinned host memory, the step itself through the public calls ---
+    # ---- end to end through the C ABI's host-buffer call: every call's x and
+    # its y, rho and gate in page-locked host memory (y, rho and gate
+    # consecutive), sequential schedule (the grouped launch has no host-buffer
+    # form) ---------------------------------------------------------------
     host = []
     h2d = d2h = 0
-    ms_e2e = ms_call = float("nan")
+    ms_call = ms_bulk = float("nan")
     for L in (layer if not args.no_extras else []):
-        s = L["spec"]
-        H = dict(x=L["x"].cpu().pin_memory(),
-                 y=torch.empty((n_tokens, s.d_out), dtype=torch.float32).pin_memory(),
-                 gate=torch.empty((n_tokens,), dtype=torch.uint8).pin_memory(),
-                 rho=torch.empty((n_tokens,), dtype=torch.float32).pin_memory())
+        s_ = L["spec"]
+        stride = (s_.d_out * 4 + 5 + 15) // 16 * 16
+        buf = torch.empty((n_tokens, stride), dtype=torch.uint8).pin_memory()
+        H = dict(x=L["x"].cpu().pin_memory(), buf=buf,
+                 yp=[buf[t, :4 * s_.d_out].view(torch.float32).view(1, s_.d_out)
+                     for t in range(n_tokens)],
+                 rp=[buf[t, 4 * s_.d_out:4 * s_.d_out + 4].view(torch.float32)
+                     for t in range(n_tokens)],
+                 gp=[buf[t, 4 * s_.d_out + 4:4 * s_.d_out + 5] for t in range(n_tokens)])
         host.append(H)
-        h2d += n_tokens * s.d * 2
-        d2h += n_tokens * (s.d_out * 4 + 1 + 4)
+        h2d += n_tokens * s_.d * 2
+        d2h += n_tokens * (s_.d_out * 4 + 5)
     if host:
+        link_schedule(layer, groups, replicas, "sequential", args.prefetch)
+        gc_ = capture_step(layer, n_tokens, replicas, stream, host=host)
+        for H in host:
+            H["buf"].fill_(0xEE)
+        ms_call = max_over_ranks(time_graph(gc_, stream, reps=max(3, args.steps // 10), warmup=2),
+                                 world)
+        gates_h = np.array([int(g[0]) for g in host[0]["gp"]], dtype=bool)
+        if not np.array_equal(gates_h, slow):
+            raise RuntimeError("host-buffer gates differ from the generated mix")
+        del gc_
+        link_schedule(layer, groups, replicas, args.schedule, args.prefetch)
+        # the same step with one bulk copy of all its inputs and outputs
+        # around the device calls (torch copies), for comparison
         ge = torch.cuda.CUDAGraph()
+        bulk = [dict(x=H["x"], y=torch.empty((n_tokens, L["spec"].d_out),
+                                                 dtype=torch.float32).pin_memory())
+                for L, H in zip(layer, host)]
         with torch.cuda.stream(stream):
             with torch.cuda.graph(ge, stream=stream):
-                for L, H in zip(layer, host):
-                    L["x"].copy_(H["x"], non_blocking=True)
+                for L, B in zip(layer, bulk):
+                    L["x"].copy_(B["x"], non_blocking=True)
                 record_step(layer, n_tokens, replicas, stream, groups=groups if grouped else None)
-                for L, H in zip(layer, host):
-                    H["y"].copy_(L["y"], non_blocking=True)
-                    H["gate"].copy_(L["gate"], non_blocking=True)
-                    H["rho"].copy_(L["rho"], non_blocking=True)
-        for H in host:
-            H["gate"].fill_(7)
-        ms_e2e = max_over_ranks(time_graph(ge, stream, reps=max(3, args.steps // 10), warmup=2),
-                                world)
-        if not np.array_equal(host[0]["gate"].numpy().astype(bool), slow):
-            raise RuntimeError("end-to-end gates differ from the generated mix")
-        # every call through the host-buffer entry point (three small copies
-        # per call)
-        link_schedule(layer, groups, replicas, "sequential", args.prefetch)
-        gc = capture_step(layer, n_tokens, replicas, stream, host=host)
-        ms_call = max_over_ranks(time_graph(gc, stream, reps=max(3, args.steps // 10), warmup=2),
+                for L, B in zip(layer, bulk):
+                    B["y"].copy_(L["y"], non_blocking=True)
+        ms_bulk = max_over_ranks(time_graph(ge, stream, reps=max(3, args.steps // 10), warmup=2),
                                  world)
-        link_schedule(layer, groups, replicas, args.schedule, args.prefetch)
+        del ge
 
     launches = args.steps * n_tokens * (2 if grouped else len(layer))
     out = {
@@ -563,23 +586,64 @@ def run_gsi(args, world, rank, local):
             "us_per_gated_linear": round(us_per_lin, 4),
         },
         "e2e": {
-            "value": None if math.isnan(ms_e2e) else round(ms_e2e * 1e3 / n_lin, 4),
+            "value": None if math.isnan(ms_call) else round(ms_call * 1e3 / n_lin, 4),
             "unit": UNIT,
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
-            "how": "per step: one copy of every x of the step from pinned host memory, the step "
-                   "through gsi_forward / gsi_group_forward, one copy of every y, gate and rho "
-                   "back to pinned host memory, graph-captured",
-            "per_call_host_api_us_per_linear": None if math.isnan(ms_call)
-            else round(ms_call * 1e3 / n_lin, 4),
+            "how": "every call through gsi_forward_host (the C ABI's host-buffer entry) on "
+                   "page-locked host buffers: the one-token kernel reads x and writes y, rho and "
+                   "gate in place over the host link (no copy nodes), sequential schedule (the "
+                   "grouped launch has no host-buffer form), graph-captured",
+            "copies_per_call": 0,
+            "bulk_copies_us_per_linear": None if math.isnan(ms_bulk)
+            else round(ms_bulk * 1e3 / n_lin, 4),
+            "bulk_copies_how": "one torch copy of all the step's x in and of all its y out around "
+                               "the device calls (grouped schedule)",
         },
         "gpu_launches": launches,
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(layer, slow, budget_s=args.cpu_budget)
+    if not args.no_extras and not args.no_configs:
+        # the other configurations, each measured on its own after the decode
+        # layer's memory is returned
+        del graph
+        for g in groups:
+            lib.gsi_group_destroy(g)
+        for L in layer:
+            for (_, _, h) in L["reps"]:
+                lib.gsi_destroy(h)
+        del layer, groups
+        _release()
+        out["configs"] = measure_configs(args, world, rank, local)
+        out["gpu_launches"] = launches + sum(c["gpu_launches"] for c in out["configs"].values())
     if rank == 0:
         print(json.dumps(out), flush=True)
+
+
+def measure_configs(args, world, rank, local):
+    """The GPT-2 QKV call, the 28-layer GPT-J stack, the OPT MLP slow-fraction
+    sweep and the batched T = 512 call, each with its own metric, roofline
+    fraction and oracle baseline on a bounded sample (the same fields as the
+    headline line)."""
+    res = {}
+    for key, wname, fn in (("gpt2_qkv_T64", "gpt2_qkv_T64", measure_gpt2),
+                           ("gptj_stack", "gptj_stack", measure_stack),
+                           ("opt_mlp", "opt_mlp", measure_opt),
+                           ("batched_T512", "batched_T512", measure_batched)):
+        d = fn(args, world, rank, local)
+        e = {k: d[k] for k in ("metric", "value", "unit", "steps", "ms_per_step") if k in d}
+        e["workload"] = d["config"]["workload"]
+        e["roofline"] = {k: d["roofline"][k] for k in ("bound", "achieved", "peak", "unit", "frac",
+                                                       "peak_kind") if k in d["roofline"]}
+        for k in ("tensor", "curve", "us_per_gated_linear", "e2e", "clocks", "gpu_launches"):
+            if k in d:
+                e[k] = d[k]
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            e["cpu_baseline"] = ref_linear(wname, 1)[4]
+        res[key] = e
+    return res
 
 
 def run_gsi_rowshard(args, world, rank, local):
@@ -676,7 +740,7 @@ def run_gsi_rowshard(args, world, rank, local):
         print(json.dumps(out), flush=True)
 
 
-def run_batched(args, world, rank, local):
+def measure_batched(args, world, rank, local):
     """The batched prefill-style gated linear: T = 512 tokens per call through
     one 4096 -> 16384 linear (k = 256, eps = 0.10, 154 slow tokens at seeded
     positions): projection, gate, compaction, gather and the two tcgen05
@@ -758,9 +822,10 @@ def run_batched(args, world, rank, local):
     tfs = flops / (us_call * 1e-6) / 1e12
     # end to end: pinned host x in, y / gate / rho out, per call
     Hx = x.cpu().pin_memory()
-    Hy = torch.empty((T, spec.d_out), dtype=torch.float32).pin_memory()
-    Hg = torch.empty((T,), dtype=torch.uint8).pin_memory()
-    Hr = torch.empty((T,), dtype=torch.float32).pin_memory()
+    Hbuf = torch.empty((T * (spec.d_out * 4 + 5),), dtype=torch.uint8).pin_memory()
+    Hy = Hbuf[:T * spec.d_out * 4].view(torch.float32).view(T, spec.d_out)
+    Hr = Hbuf[T * spec.d_out * 4:T * spec.d_out * 4 + 4 * T].view(torch.float32)
+    Hg = Hbuf[T * spec.d_out * 4 + 4 * T:]
     ge = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         with torch.cuda.graph(ge, stream=stream):
@@ -789,10 +854,22 @@ def run_batched(args, world, rank, local):
         "e2e": {"value": round(ms_e2e * 1e3 / calls, 3), "unit": "us per gated linear call",
                 "h2d_bytes_per_step": calls * T * spec.d * 2,
                 "d2h_bytes_per_step": calls * T * (spec.d_out * 4 + 5),
-                "how": "gsi_forward_host per call (pinned host buffers), graph-captured"},
+                "how": "gsi_forward_host per call (pinned host buffers; y, rho and gate "
+                       "consecutive, so one copy returns them), graph-captured",
+                "copies_per_call": 2},
         "gpu_launches": steps * calls * launches_per_call,
         "clocks": clk,
     }
+    del graph, ge
+    for rep in reps:
+        lib.gsi_destroy(rep[3])
+    del reps
+    _release()
+    return out
+
+
+def run_batched(args, world, rank, local):
+    out = measure_batched(args, world, rank, local)
     if rank == 0:
         print(json.dumps(out), flush=True)
 
@@ -1025,7 +1102,7 @@ def _line(metric, value, unit, world, steps, warmup, ms, config, **extra):
     return out
 
 
-def run_gpt2(args, world, rank, local):
+def measure_gpt2(args, world, rank, local):
     """GPT-2-small-shaped QKV linear (768 -> 2304, k = 256, eps = 0.10), T = 64
     tokens per call with 6 slow: L2-resident and latency-bound (a parity
     configuration), timed as calls in a CUDA graph."""
@@ -1068,16 +1145,23 @@ def run_gpt2(args, world, rank, local):
                           "peak_kind": f"{kind} HBM copy (L2-resident: not the bound)"},
                 gpu_launches=steps * calls * lib.gsi_forward_launch_count(L["h"], wl.T),
                 clocks=clk)
+    lib.gsi_destroy(L["h"])
+    del graph, L
+    _release()
+    return out
+
+
+def run_gpt2(args, world, rank, local):
+    out = measure_gpt2(args, world, rank, local)
     if rank == 0:
         print(json.dumps(out), flush=True)
 
 
-def run_stack(args, world, rank, local):
+def measure_stack(args, world, rank, local):
     """GPT-J-shaped 28-layer stack at decode: per layer the stacked qkv+fc_in
     call, then out_proj and fc_out as one grouped launch; depth-coherent bases
     per input chain; 256 distinct decode steps of synthetic tokens (43 slow
-    draws over step x layer x linear), weights (11 GB) beyond L2 by size.
-    Every launch prefetches the next launch's operands into L2."""
+    draws over step x layer x linear), weights (11 GB) beyond L2 by size."""
     import torch
 
     import gsi_inputs as gi
@@ -1103,9 +1187,10 @@ def run_stack(args, world, rank, local):
             lay.append(L)
         g = lib.gsi_group_create([lay[1]["h"], lay[2]["h"]])
         layers.append((lay, g))
-    for l, (lay, g) in enumerate(layers):
-        lib.gsi_set_prefetch_group(lay[0]["h"], g)
-        lib.gsi_group_set_prefetch(g, layers[(l + 1) % nL][0][0]["h"])
+    if args.prefetch > 0:
+        for l, (lay, g) in enumerate(layers):
+            lib.gsi_set_prefetch_group(lay[0]["h"], g)
+            lib.gsi_group_set_prefetch(g, layers[(l + 1) % nL][0][0]["h"])
     stream = torch.cuda.Stream()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
@@ -1145,11 +1230,23 @@ def run_stack(args, world, rank, local):
                           "frac": round(gbs / peak, 4), "traffic": None,
                           "bytes_per_fast_step": per_fast, "peak_kind": f"{kind} HBM copy"},
                 gpu_launches=steps * S * nL * 2, clocks=clk)
+    del graph
+    for lay, g in layers:
+        lib.gsi_group_destroy(g)
+        for L in lay:
+            lib.gsi_destroy(L["h"])
+    del layers
+    _release()
+    return out
+
+
+def run_stack(args, world, rank, local):
+    out = measure_stack(args, world, rank, local)
     if rank == 0:
         print(json.dumps(out), flush=True)
 
 
-def run_opt(args, world, rank, local):
+def measure_opt(args, world, rank, local):
     """OPT-6.7B-shaped MLP (fc1 4096 -> 16384, fc2 16384 -> 4096) x 32 layers at
     decode, eps = 0.05, over slow fractions 0, 2, 10, 50 and 100% (exact counts
     over step x layer x linear), with the dense bf16 W x (torch.matmul) on the
@@ -1178,7 +1275,8 @@ def run_opt(args, world, rank, local):
         layers.append(lay)
     order = [L["h"] for lay in layers for L in lay]
     for i, h in enumerate(order):
-        lib.gsi_set_prefetch(h, order[(i + 1) % len(order)])
+        lib.gsi_set_prefetch(h, order[(i + args.prefetch) % len(order)] if args.prefetch > 0
+                             else None)
     stream = torch.cuda.Stream()
     peak, kind = hbm_peak()
     steps = max(1, args.steps // 30)
@@ -1239,6 +1337,16 @@ def run_opt(args, world, rank, local):
                                        "unit": "GB/s", "frac": c0["frac_of_measured_hbm"],
                                        "traffic": None, "peak_kind": f"{kind} HBM copy"},
                 gpu_launches=steps * S * nL * 2 * len(fracs), clocks=clk)
+    for lay in layers:
+        for L in lay:
+            lib.gsi_destroy(L["h"])
+    del layers
+    _release()
+    return out
+
+
+def run_opt(args, world, rank, local):
+    out = measure_opt(args, world, rank, local)
     if rank == 0:
         print(json.dumps(out), flush=True)
 
@@ -1327,20 +1435,16 @@ def _ref_token_seconds(orc, spec, seed, tag, steps, n_fast=2, n_slow=1, batch=Fa
     return per_token(fast), per_token(slow)
 
 
-def run_reference_linear(args, world, rank):
-    """The oracle (fp64 C) on the host cores for the workloads made of gated
+def ref_linear(wname: str, steps: int):
+    """The oracle (fp64 C) on the host cores for a workload made of gated
     linears of fixed shapes (batched_T512, gpt2_qkv_T64, gptj_stack, opt_mlp):
     per shape, fast and slow tokens are timed one by one on a bounded sample,
     and the metric's unit is composed from the workload's exact fast and slow
-    counts."""
-    if rank != 0:
-        return
+    counts.  Returns (value, metric, unit, workload, cpu_baseline dict)."""
     import oracle
 
     import gsi_inputs as gi
     orc = oracle.default()
-    steps = max(1, min(args.steps, 4))
-    wname = args.workload
     batched = wname in ("batched_T512", "gpt2_qkv_T64")
     if wname == "batched_T512":
         wl = gi.batched_prefill()
@@ -1377,15 +1481,26 @@ def run_reference_linear(args, world, rank):
         how = "t_fast(fc1) + t_fast(fc2): the f = 0 point"
     else:
         raise ValueError(wname)
+    batched = wname in ("batched_T512", "gpt2_qkv_T64")
+    cpu = {"value": round(v, 3), "unit": unit, "cores": orc.num_threads(), "kind": "oracle",
+           "sample": f"per linear shape, fast and slow tokens of {steps} steps timed apart "
+                     f"({'in one call each' if batched else 'one call per token'}); {how}"}
+    return v, metric, unit, workload, cpu
+
+
+def run_reference_linear(args, world, rank):
+    """The oracle on the host cores for the workloads made of gated linears
+    of fixed shapes (ref_linear)."""
+    if rank != 0:
+        return
+    steps = max(1, min(args.steps, 4))
+    v, metric, unit, workload, cpu = ref_linear(args.workload, steps)
     out = {"metric": metric, "value": round(v, 3), "unit": unit, "n_gpus": world,
            "steps": steps, "warmup": 1, "ms_per_step": round(v / 1e3, 3),
            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic", "impl": "reference",
            "config": {"workload": workload},
-           "cpu_baseline": {"value": round(v, 3), "unit": unit, "cores": orc.num_threads(),
-                            "kind": "oracle",
-                            "sample": f"per linear shape, fast and slow tokens of {steps} steps "
-                                      f"timed apart ({'in one call each' if batched else 'one call per token'}); {how}"},
+           "cpu_baseline": cpu,
            "e2e": {"value": round(v, 3), "unit": unit, "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
@@ -1758,6 +1873,8 @@ def main(argv=None):
     ap.add_argument("--shard", choices=["none", "rows"], default="none",
                     help="rows: split the decode layer's linears by output rows over the GPUs "
                          "(NCCL all_gather of y after every call) instead of running replicas")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="report the decode layer only (without the other configurations)")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the per-linear breakdown and the end-to-end leg (profiling runs)")
     args = ap.parse_args(argv)

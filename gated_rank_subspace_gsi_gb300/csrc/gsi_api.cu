@@ -184,25 +184,87 @@ gsi_status_t gsi_forward(gsi_handle_t h, const void* x, int64_t T, float* y, uin
   return gsi::batched_launch(h, x, T, y, gate, rho, stream);
 }
 
+namespace {
+
+// One token's x from page-locked host memory into the handle's device
+// staging, by one CTA (16-byte loads, all in flight at once): the one-token
+// kernel reads x from every CTA, which is cheap from device memory (L2) and
+// dear over the host link.  Launched with programmatic dependent launch, so
+// the next kernel's CTAs stage their weights while it runs.
+__global__ void __launch_bounds__(256) stage_x_kernel(const uint4* __restrict__ src,
+                                                      uint4* __restrict__ dst, int n16) {
+  gsi::pdl_launch_dependents();
+  gsi::pdl_wait();  // x may have been written by the previous kernel
+  constexpr int kPer = 16;
+  uint4 v[kPer];
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int i = int(threadIdx.x) + j * 256;
+    if (i < n16) v[j] = src[i];
+  }
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    const int i = int(threadIdx.x) + j * 256;
+    if (i < n16) dst[i] = v[j];
+  }
+  for (int i = int(threadIdx.x) + kPer * 256; i < n16; i += 256) dst[i] = src[i];
+}
+
+// True if the device can address p directly at the same address: page-locked
+// host memory (cudaHostAlloc, cudaMallocHost, cudaHostRegister) under unified
+// addressing, or managed memory.
+bool device_addressable(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();  // clear the error of an unknown pointer
+    return false;
+  }
+  return (at.type == cudaMemoryTypeHost || at.type == cudaMemoryTypeManaged ||
+          at.type == cudaMemoryTypeDevice) &&
+         at.devicePointer == p;
+}
+
+}  // namespace
+
 gsi_status_t gsi_forward_host(gsi_handle_t h, const void* x_host, int64_t T, float* y_host,
                               uint8_t* gate_host, float* rho_host, cudaStream_t stream) {
   if (!h || T < 0) return GSI_ERR_INVALID_ARG;
   if (T == 0) return GSI_OK;
   if (!x_host || !y_host) return GSI_ERR_INVALID_ARG;
+  // One token in page-locked memory: a one-CTA kernel brings x into the
+  // device staging, and the map writes y, gate and rho in place over the host
+  // link (no copy nodes: consecutive calls chain like device calls)
+  if (T == 1 && gsi::aligned16(x_host) && device_addressable(x_host) &&
+      device_addressable(y_host) && (!gate_host || device_addressable(gate_host)) &&
+      (!rho_host || device_addressable(rho_host))) {
+    uint4* xd = static_cast<uint4*>(h->st_dev);
+    if (gsi::launch_pdl(stage_x_kernel, dim3(1), dim3(256), 0, stream,
+                        static_cast<const uint4*>(x_host), xd, int(h->d / 8)) != cudaSuccess)
+      return GSI_ERR_CUDA;
+    return gsi_forward(h, xd, 1, y_host, gate_host, rho_host, stream);
+  }
   if (T > h->st_T || (T > 1 && T > h->max_T)) return GSI_ERR_WORKSPACE;
+  // staging: x, then y, rho and gate back to back for this T (one copy
+  // returns all three when the caller's buffers are laid out the same way)
   char* p = static_cast<char*>(h->st_dev);
   void* xd = p;
   p += (size_t(h->st_T) * h->d * 2 + 255) / 256 * 256;
+  const size_t y_bytes = size_t(T) * h->d_out * 4;
   float* yd = reinterpret_cast<float*>(p);
-  p += (size_t(h->st_T) * h->d_out * 4 + 255) / 256 * 256;
-  float* rd = reinterpret_cast<float*>(p);
-  p += (size_t(h->st_T) * 4 + 255) / 256 * 256;
-  uint8_t* gd = reinterpret_cast<uint8_t*>(p);
+  float* rd = reinterpret_cast<float*>(p + y_bytes);
+  uint8_t* gd = reinterpret_cast<uint8_t*>(p + y_bytes + size_t(T) * 4);
   if (cudaMemcpyAsync(xd, x_host, size_t(T) * h->d * 2, cudaMemcpyHostToDevice, stream) != cudaSuccess)
     return GSI_ERR_CUDA;
   gsi_status_t st = gsi_forward(h, xd, T, yd, gd, rd, stream);
   if (st != GSI_OK) return st;
-  if (cudaMemcpyAsync(y_host, yd, size_t(T) * h->d_out * 4, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+  const bool packed = rho_host == reinterpret_cast<float*>(reinterpret_cast<char*>(y_host) + y_bytes) &&
+                      gate_host == reinterpret_cast<uint8_t*>(rho_host + T);
+  if (packed) {
+    if (cudaMemcpyAsync(y_host, yd, y_bytes + size_t(T) * 5, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+      return GSI_ERR_CUDA;
+    return GSI_OK;
+  }
+  if (cudaMemcpyAsync(y_host, yd, y_bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
     return GSI_ERR_CUDA;
   if (gate_host && cudaMemcpyAsync(gate_host, gd, size_t(T), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
     return GSI_ERR_CUDA;
@@ -358,6 +420,7 @@ void gsi_destroy(gsi_handle_t h) {
 }
 
 int gsi_forward_launch_count(gsi_handle_t h, int64_t T) {
+  // (gsi_forward; gsi_forward_host on page-locked memory adds one launch)
   if (!h || T <= 0) return 0;
   if (T == 1) return 1;
   return gsi::batched_launch_count(h, T);

@@ -93,13 +93,23 @@ gsi_status_t gsi_create(const void *W, const void *V_k, const void *M,
 gsi_status_t gsi_forward(gsi_handle_t h, const void *x, int64_t T, float *y,
                          uint8_t *gate, float *rho, cudaStream_t stream);
 
-/* gsi_forward on HOST buffers: copies x (T x d bf16) to device staging
- * buffers owned by the handle, runs the map, and copies y (T x d_out fp32),
- * gate and rho (either may be NULL) back to the host buffers.  All work is
- * queued on `stream`; with page-locked (pinned) host buffers the call
- * returns before the copies finish and the caller synchronises the stream
+/* gsi_forward on HOST buffers.
+ * One token (T == 1) whose buffers are all page-locked host memory that the
+ * device addresses directly (cudaHostAlloc / cudaMallocHost / cudaHostRegister
+ * under unified addressing): a one-CTA kernel copies x into the handle's
+ * device staging and the map writes y, gate and rho in place over the host
+ * link (NVLink-C2C on Grace systems) -- two kernel launches, no copy nodes,
+ * and consecutive calls on one stream chain like device calls.
+ * Otherwise: copies x (T x d bf16) to device staging buffers owned by the
+ * handle, runs the map, and copies y (T x d_out fp32), gate and rho (either
+ * may be NULL) back to the host buffers.  When the three are consecutive in
+ * one host allocation -- y, then rho at y_host + T * d_out, then gate at
+ * rho_host + T -- one copy returns all of them (two copies per call in all,
+ * instead of four).
+ * All work is queued on `stream`; with page-locked host buffers the call
+ * returns before the work finishes and the caller synchronises the stream
  * before reading y; with pageable buffers the CUDA runtime may block.
- * Staging buffers grow with gsi_reserve(). */
+ * Alignment as gsi_forward.  Staging buffers grow with gsi_reserve(). */
 gsi_status_t gsi_forward_host(gsi_handle_t h, const void *x_host, int64_t T,
                               float *y_host, uint8_t *gate_host,
                               float *rho_host, cudaStream_t stream);

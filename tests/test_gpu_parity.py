@@ -211,7 +211,8 @@ def test_T0_workspace_and_reserve(gsi, orc):
 
 @pytest.mark.parametrize("T", [1, 33])
 def test_forward_host(gsi, orc, T):
-    """The host-buffer entry point gives the device path's results."""
+    """The host-buffer entry point gives the device path's results: in place on
+    page-locked memory for one token, through staging copies otherwise."""
     import torch
     d_out, d, k = 512, 1024, 128
     W, basis, X = make_case(d_out, d, k, 0.1, T, 41)
@@ -224,6 +225,28 @@ def test_forward_host(gsi, orc, T):
     gsi.gsi_forward_host(lin.h, xh, yh, gh, rh, s)
     s.synchronize()
     check_against_oracle(orc, lin, X, yh.numpy(), gh.numpy(), rh.numpy(), what="host")
+    # y, rho and gate consecutive in one pinned allocation: one copy returns them
+    nb = T * d_out * 4
+    buf = torch.full((nb + T * 5,), 0xEE, dtype=torch.uint8).pin_memory()
+    yp = buf[:nb].view(torch.float32).view(T, d_out)
+    rp = buf[nb:nb + 4 * T].view(torch.float32)
+    gp = buf[nb + 4 * T:]
+    gsi.gsi_forward_host(lin.h, xh, yp, gp, rp, s)
+    s.synchronize()
+    assert np.array_equal(yp.numpy(), yh.numpy()) and np.array_equal(gp.numpy(), gh.numpy())
+    assert np.array_equal(rp.numpy().view(np.int32), rh.numpy().view(np.int32))
+    # pageable host memory: the staging copies (the device cannot address it)
+    xq = torch.from_numpy(X.view(np.int16).copy()).view(torch.bfloat16)
+    yq = torch.empty((T, d_out), dtype=torch.float32)
+    gq = torch.empty((T,), dtype=torch.uint8)
+    rq = torch.empty((T,), dtype=torch.float32)
+    gsi.gsi_forward_host(lin.h, xq, yq, gq, rq, s)
+    s.synchronize()
+    assert np.array_equal(yq.numpy(), yh.numpy()) and np.array_equal(gq.numpy(), gh.numpy())
+    assert np.array_equal(rq.numpy().view(np.int32), rh.numpy().view(np.int32))
+    # and the device path itself, bit for bit
+    y, g, r = lin.forward(X, one_by_one=(T == 1))
+    assert np.array_equal(y, yh.numpy()) and np.array_equal(g, gh.numpy())
     lin.close()
 
 
