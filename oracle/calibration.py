@@ -24,6 +24,10 @@ itself, not x minus a mean.
   cascade(Xs, Q0, t0, t1)         the depth cascade of section 2.3: layer 0
                                   from Q0 with t0 iterations, layer l + 1
                                   started from layer l's basis with t1
+  rank1_refine(X, V, c)           the cascade's refinement in the pages' form:
+                                  c rank-1 corrections of the start basis,
+                                  each new direction re-orthogonalised by DGKS
+  cascade_rank1(Xs, Q0, t0, c)    the depth cascade with that refinement
   principal_sines(A, B)           the comparison between two subspaces
 
 Only span(V_k) matters to the gated map: replacing V_k by V_k R for an
@@ -31,13 +35,22 @@ orthogonal k x k R leaves r and rho unchanged and M g = W V_k R R^T V_k^T x
 unchanged.  So the functions return orthonormal bases of subspaces, and
 results are compared through principal angles, never entry by entry.
 
+rank1_refine is the one function here whose result depends on the basis
+inside the span, not on the span alone: it corrects one basis vector at a
+time.  Its start basis is therefore fixed exactly (the positive-diagonal QR
+factor of the given block, which is unique).
+
 Every function is pinned in tests/test_oracle_calibration.py (closed forms
 for planted spectra, the exact two-dimensional iteration, invariance of the
 span under a change of start basis, convergence at the rate set by the
-eigenvalue gap), and the same file plants mistakes in a copy of this source
-to check that the pins catch them.
+eigenvalue gap, exact recovery of a planted rotated eigenvector by one
+rank-1 correction, orthogonality restored by the second Gram-Schmidt pass),
+and the same file plants mistakes in a copy of this source to check that the
+pins catch them.
 """
 from __future__ import annotations
+
+import math
 
 import numpy as np
 
@@ -97,6 +110,98 @@ def cascade(Xs, Q0, iters_first: int, iters_next: int):
         V = subspace_iteration(X, start, t)
         out.append(V)
         start, t = V, iters_next
+    return out
+
+
+def positive_qr_basis(V) -> np.ndarray:
+    """The Q factor of V = Q R with R upper triangular and a positive
+    diagonal (unique for a full-column-rank V): Householder QR, then every
+    column whose diagonal entry of R came out negative flips sign."""
+    Q, R = np.linalg.qr(_f64(V))
+    return Q * np.where(np.diag(R) < 0.0, -1.0, 1.0)
+
+
+DGKS_ETA = 1.0 / math.sqrt(2.0)
+
+
+def dgks_orthogonalize(B, r):
+    """(q, passes): r minus its component in span(B), B with orthonormal
+    columns, by classical Gram-Schmidt with the reorthogonalisation test of
+    Daniel, Gragg, Kaufman and Stewart: one projection q = r - B (B^T r); if
+    that left less than 1/sqrt(2) of the norm of r, the projection is applied
+    once more to q.  q is not normalised; passes is 1 or 2."""
+    B = _f64(B)
+    r = _f64(r)
+    q = r - B @ (B.T @ r)
+    if np.linalg.norm(q) < DGKS_ETA * np.linalg.norm(r):
+        q = q - B @ (B.T @ q)
+        return q, 2
+    return q, 1
+
+
+def rank1_refine(X, V, corrections: int, order=None):
+    """(Q, chosen, norms): the start basis V (d x k) refined by `corrections`
+    rank-1 corrections for the second moment C = X^T X of the tokens X.
+
+    Section 2.3 of the page starts layer l + 1's basis from layer l's and
+    refines it with a few rank-1 corrections, DGKS updates, instead of a full
+    decomposition per layer; it gives no further steps.  Reading taken:
+
+      Q = the positive-diagonal QR factor of V;  P = C Q
+      for each correction:
+        residuals R = P - Q (Q^T P): column i is (I - Q Q^T) C q_i
+        j = the column with the largest residual norm (the first such)
+        q = R[:, j] re-orthogonalised against Q by DGKS, normalised
+        the plane spanned by q_j and q: C restricted to it is
+          [[a, s], [s, b]],  a = q_j^T C q_j,  b = q^T C q,  s = q_j^T C q
+        q_j <- cos(t) q_j + sin(t) q with t = atan2(2 s, a - b) / 2, the
+        unit vector of the plane with the largest Rayleigh quotient
+        P[:, j] <- cos(t) P[:, j] + sin(t) C q
+
+    Each correction changes one column, Q <- Q + (q_j' - q_j) e_j^T, a rank-1
+    update that keeps the columns orthonormal, and never lowers
+    trace(Q^T C Q).  A residual that vanishes after re-orthogonalisation
+    (q = 0: span(Q) is invariant under C) leaves the basis as it is.
+
+    order: optional column indices, one per correction, used instead of the
+    largest-residual choice (to replay another implementation's choices).
+    chosen: the column corrected at each step; norms: (corrections x k) the
+    residual norms each choice was made from."""
+    X = _f64(X)
+    Q = positive_qr_basis(V)
+    P = X.T @ (X @ Q)
+    chosen, norms = [], []
+    for step in range(int(corrections)):
+        R = P - Q @ (Q.T @ P)
+        nr = np.linalg.norm(R, axis=0)
+        j = int(np.argmax(nr)) if order is None else int(order[step])
+        chosen.append(j)
+        norms.append(nr)
+        q, _ = dgks_orthogonalize(Q, R[:, j])
+        nq = np.linalg.norm(q)
+        if not nq > 0.0:
+            continue
+        q = q / nq
+        Cq = X.T @ (X @ q)
+        a = Q[:, j] @ P[:, j]
+        b = q @ Cq
+        s = Q[:, j] @ Cq
+        t = 0.5 * math.atan2(2.0 * s, a - b)
+        Q[:, j] = math.cos(t) * Q[:, j] + math.sin(t) * q
+        P[:, j] = math.cos(t) * P[:, j] + math.sin(t) * Cq
+    return Q, chosen, np.array(norms).reshape(len(norms), Q.shape[1])
+
+
+def cascade_rank1(Xs, Q0, iters_first: int, corrections: int, orders=None):
+    """The depth cascade in the page's form: layer 0 is
+    subspace_iteration(Xs[0], Q0, iters_first); layer l + 1 is
+    rank1_refine(Xs[l + 1], V_l, corrections) with V_l the basis just
+    computed for layer l.  orders: optional per-layer column orders for
+    rank1_refine (entry 0 unused).  Returns the list of bases."""
+    out = [subspace_iteration(Xs[0], Q0, iters_first)]
+    for li, X in enumerate(Xs[1:], start=1):
+        od = None if orders is None else orders[li]
+        out.append(rank1_refine(X, out[-1], corrections, od)[0])
     return out
 
 
