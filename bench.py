@@ -1602,6 +1602,8 @@ def run_cascade(args, world, rank, local):
     rl = cal_roofline(lib, Xs[1], Vc[0], it_next, Vp[1], ws, stream, k)
     launches = (lib.gsi_calibrate_launch_count(n, d, k, it_first)
                 + (L - 1) * lib.gsi_calibrate_launch_count(n, d, k, it_next))
+    rank1 = cascade_rank1_curve(lib, Xs, Q0, it_first, stream=stream, world=world,
+                                e_cold=e_p, ms_cold=ms_cold, steps=steps)
     out = _line(CASC_METRIC, round(ms / L, 4), "ms per layer", world, steps, args.warmup, ms,
                 {"workload": casc_workload(L, n, d, k, it_first, it_next),
                  "l2": f"inputs larger than L2: {L} layers x {n * d * 2 / 2**20:.0f} MiB of tokens",
@@ -1612,7 +1614,7 @@ def run_cascade(args, world, rank, local):
                 captured_energy={"cascade_mean": round(float(np.mean(e_c)), 6),
                                  "per_layer_cold_mean": round(float(np.mean(e_p)), 6),
                                  "max_shortfall": round(float(np.max(np.array(e_p) - np.array(e_c))), 6)},
-                gpu_launches=steps * launches, clocks=clk)
+                gpu_launches=steps * launches, clocks=clk, rank1=rank1)
     out["data"] = ("synthetic (seeded depth-coherent planted-spectrum calibration activations, "
                    "seeded Gaussian start block)")
     out["dtype"] = "bf16 GEMMs, fp32 orthonormalisation"
@@ -1655,6 +1657,54 @@ def run_cascade(args, world, rank, local):
                                          f"(fp64 numpy), {dt:.1f} s"}
     if rank == 0:
         print(json.dumps(out), flush=True)
+
+
+RANK1_CORRECTIONS = (16, 64, 256)
+
+
+def cascade_rank1_curve(lib, Xs, Q0, it_first, stream, world, e_cold, ms_cold,
+                        steps):
+    """The cascade in the page's rank-1 form (gsi_calibrate_cascade_rank1) on
+    the same layers, for a few correction counts: ms per layer (graph
+    replays), the cost cut against per-layer calibration from a random start,
+    and the energy each layer's basis captures against those per-layer
+    calibrations."""
+    import torch
+    L = len(Xs)
+    n, d = Xs[0].shape
+    k = Q0.shape[1]
+    ws = torch.empty(lib.gsi_refine_rank1_workspace_size(n, d, k), dtype=torch.uint8,
+                     device="cuda")
+    out = {"how": "layer 0 by 8 block iterations, then per layer c rank-1 corrections "
+                  "re-orthogonalised by DGKS from the previous layer's basis", "curve": []}
+    prev = None
+    for c in RANK1_CORRECTIONS:
+        Vr = [torch.empty((d, k), dtype=torch.bfloat16, device="cuda") for _ in range(L)]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                lib.gsi_calibrate_cascade_rank1(Xs, Q0, it_first, c, Vr, ws, stream=stream)
+        replay(g, stream, 1)
+        st = lib.gsi_calibrate_status(ws, stream)
+        if st != 0:
+            raise RuntimeError(f"rank-1 cascade status: {lib.gsi_status_string(st)}")
+        ms = max_over_ranks(time_graph(g, stream, reps=steps, warmup=1), world)
+        e = []
+        for layer in range(L):
+            X = Xs[layer].float()
+            e.append(float((X @ Vr[layer].float()).pow(2).sum()) / float((X * X).sum()))
+        short = np.array(e_cold) - np.array(e)
+        pt = {"corrections": c, "ms_per_layer": round(ms / L, 4),
+              "cost_cut_vs_per_layer": round(1.0 - ms / ms_cold, 4),
+              "energy_mean": round(float(np.mean(e)), 6),
+              "max_shortfall_vs_per_layer": round(float(np.max(short[1:])), 6),
+              "launches_per_layer": lib.gsi_refine_rank1_launch_count(n, d, k, c)}
+        if prev is not None:
+            pt["us_per_correction"] = round((ms - prev[1]) / ((L - 1) * (c - prev[0])) * 1e3, 2)
+        prev = (c, ms)
+        out["curve"].append(pt)
+        del g
+    return out
 
 
 def run_reference_cascade(args, world, rank):

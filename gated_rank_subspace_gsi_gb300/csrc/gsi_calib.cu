@@ -145,6 +145,7 @@ __global__ void __launch_bounds__(kGThreads) cal_gram_kernel(const float* __rest
                                                              int d, int cs, float* __restrict__ Gp,
                                                              float* __restrict__ G, int kp,
                                                              CalCtl* __restrict__ ctl,
+                                                             uint32_t* __restrict__ counters,
                                                              int only_if_need2) {
   __shared__ __align__(16) float As[kGChunk][kPtStride];
   __shared__ __align__(16) float Bs[kGChunk][kPtStride];
@@ -218,7 +219,7 @@ __global__ void __launch_bounds__(kGThreads) cal_gram_kernel(const float* __rest
   }
   __threadfence();
   __syncthreads();
-  if (tid == 0) s_last = (atomicAdd(&ctl->counters[p], 1u) == unsigned(S - 1)) ? 1 : 0;
+  if (tid == 0) s_last = (atomicAdd(&counters[p], 1u) == unsigned(S - 1)) ? 1 : 0;
   __syncthreads();
   if (!s_last) return;
   __threadfence();
@@ -227,7 +228,7 @@ __global__ void __launch_bounds__(kGThreads) cal_gram_kernel(const float* __rest
     for (int s2 = 0; s2 < S; ++s2) v += __ldcg(&Gp[(size_t(p) * S + s2) * (kCB * kCB) + e]);
     G[size_t(I * kCB + (e >> 5)) * kp + J * kCB + (e & 31)] = v;
   }
-  if (tid == 0) ctl->counters[p] = 0;
+  if (tid == 0) counters[p] = 0;
 }
 
 // ---- one-CTA blocked Cholesky of D G D + shift I -----------------------------
@@ -630,6 +631,8 @@ __global__ void __launch_bounds__(kAThreads)
   }
 }
 
+#include "gsi_rank1.cuh"
+
 // ---- host side ----------------------------------------------------------------
 
 struct CalLayout {
@@ -734,7 +737,8 @@ gsi_status_t orth_pass(const CalRun& r, const float* Yin, bool first, int only_i
   float* D = r.at<float>(r.lay.D);
   r.tb(kKindGram);
   cudaError_t e = launch_pdl(cal_gram_kernel, dim3(unsigned(np), unsigned(S)), dim3(kGThreads), 0,
-                             r.s, Yin, int(r.k), d, cs, Gp, G, int(r.kp), r.ctl, only_if_need2);
+                             r.s, Yin, int(r.k), d, cs, Gp, G, int(r.kp), r.ctl,
+                             r.ctl->counters, only_if_need2);
   r.te();
   if (e != cudaSuccess) return GSI_ERR_CUDA;
   r.tb(kKindChol);
@@ -976,6 +980,261 @@ gsi_status_t gsi_calibrate_status(const void* workspace, cudaStream_t stream) {
   if (word & kStatusBadLaunch) return GSI_ERR_LAUNCH;
   if (word & kStatusTimeout) return GSI_ERR_TIMEOUT;
   return (word & kStatusRank) ? GSI_ERR_RANK : GSI_OK;
+}
+
+}  // extern "C"
+
+// ---- rank-1 refinement of a start basis (the depth cascade's corrections) --
+
+namespace gsi {
+namespace {
+
+struct R1Layout {
+  CalLayout cal;
+  size_t VP, G2, Gp2, cnt2, ctl, H, pn, cs2, h, r, q, c, w, part, gpart, tick, total;
+  int kp2, nb2, G, ngrp, pstride;
+};
+
+R1Layout r1_layout(int64_t n, int64_t d, int64_t k) {
+  R1Layout o{};
+  o.cal = cal_layout(n, d, k);
+  size_t at = o.cal.total;
+  auto take = [&](size_t bytes) {
+    const size_t here = at;
+    at += (bytes + 255) & ~size_t(255);
+    return here;
+  };
+  o.kp2 = int((2 * k + kCB - 1) / kCB * kCB);
+  o.nb2 = o.kp2 / kCB;
+  o.G = int((d + kRW - 1) / kRW);
+  o.ngrp = (o.G + kRGrp - 1) / kRGrp;
+  o.pstride = int((2 * k + 3 + 3) / 4 * 4);
+  o.VP = take(size_t(2) * k * d * 4);
+  o.G2 = take(size_t(o.kp2) * o.kp2 * 4);
+  o.Gp2 = take(size_t(kMaxGramSlices) * tri(o.nb2) * kCB * kCB * 4);
+  o.cnt2 = take(size_t(tri(o.nb2)) * 4);
+  o.ctl = take(sizeof(R1Ctl));
+  o.H = take(size_t(k) * k * 4);
+  o.pn = take(size_t(k) * 8);
+  o.cs2 = take(size_t(k) * 8);
+  o.h = take(size_t(k) * 4);
+  o.r = take(size_t(d) * 4);
+  o.q = take(size_t(d) * 4);
+  o.c = take(size_t(d) * 4);
+  o.w = take(size_t(n) * 4);
+  o.part = take(size_t(o.G) * o.pstride * 4);
+  o.gpart = take(size_t(o.ngrp) * o.pstride * 4);
+  o.tick = take(size_t(3) * (1 + o.ngrp) * 4);
+  o.total = at;
+  return o;
+}
+
+constexpr int kR1PerCorrection = 6;  // project, subtract, their second DGKS pass, xq, xtw
+
+int r1_launches(int64_t n, int64_t d, int64_t k, int corrections, int sms) {
+  const int start = 1 + 2 * 3;  // transpose of V_in, CholeskyQR2
+  if (corrections == 0) return start + 1;
+  int kb1, kb2;
+  const int S2 = tc_nt_splits(d, k, n, sms, &kb2);
+  (void)tc_nt_splits(n, k, d, sms, &kb1);
+  // X^T, the two products and the first sum, the second sum, Gram of [V; P], init
+  const int prep = 1 + 3 + (S2 > 1 ? 1 : 0) + 1 + 1;
+  return start + prep + kR1PerCorrection * corrections + 1;
+}
+
+gsi_status_t refine_impl(const void* X, int64_t n, int64_t d, int64_t k, const void* V_in,
+                         int corrections, void* V_out, int32_t* order, void* workspace,
+                         size_t workspace_bytes, cudaStream_t stream, bool clear_status) {
+  if (!X || !V_in || !V_out || !workspace || corrections < 0 || corrections > (1 << 20))
+    return GSI_ERR_INVALID_ARG;
+  if (!aligned16(X) || !aligned16(V_in) || !aligned16(V_out) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+      (reinterpret_cast<uintptr_t>(order) & 3u) != 0)
+    return GSI_ERR_INVALID_ARG;
+  if (!cal_shape_ok(n, d, k)) return GSI_ERR_UNSUPPORTED_SHAPE;
+  const R1Layout lay = r1_layout(n, d, k);
+  if (workspace_bytes < lay.total) return GSI_ERR_WORKSPACE;
+  CalRun r;
+  r.n = n;
+  r.d = d;
+  r.k = k;
+  r.kp = (k + kCB - 1) / kCB * kCB;
+  r.nb = r.kp / kCB;
+  r.lay = lay.cal;
+  r.ws = static_cast<unsigned char*>(workspace);
+  r.ctl = r.at<CalCtl>(r.lay.ctl);
+  r.s = stream;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&r.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return GSI_ERR_CUDA;
+  gsi_status_t st = cal_prepare();
+  if (st != GSI_OK) return st;
+  if (clear_status && cudaMemsetAsync(r.ctl, 0, sizeof(CalCtl), stream) != cudaSuccess)
+    return GSI_ERR_CUDA;
+  uint32_t* cnt2 = r.at<uint32_t>(lay.cnt2);
+  if (cudaMemsetAsync(cnt2, 0, size_t(tri(lay.nb2)) * 4, stream) != cudaSuccess ||
+      cudaMemsetAsync(r.at<uint32_t>(lay.tick), 0, size_t(3) * (1 + lay.ngrp) * 4, stream) !=
+          cudaSuccess)
+    return GSI_ERR_CUDA;
+
+  const auto* Xb = static_cast<const __nv_bfloat16*>(X);
+  auto* XT = r.at<__nv_bfloat16>(r.lay.XT);
+  auto* QT = r.at<__nv_bfloat16>(r.lay.QT);
+  auto* ZT = r.at<__nv_bfloat16>(r.lay.ZT);
+  float* P1 = r.at<float>(r.lay.P1);
+  float* Y = r.at<float>(r.lay.Y);
+  float* P2 = r.at<float>(r.lay.P2);
+  float* Q1 = r.at<float>(r.lay.Q1);
+  float* V = r.at<float>(lay.VP);
+  float* P = V + size_t(k) * d;
+  uint32_t* status = &r.ctl->status;
+  const dim3 tb(256);
+
+  R1Args a{};
+  a.V = V;
+  a.P = P;
+  a.H = r.at<float>(lay.H);
+  a.pn = r.at<double>(lay.pn);
+  a.cs2 = r.at<double>(lay.cs2);
+  a.h = r.at<float>(lay.h);
+  a.r = r.at<float>(lay.r);
+  a.q = r.at<float>(lay.q);
+  a.c = r.at<float>(lay.c);
+  a.w = r.at<float>(lay.w);
+  a.part = r.at<float>(lay.part);
+  a.gpart = r.at<float>(lay.gpart);
+  a.tick = r.at<uint32_t>(lay.tick);
+  a.X = Xb;
+  a.XT = XT;
+  a.ctl = r.at<R1Ctl>(lay.ctl);
+  a.status = status;
+  a.order = order;
+  a.n = int(n);
+  a.d = int(d);
+  a.k = int(k);
+  a.G = lay.G;
+  a.ngrp = lay.ngrp;
+  a.pstride = lay.pstride;
+
+  // the start basis: the positive-diagonal QR factor of V_in (CholeskyQR2)
+  {
+    const dim3 g(unsigned((k + 31) / 32), unsigned((d + 31) / 32));
+    const cudaError_t e = launch_pdl(cal_transpose_kernel<float>, g, tb, 0, stream,
+                                     static_cast<const __nv_bfloat16*>(V_in), int(d), int(k), Y);
+    if (e != cudaSuccess) return GSI_ERR_CUDA;
+  }
+  if ((st = orth_pass(r, Y, true, 0, Q1, nullptr, nullptr)) != GSI_OK) return st;
+  if ((st = orth_pass(r, Q1, false, 0, V, corrections > 0 ? QT : nullptr, nullptr)) != GSI_OK)
+    return st;
+
+  const unsigned G = unsigned(lay.G);
+  if (corrections > 0) {
+    // P = C V = X^T (X V) on the tensor cores (V and X V rounded to bf16)
+    const dim3 gx(unsigned((d + 31) / 32), unsigned((n + 31) / 32));
+    cudaError_t e = launch_pdl(cal_transpose_kernel<__nv_bfloat16>, gx, tb, 0, stream, Xb, int(n),
+                               int(d), XT);
+    if (e != cudaSuccess) return GSI_ERR_CUDA;
+    int kb1, kb2;
+    const int S1 = tc_nt_splits(n, k, d, r.sms, &kb1);
+    const int S2 = tc_nt_splits(d, k, n, r.sms, &kb2);
+    const size_t kn = size_t(k) * n, kd = size_t(k) * d;
+    const unsigned sum_grid1 = unsigned(std::min<size_t>(4 * size_t(r.sms), (kn / 4 + 255) / 256));
+    const unsigned sum_grid2 = unsigned(std::min<size_t>(4 * size_t(r.sms), (kd / 4 + 255) / 256));
+    if ((st = tc_nt_gemm(Xb, n, QT, k, d, P1, kn, S1, kb1, status, stream)) != GSI_OK) return st;
+    e = launch_pdl(cal_sum_kernel<__nv_bfloat16>, dim3(std::max(1u, sum_grid1)), tb, 0, stream,
+                   (const float*)P1, S1, kn, kn, ZT);
+    if (e != cudaSuccess) return GSI_ERR_CUDA;
+    if ((st = tc_nt_gemm(XT, d, ZT, k, n, S2 > 1 ? P2 : P, kd, S2, kb2, status, stream)) != GSI_OK)
+      return st;
+    if (S2 > 1) {
+      e = launch_pdl(cal_sum_kernel<float>, dim3(std::max(1u, sum_grid2)), tb, 0, stream,
+                     (const float*)P2, S2, kd, kd, P);
+      if (e != cudaSuccess) return GSI_ERR_CUDA;
+    }
+    // Gram matrix of the stacked block [V; P]: H = V P^T, ||p_i||^2
+    const int np2 = tri(lay.nb2);
+    int S = std::max(1, std::min(kMaxGramSlices, (2 * r.sms + np2 - 1) / np2));
+    S = std::min(S, std::max(1, int(d) / 256));
+    int cs = int((d + S - 1) / S);
+    cs = (cs + kGChunk - 1) / kGChunk * kGChunk;
+    S = int((d + cs - 1) / cs);
+    float* G2 = r.at<float>(lay.G2);
+    e = launch_pdl(cal_gram_kernel, dim3(unsigned(np2), unsigned(S)), dim3(kGThreads), 0, stream,
+                   (const float*)V, int(2 * k), int(d), cs, r.at<float>(lay.Gp2), G2, lay.kp2, r.ctl,
+                   cnt2, 0);
+    if (e != cudaSuccess) return GSI_ERR_CUDA;
+    e = launch_pdl(r1_init_kernel, dim3(1), dim3(kRThreads), 0, stream, a, (const float*)G2,
+                   lay.kp2);
+    if (e != cudaSuccess) return GSI_ERR_CUDA;
+    const unsigned gt = unsigned((n + kRTok - 1) / kRTok);
+    for (int c = 0; c < corrections; ++c) {
+      if (launch_pdl(r1_project_kernel, dim3(G), dim3(kRThreads), 0, stream, a, 0) != cudaSuccess ||
+          launch_pdl(r1_subtract_kernel, dim3(G), dim3(kRThreads), 0, stream, a, 0) != cudaSuccess ||
+          launch_pdl(r1_project_kernel, dim3(G), dim3(kRThreads), 0, stream, a, 1) != cudaSuccess ||
+          launch_pdl(r1_subtract_kernel, dim3(G), dim3(kRThreads), 0, stream, a, 1) != cudaSuccess ||
+          launch_pdl(r1_xq_kernel, dim3(gt), dim3(kRThreads), 0, stream, a) != cudaSuccess ||
+          launch_pdl(r1_xtw_kernel, dim3(G), dim3(kRWideThreads), 0, stream, a) != cudaSuccess)
+        return GSI_ERR_CUDA;
+    }
+  }
+  const cudaError_t e = launch_pdl(r1_finish_kernel, dim3(G), dim3(kRThreads), 0, stream, a,
+                                   corrections > 0 ? 1 : 0, static_cast<__nv_bfloat16*>(V_out));
+  return e == cudaSuccess ? GSI_OK : GSI_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace gsi
+
+extern "C" {
+
+gsi_status_t gsi_refine_rank1_workspace_size(int64_t n, int64_t d, int64_t k, size_t* bytes) {
+  if (!bytes) return GSI_ERR_INVALID_ARG;
+  *bytes = 0;
+  if (!cal_shape_ok(n, d, k)) return GSI_ERR_UNSUPPORTED_SHAPE;
+  *bytes = r1_layout(n, d, k).total;
+  return GSI_OK;
+}
+
+gsi_status_t gsi_refine_rank1(const void* X, int64_t n, int64_t d, int64_t k, const void* V_in,
+                              int corrections, void* V_out, int32_t* order, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream) {
+  return refine_impl(X, n, d, k, V_in, corrections, V_out, order, workspace, workspace_bytes,
+                     stream, true);
+}
+
+gsi_status_t gsi_calibrate_cascade_rank1(const void* const* X, int layers, int64_t n, int64_t d,
+                                         int64_t k, const void* Q0, int iters_first,
+                                         int corrections, void* const* V, int32_t* order,
+                                         void* workspace, size_t workspace_bytes,
+                                         cudaStream_t stream) {
+  if (!X || !V || layers < 1 || corrections < 0) return GSI_ERR_INVALID_ARG;
+  for (int l = 0; l < layers; ++l) {
+    if (!X[l] || !V[l]) return GSI_ERR_INVALID_ARG;
+    for (int m = 0; m < l; ++m)
+      if (V[m] == V[l]) return GSI_ERR_INVALID_ARG;
+  }
+  if (!cal_shape_ok(n, d, k)) return GSI_ERR_UNSUPPORTED_SHAPE;
+  if (workspace_bytes < r1_layout(n, d, k).total) return GSI_ERR_WORKSPACE;
+  gsi_status_t st = calibrate_impl(X[0], n, d, k, Q0, iters_first, V[0], workspace,
+                                   workspace_bytes, stream, nullptr, true);
+  if (st != GSI_OK) return st;
+  for (int l = 1; l < layers; ++l) {
+    int32_t* od = order ? order + size_t(l - 1) * corrections : nullptr;
+    st = refine_impl(X[l], n, d, k, V[l - 1], corrections, V[l], od, workspace, workspace_bytes,
+                     stream, false);
+    if (st != GSI_OK) return st;
+  }
+  return GSI_OK;
+}
+
+int gsi_refine_rank1_launch_count(int64_t n, int64_t d, int64_t k, int corrections) {
+  if (!cal_shape_ok(n, d, k) || corrections < 0) return 0;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return r1_launches(n, d, k, corrections, sms);
 }
 
 }  // extern "C"

@@ -31,7 +31,8 @@ EXPORTS = ("gsi_create", "gsi_forward", "gsi_forward_host", "gsi_precompute_M",
            "gsi_set_prefetch_group", "gsi_group_create", "gsi_group_forward",
            "gsi_group_set_prefetch", "gsi_group_destroy", "gsi_calibrate_workspace_size",
            "gsi_calibrate", "gsi_calibrate_status", "gsi_calibrate_launch_count",
-           "gsi_calibrate_timed", "gsi_calibrate_cascade")
+           "gsi_calibrate_timed", "gsi_calibrate_cascade", "gsi_refine_rank1_workspace_size",
+           "gsi_refine_rank1", "gsi_calibrate_cascade_rank1", "gsi_refine_rank1_launch_count")
 
 _lock = threading.Lock()
 _lib = None
@@ -102,6 +103,18 @@ def _load():
         lib.gsi_calibrate_status.restype = ctypes.c_int
         lib.gsi_calibrate_launch_count.argtypes = [I64, I64, I64, ctypes.c_int]
         lib.gsi_calibrate_launch_count.restype = ctypes.c_int
+        lib.gsi_refine_rank1_workspace_size.argtypes = [I64, I64, I64,
+                                                        ctypes.POINTER(ctypes.c_size_t)]
+        lib.gsi_refine_rank1_workspace_size.restype = ctypes.c_int
+        lib.gsi_refine_rank1.argtypes = [P, I64, I64, I64, P, ctypes.c_int, P, P, P,
+                                         ctypes.c_size_t, P]
+        lib.gsi_refine_rank1.restype = ctypes.c_int
+        lib.gsi_calibrate_cascade_rank1.argtypes = [P, ctypes.c_int, I64, I64, I64, P,
+                                                    ctypes.c_int, ctypes.c_int, P, P, P,
+                                                    ctypes.c_size_t, P]
+        lib.gsi_calibrate_cascade_rank1.restype = ctypes.c_int
+        lib.gsi_refine_rank1_launch_count.argtypes = [I64, I64, I64, ctypes.c_int]
+        lib.gsi_refine_rank1_launch_count.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -357,3 +370,45 @@ def gsi_calibrate_cascade(Xs, Q0, iters_first: int, iters_next: int, Vs, workspa
     _check(_load().gsi_calibrate_cascade(xa, len(Xs), n, d, k, _ptr(Q0), int(iters_first),
                                          int(iters_next), va, _ptr(workspace), nbytes,
                                          _stream(stream)), "gsi_calibrate_cascade")
+
+
+def gsi_refine_rank1_workspace_size(n: int, d: int, k: int) -> int:
+    """Device scratch bytes gsi_refine_rank1 (and the rank-1 cascade) need."""
+    out = ctypes.c_size_t()
+    _check(_load().gsi_refine_rank1_workspace_size(int(n), int(d), int(k), ctypes.byref(out)),
+           "gsi_refine_rank1_workspace_size")
+    return int(out.value)
+
+
+def gsi_refine_rank1(X, V_in, corrections: int, V_out, workspace, order=None, stream=None):
+    """`corrections` rank-1 DGKS corrections of the start basis V_in (d x k
+    bf16) for the tokens X (n x d bf16), into V_out; order (int32 CUDA tensor
+    of `corrections` entries, optional) receives the corrected columns."""
+    n, d = X.shape
+    _, k = V_in.shape
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(_load().gsi_refine_rank1(_ptr(X), n, d, k, _ptr(V_in), int(corrections), _ptr(V_out),
+                                    _ptr(order), _ptr(workspace), nbytes, _stream(stream)),
+           "gsi_refine_rank1")
+
+
+def gsi_calibrate_cascade_rank1(Xs, Q0, iters_first: int, corrections: int, Vs, workspace,
+                                order=None, stream=None):
+    """Depth cascade in rank-1 form: V_0 = gsi_calibrate(Xs[0], Q0,
+    iters_first); V_l = gsi_refine_rank1(Xs[l], V_{l-1}, corrections).  order:
+    optional int32 CUDA tensor of (layers - 1) * corrections entries."""
+    if len(Xs) != len(Vs) or not Xs:
+        raise ValueError("one output basis per layer")
+    n, d = Xs[0].shape
+    _, k = Q0.shape
+    xa = _ptr_array(Xs)
+    va = _ptr_array(Vs)
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(_load().gsi_calibrate_cascade_rank1(xa, len(Xs), n, d, k, _ptr(Q0), int(iters_first),
+                                               int(corrections), va, _ptr(order),
+                                               _ptr(workspace), nbytes, _stream(stream)),
+           "gsi_calibrate_cascade_rank1")
+
+
+def gsi_refine_rank1_launch_count(n: int, d: int, k: int, corrections: int) -> int:
+    return int(_load().gsi_refine_rank1_launch_count(int(n), int(d), int(k), int(corrections)))

@@ -314,6 +314,67 @@ gsi_status_t gsi_calibrate_status(const void *workspace, cudaStream_t stream);
  * device (0 for unsupported shapes). */
 int gsi_calibrate_launch_count(int64_t n, int64_t d, int64_t k, int iters);
 
+/* ---- The depth cascade in rank-1 form ----------------------------------
+ *
+ * Section 2.3 of the page starts layer l + 1's basis from layer l's and
+ * refines it with a few rank-1 corrections (DGKS updates) instead of a full
+ * decomposition per layer.  gsi_refine_rank1 applies `corrections` such
+ * corrections to a start basis V_in for the tokens X (C = X^T X):
+ *   V = the positive-diagonal QR factor of V_in (CholeskyQR2, fp32)
+ *   each correction: j = the column with the largest residual
+ *     ||(I - V V^T) C v_j|| (the first of equals); q = that residual
+ *     re-orthogonalised against V by classical Gram-Schmidt, repeated once
+ *     when the first projection kept less than 1/sqrt(2) of its norm (the
+ *     DGKS test), normalised; v_j <- cos(t) v_j + sin(t) q with
+ *     t = atan2(2 s, a - b) / 2, a = v_j^T C v_j, b = q^T C q,
+ *     s = v_j^T C q: the unit vector of span(v_j, q) with the largest
+ *     Rayleigh quotient.  The update changes one column (rank one), keeps the
+ *     columns orthonormal and never lowers trace(V^T C V).
+ * C V is formed once on the tensor cores (bf16 operands, fp32 accumulation);
+ * each correction's C q is two fp32 products over X on the CUDA cores; the
+ * basis, C V and V^T C V are kept in fp32.  Unlike gsi_calibrate, the result
+ * depends on the basis of V_in inside its span, not on the span alone.
+ *
+ *   X            n x d bf16 tokens (device)
+ *   V_in         d x k bf16 start basis (device), full column rank
+ *   corrections  >= 0 (0 returns the QR factor of V_in rounded to bf16)
+ *   V_out        d x k bf16 output (device); may be V_in
+ *   order        device int32 array of `corrections` entries receiving the
+ *                column corrected at each step, or NULL
+ *   workspace    device scratch of gsi_refine_rank1_workspace_size() bytes,
+ *                256-byte aligned, owned by the caller; it is also a valid
+ *                gsi_calibrate workspace for the same shape
+ * Shapes and the status word as gsi_calibrate (gsi_calibrate_status reads
+ * it; a non-finite residual sets GSI_ERR_RANK).  A correction whose residual
+ * vanishes after re-orthogonalisation (span(V) invariant under C) leaves V as
+ * it is.  Asynchronous on `stream`; allocates nothing; the launch sequence
+ * does not depend on the data (graph-capturable). */
+gsi_status_t gsi_refine_rank1_workspace_size(int64_t n, int64_t d, int64_t k,
+                                             size_t *bytes);
+gsi_status_t gsi_refine_rank1(const void *X, int64_t n, int64_t d, int64_t k,
+                              const void *V_in, int corrections, void *V_out,
+                              int32_t *order, void *workspace,
+                              size_t workspace_bytes, cudaStream_t stream);
+/* The cascade in that form: layer 0 is gsi_calibrate(X[0], ..., Q0,
+ * iters_first, V[0]); layer l > 0 is gsi_refine_rank1(X[l], ..., V[l - 1],
+ * corrections, V[l]).  X and V as in gsi_calibrate_cascade; `order`, if not
+ * NULL, receives (layers - 1) x corrections column indices, layer by layer.
+ * The workspace is gsi_refine_rank1_workspace_size() bytes; the status word
+ * is cleared once, at the start.  Asynchronous on `stream`. */
+gsi_status_t gsi_calibrate_cascade_rank1(const void *const *X, int layers,
+                                         int64_t n, int64_t d, int64_t k,
+                                         const void *Q0, int iters_first,
+                                         int corrections, void *const *V,
+                                         int32_t *order, void *workspace,
+                                         size_t workspace_bytes,
+                                         cudaStream_t stream);
+/* Kernel launches one gsi_refine_rank1 issues (0 for unsupported shapes):
+ * the start basis, C V, and six launches per correction (the two of the
+ * second Gram-Schmidt pass return at once when the test does not ask for
+ * it). */
+int gsi_refine_rank1_launch_count(int64_t n, int64_t d, int64_t k,
+                                  int corrections);
+
 #ifdef __cplusplus
 }
 #endif

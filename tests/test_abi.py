@@ -129,3 +129,43 @@ def test_calibrate_cascade_argument_checks(cl):
     assert cl.gsi_calibrate_cascade(xs, 2, 64, 64, 16, A, 4, 2, vs_same, WS, 1 << 30, None) == 1
     assert cl.gsi_calibrate_cascade(xs, 2, 64, 64, 16, A, 4, 2, vs_null, WS, 1 << 30, None) == 1
     assert cl.gsi_calibrate_cascade(xs, 2, 64, 64, 16, A, 4, -1, vs_same, WS, 1 << 30, None) == 1
+
+
+def test_refine_rank1_argument_checks(cl):
+    """gsi_refine_rank1 and the rank-1 cascade reject bad arguments before any
+    CUDA call (fake pointer values, never dereferenced)."""
+    A = ctypes.c_void_p(0x10000)
+    B = ctypes.c_void_p(0x20000)
+    C = ctypes.c_void_p(0x30000)
+    WS = ctypes.c_void_p(0x100000)
+    size = ctypes.c_size_t()
+    cal = ctypes.c_size_t()
+    assert cl.gsi_refine_rank1_workspace_size(2048, 4096, 256, None) == 1
+    assert cl.gsi_refine_rank1_workspace_size(2048, 4096, 256, ctypes.byref(size)) == 0
+    assert cl.gsi_calibrate_workspace_size(2048, 4096, 256, ctypes.byref(cal)) == 0
+    need = size.value
+    assert need > cal.value + 2 * 256 * 4096 * 4   # V and C V in fp32 beyond the calibration's
+    assert cl.gsi_refine_rank1_workspace_size(2048, 4096, 48, ctypes.byref(size)) == 2
+    assert cl.gsi_refine_rank1(None, 2048, 4096, 256, B, 4, C, None, WS, need, None) == 1
+    assert cl.gsi_refine_rank1(A, 2048, 4096, 256, None, 4, C, None, WS, need, None) == 1
+    assert cl.gsi_refine_rank1(A, 2048, 4096, 256, B, -1, C, None, WS, need, None) == 1
+    assert cl.gsi_refine_rank1(A, 2048, 4096, 256, B, 4, C, ctypes.c_void_p(0x50002), WS, need,
+                               None) == 1                                   # misaligned order
+    assert cl.gsi_refine_rank1(A, 2048, 4096, 256, B, 4, C, None, ctypes.c_void_p(0x100040),
+                               need, None) == 1                             # workspace alignment
+    assert cl.gsi_refine_rank1(A, 2048, 4096, 24, B, 4, C, None, WS, need, None) == 2
+    assert cl.gsi_refine_rank1(A, 2048, 4096, 256, B, 4, C, None, WS, cal.value, None) == 5
+    xs = (ctypes.c_void_p * 2)(0x20000, 0x30000)
+    vs = (ctypes.c_void_p * 2)(0x40000, 0x60000)
+    vs_same = (ctypes.c_void_p * 2)(0x40000, 0x40000)
+    assert cl.gsi_calibrate_cascade_rank1(None, 2, 2048, 4096, 256, A, 8, 4, vs, None, WS, need,
+                                          None) == 1
+    assert cl.gsi_calibrate_cascade_rank1(xs, 0, 2048, 4096, 256, A, 8, 4, vs, None, WS, need,
+                                          None) == 1
+    assert cl.gsi_calibrate_cascade_rank1(xs, 2, 2048, 4096, 256, A, 8, 4, vs_same, None, WS,
+                                          need, None) == 1
+    assert cl.gsi_calibrate_cascade_rank1(xs, 2, 2048, 4096, 256, A, 8, -1, vs, None, WS, need,
+                                          None) == 1
+    assert cl.gsi_calibrate_cascade_rank1(xs, 2, 2048, 4096, 256, A, 8, 4, vs, None, WS,
+                                          cal.value, None) == 5             # needs the rank-1 size
+    assert cl.gsi_refine_rank1_launch_count(2048, 4096, 48, 4) == 0
