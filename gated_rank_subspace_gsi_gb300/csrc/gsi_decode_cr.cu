@@ -340,6 +340,15 @@ __device__ __forceinline__ void cr_body(const CUtensorMap* tmV, const CUtensorMa
         for (uint32_t off = 0; off < bytes_F; off += kChunk)
           bulk_g2s(smem + off, gF + off, min(kChunk, bytes_F - off), &ctl.mbar[1]);
       }
+      // This CTA's share of x (whole 128-byte lines) into L2 before the
+      // dependent-launch wait.  A prefetch reads nothing into the program,
+      // so it is safe while the previous kernel may still be writing x:
+      // those writes land in L2, which every later read of x goes through.
+      const uint32_t xbytes = uint32_t(a.d) * 2u;
+      const uint32_t xshare = max(128u, (xbytes / uint32_t(G) + 127u) & ~127u);
+      const uint32_t xlo = uint32_t(cta) * xshare;
+      if (xlo < xbytes)
+        prefetch_l2(reinterpret_cast<const char*>(a.x) + xlo, min(xshare, xbytes - xlo));
     }
     __syncwarp();
     // Prefetch: once the compute warps are past the exchange, this CTA's
