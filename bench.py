@@ -44,7 +44,7 @@ METRIC = "µs per gated linear & effective HBM GB/s (GPT-J 4096 shapes, B=1) vs 
 UNIT = "us per gated linear"
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
-DECODE_KERNEL = "gsi_decode_cr_kernel<256> + gsi_decode_cr_group_kernel<256>"
+DECODE_KERNEL = "gsi_decode_cr_group_kernel<256> (qkv_fc_in as a group of one; out_proj + fc_out)"
 DECODE_SRC = os.path.join(ROOT, "gated_rank_subspace_gsi_gb300", "csrc", "gsi_decode_cr.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gsi_decode_cr__gptj_layer_traffic.txt")
 
@@ -1853,7 +1853,7 @@ def run_sweep(args, world, rank, local):
                 eps0_us_per_call=round(ms_dense * 1e3 / T, 3),
                 roofline={"bound": "hbm", "achieved": main_pt["gbs"], "peak": peak, "unit": "GB/s",
                           "frac": round(main_pt["gbs"] / peak, 4), "traffic": None,
-                          "kernel": "gsi_decode_cr_kernel<256> (whole call)",
+                          "kernel": "gsi_decode_cr_group_kernel<256> (whole call)",
                           "peak_kind": f"{pkind} HBM copy"},
                 gpu_launches=steps * T * (1 + len(points)), clocks=clk)
     out["data"] = ("synthetic (seeded Gaussian W, power-law activations, planted population "

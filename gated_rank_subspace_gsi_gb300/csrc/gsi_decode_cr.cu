@@ -160,9 +160,6 @@ __host__ __device__ inline CrLay cr_layout(int K, int d, int rowsM, int rowsV) {
   return s;
 }
 
-__device__ __forceinline__ void red_release_u32(uint32_t* p, uint32_t v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
-}
 __device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
 }
@@ -802,13 +799,10 @@ __device__ __forceinline__ void cr_body(const CUtensorMap* tmV, const CUtensorMa
   }
 }
 
-template <int K>
-__global__ void __launch_bounds__(kBlock, 2)
-    gsi_decode_cr_kernel(const __grid_constant__ CUtensorMap tmV,
-                         const __grid_constant__ CUtensorMap tmM, const __grid_constant__ CrArgs a) {
-  cr_body<K>(&tmV, &tmM, a, int(blockIdx.x), int(gridDim.x));
-}
-
+// The one kernel of every one-token call with this K: a single handle's call
+// is a group of one.  (Two kernels alternating in the decode step, one for
+// single calls and one for groups, cost 0.24 us per gated linear more: the
+// SMs ran each phase of code that the other kernel had just displaced.)
 template <int K>
 __global__ void __launch_bounds__(kBlock, 2)
     gsi_decode_cr_group_kernel(const __grid_constant__ CrGroupMaps maps,
@@ -819,17 +813,15 @@ __global__ void __launch_bounds__(kBlock, 2)
              g.cta0[m + 1] - g.cta0[m]);
 }
 
-const void* cr_kernel_for(int64_t k, bool group) {
+const void* cr_kernel_for(int64_t k) {
   switch (k) {
-    case 64: return group ? reinterpret_cast<const void*>(&gsi_decode_cr_group_kernel<64>)
-                          : reinterpret_cast<const void*>(&gsi_decode_cr_kernel<64>);
-    case 128: return group ? reinterpret_cast<const void*>(&gsi_decode_cr_group_kernel<128>)
-                           : reinterpret_cast<const void*>(&gsi_decode_cr_kernel<128>);
-    case 256: return group ? reinterpret_cast<const void*>(&gsi_decode_cr_group_kernel<256>)
-                           : reinterpret_cast<const void*>(&gsi_decode_cr_kernel<256>);
+    case 64: return reinterpret_cast<const void*>(&gsi_decode_cr_group_kernel<64>);
+    case 128: return reinterpret_cast<const void*>(&gsi_decode_cr_group_kernel<128>);
+    case 256: return reinterpret_cast<const void*>(&gsi_decode_cr_group_kernel<256>);
     default: return nullptr;
   }
 }
+
 
 // Row boxes for `rows` owned rows: box rows a multiple of 16 and <= 256.
 void row_boxes(int rows, int* box, int* nbox) {
@@ -953,21 +945,31 @@ cudaLaunchConfig_t launch_config(dim3 grid, size_t smem, cudaStream_t s, bool pd
   return cfg;
 }
 
+// Launch the one-token kernel on `grid` CTAs for a filled argument block.
+gsi_status_t cr_launch(int64_t k, const CrGroupMaps& maps, const CrGroupArgs& ga, int grid,
+                       size_t smem, bool pdl, cudaStream_t s) {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = launch_config(dim3(grid), smem, s, pdl, attr);
+  cudaError_t err;
+  switch (k) {
+    case 64: err = cudaLaunchKernelEx(&cfg, gsi_decode_cr_group_kernel<64>, maps, ga); break;
+    case 128: err = cudaLaunchKernelEx(&cfg, gsi_decode_cr_group_kernel<128>, maps, ga); break;
+    case 256: err = cudaLaunchKernelEx(&cfg, gsi_decode_cr_group_kernel<256>, maps, ga); break;
+    default: return GSI_ERR_UNSUPPORTED_SHAPE;
+  }
+  return err == cudaSuccess ? GSI_OK : GSI_ERR_CUDA;
+}
+
 }  // namespace
 
 size_t decode_cr_acc_floats(int64_t k) { return size_t(2) * kCopies * 2 * size_t(k); }
 
 gsi_status_t decode_cr_configure(gsi_handle* h) {
-  const void* fn = cr_kernel_for(h->k, false);
-  const void* fng = cr_kernel_for(h->k, true);
-  if (!fn || !fng) return GSI_ERR_UNSUPPORTED_SHAPE;
+  const void* fn = cr_kernel_for(h->k);
+  if (!fn) return GSI_ERR_UNSUPPORTED_SHAPE;
   if (h->d > kMaxD) return GSI_ERR_UNSUPPORTED_SHAPE;  // every CTA reads all of x
   int limit = 0;
   gsi_status_t st = smem_limit(fn, h->device, &limit);
-  if (st == GSI_OK) {
-    int limit_g = 0;
-    st = smem_limit(fng, h->device, &limit_g);
-  }
   if (st != GSI_OK) return st;
   const int64_t rows_hint = (std::max(h->d_out, h->d) + 7) / 8 + 1;
   const int G = int(std::max<int64_t>(2, std::min<int64_t>({int64_t(h->num_sms), rows_hint,
@@ -987,27 +989,25 @@ gsi_status_t decode_cr_configure(gsi_handle* h) {
 
 gsi_status_t decode_cr_launch(gsi_handle* h, const void* x, float* y, uint8_t* gate, float* rho,
                               cudaStream_t s) {
-  CrArgs a;
+  CrGroupMaps maps;
+  CrGroupArgs ga;
+  std::memset(&maps, 0, sizeof maps);
+  std::memset(&ga, 0, sizeof ga);
+  std::memcpy(maps.m, h->cr_tmaps, 2 * sizeof(CUtensorMap));
+  ga.n = 1;
+  CrArgs& a = ga.a[0];
   fill_args(&a, h, h->cr_plan, x, y, gate, rho);
   prefetch_ranges(h->pf_next, h->pf_group, a.pf, a.pf_bytes);
   a.pf_part0 = 0;
   a.pf_parts = h->cr_plan.G;
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = launch_config(dim3(h->cr_plan.G), h->cr_plan.smem, s, h->use_pdl, attr);
-  const CUtensorMap* maps = reinterpret_cast<const CUtensorMap*>(h->cr_tmaps);
-  cudaError_t err;
-  switch (h->k) {
-    case 64: err = cudaLaunchKernelEx(&cfg, gsi_decode_cr_kernel<64>, maps[0], maps[1], a); break;
-    case 128: err = cudaLaunchKernelEx(&cfg, gsi_decode_cr_kernel<128>, maps[0], maps[1], a); break;
-    case 256: err = cudaLaunchKernelEx(&cfg, gsi_decode_cr_kernel<256>, maps[0], maps[1], a); break;
-    default: return GSI_ERR_UNSUPPORTED_SHAPE;
-  }
-  return err == cudaSuccess ? GSI_OK : GSI_ERR_CUDA;
+  ga.cta0[0] = 0;
+  for (int m = 1; m <= kMaxGroup; ++m) ga.cta0[m] = h->cr_plan.G;
+  return cr_launch(h->k, maps, ga, h->cr_plan.G, h->cr_plan.smem, h->use_pdl, s);
 }
 
 gsi_status_t group_configure(gsi_group* g) {
   const gsi_handle* h0 = g->h[0];
-  const void* fn = cr_kernel_for(h0->k, true);
+  const void* fn = cr_kernel_for(h0->k);
   if (!fn) return GSI_ERR_UNSUPPORTED_SHAPE;
   int limit = 0;
   gsi_status_t st = smem_limit(fn, h0->device, &limit);
@@ -1071,16 +1071,7 @@ gsi_status_t group_launch(gsi_group* g, const void* const* x, float* const* y,
   }
   for (int m = 0; m <= g->n; ++m) ga.cta0[m] = g->cta0[m];
   for (int m = g->n + 1; m <= kMaxGroup; ++m) ga.cta0[m] = g->cta0[g->n];
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = launch_config(dim3(g->cta0[g->n]), g->smem, s, true, attr);
-  cudaError_t err;
-  switch (g->k) {
-    case 64: err = cudaLaunchKernelEx(&cfg, gsi_decode_cr_group_kernel<64>, maps, ga); break;
-    case 128: err = cudaLaunchKernelEx(&cfg, gsi_decode_cr_group_kernel<128>, maps, ga); break;
-    case 256: err = cudaLaunchKernelEx(&cfg, gsi_decode_cr_group_kernel<256>, maps, ga); break;
-    default: return GSI_ERR_UNSUPPORTED_SHAPE;
-  }
-  return err == cudaSuccess ? GSI_OK : GSI_ERR_CUDA;
+  return cr_launch(g->k, maps, ga, g->cta0[g->n], g->smem, true, s);
 }
 
 }  // namespace gsi
