@@ -1603,7 +1603,8 @@ def run_cascade(args, world, rank, local):
     launches = (lib.gsi_calibrate_launch_count(n, d, k, it_first)
                 + (L - 1) * lib.gsi_calibrate_launch_count(n, d, k, it_next))
     rank1 = cascade_rank1_curve(lib, Xs, Q0, it_first, stream=stream, world=world,
-                                e_cold=e_p, ms_cold=ms_cold, steps=steps)
+                                e_cold=e_p, ms_cold=ms_cold, steps=steps,
+                                counts=[int(c) for c in args.rank1.split(",") if c.strip()])
     out = _line(CASC_METRIC, round(ms / L, 4), "ms per layer", world, steps, args.warmup, ms,
                 {"workload": casc_workload(L, n, d, k, it_first, it_next),
                  "l2": f"inputs larger than L2: {L} layers x {n * d * 2 / 2**20:.0f} MiB of tokens",
@@ -1663,7 +1664,7 @@ RANK1_CORRECTIONS = (16, 64, 256)
 
 
 def cascade_rank1_curve(lib, Xs, Q0, it_first, stream, world, e_cold, ms_cold,
-                        steps):
+                        steps, counts=RANK1_CORRECTIONS):
     """The cascade in the page's rank-1 form (gsi_calibrate_cascade_rank1) on
     the same layers, for a few correction counts: ms per layer (graph
     replays), the cost cut against per-layer calibration from a random start,
@@ -1678,7 +1679,7 @@ def cascade_rank1_curve(lib, Xs, Q0, it_first, stream, world, e_cold, ms_cold,
     out = {"how": "layer 0 by 8 block iterations, then per layer c rank-1 corrections "
                   "re-orthogonalised by DGKS from the previous layer's basis", "curve": []}
     prev = None
-    for c in RANK1_CORRECTIONS:
+    for c in counts:
         Vr = [torch.empty((d, k), dtype=torch.bfloat16, device="cuda") for _ in range(L)]
         g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
@@ -1925,6 +1926,8 @@ def main(argv=None):
                          "(NCCL all_gather of y after every call) instead of running replicas")
     ap.add_argument("--no-configs", action="store_true",
                     help="report the decode layer only (without the other configurations)")
+    ap.add_argument("--rank1", default=",".join(str(c) for c in RANK1_CORRECTIONS),
+                    help="cascade_gptj: rank-1 corrections per layer to measure (comma list)")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the per-linear breakdown and the end-to-end leg (profiling runs)")
     args = ap.parse_args(argv)
