@@ -6,10 +6,10 @@
 //   2. gate         ||r_t||^2 = ||x_t||^2 - 2 g_t.g_t + g_t^T Gm g_t with
 //                   Gm = V_k^T V_k (exact identity for r = x - V_k g),
 //                   rho_t = ||r_t|| / ||x_t||, gate_t = !(rho_t < eps)
-//   3. compaction   stable partition of 0..T-1 by gate into index lists
-//   4. gather       fast tokens' g_t (as bf16 hi + lo pairs) and slow tokens'
-//                   x_t into dense operand blocks
-//   5. GEMMs        Y_fast = G_fast M^T and Y_slow = X_slow W^T on the
+//   3. partition    stable partition of 0..T-1 by gate into index lists, and
+//      + gather     fast tokens' g_t (as bf16 hi + lo pairs) and slow tokens'
+//                   x_t into dense operand blocks, in one launch
+//   4. GEMMs        Y_fast = G_fast M^T and Y_slow = X_slow W^T on the
 //                   tcgen05 tensor cores (gsi_tc_gemm.cu), each output row
 //                   scattered back to its token's row of y.
 // Counts of fast and slow tokens stay on the device; GEMM CTAs whose token
@@ -331,88 +331,69 @@ __global__ void __launch_bounds__(256) transpose_kernel(const __nv_bfloat16* __r
   }
 }
 
-// Stable partition of token indices by gate; one CTA of 1024 threads.
-__global__ void __launch_bounds__(1024) compact_kernel(const uint8_t* __restrict__ gate, int T,
-                                                       int32_t* __restrict__ idx_fast,
-                                                       int32_t* __restrict__ idx_slow,
-                                                       int32_t* __restrict__ count) {
-  __shared__ int s_warp[32];
-  __shared__ int s_base;
-  pdl_launch_dependents();
-  pdl_wait();
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) s_base = 0;
-  __syncthreads();
-  for (int c0 = 0; c0 < T; c0 += 1024) {
-    const int t = c0 + tid;
-    const int flag = (t < T) ? int(gate[t] != 0) : 0;
-    // inclusive warp scan of slow flags
-    int v = flag;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int n = __shfl_up_sync(0xFFFFFFFFu, v, o);
-      if (lane >= o) v += n;
-    }
-    if (lane == 31) s_warp[warp] = v;
-    __syncthreads();
-    if (warp == 0) {
-      int w = s_warp[lane];
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(0xFFFFFFFFu, w, o);
-        if (lane >= o) w += n;
-      }
-      s_warp[lane] = w;  // inclusive prefix over warps
-    }
-    __syncthreads();
-    const int before_warp = warp ? s_warp[warp - 1] : 0;
-    const int slow_before = s_base + before_warp + v - flag;  // exclusive, global
-    if (t < T) {
-      if (flag) idx_slow[slow_before] = t;
-      else idx_fast[t - slow_before] = t;
-    }
-    __syncthreads();
-    if (tid == 0) s_base += s_warp[31];
-    __syncthreads();
-  }
-  if (tid == 0) {
-    count[0] = T - s_base;  // n_fast
-    count[1] = s_base;      // n_slow
-    count[2] = 0;           // the GEMM's tile queue starts empty
-  }
-}
-
-// Gather: fast tokens -> row j of the G_fast planes, hi = bf16(g) in plane 0
-// and lo = bf16(g - hi) in plane 1 (hi + lo carries g to ~2^-16 relative);
-// slow tokens -> X_slow rows (bf16 copies of x).  One CTA per token.
+// Partition and gather in one launch, one CTA per token t.  The CTA counts
+// the slow gates before t (every CTA reads the T gate bytes), which places t
+// in the stable partition [fast tokens | slow tokens]:
+//   fast: row pos = t - (slow before t) of the G_fast planes, hi = bf16(g) in
+//         plane 0 and lo = bf16(g - hi) in plane 1 (hi + lo carries g to
+//         ~2^-16 relative), and idx_fast[pos] = t;
+//   slow: row pos = (slow before t) of X_slow (a bf16 copy of x), and
+//         idx_slow[pos] = t.
+// CTA 0 also writes the counts and empties the GEMM's tile queue.
 template <int K>
-__global__ void __launch_bounds__(256) gather_kernel(const __nv_bfloat16* __restrict__ x,
-                                                     const float* __restrict__ G,
-                                                     const uint8_t* __restrict__ gate,
-                                                     const int32_t* __restrict__ idx_fast,
-                                                     const int32_t* __restrict__ idx_slow,
-                                                     const int32_t* __restrict__ count, int d,
-                                                     int max_T, __nv_bfloat16* __restrict__ Gf,
-                                                     __nv_bfloat16* __restrict__ Xs) {
+__global__ void __launch_bounds__(256) partition_gather_kernel(
+    const __nv_bfloat16* __restrict__ x, const float* __restrict__ G,
+    const uint8_t* __restrict__ gate, int T, int d, int max_T, int32_t* __restrict__ idx_fast,
+    int32_t* __restrict__ idx_slow, int32_t* __restrict__ count, __nv_bfloat16* __restrict__ Gf,
+    __nv_bfloat16* __restrict__ Xs) {
+  __shared__ int s_red[2][8];
   pdl_launch_dependents();
   pdl_wait();
-  const int j = blockIdx.x;  // position in the concatenated [fast | slow] list
-  const int n_fast = count[0], n_slow = count[1];
-  if (j < n_fast) {
-    const int t = idx_fast[j];
-    for (int a = threadIdx.x; a < K; a += blockDim.x) {
+  const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int before = 0, total = 0;
+  for (int i = tid; i < T; i += blockDim.x) {
+    const int f = gate[i] != 0;
+    total += f;
+    if (i < t) before += f;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    before += __shfl_xor_sync(0xFFFFFFFFu, before, o);
+    total += __shfl_xor_sync(0xFFFFFFFFu, total, o);
+  }
+  if (lane == 0) {
+    s_red[0][warp] = before;
+    s_red[1][warp] = total;
+  }
+  __syncthreads();
+  before = 0;
+  total = 0;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    before += s_red[0][w];
+    total += s_red[1][w];
+  }
+  if (t == 0 && tid == 0) {
+    count[0] = T - total;  // n_fast
+    count[1] = total;      // n_slow
+    count[2] = 0;          // the GEMM's tile queue starts empty
+  }
+  if (gate[t] == 0) {
+    const int pos = t - before;
+    if (tid == 0) idx_fast[pos] = t;
+    for (int a = tid; a < K; a += blockDim.x) {
       const float g = G[size_t(t) * K + a];
       const __nv_bfloat16 hi = __float2bfloat16_rn(g);
       const __nv_bfloat16 lo = __float2bfloat16_rn(g - __bfloat162float(hi));
-      Gf[size_t(j) * K + a] = hi;
-      Gf[(size_t(max_T) + j) * K + a] = lo;
+      Gf[size_t(pos) * K + a] = hi;
+      Gf[(size_t(max_T) + pos) * K + a] = lo;
     }
-  } else if (j < n_fast + n_slow) {
-    const int js = j - n_fast;
-    const int t = idx_slow[js];
+  } else {
+    const int pos = before;
+    if (tid == 0) idx_slow[pos] = t;
     const uint4* src = reinterpret_cast<const uint4*>(x + size_t(t) * d);
-    uint4* dst = reinterpret_cast<uint4*>(Xs + size_t(js) * d);
-    for (int i = threadIdx.x; i < d / 8; i += blockDim.x) dst[i] = src[i];
+    uint4* dst = reinterpret_cast<uint4*>(Xs + size_t(pos) * d);
+    for (int i = tid; i < d / 8; i += blockDim.x) dst[i] = src[i];
   }
 }
 
@@ -449,10 +430,9 @@ gsi_status_t launch_front(gsi_handle* h, const void* x, int T, uint8_t* gate, fl
     gate_kernel<K><<<(T + kGateTok - 1) / kGateTok, 256, 0, s>>>(h->bG, h->bsx, h->gram, T, h->eps,
                                                                  h->bgate, gate, rho);
   }
-  if (launch_pdl(compact_kernel, dim3(1), dim3(1024), 0, s, h->bgate, T, h->bidx_fast,
-                 h->bidx_slow, h->bcount) != cudaSuccess ||
-      launch_pdl(gather_kernel<K>, dim3(T), dim3(256), 0, s, xb, h->bG, h->bgate, h->bidx_fast,
-                 h->bidx_slow, h->bcount, int(h->d), int(h->max_T), h->bGf, h->bXs) != cudaSuccess)
+  if (launch_pdl(partition_gather_kernel<K>, dim3(T), dim3(256), 0, s, xb, h->bG, h->bgate, T,
+                 int(h->d), int(h->max_T), h->bidx_fast, h->bidx_slow, h->bcount, h->bGf,
+                 h->bXs) != cudaSuccess)
     return GSI_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? GSI_OK : GSI_ERR_CUDA;
 }
@@ -514,7 +494,7 @@ void batched_bind_workspace(gsi_handle* h, void* base, int64_t max_T) {
 
 int batched_launch_count(const gsi_handle* h, int64_t T) {
   (void)h;
-  return T > 1 ? 4 + tc_gemm_launch_count() : 0;
+  return T > 1 ? 3 + tc_gemm_launch_count() : 0;
 }
 
 gsi_status_t batched_prepare(gsi_handle* h) {

@@ -169,7 +169,7 @@ __device__ __forceinline__ Tile decode_tile(int t, int n_slow_tiles, int n_mt, i
 }
 
 // Persistent: one CTA per SM takes tiles from a device-wide counter (zeroed
-// by the compaction kernel) until none are left.  Warp 0 (one lane) takes
+// by the partition-and-gather kernel) until none are left.  Warp 0 (one lane) takes
 // each tile, publishes it to the other roles through a two-slot queue in
 // shared memory, and streams its operands through a 4-stage TMA ring that runs
 // on across tiles; warp 1 (one lane) issues the tile's MMAs into one of two
