@@ -762,7 +762,9 @@ gsi_status_t cal_prepare() {
   if (cudaFuncSetAttribute(cal_chol_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            int(chol_smem_bytes(kCalMaxNb))) != cudaSuccess ||
       cudaFuncSetAttribute(cal_apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           int(apply_smem_bytes(kCalMaxNb))) != cudaSuccess)
+                           int(apply_smem_bytes(kCalMaxNb))) != cudaSuccess ||
+      cudaFuncSetAttribute(r1_persistent_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (kRMaxK * (kRW + 1) + kRMaxVec) * 4) != cudaSuccess)
     return GSI_ERR_CUDA;
   const gsi_status_t st = tc_nt_prepare();
   if (st != GSI_OK) return st;
@@ -991,8 +993,8 @@ namespace {
 
 struct R1Layout {
   CalLayout cal;
-  size_t VP, G2, Gp2, cnt2, ctl, H, pn, cs2, h, r, q, c, w, part, gpart, tick, total;
-  int kp2, nb2, G, ngrp, pstride;
+  size_t VP, G2, Gp2, cnt2, ctl, H, pn, cs2, h, r, q, c, w, part, tot, tick, total;
+  int kp2, nb2, G, pstride;
 };
 
 R1Layout r1_layout(int64_t n, int64_t d, int64_t k) {
@@ -1007,7 +1009,6 @@ R1Layout r1_layout(int64_t n, int64_t d, int64_t k) {
   o.kp2 = int((2 * k + kCB - 1) / kCB * kCB);
   o.nb2 = o.kp2 / kCB;
   o.G = int((d + kRW - 1) / kRW);
-  o.ngrp = (o.G + kRGrp - 1) / kRGrp;
   o.pstride = int((2 * k + 3 + 3) / 4 * 4);
   o.VP = take(size_t(2) * k * d * 4);
   o.G2 = take(size_t(o.kp2) * o.kp2 * 4);
@@ -1023,13 +1024,11 @@ R1Layout r1_layout(int64_t n, int64_t d, int64_t k) {
   o.c = take(size_t(d) * 4);
   o.w = take(size_t(n) * 4);
   o.part = take(size_t(o.G) * o.pstride * 4);
-  o.gpart = take(size_t(o.ngrp) * o.pstride * 4);
-  o.tick = take(size_t(3) * (1 + o.ngrp) * 4);
+  o.tot = take(size_t(o.pstride) * 4);
+  o.tick = take(2 * 4);  // [0] the init kernel's ticket, [1] the grid barrier's counter
   o.total = at;
   return o;
 }
-
-constexpr int kR1PerCorrection = 6;  // project, subtract, their second DGKS pass, xq, xtw
 
 int r1_launches(int64_t n, int64_t d, int64_t k, int corrections, int sms) {
   const int start = 1 + 2 * 3;  // transpose of V_in, CholeskyQR2
@@ -1039,7 +1038,7 @@ int r1_launches(int64_t n, int64_t d, int64_t k, int corrections, int sms) {
   (void)tc_nt_splits(n, k, d, sms, &kb1);
   // X^T, the two products and the first sum, the second sum, Gram of [V; P], init
   const int prep = 1 + 3 + (S2 > 1 ? 1 : 0) + 1 + 1;
-  return start + prep + kR1PerCorrection * corrections + 1;
+  return start + prep + 1;  // + the persistent launch (all corrections, then V_out)
 }
 
 gsi_status_t refine_impl(const void* X, int64_t n, int64_t d, int64_t k, const void* V_in,
@@ -1052,6 +1051,7 @@ gsi_status_t refine_impl(const void* X, int64_t n, int64_t d, int64_t k, const v
       (reinterpret_cast<uintptr_t>(order) & 3u) != 0)
     return GSI_ERR_INVALID_ARG;
   if (!cal_shape_ok(n, d, k)) return GSI_ERR_UNSUPPORTED_SHAPE;
+  if (corrections > 0 && std::max(n, d) > kRMaxVec) return GSI_ERR_UNSUPPORTED_SHAPE;
   const R1Layout lay = r1_layout(n, d, k);
   if (workspace_bytes < lay.total) return GSI_ERR_WORKSPACE;
   CalRun r;
@@ -1074,7 +1074,7 @@ gsi_status_t refine_impl(const void* X, int64_t n, int64_t d, int64_t k, const v
     return GSI_ERR_CUDA;
   uint32_t* cnt2 = r.at<uint32_t>(lay.cnt2);
   if (cudaMemsetAsync(cnt2, 0, size_t(tri(lay.nb2)) * 4, stream) != cudaSuccess ||
-      cudaMemsetAsync(r.at<uint32_t>(lay.tick), 0, size_t(3) * (1 + lay.ngrp) * 4, stream) !=
+      cudaMemsetAsync(r.at<uint32_t>(lay.tick), 0, 2 * 4, stream) !=
           cudaSuccess)
     return GSI_ERR_CUDA;
 
@@ -1103,8 +1103,7 @@ gsi_status_t refine_impl(const void* X, int64_t n, int64_t d, int64_t k, const v
   a.c = r.at<float>(lay.c);
   a.w = r.at<float>(lay.w);
   a.part = r.at<float>(lay.part);
-  a.gpart = r.at<float>(lay.gpart);
-  a.tick = r.at<uint32_t>(lay.tick);
+  a.tot = r.at<float>(lay.tot);
   a.X = Xb;
   a.XT = XT;
   a.ctl = r.at<R1Ctl>(lay.ctl);
@@ -1114,7 +1113,6 @@ gsi_status_t refine_impl(const void* X, int64_t n, int64_t d, int64_t k, const v
   a.d = int(d);
   a.k = int(k);
   a.G = lay.G;
-  a.ngrp = lay.ngrp;
   a.pstride = lay.pstride;
 
   // the start basis: the positive-diagonal QR factor of V_in (CholeskyQR2)
@@ -1164,22 +1162,25 @@ gsi_status_t refine_impl(const void* X, int64_t n, int64_t d, int64_t k, const v
                    (const float*)V, int(2 * k), int(d), cs, r.at<float>(lay.Gp2), G2, lay.kp2, r.ctl,
                    cnt2, 0);
     if (e != cudaSuccess) return GSI_ERR_CUDA;
-    e = launch_pdl(r1_init_kernel, dim3(1), dim3(kRThreads), 0, stream, a, (const float*)G2,
-                   lay.kp2);
+    e = launch_pdl(r1_init_kernel, dim3(unsigned((k + kRThreads / 32 - 1) / (kRThreads / 32))),
+                   dim3(kRThreads), 0, stream, a, (const float*)G2, lay.kp2,
+                   r.at<uint32_t>(lay.tick));
     if (e != cudaSuccess) return GSI_ERR_CUDA;
-    const unsigned gt = unsigned((n + kRTok - 1) / kRTok);
-    for (int c = 0; c < corrections; ++c) {
-      if (launch_pdl(r1_project_kernel, dim3(G), dim3(kRThreads), 0, stream, a, 0) != cudaSuccess ||
-          launch_pdl(r1_subtract_kernel, dim3(G), dim3(kRThreads), 0, stream, a, 0) != cudaSuccess ||
-          launch_pdl(r1_project_kernel, dim3(G), dim3(kRThreads), 0, stream, a, 1) != cudaSuccess ||
-          launch_pdl(r1_subtract_kernel, dim3(G), dim3(kRThreads), 0, stream, a, 1) != cudaSuccess ||
-          launch_pdl(r1_xq_kernel, dim3(gt), dim3(kRThreads), 0, stream, a) != cudaSuccess ||
-          launch_pdl(r1_xtw_kernel, dim3(G), dim3(kRWideThreads), 0, stream, a) != cudaSuccess)
-        return GSI_ERR_CUDA;
-    }
+    // every correction in one launch whose CTAs wait on one another at grid
+    // barriers: all of them must be resident at once
+    const size_t dyn = (size_t(k) * (kRW + 1) + size_t(std::max(n, d))) * 4;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, r1_persistent_kernel, kRThreads,
+                                                      dyn) != cudaSuccess)
+      return GSI_ERR_CUDA;
+    if (per_sm < 1) return GSI_ERR_UNSUPPORTED_SHAPE;
+    const unsigned grid = unsigned(std::min<int64_t>(lay.G, int64_t(per_sm) * r.sms));
+    e = launch_pdl(r1_persistent_kernel, dim3(grid), dim3(kRThreads), dyn, stream, a, corrections,
+                   r.at<uint32_t>(lay.tick) + 1, static_cast<__nv_bfloat16*>(V_out));
+    return e == cudaSuccess ? GSI_OK : GSI_ERR_CUDA;
   }
-  const cudaError_t e = launch_pdl(r1_finish_kernel, dim3(G), dim3(kRThreads), 0, stream, a,
-                                   corrections > 0 ? 1 : 0, static_cast<__nv_bfloat16*>(V_out));
+  const cudaError_t e = launch_pdl(r1_finish_kernel, dim3(G), dim3(kRThreads), 0, stream, a, 0,
+                                   static_cast<__nv_bfloat16*>(V_out));
   return e == cudaSuccess ? GSI_OK : GSI_ERR_CUDA;
 }
 

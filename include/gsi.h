@@ -345,7 +345,9 @@ int gsi_calibrate_launch_count(int64_t n, int64_t d, int64_t k, int iters);
  *                256-byte aligned, owned by the caller; it is also a valid
  *                gsi_calibrate workspace for the same shape
  * Shapes and the status word as gsi_calibrate (gsi_calibrate_status reads
- * it; a non-finite residual sets GSI_ERR_RANK).  A correction whose residual
+ * it; a non-finite residual sets GSI_ERR_RANK); with corrections > 0, also
+ * n <= 32768 and d <= 32768 (one of their vectors is staged whole in shared
+ * memory), else GSI_ERR_UNSUPPORTED_SHAPE.  A correction whose residual
  * vanishes after re-orthogonalisation (span(V) invariant under C) leaves V as
  * it is.  Asynchronous on `stream`; allocates nothing; the launch sequence
  * does not depend on the data (graph-capturable). */
@@ -369,9 +371,9 @@ gsi_status_t gsi_calibrate_cascade_rank1(const void *const *X, int layers,
                                          size_t workspace_bytes,
                                          cudaStream_t stream);
 /* Kernel launches one gsi_refine_rank1 issues (0 for unsupported shapes):
- * the start basis, C V, and six launches per correction (the two of the
- * second Gram-Schmidt pass return at once when the test does not ask for
- * it). */
+ * the start basis, C V, and one persistent launch that runs every correction
+ * (its CTAs are all resident at once and meet at bounded grid barriers; a
+ * barrier that runs out sets GSI_ERR_TIMEOUT and leaves V_out unwritten). */
 int gsi_refine_rank1_launch_count(int64_t n, int64_t d, int64_t k,
                                   int corrections);
 

@@ -254,8 +254,10 @@ def test_cascade_rank1_matches_oracle(gsi, cal):
 
 
 def test_refine_launch_count(gsi):
+    """All corrections run in one persistent launch: the count does not grow
+    with the number of corrections."""
     n, d, k = 512, 256, 32
     base = gsi.gsi_refine_rank1_launch_count(n, d, k, 0)
     one = gsi.gsi_refine_rank1_launch_count(n, d, k, 1)
-    assert base > 0
-    assert gsi.gsi_refine_rank1_launch_count(n, d, k, 5) - one == 4 * 6
+    assert 0 < base < one
+    assert gsi.gsi_refine_rank1_launch_count(n, d, k, 500) == one
