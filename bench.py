@@ -327,6 +327,17 @@ def record_step(layer, n_tokens, replicas, stream, handles_subset=None, host=Non
         r = t % replicas
         if groups is not None:
             sl = slice(t, t + 1)
+            if host is not None:  # host buffers: the C ABI's host-buffer entries
+                if 0 in idx:
+                    H = host[0]
+                    lib.gsi_forward_host(layer[0]["reps"][r][2], H["x"][sl], H["yp"][t],
+                                         H["gp"][t], H["rp"][t], stream)
+                if 1 in idx or 2 in idx:
+                    Hs = host[1:]
+                    lib.gsi_group_forward_host(groups[r], [H["x"][sl] for H in Hs],
+                                               [H["yp"][t] for H in Hs], [H["gp"][t] for H in Hs],
+                                               [H["rp"][t] for H in Hs], stream)
+                continue
             if 0 in idx:
                 L0 = layer[0]
                 lib.gsi_forward(L0["reps"][r][2], L0["x"][sl], L0["y"][sl], L0["gate"][sl],
@@ -510,8 +521,9 @@ def run_gsi(args, world, rank, local):
         h2d += n_tokens * s_.d * 2
         d2h += n_tokens * (s_.d_out * 4 + 5)
     if host:
-        link_schedule(layer, groups, replicas, "sequential", args.prefetch)
-        gc_ = capture_step(layer, n_tokens, replicas, stream, host=host)
+        link_schedule(layer, groups, replicas, args.schedule, args.prefetch)
+        gc_ = capture_step(layer, n_tokens, replicas, stream, host=host,
+                           groups=groups if args.schedule == "grouped" else None)
         for H in host:
             H["buf"].fill_(0xEE)
         ms_call = max_over_ranks(time_graph(gc_, stream, reps=max(3, args.steps // 10), warmup=2),
@@ -590,10 +602,11 @@ def run_gsi(args, world, rank, local):
             "unit": UNIT,
             "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
-            "how": "every call through gsi_forward_host (the C ABI's host-buffer entry) on "
-                   "page-locked host buffers: the one-token kernel reads x and writes y, rho and "
-                   "gate in place over the host link (no copy nodes), sequential schedule (the "
-                   "grouped launch has no host-buffer form), graph-captured",
+            "how": "every call through the C ABI's host-buffer entries (gsi_forward_host, "
+                   "gsi_group_forward_host) on page-locked host buffers, in the same schedule "
+                   "as the device step: a one-CTA-per-call kernel brings x over the host link "
+                   "into device staging and the one-token kernel writes y, rho and gate in place "
+                   "(no copy nodes), graph-captured",
             "copies_per_call": 0,
             "bulk_copies_us_per_linear": None if math.isnan(ms_bulk)
             else round(ms_bulk * 1e3 / n_lin, 4),

@@ -191,10 +191,8 @@ namespace {
 // kernel reads x from every CTA, which is cheap from device memory (L2) and
 // dear over the host link.  Launched with programmatic dependent launch, so
 // the next kernel's CTAs stage their weights while it runs.
-__global__ void __launch_bounds__(256) stage_x_kernel(const uint4* __restrict__ src,
-                                                      uint4* __restrict__ dst, int n16) {
-  gsi::pdl_launch_dependents();
-  gsi::pdl_wait();  // x may have been written by the previous kernel
+__device__ __forceinline__ void stage_copy(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                           int n16) {
   constexpr int kPer = 16;
   uint4 v[kPer];
 #pragma unroll
@@ -208,6 +206,26 @@ __global__ void __launch_bounds__(256) stage_x_kernel(const uint4* __restrict__ 
     if (i < n16) dst[i] = v[j];
   }
   for (int i = int(threadIdx.x) + kPer * 256; i < n16; i += 256) dst[i] = src[i];
+}
+
+__global__ void __launch_bounds__(256) stage_x_kernel(const uint4* __restrict__ src,
+                                                      uint4* __restrict__ dst, int n16) {
+  gsi::pdl_launch_dependents();
+  gsi::pdl_wait();  // x may have been written by the previous kernel
+  stage_copy(src, dst, n16);
+}
+
+// The same for the members of a group, one CTA per member.
+struct StageJobs {
+  const uint4* src[gsi::kMaxGroup];
+  uint4* dst[gsi::kMaxGroup];
+  int n16[gsi::kMaxGroup];
+};
+__global__ void __launch_bounds__(256) stage_x_group_kernel(const __grid_constant__ StageJobs j) {
+  gsi::pdl_launch_dependents();
+  gsi::pdl_wait();
+  const int m = blockIdx.x;
+  stage_copy(j.src[m], j.dst[m], j.n16[m]);
 }
 
 // True if the device can address p directly at the same address: page-locked
@@ -383,6 +401,67 @@ gsi_status_t gsi_group_forward(gsi_group_t g, const void* const* x, float* const
         (rho && rho[m] && (reinterpret_cast<uintptr_t>(rho[m]) & 3u)))
       return GSI_ERR_INVALID_ARG;
   return gsi::group_launch(g, x, y, gate, rho, stream);
+}
+
+gsi_status_t gsi_group_forward_host(gsi_group_t g, const void* const* x_host,
+                                    float* const* y_host, uint8_t* const* gate_host,
+                                    float* const* rho_host, cudaStream_t stream) {
+  if (!g || !x_host || !y_host) return GSI_ERR_INVALID_ARG;
+  bool direct = true;
+  for (int m = 0; m < g->n; ++m) {
+    const uint8_t* gm = gate_host ? gate_host[m] : nullptr;
+    const float* rm = rho_host ? rho_host[m] : nullptr;
+    if (!x_host[m] || !y_host[m] || !gsi::aligned16(x_host[m]) ||
+        (rm && (reinterpret_cast<uintptr_t>(rm) & 3u)))
+      return GSI_ERR_INVALID_ARG;
+    direct = direct && gsi::aligned16(y_host[m]) && device_addressable(x_host[m]) &&
+             device_addressable(y_host[m]) && (!gm || device_addressable(gm)) &&
+             (!rm || device_addressable(rm));
+  }
+  const void* xd[gsi::kMaxGroup] = {};
+  for (int m = 0; m < g->n; ++m) xd[m] = g->h[m]->st_dev;
+  if (direct) {
+    StageJobs j;
+    std::memset(&j, 0, sizeof j);
+    for (int m = 0; m < g->n; ++m) {
+      j.src[m] = static_cast<const uint4*>(x_host[m]);
+      j.dst[m] = static_cast<uint4*>(g->h[m]->st_dev);
+      j.n16[m] = int(g->h[m]->d / 8);
+    }
+    if (gsi::launch_pdl(stage_x_group_kernel, dim3(unsigned(g->n)), dim3(256), 0, stream, j) !=
+        cudaSuccess)
+      return GSI_ERR_CUDA;
+    return gsi::group_launch(g, xd, y_host, gate_host, rho_host, stream);
+  }
+  // through each member's staging: x, then y, rho and gate for one token
+  float* yd[gsi::kMaxGroup] = {};
+  float* rd[gsi::kMaxGroup] = {};
+  uint8_t* gd[gsi::kMaxGroup] = {};
+  for (int m = 0; m < g->n; ++m) {
+    gsi_handle* h = g->h[m];
+    char* p = static_cast<char*>(h->st_dev) + (size_t(h->st_T) * h->d * 2 + 255) / 256 * 256;
+    yd[m] = reinterpret_cast<float*>(p);
+    rd[m] = reinterpret_cast<float*>(p + size_t(h->d_out) * 4);
+    gd[m] = reinterpret_cast<uint8_t*>(p + size_t(h->d_out) * 4 + 4);
+    if (cudaMemcpyAsync(h->st_dev, x_host[m], size_t(h->d) * 2, cudaMemcpyHostToDevice, stream) !=
+        cudaSuccess)
+      return GSI_ERR_CUDA;
+  }
+  const gsi_status_t st = gsi::group_launch(g, xd, yd, gd, rd, stream);
+  if (st != GSI_OK) return st;
+  for (int m = 0; m < g->n; ++m) {
+    gsi_handle* h = g->h[m];
+    if (cudaMemcpyAsync(y_host[m], yd[m], size_t(h->d_out) * 4, cudaMemcpyDeviceToHost, stream) !=
+        cudaSuccess)
+      return GSI_ERR_CUDA;
+    if (gate_host && gate_host[m] &&
+        cudaMemcpyAsync(gate_host[m], gd[m], 1, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+      return GSI_ERR_CUDA;
+    if (rho_host && rho_host[m] &&
+        cudaMemcpyAsync(rho_host[m], rd[m], 4, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+      return GSI_ERR_CUDA;
+  }
+  return GSI_OK;
 }
 
 gsi_status_t gsi_group_set_prefetch(gsi_group_t g, gsi_handle_t next) {

@@ -29,6 +29,7 @@ EXPORTS = ("gsi_create", "gsi_forward", "gsi_forward_host", "gsi_precompute_M",
            "gsi_reserve", "gsi_device_status", "gsi_destroy", "gsi_status_string",
            "gsi_forward_launch_count", "gsi_forward_noalloc", "gsi_set_prefetch",
            "gsi_set_prefetch_group", "gsi_group_create", "gsi_group_forward",
+           "gsi_group_forward_host",
            "gsi_group_set_prefetch", "gsi_group_destroy", "gsi_calibrate_workspace_size",
            "gsi_calibrate", "gsi_calibrate_status", "gsi_calibrate_launch_count",
            "gsi_calibrate_timed", "gsi_calibrate_cascade", "gsi_refine_rank1_workspace_size",
@@ -85,6 +86,8 @@ def _load():
         lib.gsi_group_create.restype = ctypes.c_int
         lib.gsi_group_forward.argtypes = [P, P, P, P, P, P]
         lib.gsi_group_forward.restype = ctypes.c_int
+        lib.gsi_group_forward_host.argtypes = [P, P, P, P, P, P]
+        lib.gsi_group_forward_host.restype = ctypes.c_int
         lib.gsi_group_set_prefetch.argtypes = [P, P]
         lib.gsi_group_set_prefetch.restype = ctypes.c_int
         lib.gsi_group_destroy.argtypes = [P]
@@ -235,6 +238,15 @@ def gsi_group_forward(g, xs, ys, gates=None, rhos=None, stream=None):
                                      _ptr_array(gates) if gates is not None else None,
                                      _ptr_array(rhos) if rhos is not None else None,
                                      _stream(stream)), "gsi_group_forward")
+
+
+def gsi_group_forward_host(g, xs, ys, gates=None, rhos=None, stream=None):
+    """gsi_group_forward on host buffers (lists of CPU tensors, page-locked
+    for the copy-free path)."""
+    _check(_load().gsi_group_forward_host(g, _ptr_array(xs), _ptr_array(ys),
+                                          _ptr_array(gates) if gates is not None else None,
+                                          _ptr_array(rhos) if rhos is not None else None,
+                                          _stream(stream)), "gsi_group_forward_host")
 
 
 def gsi_group_set_prefetch(g, next_h):

@@ -181,6 +181,23 @@ gsi_status_t gsi_group_forward(gsi_group_t g, const void *const *x, float *const
                                uint8_t *const *gate, float *const *rho,
                                cudaStream_t stream);
 
+/* gsi_group_forward with host buffers: for member m the same result as
+ * gsi_forward_host(handles[m], x[m], 1, y[m], gate[m], rho[m], stream).
+ * x, y: arrays of n host pointers (x 16-byte aligned); gate, rho: arrays of n
+ * host pointers (entries may be NULL) or NULL.  When every buffer is
+ * page-locked and addressable by the device, one launch of n CTAs copies each
+ * member's x over the host link into that handle's staging, and the grouped
+ * kernel writes y, gate and rho in place: no copy nodes.  Otherwise each x is
+ * copied in and each output copied back through the handles' staging.
+ * Asynchronous on `stream`: the host buffers must stay valid until it has
+ * run.  A member handle must not be used by another call on the GPU at the
+ * same time (its staging is shared). */
+gsi_status_t gsi_group_forward_host(gsi_group_t g, const void *const *x_host,
+                                    float *const *y_host,
+                                    uint8_t *const *gate_host,
+                                    float *const *rho_host,
+                                    cudaStream_t stream);
+
 /* The group's launches prefetch next's operands into L2 (as gsi_set_prefetch;
  * NULL removes the link). */
 gsi_status_t gsi_group_set_prefetch(gsi_group_t g, gsi_handle_t next);

@@ -161,3 +161,39 @@ def test_group_creation_errors(gsi, orc):
     cl.gsi_group_destroy(out)
     for lin in (a, b, c):
         lin.close()
+
+
+@pytest.mark.parametrize("pinned", [True, False])
+def test_group_forward_host_matches_device(gsi, orc, pinned):
+    """gsi_group_forward_host on page-locked buffers (one staging launch, the
+    outputs written in place over the host link) and on pageable buffers
+    (copies through the handles' staging) gives the device call's bits."""
+    import torch
+    shapes = [(4096, 4096, 256), (4096, 16384, 256)]
+    T = 6
+    cases = [_case(do, d, k, T, seed=911 + i) for i, (do, d, k) in enumerate(shapes)]
+    lins = [GpuLinear(gsi, orc, W, b.V_bits, 0.1) for (W, b, _) in cases]
+    try:
+        g = gsi.gsi_group_create([lin.h for lin in lins])
+        try:
+            xs = [to_dev(X) for (_, _, X) in cases]
+            dev = _run_group(gsi, g, lins, xs, T)
+            mk = (lambda t: t.pin_memory()) if pinned else (lambda t: t)
+            hx = [mk(x.cpu()) for x in xs]
+            hy = [mk(torch.full((T, lin.d_out), float("nan"), dtype=torch.float32)) for lin in lins]
+            hg = [mk(torch.full((T,), 7, dtype=torch.uint8)) for _ in lins]
+            hr = [mk(torch.full((T,), -1.0, dtype=torch.float32)) for _ in lins]
+            for t in range(T):
+                gsi.gsi_group_forward_host(g, [x[t:t + 1] for x in hx], [y[t] for y in hy],
+                                           [q[t:t + 1] for q in hg], [r[t:t + 1] for r in hr])
+            torch.cuda.synchronize()
+            for i in range(len(lins)):
+                assert torch.equal(hy[i], dev[i][0].cpu()), i
+                assert torch.equal(hg[i], dev[i][1].cpu()), i
+                assert torch.equal(hr[i].view(torch.int32), dev[i][2].cpu().view(torch.int32)), i
+            _check(gsi, orc, lins, [X for (_, _, X) in cases], dev, "host group")
+        finally:
+            gsi.gsi_group_destroy(g)
+    finally:
+        for lin in lins:
+            lin.close()
