@@ -136,10 +136,12 @@ __global__ void __launch_bounds__(256) gate_kernel(const float* __restrict__ G,
 // kernel's form), with g^T E g on warp-level bf16 MMAs over the handle's
 // correction tiles (upper 16 x 16 tiles of E, MMA operand order, see
 // gsi_internal.h).  All 8 warps load (the projection partials and the x rows
-// are read with many independent loads in flight); warps 0 and 1 then take
-// tokens 0..3 and 4..7: the B operand's 8 columns are those tokens' g as bf16
-// high part and remainder (column 2j + part for token j), so lane (grp, tig)
-// accumulates token tig.
+// are read with many independent loads in flight).  The correction then runs
+// on all 8 warps: warp w takes tokens 4 (w % 2) .. 4 (w % 2) + 3 and every
+// fourth tile (tile index = w / 2 mod 4); the B operand's 8 columns are those
+// tokens' g as bf16 high part and remainder (column 2j + part for token j),
+// so lane (grp, tig) accumulates token tig.  The four warps' partial sums of a
+// token are added in warp order.
 constexpr int kGateMmaTok = 8;
 constexpr int kGateMmaThreads = 256;
 constexpr int kGatePad = 8;  // floats of padding per staged g row (no bank conflicts)
@@ -159,6 +161,7 @@ __global__ void __launch_bounds__(kGateMmaThreads) gate_mma_kernel(
   uint4* sF = reinterpret_cast<uint4*>(smem);                          // [kTiles][32]
   float* sg = reinterpret_cast<float*>(smem + size_t(kTiles) * 512);   // [8][kRow]
   __shared__ float s_sx[kGateMmaTok], s_gg[kGateMmaTok];
+  __shared__ float s_q[4][kGateMmaTok];
   __shared__ uint64_t s_bar;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int grp = lane >> 2, tig = lane & 3;
@@ -242,9 +245,9 @@ __global__ void __launch_bounds__(kGateMmaThreads) gate_mma_kernel(
   }
   const bool ok = mbar_wait_bounded(&s_bar, 0, status);
   __syncthreads();
-  if (warp >= 2) return;  // no further block barrier below
+  const int tg = warp & 1, ts = warp >> 1;  // token group, tile subset
   // B operands of this warp's 4 tokens, one per column block J
-  const float* gb = sg + (warp * 4 + grp / 2) * kRow;
+  const float* gb = sg + (tg * 4 + grp / 2) * kRow;
   const bool low = (grp & 1) != 0;
   uint2 bfr[T16];
 #pragma unroll
@@ -262,7 +265,7 @@ __global__ void __launch_bounds__(kGateMmaThreads) gate_mma_kernel(
   }
   // g^T E g: tile (I, J) contributes g_I . (F_IJ g_J); lane (grp, tig) holds
   // columns 2 tig (high) and 2 tig + 1 (low) of token tig, rows grp, grp + 8
-  const float* gq = sg + (warp * 4 + tig) * kRow;
+  const float* gq = sg + (tg * 4 + tig) * kRow;
   float q = 0.f;
   if (ok) {
 #pragma unroll
@@ -270,6 +273,7 @@ __global__ void __launch_bounds__(kGateMmaThreads) gate_mma_kernel(
       const float gI0 = gq[I * 16 + grp], gI8 = gq[I * 16 + grp + 8];
 #pragma unroll
       for (int J = I; J < T16; ++J) {
+        if ((corr_tile_index(I, J, T16) & 3) != ts) continue;
         float dd[4] = {0.f, 0.f, 0.f, 0.f};
         const uint4 A = sF[corr_tile_index(I, J, T16) * 32 + lane];
         asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
@@ -281,12 +285,15 @@ __global__ void __launch_bounds__(kGateMmaThreads) gate_mma_kernel(
       }
     }
   }
-  // sum over grp (lanes of equal tig)
+  // sum over grp (lanes of equal tig), then over the four tile subsets
   q += __shfl_xor_sync(0xFFFFFFFFu, q, 4);
   q += __shfl_xor_sync(0xFFFFFFFFu, q, 8);
   q += __shfl_xor_sync(0xFFFFFFFFu, q, 16);
-  if (lane < 4) {
-    const int tl = warp * 4 + lane, t = t0 + tl;
+  if (lane < 4) s_q[ts][tg * 4 + lane] = q;
+  __syncthreads();
+  if (tid < kGateMmaTok) {
+    const int tl = tid, t = t0 + tl;
+    q = ((s_q[0][tl] + s_q[1][tl]) + s_q[2][tl]) + s_q[3][tl];
     if (t < T) {
       const float sxv = s_sx[tl];
       float rho;
