@@ -867,9 +867,10 @@ def measure_batched(args, world, rank, local):
         "e2e": {"value": round(ms_e2e * 1e3 / calls, 3), "unit": "us per gated linear call",
                 "h2d_bytes_per_step": calls * T * spec.d * 2,
                 "d2h_bytes_per_step": calls * T * (spec.d_out * 4 + 5),
-                "how": "gsi_forward_host per call (pinned host buffers; y, rho and gate "
-                       "consecutive, so one copy returns them), graph-captured",
-                "copies_per_call": 2},
+                "how": "gsi_forward_host per call on pinned host buffers: x copied in, the "
+                       "kernels write y, rho and gate in place over the host link while "
+                       "they run, graph-captured",
+                "copies_per_call": 1},
         "gpu_launches": steps * calls * launches_per_call,
         "clocks": clk,
     }

@@ -262,10 +262,21 @@ gsi_status_t gsi_forward_host(gsi_handle_t h, const void* x_host, int64_t T, flo
     return gsi_forward(h, xd, 1, y_host, gate_host, rho_host, stream);
   }
   if (T > h->st_T || (T > 1 && T > h->max_T)) return GSI_ERR_WORKSPACE;
-  // staging: x, then y, rho and gate back to back for this T (one copy
-  // returns all three when the caller's buffers are laid out the same way)
   char* p = static_cast<char*>(h->st_dev);
   void* xd = p;
+  // Many tokens in page-locked memory: x is copied in once, and the kernels
+  // write y, gate and rho in place over the host link while the GEMMs run
+  // (no copy of y back)
+  if (gsi::aligned16(y_host) && device_addressable(y_host) &&
+      (!gate_host || device_addressable(gate_host)) && (!rho_host || device_addressable(rho_host)) &&
+      (!rho_host || (reinterpret_cast<uintptr_t>(rho_host) & 3u) == 0)) {
+    if (cudaMemcpyAsync(xd, x_host, size_t(T) * h->d * 2, cudaMemcpyHostToDevice, stream) !=
+        cudaSuccess)
+      return GSI_ERR_CUDA;
+    return gsi_forward(h, xd, T, y_host, gate_host, rho_host, stream);
+  }
+  // staging: x, then y, rho and gate back to back for this T (one copy
+  // returns all three when the caller's buffers are laid out the same way)
   p += (size_t(h->st_T) * h->d * 2 + 255) / 256 * 256;
   const size_t y_bytes = size_t(T) * h->d_out * 4;
   float* yd = reinterpret_cast<float*>(p);

@@ -100,9 +100,12 @@ gsi_status_t gsi_forward(gsi_handle_t h, const void *x, int64_t T, float *y,
  * device staging and the map writes y, gate and rho in place over the host
  * link (NVLink-C2C on Grace systems) -- two kernel launches, no copy nodes,
  * and consecutive calls on one stream chain like device calls.
- * Otherwise: copies x (T x d bf16) to device staging buffers owned by the
- * handle, runs the map, and copies y (T x d_out fp32), gate and rho (either
- * may be NULL) back to the host buffers.  When the three are consecutive in
+ * More tokens with y, gate and rho in such memory: x (T x d bf16) is
+ * copied into the handle's device staging, and the kernels write y, gate and
+ * rho in place over the host link while they run (no copy of y back).
+ * Otherwise: copies x to device staging buffers owned by the handle, runs
+ * the map, and copies y (T x d_out fp32), gate and rho (either may be NULL)
+ * back to the host buffers.  When the three are consecutive in
  * one host allocation -- y, then rho at y_host + T * d_out, then gate at
  * rho_host + T -- one copy returns all of them (two copies per call in all,
  * instead of four).
