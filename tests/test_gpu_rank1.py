@@ -112,6 +112,19 @@ def test_refine_matches_oracle(gsi, cal, n, d, k, c):
     assert e_g > e_0, "the corrections did not raise the captured energy"
 
 
+def test_refine_more_slices_than_ctas(gsi, cal):
+    """d = 8200: 257 slices of 32 columns (the last one ragged), more than the
+    resident grid (at most one 512-thread CTA per SM), so CTAs own several
+    slices and reload each one from memory in every phase."""
+    n, d, k, c = 512, 8200, 32, 12
+    X_bits, V_bits = _start_pair(n, d, k, seed=461)
+    Vg, order, st = _refine(gsi, X_bits, V_bits, c)
+    assert st == 0, gsi.gsi_status_string(st)
+    X, V_in = gi.bf16_bits_to_f64(X_bits), gi.bf16_bits_to_f64(V_bits)
+    _, e_g, _, e_0 = _check_replay(cal, X, V_in, c, Vg, order, f"n={n} d={d} k={k} c={c}")
+    assert e_g > e_0
+
+
 def test_refine_gptj_size(gsi, cal):
     """The GPT-J-shaped refinement the cascade benchmark runs per layer
     (n = 2048 tokens, d = 4096, k = 256), 32 corrections."""
