@@ -13,13 +13,15 @@
 // bf16 planes hi = bf16(g), lo = bf16(g - hi); both accumulate into the same
 // TMEM tile, which keeps g to ~2^-16 relative although the operands are bf16.
 //
-// Persistent CTAs (192 threads, one per SM) take 128-row x 256-token tiles of
-// both GEMMs from a device-side queue, slow tiles first: warp 0 issues TMA
+// Persistent CTAs (192 threads, one per SM) take 128-row x 256-token slow
+// tiles and 128-row x 128-token fast tiles from a device-side queue, slow
+// tiles first: warp 0 issues TMA
 // loads (one elected lane), warp 1 allocates TMEM and issues tcgen05.mma (one
 // elected lane) into one of two 256-column accumulators, warps 2-5 drain the
 // other (tcgen05.ld 32x32b) and scatter each token column to its row of y.
-// A 4-stage mbarrier ring of 128x64 (A) and up to 256x64 (B) bf16 tiles,
-// 128-byte swizzled, runs on across a CTA's tiles.
+// A 4-stage mbarrier ring of 128x64 (A) and up to 256x64 (B: X_slow rows, or
+// 128 rows of each g plane) bf16 tiles, 128-byte swizzled, runs on across a
+// CTA's tiles.
 #include <cuda.h>
 
 #include <algorithm>
@@ -33,7 +35,8 @@ namespace gsi {
 namespace {
 
 constexpr int kBM = 128;           // weight rows per tile (MMA M)
-constexpr int kBN = 256;           // token rows per tile (max MMA N)
+constexpr int kBN = 256;           // slow token rows per tile (max MMA N)
+constexpr int kBNF = 128;          // fast token rows per tile (both g planes in one stage)
 constexpr int kBK = 64;            // K elements per stage (128 bytes of bf16)
 constexpr int kStages = 4;
 constexpr int kABytes = kBM * kBK * 2;   // 16 KiB
@@ -142,10 +145,12 @@ __device__ __forceinline__ void mbar_arrive_cta(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_addr(bar)) : "memory");
 }
 
-// One tile of the two GEMMs: 128 output rows (o0) x up to 256 tokens (j0).
-// Slow tiles come first in the numbering (the long ones start first), then
-// fast tiles; within a kind, consecutive tiles share a token tile and walk the
-// output rows, so their B operand stays in L2.
+// One tile of the two GEMMs: 128 output rows (o0) x up to 256 slow tokens or
+// up to 128 fast tokens (j0).  Slow tiles come first in the numbering (the
+// long ones start first), then fast tiles; within a kind, consecutive tiles
+// share a token tile and walk the output rows, so their B operand stays in
+// L2.  A fast tile's stage holds one A box of M and the same rows of both g
+// planes (hi, lo) beside it, so M is read once per tile.
 struct Tile {
   bool slow;
   int o0, j0, nvalid, N, num_kb, bx1, bx2, b_bytes;
@@ -157,14 +162,17 @@ __device__ __forceinline__ Tile decode_tile(int t, int n_slow_tiles, int n_mt, i
   u.slow = t < n_slow_tiles;
   const int tt = u.slow ? t : t - n_slow_tiles;
   const int mt = tt % n_mt, jt = tt / n_mt;
+  const int bn = u.slow ? kBN : kBNF;
   u.o0 = mt * kBM;
-  u.j0 = jt * kBN;
-  u.nvalid = min(kBN, (u.slow ? n_slow : n_fast) - u.j0);
+  u.j0 = jt * bn;
+  u.nvalid = min(bn, (u.slow ? n_slow : n_fast) - u.j0);
   u.N = (u.nvalid + 15) & ~15;
-  u.num_kb = u.slow ? (a.d + kBK - 1) / kBK : 2 * ((a.k + kBK - 1) / kBK);
+  u.num_kb = u.slow ? (a.d + kBK - 1) / kBK : (a.k + kBK - 1) / kBK;
   u.bx1 = u.N > 192 ? 0 : box_index(u.N);
-  u.bx2 = (u.N > 128 && u.N <= 192) ? box_index(u.N - 128) : -1;
-  u.b_bytes = (box_rows(u.bx1) + (u.bx2 >= 0 ? box_rows(u.bx2) : 0)) * kBK * 2;
+  u.bx2 = (u.slow && u.N > 128 && u.N <= 192) ? box_index(u.N - 128) : -1;
+  // slow: one or two boxes of X_slow; fast: one box of each g plane
+  u.b_bytes = (u.slow ? box_rows(u.bx1) + (u.bx2 >= 0 ? box_rows(u.bx2) : 0)
+                      : 2 * box_rows(u.bx1)) * kBK * 2;
   return u;
 }
 
@@ -193,8 +201,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int n_fast = a.count[0], n_slow = a.count[1];
   const int n_mt = (a.d_out + kBM - 1) / kBM;
   const int n_slow_tiles = n_mt * ((n_slow + kBN - 1) / kBN);
-  const int total = n_slow_tiles + n_mt * ((n_fast + kBN - 1) / kBN);
-  const int kb_half = (a.k + kBK - 1) / kBK;
+  const int total = n_slow_tiles + n_mt * ((n_fast + kBNF - 1) / kBNF);
 
   const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
   unsigned char* tiles = smem_raw + (base - smem_addr(smem_raw));
@@ -242,15 +249,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           unsigned char* sa = tiles + size_t(s) * kStageBytes;
           unsigned char* sb = sa + kABytes;
+          unsigned char* sb2 = sb + box_rows(u.bx1) * kBK * 2;
           mbar_arrive_expect_tx(&full_bar[s], uint32_t(kABytes + u.b_bytes));
-          const int plane = u.slow ? 0 : kb / kb_half;
-          const int kc = (u.slow ? kb : kb % kb_half) * kBK;
-          const CUtensorMap* bm = u.slow ? maps.Xs : (plane ? maps.Glo : maps.Ghi);
-          tma_load_2d(sa, u.slow ? &maps.W : &maps.M, kc, u.o0, &full_bar[s]);
-          tma_load_2d(sb, &bm[u.bx1], kc, u.j0, &full_bar[s]);
-          if (u.bx2 >= 0)
-            tma_load_2d(sb + box_rows(u.bx1) * kBK * 2, &bm[u.bx2], kc, u.j0 + box_rows(u.bx1),
-                        &full_bar[s]);
+          const int kc = kb * kBK;
+          if (u.slow) {
+            tma_load_2d(sa, &maps.W, kc, u.o0, &full_bar[s]);
+            tma_load_2d(sb, &maps.Xs[u.bx1], kc, u.j0, &full_bar[s]);
+            if (u.bx2 >= 0)
+              tma_load_2d(sb2, &maps.Xs[u.bx2], kc, u.j0 + box_rows(u.bx1), &full_bar[s]);
+          } else {
+            tma_load_2d(sa, &maps.M, kc, u.o0, &full_bar[s]);
+            tma_load_2d(sb, &maps.Ghi[u.bx1], kc, u.j0, &full_bar[s]);
+            tma_load_2d(sb2, &maps.Glo[u.bx1], kc, u.j0, &full_bar[s]);
+          }
         }
         if (!ok) break;
       }
@@ -284,6 +295,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int kk = 0; kk < kBK / 16; ++kk)
             tc_mma_bf16(acc, sw128_kmajor_desc(sa + kk * 32), sw128_kmajor_desc(sb + kk * 32), idesc,
                         (kb | kk) != 0 ? 1u : 0u);
+          if (!u.slow) {
+            // the lo plane of the same tokens, against the same A box
+            const uint32_t sb2 = sb + uint32_t(box_rows(u.bx1) * kBK * 2);
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              tc_mma_bf16(acc, sw128_kmajor_desc(sa + kk * 32), sw128_kmajor_desc(sb2 + kk * 32),
+                          idesc, 1u);
+          }
           tc_commit(&empty_bar[s]);
         }
         if (!ok) break;
@@ -635,8 +654,8 @@ gsi_status_t tc_gemm_launch(gsi_handle* h, const TcGemmArgs& a, cudaStream_t s) 
       return GSI_ERR_CUDA;
   }
   // at most one CTA per SM (the ring takes most of shared memory), and no more
-  // CTAs than tiles could exist
-  const int n_tiles = (a.T + kBN - 1) / kBN;
+  // CTAs than tiles could exist (slow tiles of 256 tokens, fast of 128)
+  const int n_tiles = (a.T + kBNF - 1) / kBNF;
   const int max_tiles = ((a.d_out + kBM - 1) / kBM) * (n_tiles + 1);
   dim3 grid(unsigned(std::max(1, std::min(sms, max_tiles))));
   return launch_pdl(tc_gemm_kernel, grid, dim3(kTcThreads), kTcSmem, s, *maps, a) == cudaSuccess

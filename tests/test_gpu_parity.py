@@ -84,6 +84,28 @@ def test_batched(gsi, orc, d_out, d, k, T):
     lin.close()
 
 
+@pytest.mark.parametrize("rows", ["fewer", "more"])
+def test_batched_all_slow_row_blocks(gsi, orc, rows):
+    """Every token slow (eps = 0), so the GEMM kernel streams W alone.
+    fewer: fewer 128-row blocks of W than the GEMM's CTAs (one per SM), so
+    some CTAs take no slow tile; more: more row blocks than CTAs, so CTAs take
+    several slow tiles from the queue one after another.  The output must
+    repeat bit for bit."""
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    d, k, T = 2048, 128, 72
+    d_out = 680 if rows == "fewer" else 128 * (sms + 8) + 40
+    W, basis, X = make_case(d_out, d, k, 0.1, T, 41)
+    lin = GpuLinear(gsi, orc, W, basis.V_bits, 0.0)
+    y, g, r = lin.forward(X)
+    assert (g == 1).all() and np.isfinite(y).all()
+    sel = None if rows == "fewer" else np.r_[0:200, d_out - 300:d_out]
+    check_against_oracle(orc, lin, X, y, g, r, rows=sel, what=f"all slow, {rows} row blocks")
+    y2, _, _ = lin.forward(X)
+    assert np.array_equal(y2.view(np.int32), y.view(np.int32))
+    lin.close()
+
+
 @pytest.mark.parametrize("T", [1, 40])
 def test_eps_zero_and_inf(gsi, orc, T):
     """eps = 0: every token slow, y = W x.  eps = inf: every token fast."""
