@@ -181,56 +181,80 @@ __global__ void __launch_bounds__(kGateMmaThreads) gate_mma_kernel(
   }
   pdl_launch_dependents();
   pdl_wait();  // the projection's output and x are now visible
-  // g of the 8 tokens: float4 units, every slice's load issued before the adds
-  for (int q = tid; q < kGateMmaTok * K / 4; q += kGateMmaThreads) {
-    const int t = q / (K / 4), a4 = q % (K / 4);
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (t0 + t < T) {
-      const size_t o = size_t(t0 + t) * K + size_t(a4) * 4;
-      if (S > 0) {
-        float4 part[tc_proj_max_splits()];
+  // Every load of the CTA is issued before the first add: the S projection
+  // partials of the 8 tokens' g (float4 units, kGU per thread) and the x rows
+  // (warp w takes token w, kXU 16-byte chunks per lane and pass).
+  constexpr int kGU = (kGateMmaTok * K / 4 + kGateMmaThreads - 1) / kGateMmaThreads;
+  constexpr int kXU = 16;
+  float4 part[kGU][tc_proj_max_splits()];
+  float4 gv[kGU];
 #pragma unroll
-        for (int sl = 0; sl < tc_proj_max_splits(); ++sl)
-          part[sl] = sl < S ? *reinterpret_cast<const float4*>(P + size_t(sl) * split_stride + o)
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int u = 0; u < kGU; ++u) {
+    const int q = tid + u * kGateMmaThreads;
+    const int t = q / (K / 4), a4 = q % (K / 4);
+    const bool live = q < kGateMmaTok * K / 4 && t0 + t < T;
+    const size_t o = size_t(t0 + t) * K + size_t(a4) * 4;
+    gv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int sl = 0; sl < tc_proj_max_splits(); ++sl)
+      part[u][sl] = (live && sl < S) ? *reinterpret_cast<const float4*>(P + size_t(sl) * split_stride + o)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (live && S == 0) gv[u] = *reinterpret_cast<const float4*>(G + o);
+  }
+  // ||x_t||^2 (x_i^2 is exact in fp32; four partial sums per lane)
+  const int tx = t0 + warp;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + size_t(tx) * d);
+  const int nch = d / 8;
+  float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+  {
+    uint4 ch[kXU];
+#pragma unroll
+    for (int u = 0; u < kXU; ++u) {
+      const int c = lane + u * 32;
+      ch[u] = (tx < T && c < nch) ? xr[c] : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < kGU; ++u) {
+      const int q = tid + u * kGateMmaThreads;
+      if (q >= kGateMmaTok * K / 4) continue;
+      const int t = q / (K / 4), a4 = q % (K / 4);
+      if (S > 0) {
 #pragma unroll
         for (int sl = 0; sl < tc_proj_max_splits(); ++sl) {
-          v.x += part[sl].x;
-          v.y += part[sl].y;
-          v.z += part[sl].z;
-          v.w += part[sl].w;
+          gv[u].x += part[u][sl].x;
+          gv[u].y += part[u][sl].y;
+          gv[u].z += part[u][sl].z;
+          gv[u].w += part[u][sl].w;
         }
-        *reinterpret_cast<float4*>(G + o) = v;
-      } else {
-        v = *reinterpret_cast<const float4*>(G + o);
+        if (t0 + t < T) *reinterpret_cast<float4*>(G + size_t(t0 + t) * K + size_t(a4) * 4) = gv[u];
       }
+      *reinterpret_cast<float4*>(sg + t * kRow + a4 * 4) = gv[u];
     }
-    *reinterpret_cast<float4*>(sg + t * kRow + a4 * 4) = v;
+#pragma unroll
+    for (int u = 0; u < kXU; ++u) {
+      float f[8];
+      bf16x8_to_f32(ch[u], f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc4[e & 3] = fmaf(f[e], f[e], acc4[e & 3]);
+    }
   }
-  // ||x_t||^2: warp w takes token w, 8 chunks in flight per lane and four
-  // partial sums (x_i^2 is exact in fp32)
-  {
-    const int t = t0 + warp;
-    float acc4[4] = {0.f, 0.f, 0.f, 0.f};
-    if (t < T) {
-      const uint4* xr = reinterpret_cast<const uint4*>(x + size_t(t) * d);
-      const int nch = d / 8;
-      for (int c0 = lane; c0 < nch; c0 += 32 * 8) {
-        uint4 ch[8];
+  // rows longer than 32 * kXU chunks (d > 4096): further passes
+  for (int c0 = lane + 32 * kXU; tx < T && c0 < nch; c0 += 32 * kXU) {
+    uint4 ch[kXU];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int c = c0 + u * 32;
-          ch[u] = c < nch ? xr[c] : make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          float f[8];
-          bf16x8_to_f32(ch[u], f);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) acc4[e & 3] = fmaf(f[e], f[e], acc4[e & 3]);
-        }
-      }
+    for (int u = 0; u < kXU; ++u) {
+      const int c = c0 + u * 32;
+      ch[u] = c < nch ? xr[c] : make_uint4(0u, 0u, 0u, 0u);
     }
+#pragma unroll
+    for (int u = 0; u < kXU; ++u) {
+      float f[8];
+      bf16x8_to_f32(ch[u], f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc4[e & 3] = fmaf(f[e], f[e], acc4[e & 3]);
+    }
+  }
+  {
     float sxv = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
     sxv = warp_sum_xor<32>(sxv);
     if (lane == 0) s_sx[warp] = sxv;

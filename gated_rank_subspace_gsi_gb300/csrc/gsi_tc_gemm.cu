@@ -326,17 +326,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int32_t* idx = u.slow ? a.idx_slow : a.idx_fast;
       if (ok) {
         for (int c0 = 0; c0 < u.N; c0 += 32) {
+          // lane l holds the token of column c0 + l; each column's is broadcast
+          const int my_tok = c0 + lane < u.nvalid ? __ldg(idx + u.j0 + c0 + lane) : 0;
           uint32_t r[32];
           tmem_ld_32x32b_x32(tmem + (uint32_t(qw * 32) << 16) + uint32_t(q * kBN + c0), r);
-          if (o < a.d_out) {
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-              const int j = c0 + jj;
-              if (j < u.nvalid) {
-                const int tok = __ldg(idx + u.j0 + j);
-                a.y[size_t(tok) * a.d_out + o] = __uint_as_float(r[jj]);
-              }
-            }
+          for (int jj = 0; jj < 32; ++jj) {
+            const int tok = __shfl_sync(0xFFFFFFFFu, my_tok, jj);
+            if (c0 + jj < u.nvalid && o < a.d_out)
+              a.y[size_t(tok) * a.d_out + o] = __uint_as_float(r[jj]);
           }
         }
       }
@@ -372,37 +370,41 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // gate kernel sums the S partials in a fixed order.  Same warp roles as
 // tc_gemm_kernel.
 constexpr int kPN = 64;  // tokens per tile (MMA N)
-constexpr int kPStages = 4;
+constexpr int kPStages = 4;       // ring depth when the grid is more than one wave
+constexpr int kPMaxStages = 8;    // when every CTA is resident at once: a whole slice in flight
 constexpr int kPABytes = kBM * kBK * 2;  // 16 KiB
 constexpr int kPBBytes = kPN * kBK * 2;  // 8 KiB
 constexpr int kPStageBytes = kPABytes + kPBBytes;
 constexpr int kPTmemCols = 64;
 constexpr size_t kPSmem = size_t(kPStages) * kPStageBytes + 1024;
+constexpr size_t kPMaxSmem = size_t(kPMaxStages) * kPStageBytes + 1024;
 
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_proj_kernel(const __grid_constant__ CUtensorMap tmVT, const __grid_constant__ CUtensorMap tmX,
                    TcProjArgs a) {
   extern __shared__ unsigned char smem_raw[];
-  __shared__ uint64_t full_bar[kPStages];
-  __shared__ uint64_t empty_bar[kPStages];
+  __shared__ uint64_t full_bar[kPMaxStages];
+  __shared__ uint64_t empty_bar[kPMaxStages];
   __shared__ uint64_t accum_bar;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int s_issued;
 
   pdl_launch_dependents();
-  pdl_wait();  // x may come from the previous kernel
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m0 = blockIdx.x * kBM, t0 = blockIdx.y * kPN, sl = blockIdx.z;
   const int nkb_all = (a.d + kBK - 1) / kBK;
   const int kb0 = min(nkb_all, sl * a.kb_per), kb1 = min(nkb_all, kb0 + a.kb_per);
   const int num_kb = kb1 - kb0;
   const int nvalid = min(kPN, a.T - t0);
+  const int stages = min(max(a.stages, 1), kPMaxStages);
+  // stages whose A box is loaded before the wait (A fixed for the launch)
+  const int pre = a.a_fixed ? min(num_kb, stages) : 0;
 
   const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
   unsigned char* tiles = smem_raw + (base - smem_addr(smem_raw));
   if (threadIdx.x == 0) {
-    for (int st = 0; st < kPStages; ++st) {
+    for (int st = 0; st < stages; ++st) {
       mbar_init(&full_bar[st], 1);
       mbar_init(&empty_bar[st], 1);
     }
@@ -410,7 +412,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     s_abort = 0;
     s_issued = 0;
     fence_mbar_init();
+    for (int i = 0; i < pre; ++i) {
+      mbar_arrive_expect_tx(&full_bar[i], kPStageBytes);
+      tma_load_2d(tiles + size_t(i) * kPStageBytes, &tmVT, (kb0 + i) * kBK, m0, &full_bar[i]);
+    }
   }
+  pdl_wait();  // x may come from the previous kernel
   if (warp == 1) tmem_alloc(&s_tmem, kPTmemCols);
   tc_fence_before();
   __syncthreads();
@@ -421,13 +428,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       int i = 0;
       for (; i < num_kb; ++i) {
-        const int st = i % kPStages;
-        if (i >= kPStages &&
-            !wait_bounded(&empty_bar[st], ((i / kPStages) & 1) ^ 1, a.status, &s_abort))
+        const int st = i % stages;
+        if (i >= stages &&
+            !wait_bounded(&empty_bar[st], ((i / stages) & 1) ^ 1, a.status, &s_abort))
           break;
         unsigned char* sa = tiles + size_t(st) * kPStageBytes;
-        mbar_arrive_expect_tx(&full_bar[st], kPStageBytes);
-        tma_load_2d(sa, &tmVT, (kb0 + i) * kBK, m0, &full_bar[st]);
+        if (i >= pre) {
+          mbar_arrive_expect_tx(&full_bar[st], kPStageBytes);
+          tma_load_2d(sa, &tmVT, (kb0 + i) * kBK, m0, &full_bar[st]);
+        }
         tma_load_2d(sa + kPABytes, &tmX, (kb0 + i) * kBK, t0, &full_bar[st]);
       }
       s_issued = i;
@@ -436,8 +445,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(kBM, kPN);
       for (int i = 0; i < num_kb; ++i) {
-        const int st = i % kPStages;
-        if (!wait_bounded(&full_bar[st], (i / kPStages) & 1, a.status, &s_abort)) break;
+        const int st = i % stages;
+        if (!wait_bounded(&full_bar[st], (i / stages) & 1, a.status, &s_abort)) break;
         tc_fence_after();
         const uint32_t sa = base + uint32_t(st) * kPStageBytes;
         const uint32_t sb = sa + kPABytes;
@@ -474,10 +483,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   if (threadIdx.x == 0 && s_abort) {
     const int issued = s_issued;
-    for (int i = max(0, issued - kPStages); i < issued; ++i) {
-      const int st = i % kPStages;
+    for (int i = max(0, issued - stages); i < issued; ++i) {
+      const int st = i % stages;
       const uint64_t tw = globaltimer_ns();
-      while (!mbar_try_wait(&full_bar[st], (i / kPStages) & 1) &&
+      while (!mbar_try_wait(&full_bar[st], (i / stages) & 1) &&
              globaltimer_ns() - tw < kWaitLimitNs) {
       }
     }
@@ -539,6 +548,14 @@ bool tma_encode_bf16_2d(void* map, const void* base, uint64_t rows, uint64_t col
 
 int tc_gemm_launch_count() { return 1; }
 
+// Ring depth of a projection launch: a whole slice in flight (up to 8 stages,
+// about 193 KB of shared memory, one CTA per SM) when every CTA of the grid is
+// resident at once; else 4 stages, so that two CTAs share an SM.
+int proj_stages(int64_t ctas, int kb_per, int num_sms) {
+  return ctas <= num_sms ? std::max(1, std::min(kPMaxStages, kb_per)) : kPStages;
+}
+size_t proj_smem(int stages) { return size_t(stages) * kPStageBytes + 1024; }
+
 bool tc_proj_supported(const gsi_handle* h) { return h->k == 128 || h->k == 256; }
 
 gsi_status_t tc_proj_prepare(gsi_handle* h) {
@@ -548,7 +565,7 @@ gsi_status_t tc_proj_prepare(gsi_handle* h) {
   static bool attr = false;
   if (!attr) {
     if (cudaFuncSetAttribute(tc_proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(kPSmem)) != cudaSuccess)
+                             int(kPMaxSmem)) != cudaSuccess)
       return GSI_ERR_CUDA;
     attr = true;
   }
@@ -568,7 +585,7 @@ gsi_status_t tc_nt_prepare() {
   static bool attr = false;
   if (!attr) {
     if (cudaFuncSetAttribute(tc_proj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(kPSmem)) != cudaSuccess)
+                             int(kPMaxSmem)) != cudaSuccess)
       return GSI_ERR_CUDA;
     attr = true;
   }
@@ -601,7 +618,17 @@ gsi_status_t tc_nt_gemm(const void* A, int64_t rows_a, const void* B, int64_t ro
   a.split_stride = split_stride;
   a.status = status;
   dim3 grid(unsigned((rows_a + kBM - 1) / kBM), unsigned((rows_b + kPN - 1) / kPN), unsigned(S));
-  return launch_pdl(tc_proj_kernel, grid, dim3(kTcThreads), kPSmem, s, tmA, tmB, a) == cudaSuccess
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return GSI_ERR_CUDA;
+  }
+  a.stages = proj_stages(int64_t(grid.x) * grid.y * grid.z, kb_per, sms);
+  a.a_fixed = 0;  // A may be written by an earlier kernel of the stream
+  return launch_pdl(tc_proj_kernel, grid, dim3(kTcThreads), proj_smem(a.stages), s, tmA, tmB, a) ==
+                 cudaSuccess
              ? GSI_OK
              : GSI_ERR_CUDA;
 }
@@ -618,8 +645,11 @@ gsi_status_t tc_proj_launch(gsi_handle* h, const void* x, int64_t T, int S, int 
   a.split_stride = size_t(h->max_T) * h->k;
   a.status = h->status;
   dim3 grid(unsigned(h->k / kBM), unsigned((T + kPN - 1) / kPN), unsigned(S));
+  a.stages = proj_stages(int64_t(grid.x) * grid.y * grid.z, kb_per, h->num_sms);
+  a.a_fixed = 1;  // the handle's V_k^T, written once when the workspace was bound
   const CUtensorMap* vt = reinterpret_cast<const CUtensorMap*>(h->tmaps_proj);
-  return launch_pdl(tc_proj_kernel, grid, dim3(kTcThreads), kPSmem, s, *vt, tmX, a) == cudaSuccess
+  return launch_pdl(tc_proj_kernel, grid, dim3(kTcThreads), proj_smem(a.stages), s, *vt, tmX, a) ==
+                 cudaSuccess
              ? GSI_OK
              : GSI_ERR_CUDA;
 }

@@ -39,6 +39,9 @@ __host__ __device__ constexpr int tc_proj_max_splits() { return kProjMaxSplits; 
 struct TcProjArgs {
   float* P;             // [S][max_T][k] partials
   int T, d, k, kb_per;  // kb_per: 64-wide reduction steps per slice
+  int stages;           // TMA ring depth (<= 8; the launch sizes shared memory to it)
+  int a_fixed;          // 1: no kernel of the stream writes A (the handle's V_k^T), so
+                        // the first stages' A boxes load before the dependent-launch wait
   size_t split_stride;  // floats between slices
   uint32_t* status;
 };
