@@ -146,6 +146,32 @@ constexpr int kGateMmaTok = 8;
 constexpr int kGateMmaThreads = 256;
 constexpr int kGatePad = 8;  // floats of padding per staged g row (no bank conflicts)
 
+// One warp's share of g^T E g: the correction tiles (I, J), I <= J, whose
+// storage index is TS mod 4, in (I, J) order.  Tile (I, J) contributes
+// g_I . (F_IJ g_J); lane (grp, tig) holds columns 2 tig (high part) and
+// 2 tig + 1 (low part) of token tig, rows grp and grp + 8.
+template <int T16, int TS>
+__device__ __forceinline__ float gate_corr_subset(const uint4* sF, const float* gq,
+                                                  const uint2 (&bfr)[T16], int lane, int grp) {
+  float q = 0.f;
+#pragma unroll
+  for (int I = 0; I < T16; ++I) {
+#pragma unroll
+    for (int J = I; J < T16; ++J) {
+      if ((corr_tile_index(I, J, T16) & 3) != TS) continue;
+      float dd[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint4 A = sF[corr_tile_index(I, J, T16) * 32 + lane];
+      asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+          "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+          : "+f"(dd[0]), "+f"(dd[1]), "+f"(dd[2]), "+f"(dd[3])
+          : "r"(A.x), "r"(A.y), "r"(A.z), "r"(A.w), "r"(bfr[J].x), "r"(bfr[J].y));
+      q = fmaf(gq[I * 16 + grp], dd[0] + dd[1], q);
+      q = fmaf(gq[I * 16 + grp + 8], dd[2] + dd[3], q);
+    }
+  }
+  return q;
+}
+
 // With S > 0, g is the sum (in slice order) of the S projection partials P[s]
 // and is also written to G for the gather; with S = 0 it is read from G.
 template <int K>
@@ -287,26 +313,17 @@ __global__ void __launch_bounds__(kGateMmaThreads) gate_mma_kernel(
     }
     bfr[J] = make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
   }
-  // g^T E g: tile (I, J) contributes g_I . (F_IJ g_J); lane (grp, tig) holds
-  // columns 2 tig (high) and 2 tig + 1 (low) of token tig, rows grp, grp + 8
+  // g^T E g over this warp's tile subset
   const float* gq = sg + (tg * 4 + tig) * kRow;
   float q = 0.f;
   if (ok) {
-#pragma unroll
-    for (int I = 0; I < T16; ++I) {
-      const float gI0 = gq[I * 16 + grp], gI8 = gq[I * 16 + grp + 8];
-#pragma unroll
-      for (int J = I; J < T16; ++J) {
-        if ((corr_tile_index(I, J, T16) & 3) != ts) continue;
-        float dd[4] = {0.f, 0.f, 0.f, 0.f};
-        const uint4 A = sF[corr_tile_index(I, J, T16) * 32 + lane];
-        asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-            "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-            : "+f"(dd[0]), "+f"(dd[1]), "+f"(dd[2]), "+f"(dd[3])
-            : "r"(A.x), "r"(A.y), "r"(A.z), "r"(A.w), "r"(bfr[J].x), "r"(bfr[J].y));
-        q = fmaf(gI0, dd[0] + dd[1], q);
-        q = fmaf(gI8, dd[2] + dd[3], q);
-      }
+    // the subset is a template argument, so that each warp's tiles unroll to
+    // straight-line code whose shared-memory loads and MMAs overlap
+    switch (ts) {
+      case 0: q = gate_corr_subset<T16, 0>(sF, gq, bfr, lane, grp); break;
+      case 1: q = gate_corr_subset<T16, 1>(sF, gq, bfr, lane, grp); break;
+      case 2: q = gate_corr_subset<T16, 2>(sF, gq, bfr, lane, grp); break;
+      default: q = gate_corr_subset<T16, 3>(sF, gq, bfr, lane, grp); break;
     }
   }
   // sum over grp (lanes of equal tig), then over the four tile subsets
