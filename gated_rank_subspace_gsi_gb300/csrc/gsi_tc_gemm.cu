@@ -465,16 +465,41 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_after();
     const int row = m0 + q * 32 + lane;
     float* P = a.P + size_t(sl) * a.split_stride;
-    for (int c0 = 0; c0 < kPN; c0 += 32) {
-      uint32_t r[32];
-      tmem_ld_32x32b_x32(tmem + (uint32_t(q * 32) << 16) + uint32_t(c0), r);
-      if (row < a.k) {
+    if (ok && num_kb > 0 && a.k % 4 == 0 && (reinterpret_cast<uintptr_t>(P) & 15) == 0) {
+      // Each 32 x 32 chunk goes through shared memory (the ring, drained
+      // once the accumulator is complete) so that the warp writes 16-byte
+      // vectors: lane (token j = lane / 8 + 4 p, rows 4 (lane % 8) .. + 3).
+      float* stg = reinterpret_cast<float*>(tiles) + q * (32 * 33);
+      const int jq = lane >> 3, o4 = (lane & 7) * 4;
+      const int rq = m0 + q * 32 + o4;
+      for (int c0 = 0; c0 < kPN; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tmem + (uint32_t(q * 32) << 16) + uint32_t(c0), r);
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          const int j = c0 + jj;
-          // a slice with no reduction steps contributes zero
-          if (j < nvalid)
-            P[size_t(t0 + j) * a.k + row] = (ok && num_kb > 0) ? __uint_as_float(r[jj]) : 0.f;
+        for (int jj = 0; jj < 32; ++jj) stg[jj * 33 + lane] = __uint_as_float(r[jj]);
+        __syncwarp();
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+          const int jj = 4 * p + jq, j = c0 + jj;
+          const float* src = stg + jj * 33 + o4;
+          if (j < nvalid && rq < a.k)
+            *reinterpret_cast<float4*>(P + size_t(t0 + j) * a.k + rq) =
+                make_float4(src[0], src[1], src[2], src[3]);
+        }
+        __syncwarp();
+      }
+    } else {
+      for (int c0 = 0; c0 < kPN; c0 += 32) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tmem + (uint32_t(q * 32) << 16) + uint32_t(c0), r);
+        if (row < a.k) {
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) {
+            const int j = c0 + jj;
+            // a slice with no reduction steps contributes zero
+            if (j < nvalid)
+              P[size_t(t0 + j) * a.k + row] = (ok && num_kb > 0) ? __uint_as_float(r[jj]) : 0.f;
+          }
         }
       }
     }
