@@ -38,16 +38,22 @@ constexpr int kBM = 128;           // weight rows per tile (MMA M)
 constexpr int kBN = 256;           // slow token rows per tile (max MMA N)
 constexpr int kBNF = 128;          // fast token rows per tile (both g planes in one stage)
 constexpr int kBK = 64;            // K elements per stage (128 bytes of bf16)
-constexpr int kStages = 4;
+constexpr int kStages = 4;          // stages of the fast ring
+constexpr int kMaxSlowStages = 8;   // at most, on the slow ring
 constexpr int kABytes = kBM * kBK * 2;   // 16 KiB
 constexpr int kBBytes = kBN * kBK * 2;   // 32 KiB
 constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kRingBytes = 216 * 1024;  // both rings share this memory
 constexpr int kTcThreads = 192;
 constexpr int kTmemCols = 512;  // two 256-column accumulators
-constexpr size_t kTcSmem = size_t(kStages) * kStageBytes + 1024;  // + alignment slack
-// The GEMM kernel's ring has 4 stages of the largest tiles (A 128 x 64,
-// B 256 x 64); a shorter token tile loads B as one or two boxes of 32, 64,
-// 128 or 256 rows that just cover it.
+constexpr size_t kTcSmem = size_t(kRingBytes) + 1024;  // + alignment slack
+// The GEMM kernel has two TMA rings over the same shared memory.  The slow
+// ring's stage is one A box of W and the one or two boxes of X_slow that
+// cover the first slow token tile (128 + 32 rows for 154 tokens: 36 KB, six
+// stages); the fast ring has 4 stages of 48 KB (A 128 x 64 and both g planes
+// of 128 tokens).  A shorter token tile loads B as boxes of 32, 64, 128 or 256
+// rows that just cover it.  A CTA takes its slow tiles before its fast ones,
+// so it switches rings at most once, after every slow stage is released.
 constexpr int kBoxRows[4] = {256, 128, 64, 32};  // host: the maps' box heights
 __host__ __device__ constexpr int box_rows(int i) { return 256 >> i; }  // = kBoxRows[i]
 struct TcMaps {
@@ -187,13 +193,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs a) {
   constexpr int kQ = 2;  // tiles in flight: queue slots and TMEM accumulators
   extern __shared__ unsigned char smem_raw[];
-  __shared__ uint64_t full_bar[kStages];
+  __shared__ uint64_t full_bar[kStages];   // fast ring
   __shared__ uint64_t empty_bar[kStages];
+  __shared__ uint64_t sfull_bar[kMaxSlowStages];   // slow ring
+  __shared__ uint64_t sempty_bar[kMaxSlowStages];
   __shared__ uint64_t tq_full[kQ], tq_empty[kQ], acc_full[kQ], acc_empty[kQ];
   __shared__ int s_tile[kQ];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ int s_issued;
+  __shared__ int s_issued, s_issued_slow;
 
   pdl_launch_dependents();
   pdl_wait();  // token counts, index lists, gathered operands and the tile counter are visible
@@ -202,6 +210,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int n_mt = (a.d_out + kBM - 1) / kBM;
   const int n_slow_tiles = n_mt * ((n_slow + kBN - 1) / kBN);
   const int total = n_slow_tiles + n_mt * ((n_fast + kBNF - 1) / kBNF);
+  // the slow ring: stage = A + the first (largest) slow token tile's B boxes
+  const int slow_stage =
+      n_slow_tiles > 0 ? kABytes + decode_tile(0, n_slow_tiles, n_mt, n_fast, n_slow, a).b_bytes
+                       : kStageBytes;
+  const int S = min(kMaxSlowStages, kRingBytes / slow_stage);
 
   const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
   unsigned char* tiles = smem_raw + (base - smem_addr(smem_raw));
@@ -211,6 +224,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
+    for (int s = 0; s < kMaxSlowStages; ++s) {
+      mbar_init(&sfull_bar[s], 1);
+      mbar_init(&sempty_bar[s], 1);
+    }
     for (int q = 0; q < kQ; ++q) {
       mbar_init(&tq_full[q], 1);
       mbar_init(&tq_empty[q], 5);   // the MMA lane and the 4 epilogue warps
@@ -219,6 +236,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     s_abort = 0;
     s_issued = 0;
+    s_issued_slow = 0;
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc(&s_tmem, kTmemCols);
@@ -229,7 +247,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      int g = 0;  // K steps issued over all tiles: stage g % kStages
+      int g = 0;   // K steps issued on the fast ring: stage g % kStages
+      int gs = 0;  // K steps issued on the slow ring: stage gs % S
+      bool drained = false;
       for (int i = 0;; ++i) {
         const int q = i % kQ;
         if (i >= kQ && !wait_bounded(&tq_empty[q], ((i / kQ) & 1) ^ 1, a.status, &s_abort)) break;
@@ -240,36 +260,54 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (t < 0) break;
         const Tile u = decode_tile(t, n_slow_tiles, n_mt, n_fast, n_slow, a);
         bool ok = true;
-        for (int kb = 0; kb < u.num_kb; ++kb, ++g) {
-          const int s = g % kStages;
-          if (g >= kStages &&
-              !wait_bounded(&empty_bar[s], ((g / kStages) & 1) ^ 1, a.status, &s_abort)) {
-            ok = false;
-            break;
-          }
-          unsigned char* sa = tiles + size_t(s) * kStageBytes;
-          unsigned char* sb = sa + kABytes;
-          unsigned char* sb2 = sb + box_rows(u.bx1) * kBK * 2;
-          mbar_arrive_expect_tx(&full_bar[s], uint32_t(kABytes + u.b_bytes));
+        if (!u.slow && !drained) {
+          // the fast ring reuses the slow ring's memory: every slow stage
+          // issued must have been released by its MMAs first
+          for (int h = max(0, gs - S); h < gs && ok; ++h)
+            ok = wait_bounded(&sempty_bar[h % S], (h / S) & 1, a.status, &s_abort);
+          drained = true;
+        }
+        for (int kb = 0; ok && kb < u.num_kb; ++kb) {
           const int kc = kb * kBK;
           if (u.slow) {
-            tma_load_2d(sa, &maps.W, kc, u.o0, &full_bar[s]);
-            tma_load_2d(sb, &maps.Xs[u.bx1], kc, u.j0, &full_bar[s]);
+            const int s = gs % S;
+            if (gs >= S && !wait_bounded(&sempty_bar[s], ((gs / S) & 1) ^ 1, a.status, &s_abort)) {
+              ok = false;
+              break;
+            }
+            unsigned char* sa = tiles + size_t(s) * slow_stage;
+            unsigned char* sb = sa + kABytes;
+            mbar_arrive_expect_tx(&sfull_bar[s], uint32_t(kABytes + u.b_bytes));
+            tma_load_2d(sa, &maps.W, kc, u.o0, &sfull_bar[s]);
+            tma_load_2d(sb, &maps.Xs[u.bx1], kc, u.j0, &sfull_bar[s]);
             if (u.bx2 >= 0)
-              tma_load_2d(sb2, &maps.Xs[u.bx2], kc, u.j0 + box_rows(u.bx1), &full_bar[s]);
+              tma_load_2d(sb + box_rows(u.bx1) * kBK * 2, &maps.Xs[u.bx2], kc,
+                          u.j0 + box_rows(u.bx1), &sfull_bar[s]);
+            ++gs;
           } else {
+            const int s = g % kStages;
+            if (g >= kStages &&
+                !wait_bounded(&empty_bar[s], ((g / kStages) & 1) ^ 1, a.status, &s_abort)) {
+              ok = false;
+              break;
+            }
+            unsigned char* sa = tiles + size_t(s) * kStageBytes;
+            unsigned char* sb = sa + kABytes;
+            mbar_arrive_expect_tx(&full_bar[s], uint32_t(kABytes + u.b_bytes));
             tma_load_2d(sa, &maps.M, kc, u.o0, &full_bar[s]);
             tma_load_2d(sb, &maps.Ghi[u.bx1], kc, u.j0, &full_bar[s]);
-            tma_load_2d(sb2, &maps.Glo[u.bx1], kc, u.j0, &full_bar[s]);
+            tma_load_2d(sb + box_rows(u.bx1) * kBK * 2, &maps.Glo[u.bx1], kc, u.j0, &full_bar[s]);
+            ++g;
           }
         }
         if (!ok) break;
       }
       s_issued = g;
+      s_issued_slow = gs;
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      int g = 0;
+      int g = 0, gs = 0;  // K steps consumed on the fast and the slow ring
       for (int i = 0;; ++i) {
         const int q = i % kQ;
         if (!wait_bounded(&tq_full[q], (i / kQ) & 1, a.status, &s_abort)) break;
@@ -282,14 +320,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t acc = tmem + uint32_t(q * kBN);
         const uint32_t idesc = idesc_bf16_f32(kBM, u.N);
         bool ok = true;
-        for (int kb = 0; kb < u.num_kb; ++kb, ++g) {
-          const int s = g % kStages;
-          if (!wait_bounded(&full_bar[s], (g / kStages) & 1, a.status, &s_abort)) {
+        for (int kb = 0; kb < u.num_kb; ++kb) {
+          const int s = u.slow ? gs % S : g % kStages;
+          uint64_t* fb = u.slow ? &sfull_bar[s] : &full_bar[s];
+          uint64_t* eb = u.slow ? &sempty_bar[s] : &empty_bar[s];
+          const uint32_t par = u.slow ? (gs / S) & 1 : (g / kStages) & 1;
+          if (!wait_bounded(fb, par, a.status, &s_abort)) {
             ok = false;
             break;
           }
+          if (u.slow) ++gs; else ++g;
           tc_fence_after();
-          const uint32_t sa = base + uint32_t(s) * kStageBytes;
+          const uint32_t sa = base + uint32_t(s) * uint32_t(u.slow ? slow_stage : kStageBytes);
           const uint32_t sb = sa + kABytes;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
@@ -303,7 +345,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               tc_mma_bf16(acc, sw128_kmajor_desc(sa + kk * 32), sw128_kmajor_desc(sb2 + kk * 32),
                           idesc, 1u);
           }
-          tc_commit(&empty_bar[s]);
+          tc_commit(eb);
         }
         if (!ok) break;
         tc_commit(&acc_full[q]);
@@ -348,11 +390,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   if (threadIdx.x == 0 && s_abort) {
     // make sure no bulk copy is still writing into this CTA's shared memory
-    const int issued = s_issued;
+    const int issued = s_issued, issued_slow = s_issued_slow;
     for (int g = max(0, issued - kStages); g < issued; ++g) {
-      const int s = g % kStages;
       const uint64_t t0 = globaltimer_ns();
-      while (!mbar_try_wait(&full_bar[s], (g / kStages) & 1) && globaltimer_ns() - t0 < kWaitLimitNs) {
+      while (!mbar_try_wait(&full_bar[g % kStages], (g / kStages) & 1) &&
+             globaltimer_ns() - t0 < kWaitLimitNs) {
+      }
+    }
+    for (int g = max(0, issued_slow - S); g < issued_slow; ++g) {
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(&sfull_bar[g % S], (g / S) & 1) && globaltimer_ns() - t0 < kWaitLimitNs) {
       }
     }
   }
