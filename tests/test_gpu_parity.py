@@ -106,6 +106,29 @@ def test_batched_all_slow_row_blocks(gsi, orc, rows):
     lin.close()
 
 
+@pytest.mark.parametrize("k,T", [(64, 8192), (256, 8200)])
+def test_batched_long_calls(gsi, orc, k, T):
+    """Calls of 8192 and 8200 tokens (a reserved workspace): a gate grid of
+    over a thousand CTAs, a partition over 8200 tokens and a GEMM tile queue
+    of several token tiles per weight band; both projections (CUDA cores at
+    k = 64, tensor cores at k = 256).  Every gate and rho is checked, y on
+    sampled tokens."""
+    d_out, d = 96, 512
+    W, basis, X = make_case(d_out, d, k, 0.1, T, 51 + k)
+    lin = GpuLinear(gsi, orc, W, basis.V_bits, 0.1, max_T=T)
+    y, g, r = lin.forward(X)
+    assert 0 < g.sum() < T and np.isfinite(y).all()
+    rng = np.random.default_rng(7)
+    sample = np.unique(np.r_[0:40, T - 40:T, rng.choice(T, 200, replace=False)])
+    check_against_oracle(orc, lin, X, y, g, r, tokens=sample, what=f"long call k={k} T={T}")
+    # every gate and rho, from the oracle's rho alone
+    V = gi.bf16_bits_to_f64(basis.V_bits)
+    rho_ref = orc.forward(None, V, None, lin.eps, gi.bf16_bits_to_f64(X))["rho"]
+    out = np.abs(rho_ref - lin.eps) > 1e-4
+    assert np.array_equal(g[out].astype(bool), rho_ref[out] >= lin.eps)
+    lin.close()
+
+
 @pytest.mark.parametrize("T", [1, 40])
 def test_eps_zero_and_inf(gsi, orc, T):
     """eps = 0: every token slow, y = W x.  eps = inf: every token fast."""
