@@ -398,6 +398,26 @@ __global__ void __launch_bounds__(256) partition_gather_kernel(
   pdl_launch_dependents();
   pdl_wait();
   const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // this token's x row and g row are loaded together with the gate bytes
+  // (one round trip to memory instead of two); the branch uses one of them
+  constexpr int kXR = 8;  // 16-byte chunks of x per thread held in registers
+  const int nch = d / 8;
+  const bool x_in_regs = nch <= kXR * int(blockDim.x);
+  uint4 xr[kXR];
+  const uint4* src = reinterpret_cast<const uint4*>(x + size_t(t) * d);
+  if (x_in_regs) {
+#pragma unroll
+    for (int u = 0; u < kXR; ++u) {
+      const int i = tid + u * int(blockDim.x);
+      xr[u] = i < nch ? src[i] : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  float gr[(K + 255) / 256];
+#pragma unroll
+  for (int u = 0; u < (K + 255) / 256; ++u) {
+    const int a = tid + u * 256;
+    gr[u] = a < K ? G[size_t(t) * K + a] : 0.f;
+  }
   int before = 0, total = 0;
   for (int i = tid; i < T; i += blockDim.x) {
     const int f = gate[i] != 0;
@@ -429,19 +449,30 @@ __global__ void __launch_bounds__(256) partition_gather_kernel(
   if (gate[t] == 0) {
     const int pos = t - before;
     if (tid == 0) idx_fast[pos] = t;
-    for (int a = tid; a < K; a += blockDim.x) {
-      const float g = G[size_t(t) * K + a];
-      const __nv_bfloat16 hi = __float2bfloat16_rn(g);
-      const __nv_bfloat16 lo = __float2bfloat16_rn(g - __bfloat162float(hi));
-      Gf[size_t(pos) * K + a] = hi;
-      Gf[(size_t(max_T) + pos) * K + a] = lo;
+#pragma unroll
+    for (int u = 0; u < (K + 255) / 256; ++u) {
+      const int a = tid + u * 256;
+      if (a < K) {
+        const float g = gr[u];
+        const __nv_bfloat16 hi = __float2bfloat16_rn(g);
+        const __nv_bfloat16 lo = __float2bfloat16_rn(g - __bfloat162float(hi));
+        Gf[size_t(pos) * K + a] = hi;
+        Gf[(size_t(max_T) + pos) * K + a] = lo;
+      }
     }
   } else {
     const int pos = before;
     if (tid == 0) idx_slow[pos] = t;
-    const uint4* src = reinterpret_cast<const uint4*>(x + size_t(t) * d);
     uint4* dst = reinterpret_cast<uint4*>(Xs + size_t(pos) * d);
-    for (int i = tid; i < d / 8; i += blockDim.x) dst[i] = src[i];
+    if (x_in_regs) {
+#pragma unroll
+      for (int u = 0; u < kXR; ++u) {
+        const int i = tid + u * int(blockDim.x);
+        if (i < nch) dst[i] = xr[u];
+      }
+    } else {
+      for (int i = tid; i < nch; i += blockDim.x) dst[i] = src[i];
+    }
   }
 }
 
