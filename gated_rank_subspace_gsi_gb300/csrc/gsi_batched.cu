@@ -186,6 +186,8 @@ __global__ void __launch_bounds__(kGateMmaThreads) gate_mma_kernel(
   extern __shared__ __align__(128) unsigned char smem[];
   uint4* sF = reinterpret_cast<uint4*>(smem);                          // [kTiles][32]
   float* sg = reinterpret_cast<float*>(smem + size_t(kTiles) * 512);   // [8][kRow]
+  uint2* sB = reinterpret_cast<uint2*>(smem + size_t(kTiles) * 512 +
+                                       size_t(kGateMmaTok) * kRow * 4);  // [2][T16][32]
   __shared__ float s_sx[kGateMmaTok], s_gg[kGateMmaTok];
   __shared__ float s_q[4][kGateMmaTok];
   __shared__ uint64_t s_bar;
@@ -293,26 +295,31 @@ __global__ void __launch_bounds__(kGateMmaThreads) gate_mma_kernel(
     v = warp_sum_xor<32>(v);
     if (lane == 0) s_gg[warp] = v;
   }
+  // B operands of both token groups (4 tokens each), one per column block J
+  // and lane, built once for the CTA while the correction tiles land: lane
+  // (grp, tig) holds rows 2 tig, 2 tig + 1, 2 tig + 8, 2 tig + 9 of token
+  // grp / 2, as the bf16 high part (grp even) or remainder (grp odd)
+  for (int e = tid; e < 2 * T16 * 32; e += kGateMmaThreads) {
+    const int ln = e & 31, J = (e >> 5) % T16, tgi = e / (32 * T16);
+    const int gp = ln >> 2, tg4 = ln & 3;
+    const float* gb = sg + (tgi * 4 + gp / 2) * kRow;
+    const int a = J * 16 + 2 * tg4;
+    const float v[4] = {gb[a], gb[a + 1], gb[a + 8], gb[a + 9]};
+    uint32_t p[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const __nv_bfloat16 hi = __float2bfloat16_rn(v[q]);
+      const __nv_bfloat16 part = (gp & 1) ? __float2bfloat16_rn(v[q] - __bfloat162float(hi)) : hi;
+      p[q] = __bfloat16_as_ushort(part);
+    }
+    sB[e] = make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
+  }
   const bool ok = mbar_wait_bounded(&s_bar, 0, status);
   __syncthreads();
   const int tg = warp & 1, ts = warp >> 1;  // token group, tile subset
-  // B operands of this warp's 4 tokens, one per column block J
-  const float* gb = sg + (tg * 4 + grp / 2) * kRow;
-  const bool low = (grp & 1) != 0;
   uint2 bfr[T16];
 #pragma unroll
-  for (int J = 0; J < T16; ++J) {
-    const int a = J * 16 + 2 * tig;
-    float v[4] = {gb[a], gb[a + 1], gb[a + 8], gb[a + 9]};
-    uint32_t p[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const __nv_bfloat16 hi = __float2bfloat16_rn(v[e]);
-      const __nv_bfloat16 part = low ? __float2bfloat16_rn(v[e] - __bfloat162float(hi)) : hi;
-      p[e] = __bfloat16_as_ushort(part);
-    }
-    bfr[J] = make_uint2(p[0] | (p[1] << 16), p[2] | (p[3] << 16));
-  }
+  for (int J = 0; J < T16; ++J) bfr[J] = sB[(tg * T16 + J) * 32 + lane];
   // g^T E g over this warp's tile subset
   const float* gq = sg + (tg * 4 + tig) * kRow;
   float q = 0.f;
@@ -360,7 +367,8 @@ __global__ void __launch_bounds__(kGateMmaThreads) gate_mma_kernel(
 template <int K>
 size_t gate_mma_smem() {
   constexpr int T16 = K / 16;
-  return size_t(T16) * (T16 + 1) / 2 * 512 + size_t(kGateMmaTok) * (K + kGatePad) * 4;
+  return size_t(T16) * (T16 + 1) / 2 * 512 + size_t(kGateMmaTok) * (K + kGatePad) * 4 +
+         size_t(2) * T16 * 32 * 8;
 }
 
 // V_k (d x k) -> V_k^T (k x d), 32 x 32 tiles through shared memory.
