@@ -179,7 +179,8 @@ __global__ void __launch_bounds__(kGateMmaThreads) gate_mma_kernel(
     float* __restrict__ G, const float* __restrict__ P, int S, size_t split_stride,
     const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ F, int T, int d,
     float eps, uint8_t* __restrict__ gate_int, uint8_t* __restrict__ gate_out,
-    float* __restrict__ rho_out, uint32_t* __restrict__ status) {
+    float* __restrict__ rho_out, uint32_t* __restrict__ status, const float* __restrict__ sxp,
+    size_t sxp_stride) {
   constexpr int T16 = K / 16;
   constexpr int kTiles = T16 * (T16 + 1) / 2;
   constexpr int kRow = K + kGatePad;
@@ -229,10 +230,13 @@ __global__ void __launch_bounds__(kGateMmaThreads) gate_mma_kernel(
                                      : make_float4(0.f, 0.f, 0.f, 0.f);
     if (live && S == 0) gv[u] = *reinterpret_cast<const float4*>(G + o);
   }
-  // ||x_t||^2 (x_i^2 is exact in fp32; four partial sums per lane)
+  // ||x_t||^2 (x_i^2 is exact in fp32; four partial sums per lane): from the
+  // tensor-core projection's per-slice sums when it made them, else from x
   const int tx = t0 + warp;
+  const bool x_from_slices = S > 0 && sxp != nullptr;
+  const float sx_slice = (x_from_slices && lane < S && tx < T) ? sxp[size_t(lane) * sxp_stride + tx] : 0.f;
   const uint4* xr = reinterpret_cast<const uint4*>(x + size_t(tx) * d);
-  const int nch = d / 8;
+  const int nch = x_from_slices ? 0 : d / 8;
   float acc4[4] = {0.f, 0.f, 0.f, 0.f};
   {
     uint4 ch[kXU];
@@ -283,7 +287,7 @@ __global__ void __launch_bounds__(kGateMmaThreads) gate_mma_kernel(
     }
   }
   {
-    float sxv = (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
+    float sxv = x_from_slices ? sx_slice : (acc4[0] + acc4[1]) + (acc4[2] + acc4[3]);
     sxv = warp_sum_xor<32>(sxv);
     if (lane == 0) s_sx[warp] = sxv;
   }
@@ -507,7 +511,8 @@ gsi_status_t launch_front(gsi_handle* h, const void* x, int T, uint8_t* gate, fl
       if (launch_pdl(gate_mma_kernel<K>, dim3((T + kGateMmaTok - 1) / kGateMmaTok),
                      dim3(kGateMmaThreads), gate_mma_smem<K>(), s, h->bG, h->bP, S,
                      size_t(h->max_T) * K, xb, h->cr_F, T, int(h->d), h->eps, h->bgate, gate,
-                     rho, h->status) != cudaSuccess)
+                     rho, h->status, S > 0 ? static_cast<const float*>(h->bsxp) : nullptr,
+                     size_t(h->max_T)) != cudaSuccess)
         return GSI_ERR_CUDA;
     } else {
       gate_kernel<K><<<(T + kGateTok - 1) / kGateTok, 256, 0, s>>>(h->bG, h->bsx, h->gram, T,
@@ -540,6 +545,7 @@ size_t batched_workspace_bytes(int64_t max_T, int64_t d, int64_t k) {
   if (k == 128 || k == 256) {
     b += align256(size_t(k) * d * 2);                          // bVT
     b += align256(size_t(kProjMaxSplits) * max_T * k * 4);     // bP
+    b += align256(size_t(kProjMaxSplits) * max_T * 4);         // bsxp
   }
   return b;
 }
@@ -572,9 +578,11 @@ void batched_bind_workspace(gsi_handle* h, void* base, int64_t max_T) {
   h->bXs = reinterpret_cast<__nv_bfloat16*>(take(size_t(max_T) * h->d * 2));
   h->bVT = nullptr;
   h->bP = nullptr;
+  h->bsxp = nullptr;
   if (h->k == 128 || h->k == 256) {
     h->bVT = reinterpret_cast<__nv_bfloat16*>(take(size_t(h->k) * h->d * 2));
     h->bP = reinterpret_cast<float*>(take(size_t(kProjMaxSplits) * max_T * h->k * 4));
+    h->bsxp = reinterpret_cast<float*>(take(size_t(kProjMaxSplits) * max_T * 4));
   }
   h->max_T = max_T;
 }

@@ -90,6 +90,7 @@ struct gsi_handle {
   __nv_bfloat16* bXs = nullptr;// max_T x d   gathered x of slow tokens
   __nv_bfloat16* bVT = nullptr;// k x d       V_k transposed (tensor-core projection)
   float* bP = nullptr;         // [8][max_T][k] projection partials (tensor-core projection)
+  float* bsxp = nullptr;       // [8][max_T] ||x||^2 over each slice (tensor-core projection)
   alignas(64) unsigned char tmaps_proj[128] = {};  // TMA map of bVT
   // TMA tensor maps of the tcgen05 GEMMs (CUtensorMap, 128 bytes each):
   // W, M, G_fast hi plane, G_fast lo plane, X_slow

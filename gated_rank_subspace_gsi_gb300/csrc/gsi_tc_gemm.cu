@@ -447,13 +447,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int stages = min(max(a.stages, 1), kPMaxStages);
   // stages whose A box is loaded before the wait (A fixed for the launch)
   const int pre = a.a_fixed ? min(num_kb, stages) : 0;
+  // the CTAs of entries 0..127 also sum the squares of their staged x tiles:
+  // a stage is released by the MMAs' commit and by the 4 epilogue warps
+  const bool do_sx = a.sxp != nullptr && blockIdx.x == 0;
 
   const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
   unsigned char* tiles = smem_raw + (base - smem_addr(smem_raw));
   if (threadIdx.x == 0) {
     for (int st = 0; st < stages; ++st) {
       mbar_init(&full_bar[st], 1);
-      mbar_init(&empty_bar[st], 1);
+      mbar_init(&empty_bar[st], do_sx ? 5 : 1);
     }
     mbar_init(&accum_bar, 1);
     s_abort = 0;
@@ -508,6 +511,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else {
     // epilogue: warps 2..5 own TMEM lane quarters (warp % 4); entry m0 + row
     const int q = warp & 3;
+    if (do_sx) {
+      // ||x||^2 over this slice: warp q takes tokens 16 q .. 16 q + 15 of the
+      // tile, lane l token 16 q + l / 2 and half l % 2 of its 128-byte row
+      // (the row's chunks are swizzled, which a sum of squares ignores);
+      // rows past T are the tensor map's zero fill
+      float sxl = 0.f;
+      const int r = 16 * q + (lane >> 1);
+      for (int i = 0; i < num_kb; ++i) {
+        const int st = i % stages;
+        if (!wait_bounded(&full_bar[st], (i / stages) & 1, a.status, &s_abort)) break;
+        const uint4* xrow = reinterpret_cast<const uint4*>(tiles + size_t(st) * kPStageBytes +
+                                                           kPABytes + size_t(r) * 128) +
+                            (lane & 1) * 4;
+        float part = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float f[8];
+          bf16x8_to_f32(xrow[c], f);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) part = fmaf(f[e], f[e], part);
+        }
+        sxl += part;
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cta(&empty_bar[st]);
+      }
+      sxl += __shfl_xor_sync(0xFFFFFFFFu, sxl, 1);
+      if ((lane & 1) == 0 && r < nvalid)
+        a.sxp[size_t(sl) * a.sxp_stride + size_t(t0 + r)] = num_kb > 0 ? sxl : 0.f;
+    }
     const bool ok = wait_bounded(&accum_bar, 0, a.status, &s_abort);
     tc_fence_after();
     const int row = m0 + q * 32 + lane;
@@ -699,6 +731,8 @@ gsi_status_t tc_nt_gemm(const void* A, int64_t rows_a, const void* B, int64_t ro
   }
   a.stages = proj_stages(int64_t(grid.x) * grid.y * grid.z, kb_per, sms);
   a.a_fixed = 0;  // A may be written by an earlier kernel of the stream
+  a.sxp = nullptr;
+  a.sxp_stride = 0;
   return launch_pdl(tc_proj_kernel, grid, dim3(kTcThreads), proj_smem(a.stages), s, tmA, tmB, a) ==
                  cudaSuccess
              ? GSI_OK
@@ -719,6 +753,8 @@ gsi_status_t tc_proj_launch(gsi_handle* h, const void* x, int64_t T, int S, int 
   dim3 grid(unsigned(h->k / kBM), unsigned((T + kPN - 1) / kPN), unsigned(S));
   a.stages = proj_stages(int64_t(grid.x) * grid.y * grid.z, kb_per, h->num_sms);
   a.a_fixed = 1;  // the handle's V_k^T, written once when the workspace was bound
+  a.sxp = h->bsxp;
+  a.sxp_stride = size_t(h->max_T);
   const CUtensorMap* vt = reinterpret_cast<const CUtensorMap*>(h->tmaps_proj);
   return launch_pdl(tc_proj_kernel, grid, dim3(kTcThreads), proj_smem(a.stages), s, *vt, tmX, a) ==
                  cudaSuccess

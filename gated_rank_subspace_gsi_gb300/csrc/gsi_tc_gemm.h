@@ -44,6 +44,10 @@ struct TcProjArgs {
                         // the first stages' A boxes load before the dependent-launch wait
   size_t split_stride;  // floats between slices
   uint32_t* status;
+  float* sxp;           // if set (the CTAs of the first 128 entries): ||x_t||^2 over the
+                        // slice, sxp[s * sxp_stride + t]; the epilogue warps sum the
+                        // staged x tiles while the MMAs run
+  size_t sxp_stride;
 };
 bool tc_proj_supported(const gsi_handle* h);
 gsi_status_t tc_proj_prepare(gsi_handle* h);
