@@ -191,7 +191,7 @@ namespace {
 // kernel reads x from every CTA, which is cheap from device memory (L2) and
 // dear over the host link.  Launched with programmatic dependent launch, so
 // the next kernel's CTAs stage their weights while it runs.
-__device__ __forceinline__ void stage_copy(const uint4* __restrict__ src, uint4* __restrict__ dst,
+__device__ __forceinline__ void stage_copy(const uint4* src, uint4* dst,
                                            int n16) {
   constexpr int kPer = 16;
   uint4 v[kPer];
@@ -208,8 +208,8 @@ __device__ __forceinline__ void stage_copy(const uint4* __restrict__ src, uint4*
   for (int i = int(threadIdx.x) + kPer * 256; i < n16; i += 256) dst[i] = src[i];
 }
 
-__global__ void __launch_bounds__(256) stage_x_kernel(const uint4* __restrict__ src,
-                                                      uint4* __restrict__ dst, int n16) {
+__global__ void __launch_bounds__(256) stage_x_kernel(const uint4* src,
+                                                      uint4* dst, int n16) {
   gsi::pdl_launch_dependents();
   gsi::pdl_wait();  // x may have been written by the previous kernel
   stage_copy(src, dst, n16);

@@ -176,10 +176,10 @@ __device__ __forceinline__ float gate_corr_subset(const uint4* sF, const float* 
 // and is also written to G for the gather; with S = 0 it is read from G.
 template <int K>
 __global__ void __launch_bounds__(kGateMmaThreads) gate_mma_kernel(
-    float* __restrict__ G, const float* __restrict__ P, int S, size_t split_stride,
-    const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ F, int T, int d,
-    float eps, uint8_t* __restrict__ gate_int, uint8_t* __restrict__ gate_out,
-    float* __restrict__ rho_out, uint32_t* __restrict__ status, const float* __restrict__ sxp,
+    float* G, const float* P, int S, size_t split_stride,
+    const __nv_bfloat16* x, const __nv_bfloat16* F, int T, int d,
+    float eps, uint8_t* gate_int, uint8_t* gate_out,
+    float* rho_out, uint32_t* status, const float* sxp,
     size_t sxp_stride) {
   constexpr int T16 = K / 16;
   constexpr int kTiles = T16 * (T16 + 1) / 2;
@@ -402,10 +402,10 @@ __global__ void __launch_bounds__(256) transpose_kernel(const __nv_bfloat16* __r
 // CTA 0 also writes the counts and empties the GEMM's tile queue.
 template <int K>
 __global__ void __launch_bounds__(256) partition_gather_kernel(
-    const __nv_bfloat16* __restrict__ x, const float* __restrict__ G,
-    const uint8_t* __restrict__ gate, int T, int d, int max_T, int32_t* __restrict__ idx_fast,
-    int32_t* __restrict__ idx_slow, int32_t* __restrict__ count, __nv_bfloat16* __restrict__ Gf,
-    __nv_bfloat16* __restrict__ Xs) {
+    const __nv_bfloat16* x, const float* G,
+    const uint8_t* gate, int T, int d, int max_T, int32_t* idx_fast,
+    int32_t* idx_slow, int32_t* count, __nv_bfloat16* Gf,
+    __nv_bfloat16* Xs) {
   __shared__ int s_red[2][8];
   pdl_launch_dependents();
   pdl_wait();

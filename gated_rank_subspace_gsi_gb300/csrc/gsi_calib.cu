@@ -88,9 +88,9 @@ __device__ __forceinline__ void store_val<__nv_bfloat16>(__nv_bfloat16* p, float
 }
 
 template <typename OutT>
-__global__ void __launch_bounds__(256) cal_transpose_kernel(const __nv_bfloat16* __restrict__ in,
+__global__ void __launch_bounds__(256) cal_transpose_kernel(const __nv_bfloat16* in,
                                                             int rows, int cols,
-                                                            OutT* __restrict__ out) {
+                                                            OutT* out) {
   __shared__ float tile[32][33];
   pdl_launch_dependents();
   pdl_wait();
@@ -110,9 +110,9 @@ __global__ void __launch_bounds__(256) cal_transpose_kernel(const __nv_bfloat16*
 
 // ---- sum of S split-K partials, fixed order (count % 4 == 0) ---------------
 template <typename OutT>
-__global__ void __launch_bounds__(256) cal_sum_kernel(const float* __restrict__ P, int S,
+__global__ void __launch_bounds__(256) cal_sum_kernel(const float* P, int S,
                                                       size_t stride, size_t count,
-                                                      OutT* __restrict__ out) {
+                                                      OutT* out) {
   pdl_launch_dependents();
   pdl_wait();
   const size_t n4 = count / 4;
@@ -141,11 +141,11 @@ __global__ void __launch_bounds__(256) cal_sum_kernel(const float* __restrict__ 
 constexpr int kGThreads = 256;
 constexpr int kGChunk = 64;
 
-__global__ void __launch_bounds__(kGThreads) cal_gram_kernel(const float* __restrict__ Q, int k,
-                                                             int d, int cs, float* __restrict__ Gp,
-                                                             float* __restrict__ G, int kp,
-                                                             CalCtl* __restrict__ ctl,
-                                                             uint32_t* __restrict__ counters,
+__global__ void __launch_bounds__(kGThreads) cal_gram_kernel(const float* Q, int k,
+                                                             int d, int cs, float* Gp,
+                                                             float* G, int kp,
+                                                             CalCtl* ctl,
+                                                             uint32_t* counters,
                                                              int only_if_need2) {
   __shared__ __align__(16) float As[kGChunk][kPtStride];
   __shared__ __align__(16) float Bs[kGChunk][kPtStride];
@@ -346,9 +346,9 @@ __device__ __forceinline__ void chol_diag_inverse(const float* AJJ, float* R, fl
 }
 
 __global__ void __launch_bounds__(kCThreads, 1)
-    cal_chol_kernel(const float* __restrict__ G, int k, int kp, float shift, int first_pass,
-                    float* __restrict__ Lg, float* __restrict__ LIg, float* __restrict__ Dg,
-                    CalCtl* __restrict__ ctl, int only_if_need2) {
+    cal_chol_kernel(const float* G, int k, int kp, float shift, int first_pass,
+                    float* Lg, float* LIg, float* Dg,
+                    CalCtl* ctl, int only_if_need2) {
   extern __shared__ __align__(16) float csm[];
   __shared__ int s_bad;
   __shared__ int s_small;
@@ -532,10 +532,10 @@ size_t apply_smem_bytes(int nb) {
 }
 
 __global__ void __launch_bounds__(kAThreads)
-    cal_apply_kernel(const float* __restrict__ Y, int k, int d, int kp, const float* __restrict__ Dg,
-                     const float* __restrict__ Lg, const float* __restrict__ LIg,
-                     float* __restrict__ outF, __nv_bfloat16* __restrict__ outB,
-                     __nv_bfloat16* __restrict__ outV, const CalCtl* __restrict__ ctl,
+    cal_apply_kernel(const float* Y, int k, int d, int kp, const float* Dg,
+                     const float* Lg, const float* LIg,
+                     float* outF, __nv_bfloat16* outB,
+                     __nv_bfloat16* outV, const CalCtl* ctl,
                      int only_if_need2) {
   extern __shared__ __align__(16) float asm_[];
   pdl_launch_dependents();

@@ -84,7 +84,7 @@ struct R1Args {
 
 // V's slice of 32 columns into shared memory (rows of 33, zero past d),
 // 2 x kRBatch rows per warp in flight.
-__device__ __forceinline__ void r1_load_slice(const float* __restrict__ V, int k, int d, int x0,
+__device__ __forceinline__ void r1_load_slice(const float* V, int k, int d, int x0,
                                               float* Vs) {
   constexpr int kW = kRThreads / 32, kB = 2 * kRBatch;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -182,7 +182,7 @@ __device__ __forceinline__ float r1_f(R1F2 x) { return x.hi + x.lo; }
 // shared memory (staged once per CTA), lanes over chunks with kRBatch chunks
 // of the row in flight; the total in every lane of the warp (fixed order:
 // each lane's chunks, then a butterfly).
-__device__ __forceinline__ float r1_row_dot_s(const __nv_bfloat16* __restrict__ row,
+__device__ __forceinline__ float r1_row_dot_s(const __nv_bfloat16* row,
                                               const float* vs, int len8) {
   const int lane = threadIdx.x & 31;
   const uint4* xr = reinterpret_cast<const uint4*>(row);
@@ -192,18 +192,18 @@ __device__ __forceinline__ float r1_row_dot_s(const __nv_bfloat16* __restrict__ 
   for (; i0 + 32 * (kRBatch - 1) < len8; i0 += 32 * kRBatch) {
     uint4 xv[kRBatch];
 #pragma unroll
-    for (int u = 0; u < kRBatch; ++u) xv[u] = __ldg(xr + i0 + 32 * u);
+    for (int u = 0; u < kRBatch; ++u) xv[u] = *(xr + i0 + 32 * u);
 #pragma unroll
     for (int u = 0; u < kRBatch; ++u)
       acc = r1_dot8(xv[u], vr[2 * (i0 + 32 * u)], vr[2 * (i0 + 32 * u) + 1], acc);
   }
-  for (; i0 < len8; i0 += 32) acc = r1_dot8(__ldg(xr + i0), vr[2 * i0], vr[2 * i0 + 1], acc);
+  for (; i0 < len8; i0 += 32) acc = r1_dot8(*(xr + i0), vr[2 * i0], vr[2 * i0 + 1], acc);
   return warp_sum(acc);
 }
 
 // r1_row_dot_s for two rows at once (both rows' chunks in flight together).
-__device__ __forceinline__ float2 r1_row_dot2_s(const __nv_bfloat16* __restrict__ r0,
-                                                const __nv_bfloat16* __restrict__ r1,
+__device__ __forceinline__ float2 r1_row_dot2_s(const __nv_bfloat16* r0,
+                                                const __nv_bfloat16* r1,
                                                 const float* vs, int len8) {
   const int lane = threadIdx.x & 31;
   const uint4* x0 = reinterpret_cast<const uint4*>(r0);
@@ -215,8 +215,8 @@ __device__ __forceinline__ float2 r1_row_dot2_s(const __nv_bfloat16* __restrict_
     uint4 xa[kRBatch], xb[kRBatch];
 #pragma unroll
     for (int u = 0; u < kRBatch; ++u) {
-      xa[u] = __ldg(x0 + i0 + 32 * u);
-      xb[u] = __ldg(x1 + i0 + 32 * u);
+      xa[u] = *(x0 + i0 + 32 * u);
+      xb[u] = *(x1 + i0 + 32 * u);
     }
 #pragma unroll
     for (int u = 0; u < kRBatch; ++u) {
@@ -227,8 +227,8 @@ __device__ __forceinline__ float2 r1_row_dot2_s(const __nv_bfloat16* __restrict_
   }
   for (; i0 < len8; i0 += 32) {
     const float4 va = vr[2 * i0], vb = vr[2 * i0 + 1];
-    a0 = r1_dot8(__ldg(x0 + i0), va, vb, a0);
-    a1 = r1_dot8(__ldg(x1 + i0), va, vb, a1);
+    a0 = r1_dot8(*(x0 + i0), va, vb, a0);
+    a1 = r1_dot8(*(x1 + i0), va, vb, a1);
   }
   return make_float2(warp_sum(a0), warp_sum(a1));
 }
@@ -431,8 +431,8 @@ __device__ void r1_apply_c_slice(const R1Args& a, int sl, int j, float qinv, flo
 // (q, then w).  A barrier that runs out (1 s) sets the timeout bit and ends the
 // launch in every CTA; V_out is then not written.
 __global__ void __launch_bounds__(kRThreads) r1_persistent_kernel(R1Args a, int corrections,
-                                                                  uint32_t* __restrict__ bar,
-                                                                  __nv_bfloat16* __restrict__ Vout) {
+                                                                  uint32_t* bar,
+                                                                  __nv_bfloat16* Vout) {
   extern __shared__ __align__(16) float r1_dyn[];
   float* Vs = r1_dyn;
   float* vsh = r1_dyn + a.k * (kRW + 1);  // 16-byte aligned: k is a multiple of 16
@@ -653,8 +653,8 @@ __global__ void __launch_bounds__(kRThreads) r1_persistent_kernel(R1Args a, int 
 // kp2 x kp2, lower tiles: G2[k + i][m] = p_i . v_m), one row i per warp with
 // the lanes over m, k / 8 CTAs; the CTA that finishes last (a ticket, no
 // wait) picks the first column and clears the control block.
-__global__ void __launch_bounds__(kRThreads) r1_init_kernel(R1Args a, const float* __restrict__ G2,
-                                                            int kp2, uint32_t* __restrict__ tick) {
+__global__ void __launch_bounds__(kRThreads) r1_init_kernel(R1Args a, const float* G2,
+                                                            int kp2, uint32_t* tick) {
   constexpr int kW = kRThreads / 32;
   __shared__ double s_dd[kRThreads];
   __shared__ int s_ii[kRThreads];
@@ -726,7 +726,7 @@ __global__ void __launch_bounds__(kRThreads) r1_init_kernel(R1Args a, const floa
 // finish: the pending rotation applied to this slice of V, and V written as
 // the d x k bf16 basis.  With no correction (jp = -1) V is the start basis.
 __global__ void __launch_bounds__(kRThreads) r1_finish_kernel(R1Args a, int any,
-                                                              __nv_bfloat16* __restrict__ Vout) {
+                                                              __nv_bfloat16* Vout) {
   __shared__ float Vs[kRMaxK * (kRW + 1)];
   pdl_launch_dependents();
   pdl_wait();

@@ -369,7 +369,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (ok) {
         for (int c0 = 0; c0 < u.N; c0 += 32) {
           // lane l holds the token of column c0 + l; each column's is broadcast
-          const int my_tok = c0 + lane < u.nvalid ? __ldg(idx + u.j0 + c0 + lane) : 0;
+          const int my_tok = c0 + lane < u.nvalid ? *(idx + u.j0 + c0 + lane) : 0;
           uint32_t r[32];
           tmem_ld_32x32b_x32(tmem + (uint32_t(qw * 32) << 16) + uint32_t(q * kBN + c0), r);
 #pragma unroll

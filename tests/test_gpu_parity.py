@@ -129,6 +129,31 @@ def test_batched_long_calls(gsi, orc, k, T):
     lin.close()
 
 
+@pytest.mark.parametrize("k", [128, 256])
+def test_batched_fresh_handles_repeat(gsi, orc, k):
+    """The batched kernels run with programmatic dependent launch: a kernel's
+    CTAs start while the previous kernel runs, and every read of what that
+    kernel writes must come after the dependent-launch wait.  Twelve fresh
+    handles (first calls, when most SMs are free for the early CTAs), each
+    call's gates against the oracle's.  A read moved above the wait showed as
+    wrong gates in about three calls of four at k = 128."""
+    d_out, d, T = 2048, 4096, 96
+    W = gi.gaussian_weights(d_out, d, 302 + k)
+    basis = gi.random_basis(d, k, 302 + k)
+    X = gi.tokens(basis, np.where(np.arange(T) % 3 == 0, 0.3, 0.05), 302 + k)
+    V = gi.bf16_bits_to_f64(basis.V_bits)
+    rho_ref = orc.forward(None, V, None, 0.1, gi.bf16_bits_to_f64(X))["rho"]
+    want = (rho_ref >= np.float32(0.1)).astype(np.uint8)
+    lin = GpuLinear(gsi, orc, W, basis.V_bits, 0.1)
+    for _ in range(12):
+        gsi.gsi_destroy(lin.h)
+        lin.h = gsi.gsi_create(lin.W_dev, lin.V_dev, lin.M_dev, 0.1)
+        y, g, r = lin.forward(X)
+        assert np.array_equal(g, want)
+        assert np.abs(r.astype(np.float64) - rho_ref).max() <= 1e-4
+    lin.close()
+
+
 @pytest.mark.parametrize("T", [1, 40])
 def test_eps_zero_and_inf(gsi, orc, T):
     """eps = 0: every token slow, y = W x.  eps = inf: every token fast."""
