@@ -15,13 +15,13 @@
 //
 // Persistent CTAs (192 threads, one per SM) take 128-row x 256-token slow
 // tiles and 128-row x 128-token fast tiles from a device-side queue, slow
-// tiles first: warp 0 issues TMA
-// loads (one elected lane), warp 1 allocates TMEM and issues tcgen05.mma (one
-// elected lane) into one of two 256-column accumulators, warps 2-5 drain the
-// other (tcgen05.ld 32x32b) and scatter each token column to its row of y.
-// A 4-stage mbarrier ring of 128x64 (A) and up to 256x64 (B: X_slow rows, or
-// 128 rows of each g plane) bf16 tiles, 128-byte swizzled, runs on across a
-// CTA's tiles.
+// tiles first: warp 0 issues TMA loads (one elected lane), warp 1 allocates
+// TMEM and issues tcgen05.mma (one elected lane) into one of two 256-column
+// accumulators, warps 2-5 drain the other (tcgen05.ld 32x32b) and scatter
+// each token column to its row of y.  Operands stream through mbarrier rings
+// of 128-byte-swizzled bf16 boxes that run on across a CTA's tiles: the slow
+// ring (a 128x64 box of W and the X_slow boxes of the token tile per stage)
+// and the fast ring (a 128x64 box of M and 128 rows of both g planes).
 #include <cuda.h>
 
 #include <algorithm>
@@ -183,12 +183,12 @@ __device__ __forceinline__ Tile decode_tile(int t, int n_slow_tiles, int n_mt, i
 }
 
 // Persistent: one CTA per SM takes tiles from a device-wide counter (zeroed
-// by the partition-and-gather kernel) until none are left.  Warp 0 (one lane) takes
-// each tile, publishes it to the other roles through a two-slot queue in
-// shared memory, and streams its operands through a 4-stage TMA ring that runs
-// on across tiles; warp 1 (one lane) issues the tile's MMAs into one of two
-// TMEM accumulators; warps 2-5 drain the other accumulator of the previous
-// tile meanwhile and scatter it to y.  Every wait is bounded.
+// by the partition-and-gather kernel) until none are left.  Warp 0 (one lane)
+// takes each tile, publishes it to the other roles through a two-slot queue
+// in shared memory, and streams its operands through the slow or the fast TMA
+// ring; warp 1 (one lane) issues the tile's MMAs into one of two TMEM
+// accumulators; warps 2-5 drain the other accumulator of the previous tile
+// meanwhile and scatter it to y.  Every wait is bounded.
 __global__ void __launch_bounds__(kTcThreads, 1)
     tc_gemm_kernel(const __grid_constant__ TcMaps maps, TcGemmArgs a) {
   constexpr int kQ = 2;  // tiles in flight: queue slots and TMEM accumulators
@@ -413,9 +413,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // ---- projection G = X V_k as a GEMM (T > 1) ------------------------------
 // D (128 entries of g x 64 tokens) = V^T rows (A, K-major: the handle's
 // transposed copy of V_k) . X rows (B, K-major), over one of S slices of the
-// reduction dimension d; each CTA writes its fp32 partial to P[s], and the
-// gate kernel sums the S partials in a fixed order.  Same warp roles as
-// tc_gemm_kernel.
+// reduction dimension d; each CTA writes its fp32 partial to P[s] (16-byte
+// stores staged through the drained ring), and the gate kernel sums the S
+// partials in a fixed order.  Same warp roles as tc_gemm_kernel.  For the
+// batched path (a_fixed) the V^T boxes of the first stages load before the
+// dependent-launch wait, and the CTAs of entries 0..127 also sum the squares
+// of each staged x tile on their epilogue warps (||x||^2 over the slice).
 constexpr int kPN = 64;  // tokens per tile (MMA N)
 constexpr int kPStages = 4;       // ring depth when the grid is more than one wave
 constexpr int kPMaxStages = 8;    // when every CTA is resident at once: a whole slice in flight
