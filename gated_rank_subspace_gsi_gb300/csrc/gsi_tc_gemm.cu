@@ -426,7 +426,6 @@ constexpr int kPABytes = kBM * kBK * 2;  // 16 KiB
 constexpr int kPBBytes = kPN * kBK * 2;  // 8 KiB
 constexpr int kPStageBytes = kPABytes + kPBBytes;
 constexpr int kPTmemCols = 64;
-constexpr size_t kPSmem = size_t(kPStages) * kPStageBytes + 1024;
 constexpr size_t kPMaxSmem = size_t(kPMaxStages) * kPStageBytes + 1024;
 
 __global__ void __launch_bounds__(kTcThreads, 1)
