@@ -734,8 +734,10 @@ __device__ __forceinline__ void cr_body(const CUtensorMap* tmV, const CUtensorMa
     }
   } else {
     // W_c x, W streamed from HBM: 4 rows per warp at a time, 4 16-byte
-    // pieces per row and lane in flight; the order of each row's sum does not
-    // depend on which CTA or warp owns the row
+    // pieces per row and lane in flight, refilled half at a time (the next
+    // step's pieces 0-1 load while pieces 2-3 are summed), so that the loads in
+    // flight never drain to zero; the order of each row's sum does not depend
+    // on which CTA or warp owns the row
     const int nch = a.d / 8;
     uint4* x4 = reinterpret_cast<uint4*>(smem);  // the M slice is not needed here
     {
@@ -758,23 +760,54 @@ __device__ __forceinline__ void cr_body(const CUtensorMap* tmV, const CUtensorMa
         wr[q] = reinterpret_cast<const uint4*>(a.W + size_t(m0 + r) * a.d);
       }
       int jj = lane;
-      for (; jj + 96 < nch; jj += 128) {
-        uint4 wv[4][4];
+      if (jj + 96 < nch) {
+        uint4 wa[4][2], wb[4][2];  // pieces 0-1 and 2-3 of the step at jj
 #pragma unroll
         for (int q = 0; q < 4; ++q)
 #pragma unroll
-          for (int p = 0; p < 4; ++p) wv[q][p] = ld_stream_v4(wr[q] + jj + 32 * p);
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-          float xf[8];
-          bf16x8_to_f32(x4[jj + 32 * p], xf);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            float f[8];
-            bf16x8_to_f32(wv[q][p], f);
-#pragma unroll
-            for (int t = 0; t < 8; ++t) acc4[q] = fmaf(f[t], xf[t], acc4[q]);
+          for (int p = 0; p < 2; ++p) {
+            wa[q][p] = ld_stream_v4(wr[q] + jj + 32 * p);
+            wb[q][p] = ld_stream_v4(wr[q] + jj + 32 * (p + 2));
           }
+        while (true) {
+          const int jn = jj + 128;
+          const bool next = jn + 96 < nch;
+#pragma unroll
+          for (int p = 0; p < 2; ++p) {
+            float xf[8];
+            bf16x8_to_f32(x4[jj + 32 * p], xf);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              float f[8];
+              bf16x8_to_f32(wa[q][p], f);
+#pragma unroll
+              for (int t = 0; t < 8; ++t) acc4[q] = fmaf(f[t], xf[t], acc4[q]);
+            }
+          }
+          if (next) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+              for (int p = 0; p < 2; ++p) wa[q][p] = ld_stream_v4(wr[q] + jn + 32 * p);
+          }
+#pragma unroll
+          for (int p = 0; p < 2; ++p) {
+            float xf[8];
+            bf16x8_to_f32(x4[jj + 32 * (p + 2)], xf);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              float f[8];
+              bf16x8_to_f32(wb[q][p], f);
+#pragma unroll
+              for (int t = 0; t < 8; ++t) acc4[q] = fmaf(f[t], xf[t], acc4[q]);
+            }
+          }
+          jj = jn;
+          if (!next) break;
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int p = 0; p < 2; ++p) wb[q][p] = ld_stream_v4(wr[q] + jj + 32 * (p + 2));
         }
       }
       for (; jj < nch; jj += 32) {
