@@ -128,14 +128,15 @@ struct CrCtl {
 // Dynamic shared-memory layout (byte offsets from the 1024-aligned base),
 // identical on host and device.
 //   A   [0, B): the M slice (K / 64 column blocks of rowsM x 128 bytes, TMA
-//       swizzled); x on the slow path
+//       swizzled); x on the slow path, then (d a multiple of 1024) its
+//       per-segment row sums where they fit (else at the head of B)
 //   B   [B, B + b): the V_k slice (same layout)
 //   aux g, the B fragments of g and the M g partials: the tail of B (dead
 //       once the projection is done) when they fit, else after it
 // The gate CTA, which stages neither slice, keeps the correction tiles at
 // [0, F), which ends before aux.  x slice and control words follow.
 struct CrLay {
-  size_t B, g, bfrag, yp, xs, ctl, total;
+  size_t B, part, g, bfrag, yp, xs, ctl, total;
 };
 __host__ __device__ inline size_t cr_al(size_t v, size_t a) { return (v + a - 1) / a * a; }
 __host__ __device__ inline CrLay cr_layout(int K, int d, int rowsM, int rowsV) {
@@ -148,6 +149,18 @@ __host__ __device__ inline CrLay cr_layout(int K, int d, int rowsM, int rowsV) {
   const size_t n_g = cr_al(size_t(K) * 4, 16), n_bf = cr_al(size_t(K / 16) * 64, 16);
   const size_t n_yp = cr_al(size_t(rowsM) * (K / 64) * 4, 16);
   const size_t aux = n_g + n_bf + n_yp;
+  // The slow path's per-segment row sums (d a multiple of 1024): after x in
+  // A, else at the head of the V_k slice (dead by then) ahead of aux, else
+  // in A grown to hold them.
+  const size_t n_part = d % 1024 == 0 ? size_t(rowsM) * (d / 1024) * 4 : 0;
+  if (a_x + n_part <= s.B) {
+    s.part = a_x;
+  } else if (aux <= b && n_part <= b - aux) {
+    s.part = s.B;
+  } else {
+    s.part = a_x;
+    s.B = cr_al(a_x + n_part, 1024);
+  }
   size_t ax = aux <= b ? s.B + b - aux : s.B + b;
   ax = ax > cr_al(a_F, 16) ? ax : cr_al(a_F, 16);
   s.g = ax;
@@ -751,6 +764,93 @@ __device__ __forceinline__ void cr_body(const CUtensorMap* tmV, const CUtensorMa
         if (tid + j * kThreads < nch) x4[tid + j * kThreads] = xv[j];
     }
     sync_compute();
+    if (nch % 128 == 0) {
+      // d a multiple of 1024: the work is cut into units of 4 rows x one
+      // 1024-element segment, dealt to the warps in turn so that every warp
+      // streams the same number of bytes; the next unit's pieces load while
+      // this unit's are summed.  A row's sum is the sum, in segment order, of
+      // its segments' warp sums (each a lane chain of 4 pieces, then the xor
+      // tree), staged in shared memory: its order depends on d alone.
+      const int P = nch / 128;
+      const int nU = (nM + 3) / 4 * P;
+      float* s_part = reinterpret_cast<float*>(smem + lay.part);  // [row][P]
+      int u = warp;
+      const uint4* wr[4];
+      auto unit_ptrs = [&](int uu) {
+        const int r0 = uu / P * 4, c0 = (uu - uu / P * P) * 128 + lane;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          wr[q] = reinterpret_cast<const uint4*>(a.W + size_t(m0 + min(r0 + q, nM - 1)) * a.d) + c0;
+      };
+      if (u < nU) {
+        unit_ptrs(u);
+        uint4 wa[4][2], wb[4][2];  // pieces 0-1 and 2-3 of the unit
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+          for (int p = 0; p < 2; ++p) {
+            wa[q][p] = ld_stream_v4(wr[q] + 32 * p);
+            wb[q][p] = ld_stream_v4(wr[q] + 32 * (p + 2));
+          }
+        while (true) {
+          const int un = u + kWarps;
+          const bool next = un < nU;
+          const int gi = u / P, seg = u - gi * P;
+          const uint4* xs4 = x4 + seg * 128 + lane;
+          if (next) unit_ptrs(un);  // all of this unit's pieces are loaded
+          float acc4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int p = 0; p < 2; ++p) {
+            float xf[8];
+            bf16x8_to_f32(xs4[32 * p], xf);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              float f[8];
+              bf16x8_to_f32(wa[q][p], f);
+#pragma unroll
+              for (int t = 0; t < 8; ++t) acc4[q] = fmaf(f[t], xf[t], acc4[q]);
+            }
+          }
+          if (next) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+              for (int p = 0; p < 2; ++p) wa[q][p] = ld_stream_v4(wr[q] + 32 * p);
+          }
+#pragma unroll
+          for (int p = 0; p < 2; ++p) {
+            float xf[8];
+            bf16x8_to_f32(xs4[32 * (p + 2)], xf);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              float f[8];
+              bf16x8_to_f32(wb[q][p], f);
+#pragma unroll
+              for (int t = 0; t < 8; ++t) acc4[q] = fmaf(f[t], xf[t], acc4[q]);
+            }
+          }
+          if (next) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+              for (int p = 0; p < 2; ++p) wb[q][p] = ld_stream_v4(wr[q] + 32 * (p + 2));
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float v = warp_sum_xor<32>(acc4[q]);
+            if (lane == q && gi * 4 + q < nM) s_part[(gi * 4 + q) * P + seg] = v;
+          }
+          u = un;
+          if (!next) break;
+        }
+      }
+      sync_compute();
+      for (int r = tid; r < nM; r += kThreads) {
+        float v = 0.f;
+        for (int q = 0; q < P; ++q) v += s_part[r * P + q];
+        a.y[m0 + r] = v;
+      }
+    } else
     for (int rb = warp * 4; rb < nM; rb += kWarps * 4) {
       float acc4[4] = {0.f, 0.f, 0.f, 0.f};
       const uint4* wr[4];

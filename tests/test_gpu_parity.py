@@ -20,9 +20,10 @@ pytestmark = pytest.mark.gpu
 # and the decode kernel's per-CTA slices; every supported k.
 SHAPES = [(24, 64, 16), (40, 136, 32), (96, 264, 64), (200, 512, 128), (2304, 768, 256),
           (136, 1024, 512), (1000, 4104, 256)]
-# One-token shapes besides: 10 row blocks of M per CTA (one warp each) and 19
-# row blocks staged as two TMA row boxes.
-DECODE_SHAPES = SHAPES + [(22800, 1024, 256), (45600, 1024, 128)]
+# One-token shapes besides: 10 row blocks of M per CTA (one warp each), 19
+# row blocks staged as two TMA row boxes, and a d of 2 x 1024 with a ragged
+# d_out (the slow path's steps run on across groups of 4 rows).
+DECODE_SHAPES = SHAPES + [(22800, 1024, 256), (45600, 1024, 128), (1000, 2048, 64)]
 
 
 def spread_rho(eps: float, T: int, seed: int) -> np.ndarray:
