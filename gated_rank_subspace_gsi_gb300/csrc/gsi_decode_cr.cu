@@ -752,6 +752,7 @@ __device__ __forceinline__ void cr_body(const CUtensorMap* tmV, const CUtensorMa
     // flight never drain to zero; the order of each row's sum does not depend
     // on which CTA or warp owns the row
     const int nch = a.d / 8;
+    const uint64_t pol = l2_evict_first_policy();  // W is read once per call
     uint4* x4 = reinterpret_cast<uint4*>(smem);  // the M slice is not needed here
     {
       uint4 xv[kMaxXChunks];
@@ -789,8 +790,8 @@ __device__ __forceinline__ void cr_body(const CUtensorMap* tmV, const CUtensorMa
         for (int q = 0; q < 4; ++q)
 #pragma unroll
           for (int p = 0; p < 2; ++p) {
-            wa[q][p] = ld_stream_v4(wr[q] + 32 * p);
-            wb[q][p] = ld_stream_v4(wr[q] + 32 * (p + 2));
+            wa[q][p] = ld_stream_v4(wr[q] + 32 * p, pol);
+            wb[q][p] = ld_stream_v4(wr[q] + 32 * (p + 2), pol);
           }
         while (true) {
           const int un = u + kWarps;
@@ -815,7 +816,7 @@ __device__ __forceinline__ void cr_body(const CUtensorMap* tmV, const CUtensorMa
 #pragma unroll
             for (int q = 0; q < 4; ++q)
 #pragma unroll
-              for (int p = 0; p < 2; ++p) wa[q][p] = ld_stream_v4(wr[q] + 32 * p);
+              for (int p = 0; p < 2; ++p) wa[q][p] = ld_stream_v4(wr[q] + 32 * p, pol);
           }
 #pragma unroll
           for (int p = 0; p < 2; ++p) {
@@ -833,7 +834,7 @@ __device__ __forceinline__ void cr_body(const CUtensorMap* tmV, const CUtensorMa
 #pragma unroll
             for (int q = 0; q < 4; ++q)
 #pragma unroll
-              for (int p = 0; p < 2; ++p) wb[q][p] = ld_stream_v4(wr[q] + 32 * (p + 2));
+              for (int p = 0; p < 2; ++p) wb[q][p] = ld_stream_v4(wr[q] + 32 * (p + 2), pol);
           }
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -866,8 +867,8 @@ __device__ __forceinline__ void cr_body(const CUtensorMap* tmV, const CUtensorMa
         for (int q = 0; q < 4; ++q)
 #pragma unroll
           for (int p = 0; p < 2; ++p) {
-            wa[q][p] = ld_stream_v4(wr[q] + jj + 32 * p);
-            wb[q][p] = ld_stream_v4(wr[q] + jj + 32 * (p + 2));
+            wa[q][p] = ld_stream_v4(wr[q] + jj + 32 * p, pol);
+            wb[q][p] = ld_stream_v4(wr[q] + jj + 32 * (p + 2), pol);
           }
         while (true) {
           const int jn = jj + 128;
@@ -888,7 +889,7 @@ __device__ __forceinline__ void cr_body(const CUtensorMap* tmV, const CUtensorMa
 #pragma unroll
             for (int q = 0; q < 4; ++q)
 #pragma unroll
-              for (int p = 0; p < 2; ++p) wa[q][p] = ld_stream_v4(wr[q] + jn + 32 * p);
+              for (int p = 0; p < 2; ++p) wa[q][p] = ld_stream_v4(wr[q] + jn + 32 * p, pol);
           }
 #pragma unroll
           for (int p = 0; p < 2; ++p) {
@@ -907,7 +908,7 @@ __device__ __forceinline__ void cr_body(const CUtensorMap* tmV, const CUtensorMa
 #pragma unroll
           for (int q = 0; q < 4; ++q)
 #pragma unroll
-            for (int p = 0; p < 2; ++p) wb[q][p] = ld_stream_v4(wr[q] + jj + 32 * (p + 2));
+            for (int p = 0; p < 2; ++p) wb[q][p] = ld_stream_v4(wr[q] + jj + 32 * (p + 2), pol);
         }
       }
       for (; jj < nch; jj += 32) {
@@ -916,7 +917,7 @@ __device__ __forceinline__ void cr_body(const CUtensorMap* tmV, const CUtensorMa
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           float f[8];
-          bf16x8_to_f32(ld_stream_v4(wr[q] + jj), f);
+          bf16x8_to_f32(ld_stream_v4(wr[q] + jj, pol), f);
 #pragma unroll
           for (int t = 0; t < 8; ++t) acc4[q] = fmaf(f[t], xf[t], acc4[q]);
         }
