@@ -78,6 +78,7 @@ constexpr int kCountShift = 58;             // arrivals above the summed fixed p
 constexpr int kMaxBoxRows = 256;            // TMA box limit
 constexpr int kMaxPf = 12;                  // prefetch ranges (3 per handle, up to 4 handles)
 constexpr size_t kCoresidentSmem = 115712;  // 2 x (this + 1 KB reserved) <= 228 KB per SM
+constexpr int kSlowAhead = 2;               // slow path: units of W prefetched ahead per warp
 constexpr int kMaxXChunks = 8;              // 16-byte chunks of x per thread: d <= 16384
 constexpr int kMaxD = kMaxXChunks * kThreads * 8;
 
@@ -783,7 +784,18 @@ __device__ __forceinline__ void cr_body(const CUtensorMap* tmV, const CUtensorMa
         for (int q = 0; q < 4; ++q)
           wr[q] = reinterpret_cast<const uint4*>(a.W + size_t(m0 + min(r0 + q, nM - 1)) * a.d) + c0;
       };
+      // Lanes 0-3 prefetch into L2 the 2 KB row segments of this warp's unit
+      // kSlowAhead turns ahead, so that more of W is in flight than the
+      // registers hold and the register loads find it in L2.
+      auto unit_prefetch = [&](int uu) {
+        if (lane < 4 && uu < nU) {
+          const int r = min(uu / P * 4 + lane, nM - 1), c = (uu - uu / P * P) * 1024;
+          prefetch_l2(a.W + size_t(m0 + r) * a.d + c, 2048u);
+        }
+      };
       if (u < nU) {
+#pragma unroll 1
+        for (int i = 1; i <= kSlowAhead; ++i) unit_prefetch(u + i * kWarps);
         unit_ptrs(u);
         uint4 wa[4][2], wb[4][2];  // pieces 0-1 and 2-3 of the unit
 #pragma unroll
@@ -799,6 +811,7 @@ __device__ __forceinline__ void cr_body(const CUtensorMap* tmV, const CUtensorMa
           const int gi = u / P, seg = u - gi * P;
           const uint4* xs4 = x4 + seg * 128 + lane;
           if (next) unit_ptrs(un);  // all of this unit's pieces are loaded
+          unit_prefetch(u + (kSlowAhead + 1) * kWarps);
           float acc4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int p = 0; p < 2; ++p) {
